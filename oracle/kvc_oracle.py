@@ -1,0 +1,317 @@
+"""fp64 NumPy oracle for the paged KV-cache hot path (test infrastructure only).
+
+Nothing in the product imports this file.  It is a direct restatement of the
+definitions on the source pages, with no blocking, fusion or reordering:
+
+* Address mapping -- "external-cannbot-model-model-infer-kvcache", 3.1
+  "Physical Memory Layout and Logical Mapping" (Mapping Formula and its
+  example), 3.3 "slot_mapping Construction"; hotelren.com notes "Paged KV
+  Cache + Packed Sequence", 2.2 (logical block / slot / flat offset).
+* Cache write -- ai6s.net KVCache article, section 4.2 "KVCache computation
+  logic": new rows are copied, unchanged, into the cache position that the
+  write index names.  Here the index is the slot of the mapping formula.
+* Paged attention -- KVCache skill Mode 2 (FA reads the block cache through
+  block_table with per-sequence actual KV lengths), Appendix C (sparse_mode 0
+  for decode, 3 = causal for prefill); hotelren.com notes 3.2-3.3 (causal
+  within a sequence only; packed token -> request -> logical block -> physical
+  block) and 5.1 (rebuild each sequence's logical K/V matrix from the
+  blocks).
+* MLA -- KVCache skill Mode 3: key = value = cache_nope, plus a separate rope
+  part for query and key.
+
+Readings where the pages are silent (each listed in the design doc):
+  - q head h uses kv head h // (Hq / Hkv) (contiguous GQA groups);
+  - causal attention includes the query's own position;
+  - seq_lens counts cached tokens including the one written this step;
+  - a sequence with no visible key returns exact zeros;
+  - a negative slot in slot_mapping means "do not write".
+
+All floating-point work is float64.  Inputs given as fp16/bf16 values must be
+converted to float64 by the caller (the conversion is exact).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Sizes (ai6s.net article section 3; hotelren.com notes 1.1, 2.3, 4.1)
+# ---------------------------------------------------------------------------
+
+
+def kv_cache_bytes(num_layers: int, seq_len: int, num_heads: int, head_dim: int,
+                   dtype_bytes: int) -> int:
+    """Total KV cache size L x S x 2 x H x d x B in bytes.
+
+    ai6s.net KVCache article, section 3 item 1 ("basic formula"): every layer
+    caches one K and one V vector of width d per head per token.
+    """
+    return num_layers * seq_len * 2 * num_heads * head_dim * dtype_bytes
+
+
+def max_seq_len_for_memory(free_bytes: float, num_layers: int, num_heads: int,
+                           head_dim: int, dtype_bytes: int) -> float:
+    """Largest S with L x S x 2 x H x d x B <= free_bytes (section 3 item 4).
+
+    The article inverts the size formula to size the context for a given
+    amount of free device memory.
+    """
+    return free_bytes / (num_layers * 2 * num_heads * head_dim * dtype_bytes)
+
+
+def cache_manager_mem_need_gib(num_blocks: int, block_size: int, num_kv_heads: int,
+                               head_size: int, num_layers: int, dtype_bytes: int) -> float:
+    """GiB a block-pool cache manager allocates (ai6s.net article 4.1).
+
+    The ND pool holds one K and one V tensor of shape
+    [num_blocks, block_size, num_kv_heads, head_size] per layer.
+    """
+    return (num_blocks * block_size * num_kv_heads * head_size * num_layers * 2
+            * dtype_bytes) / 1024 / 1024 / 1024
+
+
+def kv_bytes_per_token_per_layer(hidden_size: int, dtype_bytes: int) -> int:
+    """2 (K and V) x hidden_size x bytes (hotelren.com notes 1.1)."""
+    return 2 * hidden_size * dtype_bytes
+
+
+def blocks_for_tokens(num_tokens: int, block_size: int) -> int:
+    """Physical blocks a sequence of num_tokens occupies: ceil(n / block_size).
+
+    hotelren.com notes 2.1 (allocate_slots rounds the token count up to whole
+    blocks) and 2.3 (page-table rows per request).
+    """
+    return (num_tokens + block_size - 1) // block_size
+
+
+def pack_lengths(lens):
+    """Packed-sequence bookkeeping (hotelren.com notes 3.1 and 4.1).
+
+    Returns (seq_offset, position_ids, packed_total, padded_total):
+    seq_offset is the prefix sum with a leading 0 (the cu_seqlens array),
+    position_ids restart at 0 for every sequence, padded_total pads every
+    sequence to the longest one.
+    """
+    lens = [int(x) for x in lens]
+    seq_offset = [0]
+    for n in lens:
+        seq_offset.append(seq_offset[-1] + n)
+    position_ids = [p for n in lens for p in range(n)]
+    padded = (max(lens) if lens else 0) * len(lens)
+    return seq_offset, position_ids, seq_offset[-1], padded
+
+
+# ---------------------------------------------------------------------------
+# Address mapping (KVCache skill 3.1-3.3; hotelren.com notes 2.2)
+# ---------------------------------------------------------------------------
+
+
+def logical_to_physical(block_table, seq: int, pos: int, block_size: int):
+    """(logical block, in-block offset, physical block, slot) of one position.
+
+    KVCache skill 3.1 "Mapping Formula": logical block = pos // block_size,
+    offset = pos % block_size, physical block = block_table[seq, logical],
+    slot = physical * block_size + offset.
+    """
+    lb = pos // block_size
+    off = pos % block_size
+    pb = int(block_table[seq][lb])
+    return lb, off, pb, pb * block_size + off
+
+
+def sequential_block_table(batch: int, max_seq_len: int, block_size: int) -> np.ndarray:
+    """Static block table arange(total).reshape(batch, -1) (KVCache skill 3.2)."""
+    per_seq = max_seq_len // block_size
+    return np.arange(batch * per_seq, dtype=np.int64).reshape(batch, per_seq)
+
+
+def sequential_slot(seq: int, pos: int, max_seq_len: int) -> int:
+    """Slot under sequential allocation: seq * max_seq_len + pos (KVCache skill 3.3)."""
+    return seq * max_seq_len + pos
+
+
+def slot_mapping(block_table, block_size: int, start_pos, cu_seqlens=None) -> np.ndarray:
+    """Cache slot of every token to be written.
+
+    Decode form (cu_seqlens is None): one token per sequence s, written at
+    position start_pos[s] (the current kv_len, KVCache skill 3.3 "Decode").
+    Packed form: token t of sequence s (cu_seqlens[s] <= t < cu_seqlens[s+1])
+    sits at position start_pos[s] + (t - cu_seqlens[s]) (hotelren.com notes
+    3.3: packed token -> request and offset -> logical block -> physical
+    block).  Every position is mapped by logical_to_physical.
+    """
+    start_pos = [int(x) for x in start_pos]
+    out = []
+    if cu_seqlens is None:
+        for s, p in enumerate(start_pos):
+            out.append(logical_to_physical(block_table, s, p, block_size)[3])
+    else:
+        cu = [int(x) for x in cu_seqlens]
+        for s in range(len(cu) - 1):
+            for t in range(cu[s], cu[s + 1]):
+                p = start_pos[s] + (t - cu[s])
+                out.append(logical_to_physical(block_table, s, p, block_size)[3])
+    return np.asarray(out, dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# Cache write (ai6s.net article 4.2)
+# ---------------------------------------------------------------------------
+
+
+def reshape_and_cache(key, value, key_cache, value_cache, slots):
+    """Copy token rows into the paged cache at their slots; returns new caches.
+
+    key [T, Hkv, Dk] -> key_cache [num_blocks, block_size, Hkv, Dk] at
+    (slot // block_size, slot % block_size); the same for value.  Works on any
+    dtype (callers pass raw 16-bit patterns so the copy is checked bit for
+    bit).  A negative slot writes nothing.  value/value_cache may be None.
+    """
+    kc = np.array(key_cache, copy=True)
+    vc = None if value_cache is None else np.array(value_cache, copy=True)
+    bs = kc.shape[1]
+    for t, slot in enumerate(np.asarray(slots).tolist()):
+        if slot < 0:
+            continue
+        kc[slot // bs, slot % bs] = key[t]
+        if vc is not None:
+            vc[slot // bs, slot % bs] = value[t]
+    return kc, vc
+
+
+def gather_sequence(cache, block_table_row, length: int):
+    """Rebuild one sequence's logical cache rows [length, ...] from its blocks.
+
+    hotelren.com notes 5.1: recover each sequence's logical K/V matrix from
+    block_table and the per-block slots, position by position.
+    """
+    bs = cache.shape[1]
+    rows = [cache[int(block_table_row[j // bs]), j % bs] for j in range(length)]
+    if not rows:
+        return np.zeros((0,) + cache.shape[2:], dtype=cache.dtype)
+    return np.stack(rows, axis=0)
+
+
+# ---------------------------------------------------------------------------
+# Attention (KVCache skill Mode 2, Mode 3, Appendix C)
+# ---------------------------------------------------------------------------
+
+
+def softmax_attention(q, K, V, scale: float):
+    """o = sum_j softmax_j(scale * q . K_j) V_j in float64.
+
+    q [D], K [L, D], V [L, Dv].  Uses the max-subtracted exponential (exact in
+    real arithmetic).  With L == 0 there is no visible key and the result is
+    a row of zeros (our reading of the fully-masked row).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1], dtype=np.float64)
+    s = scale * (K @ q)
+    w = np.exp(s - s.max())
+    return (w / w.sum()) @ V
+
+
+def kv_head_of(q_head: int, num_q_heads: int, num_kv_heads: int) -> int:
+    """GQA grouping: contiguous groups of Hq/Hkv query heads share a kv head."""
+    return q_head // (num_q_heads // num_kv_heads)
+
+
+def paged_decode(q, key_cache, value_cache, block_table, seq_lens, scale: float):
+    """Decode attention over the paged cache (KVCache skill Mode 2, sparse_mode 0).
+
+    q [B, Hq, D]; caches [num_blocks, block_size, Hkv, D]; block_table
+    [B, max_blocks]; seq_lens[b] = cached tokens of sequence b (including the
+    token written this step).  Returns float64 [B, Hq, Dv].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, _ = q.shape
+    Hkv = key_cache.shape[2]
+    Dv = value_cache.shape[3]
+    out = np.zeros((B, Hq, Dv), dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        K = gather_sequence(key_cache, block_table[b], L)
+        V = gather_sequence(value_cache, block_table[b], L)
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            out[b, h] = softmax_attention(q[b, h], K[:, g, :], V[:, g, :], scale)
+    return out
+
+
+def contiguous_decode(q, key_lin, value_lin, seq_lens, scale: float):
+    """Decode over a contiguous per-sequence cache [B, max_len, Hkv, D].
+
+    The linear-cache golden of the "double-track" check in hotelren.com
+    notes 5.4: the paged result must equal this one.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, _ = q.shape
+    Hkv = key_lin.shape[2]
+    out = np.zeros((B, Hq, value_lin.shape[3]), dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            out[b, h] = softmax_attention(q[b, h], key_lin[b, :L, g, :],
+                                          value_lin[b, :L, g, :], scale)
+    return out
+
+
+def varlen_prefill_paged(q, key, value, cu_seqlens, context_lens, slots, block_table,
+                         key_cache, value_cache, scale: float):
+    """Packed varlen causal prefill that first writes its K/V into the paged cache.
+
+    Sequence s owns packed tokens cu_seqlens[s] .. cu_seqlens[s+1]-1; token i
+    of it sits at position context_lens[s] + i.  Its K/V rows go to the cache
+    through `slots` (ai6s.net article 4.2), then it attends causally to
+    positions 0 .. context_lens[s] + i of its own sequence only, read back
+    through block_table (hotelren.com notes 3.2-3.3; KVCache skill Appendix
+    C sparse_mode 3).  Returns (out [T, Hq, Dv] float64, key_cache',
+    value_cache').
+    """
+    kc, vc = reshape_and_cache(key, value, key_cache, value_cache, slots)
+    q = np.asarray(q, dtype=np.float64)
+    T, Hq, _ = q.shape
+    Hkv = kc.shape[2]
+    out = np.zeros((T, Hq, vc.shape[3]), dtype=np.float64)
+    cu = [int(x) for x in cu_seqlens]
+    for s in range(len(cu) - 1):
+        ctx = 0 if context_lens is None else int(context_lens[s])
+        n = cu[s + 1] - cu[s]
+        total = ctx + n
+        K = gather_sequence(kc, block_table[s], total).astype(np.float64)
+        V = gather_sequence(vc, block_table[s], total).astype(np.float64)
+        for i in range(n):
+            visible = ctx + i + 1
+            for h in range(Hq):
+                g = kv_head_of(h, Hq, Hkv)
+                out[cu[s] + i, h] = softmax_attention(q[cu[s] + i, h], K[:visible, g, :],
+                                                      V[:visible, g, :], scale)
+    return out, kc, vc
+
+
+def mla_paged_decode(q_nope, q_rope, cache_nope, cache_rope, block_table, seq_lens,
+                     scale: float):
+    """MLA absorb decode (KVCache skill Mode 3).
+
+    key = [cache_nope | cache_rope] (512 + 64 wide), value = cache_nope; all H
+    query heads share the single latent head.  q_nope [B, H, 512], q_rope
+    [B, H, 64]; caches [num_blocks, block_size, 1, width].  Returns float64
+    [B, H, 512].
+    """
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    q_rope = np.asarray(q_rope, dtype=np.float64)
+    B, H, _ = q_nope.shape
+    out = np.zeros((B, H, cache_nope.shape[3]), dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        Kn = gather_sequence(cache_nope, block_table[b], L)[:, 0, :].astype(np.float64)
+        Kr = gather_sequence(cache_rope, block_table[b], L)[:, 0, :].astype(np.float64)
+        K = np.concatenate([Kn, Kr], axis=1)
+        for h in range(H):
+            qh = np.concatenate([q_nope[b, h], q_rope[b, h]])
+            out[b, h] = softmax_attention(qh, K, Kn, scale)
+    return out
