@@ -1,0 +1,397 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one decode layer step of the GQA 8B-shape workload (bf16, 32 q /
+8 kv heads, head_dim 128, block_size 128, batch 64, lognormal KV lengths):
+slot mapping of the new token, its cache write, and paged decode attention
+with split-KV and the merge.  Inputs stay resident in HBM; the K/V read per
+step (~0.6 GB) is larger than L2, so no flush is needed between steps.
+
+Printed: one JSON line (metric = achieved HBM GB/s of algorithmic bytes, plus
+decode tokens/s, the roofline of the dominant kernel, the CPU oracle as a
+reported baseline, and an end-to-end figure through the public API with host
+buffers).  ``--impl reference`` times the CPU oracle on the same workload.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload (the path shards by sequence with no exchange), timing is the max
+over ranks, value is the sum of all ranks' work.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+# The oracle baseline is reported per core: keep NumPy's BLAS single-threaded.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from synth import CONFIGS, make_config  # noqa: E402
+
+WORKLOAD = "gqa8b_decode"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_bytes(seq_lens, Hq, Hkv, D, bs, elt=2):
+    """Algorithmic bytes of one paged decode: K/V rows attended, Q, O, table, lengths."""
+    toks = int(sum(int(x) for x in seq_lens))
+    blocks = sum(-(-int(x) // bs) for x in seq_lens)
+    B = len(seq_lens)
+    return toks * Hkv * D * 2 * elt + 2 * B * Hq * D * elt + 4 * blocks + 4 * B
+
+
+def write_bytes(B, Hkv, D, elt=2):
+    """New K/V rows read + written into the cache, plus slot ints written and read."""
+    return 2 * (2 * B * Hkv * D * elt) + 3 * 4 * B
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for name in ("paged_decode.cu", "kvc_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_135_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(profile_md, digest):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the source."""
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile_md)).read()
+    except OSError:
+        return None
+    m_d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    m_t = re.search(r"traffic_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
+    if not m_d or not m_t or m_d.group(1) != digest:
+        return None
+    return float(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class DecodeStep:
+    """Device-resident decode-layer step through the public API."""
+
+    def __init__(self, kvc, case, device):
+        self.kvc = kvc
+        self.case = case
+        dv = device
+        self.q = case.q.to(dv)
+        self.kc = case.key_cache.to(dv)
+        self.vc = case.value_cache.to(dv)
+        self.bt = case.block_table.to(dv)
+        self.sl = case.seq_lens.to(dv)
+        self.nk = case.new_key.to(dv)
+        self.nv = case.new_value.to(dv)
+        self.wp = case.write_pos.to(dv)
+        self.out = torch.empty_like(self.q)
+        self.slots = torch.empty(self.q.shape[0], dtype=torch.int32, device=dv)
+        m = case.meta
+        self.Hq, self.Hkv, self.D = m["num_q_heads"], m["num_kv_heads"], m["head_dim"]
+        n = kvc.decode_workspace_size(self.Hq, self.Hkv, self.D)
+        self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dv)
+        self.nb = self.kc.shape[0]
+
+    def write(self):
+        k = self.kvc
+        k.build_slot_mapping(self.bt, self.case.block_size, self.wp, self.nb, out=self.slots)
+        k.reshape_and_cache(self.nk, self.nv, self.kc, self.vc, self.slots)
+
+    def decode(self):
+        self.kvc.paged_decode(self.q, self.kc, self.vc, self.bt, self.sl, self.case.scale,
+                              out=self.out, workspace=self.ws)
+
+    LAUNCHES = 4  # slot mapping, cache write, decode, split-KV merge
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_rate(case, budget_s=12.0):
+    """Time the oracle on sequences of the workload until ~budget_s has elapsed."""
+    from oracle import kvc_oracle as O
+    m = case.meta
+    bs = case.block_size
+    done_bytes, t_total, n_seq = 0, 0.0, 0
+    B = case.q.shape[0]
+    for b in range(B):
+        L = int(case.seq_lens[b])
+        nblk = max(1, -(-L // bs))
+        ids = case.block_table[b, :nblk].long()
+        k = case.key_cache[ids.to(case.key_cache.device)].double().cpu().numpy()
+        v = case.value_cache[ids.to(case.value_cache.device)].double().cpu().numpy()
+        q = case.q[b:b + 1].double().cpu().numpy()
+        table = np.arange(nblk)[None]
+        t0 = time.perf_counter()
+        O.paged_decode(q, k, v, table, [L], case.scale)
+        t_total += time.perf_counter() - t0
+        done_bytes += decode_bytes([L], m["num_q_heads"], m["num_kv_heads"], m["head_dim"], bs)
+        n_seq += 1
+        if t_total > budget_s:
+            break
+    return done_bytes / t_total / 1e9, n_seq, B, t_total
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    case = make_config(WORKLOAD, seed=0)
+    budget = max(2.0, min(20.0, 90.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        gbs, n_seq, B, t = cpu_oracle_rate(case, budget_s=budget)
+        if i >= args.warmup:
+            vals.append((gbs, n_seq, t))
+    value = statistics.median(v[0] for v in vals)
+    n_seq = vals[0][1]
+    print(json.dumps({
+        "impl": "reference", "metric": "paged decode achieved HBM GB/s (algorithmic bytes)",
+        "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(v[2] for v in vals),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": CONFIGS[WORKLOAD]["about"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {n_seq} of 64 sequences per step (fp64 NumPy oracle)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import paged_kv_cache_135_gb300 as kvc
+    kvc.build()
+    kvc.lib()
+
+    case = make_config(WORKLOAD, seed=rank, value_device=str(dev))
+    m = case.meta
+    step = DecodeStep(kvc, case, dev)
+    B = case.q.shape[0]
+    lens = case.seq_lens.tolist()
+    d_bytes = decode_bytes(lens, m["num_q_heads"], m["num_kv_heads"], m["head_dim"],
+                           case.block_size)
+    w_bytes = write_bytes(B, m["num_kv_heads"], m["head_dim"])
+    step_bytes = d_bytes + w_bytes
+
+    for _ in range(args.warmup):
+        step.write()
+        step.decode()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step.write()
+            ev[i][0].record(stream)
+            step.decode()
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
+    tokens_per_s = ws * B / (ms_per_step * 1e-3)
+
+    # End to end through the public API: per step, pinned host inputs -> device,
+    # the step, device -> pinned host output, synchronised.
+    h = {k: getattr(case, k).cpu().pin_memory() for k in
+         ("q", "new_key", "new_value", "block_table", "seq_lens", "write_pos")}
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = h_out.numel() * h_out.element_size()
+    for i in range(3 + args.e2e_steps):
+        if i == 3:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        step.q.copy_(h["q"], non_blocking=True)
+        step.nk.copy_(h["new_key"], non_blocking=True)
+        step.nv.copy_(h["new_value"], non_blocking=True)
+        step.bt.copy_(h["block_table"], non_blocking=True)
+        step.sl.copy_(h["seq_lens"], non_blocking=True)
+        step.wp.copy_(h["write_pos"], non_blocking=True)
+        step.write()
+        step.decode()
+        h_out.copy_(step.out, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    peak, peak_kind = peaks()
+    dec_avg_ms = statistics.mean(dec_ms)
+    achieved = d_bytes / (dec_avg_ms * 1e-3) / 1e9
+    digest = kernel_source_digest()
+    traffic = recorded_traffic("paged_decode_gqa8b.md", digest)
+
+    if rank == 0:
+        res = {
+            "metric": "paged decode achieved HBM GB/s (algorithmic bytes) and decode tokens/s",
+            "value": value,
+            "unit": "GB/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": CONFIGS[WORKLOAD]["about"],
+                "batch": B, "num_q_heads": m["num_q_heads"], "num_kv_heads": m["num_kv_heads"],
+                "head_dim": m["head_dim"], "block_size": case.block_size,
+                "kv_tokens": int(sum(lens)), "step": "slot mapping + cache write + paged decode "
+                "(split-KV + merge)", "algorithmic_bytes_per_step": step_bytes,
+                "l2": "no flush: each step reads %.0f MB of K/V, more than the 129 MB L2"
+                      % (d_bytes / 1e6),
+                "parallelism": f"replicas x{ws}",
+            },
+            "decode_tokens_per_s": tokens_per_s,
+            "pct_of_nominal_8tbps": 100.0 * value / NOMINAL_HBM_GBS,
+            "roofline": {
+                "kernel": "paged_decode_kernel + paged_decode_merge_kernel (one kvc_paged_decode)",
+                "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                "algorithmic_bytes_per_launch": d_bytes, "avg_launch_ms": dec_avg_ms,
+                "frac_of_nominal_8tbps": achieved / NOMINAL_HBM_GBS,
+            },
+            "e2e": {"value": ws * step_bytes / e2e_s / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_s * 1e3, "tokens_per_s": ws * B / e2e_s},
+            "gpu_launches": DecodeStep.LAUNCHES * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            gbs, n_seq, Btot, t = cpu_oracle_rate(case)
+            res["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                   "sample": f"{n_seq} of {Btot} sequences, fp64 NumPy oracle, "
+                                             f"{t:.1f} s"}
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

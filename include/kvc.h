@@ -1,0 +1,178 @@
+/*
+ * kvc.h -- C ABI of the GB300 (sm_103a) paged KV-cache attention library.
+ *
+ * The operations restate the problem posed by these pages:
+ *   [SKILL] "external-cannbot-model-model-infer-kvcache" (KVCache Optimization
+ *           Skill): Mode 2 "Paged attention + FA fused operator", Mode 3 "MLA
+ *           compressed cache", 3.1 "Physical Memory Layout and Logical
+ *           Mapping", 3.3 "slot_mapping Construction", 3.4
+ *           "actual_seq_lengths Construction", Appendix C "sparse_mode".
+ *   [ATB]   ai6s.net KVCache article, section 4: cache allocation in the ND
+ *           layout [num_blocks, block_size, num_heads, head_size] and the
+ *           cache write loop.
+ *   [NOTES] hotelren.com notes "Paged KV Cache + Packed Sequence", sections
+ *           2.2 (index arithmetic), 3.1-3.3 (seq_offset / cu_seqlens, causal
+ *           within a sequence, packed -> paged index chain).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is a DEVICE pointer to a contiguous row-major
+ *   tensor, 16-byte aligned.  The caller owns every buffer (including the
+ *   workspace); the library never allocates or frees device memory.
+ * - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *   stream); a call returns as soon as its kernels are launched.
+ * - The KV cache layout is ND: [num_blocks, block_size, num_kv_heads,
+ *   head_dim] ([ATB] section 4.1; [SKILL] 3.1).  block_table is int32
+ *   [num_seqs, max_blocks_per_seq] ([SKILL] note 4); position p of sequence
+ *   s lives at slot block_table[s][p / block_size] * block_size +
+ *   p % block_size ([SKILL] 3.1 Mapping Formula).  Table entries past a
+ *   sequence's length are never read.
+ * - seq_lens[s] counts the cached tokens a decode attends to, INCLUDING the
+ *   token written this step ([SKILL] 3.6: FA reads kv_len + 1).
+ * - cu_seqlens has num_seqs + 1 entries with a leading 0 ([NOTES] 3.1
+ *   seq_offset).  The pages' TND actual_seq_lengths is cu_seqlens[1:].
+ * - q head h uses kv head h / (num_q_heads / num_kv_heads).
+ * - `scale` multiplies q.k before the softmax and has no default ([SKILL]
+ *   Appendix A warns that a silently defaulted scale of 1.0 corrupts results).
+ * - Outputs are rounded to the input dtype with round-to-nearest-even; the
+ *   softmax and all accumulation run in fp32.
+ * - A sequence with no visible key produces a row of zeros.
+ *
+ * Errors
+ * ------
+ * - Bad arguments are rejected on the host before anything is launched:
+ *   KVC_ERR_INVALID_ARG (null pointer, bad size, misalignment) or
+ *   KVC_ERR_UNSUPPORTED (a legal shape this build does not implement).
+ * - KVC_ERR_WORKSPACE: the workspace is smaller than the size query says.
+ * - KVC_ERR_CUDA: a launch failed (cudaGetLastError after launch).
+ * - Data errors found on the device never trap.  The kernel skips the bad
+ *   access and, if `err_flag` (a device uint32, may be NULL) is given, ORs
+ *   one of the KVC_FLAG_* bits into it.  The caller reads it after syncing.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; the library's functions only pass it to kernel launches. */
+struct CUstream_st;
+typedef struct CUstream_st* kvc_stream_t;
+
+typedef enum {
+  KVC_OK = 0,
+  KVC_ERR_INVALID_ARG = 1,
+  KVC_ERR_UNSUPPORTED = 2,
+  KVC_ERR_CUDA = 3,
+  KVC_ERR_WORKSPACE = 4
+} kvc_status;
+
+typedef enum { KVC_F16 = 0, KVC_BF16 = 1 } kvc_dtype;
+
+/* Bits a kernel ORs into *err_flag. */
+#define KVC_FLAG_BLOCK_ID_RANGE 0x1u /* block_table entry outside [0, num_blocks)        */
+#define KVC_FLAG_SLOT_RANGE     0x2u /* slot >= num_blocks * block_size                   */
+#define KVC_FLAG_LEN_RANGE      0x4u /* length < 0 or beyond max_blocks_per_seq*block_size */
+#define KVC_FLAG_WAIT_TIMEOUT   0x8u /* a bounded on-chip wait gave up (kernel returned)   */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* kvc_status_string(kvc_status status);
+
+/* Library ABI version (major * 100 + minor). */
+int kvc_version(void);
+
+/*
+ * kvc_build_slot_mapping -- slot of every token to be written.
+ * [SKILL] 3.1 Mapping Formula and 3.3 slot_mapping Construction; [NOTES] 2.2
+ * (logical block, slot, flat offset) and 3.3 (packed token -> request ->
+ * logical block -> physical block).
+ *
+ *   cu_seqlens == NULL (decode form): num_tokens == num_seqs; token s is the
+ *     new token of sequence s at position start_pos[s] (its current kv_len).
+ *   cu_seqlens != NULL (packed form): token t with cu_seqlens[s] <= t <
+ *     cu_seqlens[s+1] sits at position start_pos[s] + (t - cu_seqlens[s]).
+ *   slot_mapping[t] = block_table[s][p / block_size] * block_size
+ *                     + p % block_size                                (int32)
+ *
+ * block_table: int32 [num_seqs, max_blocks_per_seq]; cu_seqlens: int32
+ * [num_seqs + 1] or NULL; start_pos: int32 [num_seqs]; slot_mapping: int32
+ * [num_tokens] (output).  A position past the table or a table entry outside
+ * [0, num_blocks) yields slot -1 (skipped by the write) and sets
+ * KVC_FLAG_LEN_RANGE / KVC_FLAG_BLOCK_ID_RANGE.
+ */
+kvc_status kvc_build_slot_mapping(const int32_t* block_table, int max_blocks_per_seq,
+                                  const int32_t* cu_seqlens, const int32_t* start_pos,
+                                  int num_seqs, int num_tokens, int block_size, int num_blocks,
+                                  int32_t* slot_mapping, uint32_t* err_flag,
+                                  kvc_stream_t stream);
+
+/*
+ * kvc_reshape_and_cache -- copy new K/V rows into the paged cache.
+ * [ATB] section 4.2 (the KVCache operator copies each request's new rows into
+ * the cache unchanged); [SKILL] 3.3 (slot_mapping drives cache writes).
+ *
+ *   key_cache[slot / block_size][slot % block_size][:][:] = key[t][:][:]
+ *   value_cache[...]                                      = value[t][:][:]
+ *
+ * key: [num_tokens, num_kv_heads, head_dim_k]; value: [num_tokens,
+ * num_kv_heads, head_dim_v] or NULL (then value_cache must be NULL too);
+ * caches: [num_blocks, block_size, num_kv_heads, head_dim_*].  The copy is
+ * bit-exact.  slot_mapping[t] < 0 skips token t; a slot >= num_blocks *
+ * block_size is skipped and sets KVC_FLAG_SLOT_RANGE.  Duplicate slots in one
+ * call leave the cache row unspecified.  head_dim_k and head_dim_v must be
+ * multiples of 8 (16-byte rows); for MLA pass cache_nope as key and
+ * cache_rope as value (head_dim_k = 512, head_dim_v = 64, num_kv_heads = 1).
+ */
+kvc_status kvc_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                 void* value_cache, const int32_t* slot_mapping, int num_tokens,
+                                 int num_kv_heads, int head_dim_k, int head_dim_v,
+                                 int block_size, int num_blocks, kvc_dtype dtype,
+                                 uint32_t* err_flag, kvc_stream_t stream);
+
+/*
+ * Bytes of workspace kvc_paged_decode needs for this head shape when it runs
+ * with `num_ctas` persistent CTAs (0 = the automatic choice for the current
+ * device: SM count x resident CTAs per SM).  Independent of batch and lengths.
+ */
+size_t kvc_paged_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
+                                       int num_ctas);
+
+/*
+ * kvc_paged_decode -- one query token per sequence against the paged cache.
+ * [SKILL] Mode 2 (FA with block_table, block_size, actual_seq_kvlen,
+ * num_query_heads / num_key_value_heads) with sparse_mode 0 (no mask,
+ * Appendix C); [NOTES] 4.2 (the kernel walks the physical blocks of its
+ * sequence).
+ *
+ *   out[b][h][:] = sum_{j < seq_lens[b]} softmax_j(scale * q[b][h] . K_b[j][g])
+ *                  V_b[j][g],   g = h / (num_q_heads / num_kv_heads),
+ *   K_b[j] = key_cache[block_table[b][j / block_size]][j % block_size].
+ *
+ * q, out: [batch, num_q_heads, head_dim]; caches: [num_blocks, block_size,
+ * num_kv_heads, head_dim]; block_table: int32 [batch, max_blocks_per_seq];
+ * seq_lens: int32 [batch].
+ * Supported: head_dim 64 or 128; num_q_heads / num_kv_heads <= 16; block_size
+ * a power of two >= 8; batch <= 1024.
+ * Long sequences are split across CTAs (split-KV); the partial softmax states
+ * go to `workspace` (device, >= kvc_paged_decode_workspace_size bytes, no
+ * initialisation needed) and a second kernel merges them.  num_ctas = 0 picks
+ * the device's resident capacity; any positive value is valid (tests use it
+ * to force 1..many splits).  Results do not depend on the physical block IDs
+ * and are bitwise reproducible for a fixed num_ctas.
+ */
+kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* value_cache,
+                            const int32_t* block_table, const int32_t* seq_lens, void* out,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                            kvc_dtype dtype, int num_ctas, void* workspace,
+                            size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

@@ -1,0 +1,174 @@
+"""Python binding of the kvc CUDA library (GB300, sm_103a).
+
+Argument marshalling only: every step of the hot path runs in the CUDA
+kernels behind the C ABI declared in ``include/kvc.h``.  Tensors must be
+contiguous CUDA tensors; work is enqueued on torch's current CUDA stream.
+There is no CPU fallback: if ``_build/libkvc.so`` is missing, every call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libkvc.so")
+
+KVC_OK, KVC_ERR_INVALID_ARG, KVC_ERR_UNSUPPORTED, KVC_ERR_CUDA, KVC_ERR_WORKSPACE = range(5)
+KVC_F16, KVC_BF16 = 0, 1
+FLAG_BLOCK_ID_RANGE, FLAG_SLOT_RANGE, FLAG_LEN_RANGE, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
+
+_DT = {torch.float16: KVC_F16, torch.bfloat16: KVC_BF16}
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "kvc_status_string": (ctypes.c_char_p, [_I]),
+    "kvc_version": (_I, []),
+    "kvc_build_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "kvc_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "kvc_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
+    "kvc_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                              _P, _S, _P, _P]),
+}
+
+
+class KvcError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        name = lib().kvc_status_string(status).decode()
+        super().__init__(f"{fn} failed: {name}")
+
+
+def build(force: bool = False) -> str:
+    """Compile libkvc.so in-tree (nvcc, sm_103a)."""
+    from . import builder
+    return builder.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"kvc CUDA library not built ({LIB_PATH} missing); "
+                               "run paged_kv_cache_135_gb300.build() first")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _cuda(name, t, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _check(fn, status):
+    if status != KVC_OK:
+        raise KvcError(fn, status)
+
+
+def _flag(err_flag):
+    if err_flag is None:
+        return None
+    _cuda("err_flag", err_flag, torch.int32)
+    return err_flag.data_ptr()
+
+
+def build_slot_mapping(block_table: torch.Tensor, block_size: int, start_pos: torch.Tensor,
+                       num_blocks: int, cu_seqlens: Optional[torch.Tensor] = None,
+                       num_tokens: Optional[int] = None, out: Optional[torch.Tensor] = None,
+                       err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """int32 slot of every token to be written (decode form if cu_seqlens is None)."""
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("start_pos", start_pos, torch.int32)
+    S = start_pos.numel()
+    if cu_seqlens is not None:
+        _cuda("cu_seqlens", cu_seqlens, torch.int32)
+        if num_tokens is None:
+            raise ValueError("num_tokens is required with cu_seqlens")
+        T = int(num_tokens)
+    else:
+        T = S
+    if out is None:
+        out = torch.empty(T, dtype=torch.int32, device=block_table.device)
+    _cuda("out", out, torch.int32)
+    _check("kvc_build_slot_mapping", lib().kvc_build_slot_mapping(
+        block_table.data_ptr(), block_table.shape[1], _ptr(cu_seqlens), start_pos.data_ptr(), S,
+        T, block_size, num_blocks, out.data_ptr(), _flag(err_flag), _stream()))
+    return out
+
+
+def reshape_and_cache(key: torch.Tensor, value: Optional[torch.Tensor], key_cache: torch.Tensor,
+                      value_cache: Optional[torch.Tensor], slot_mapping: torch.Tensor,
+                      err_flag: Optional[torch.Tensor] = None) -> None:
+    """Copy key[t] (and value[t]) into the paged caches at slot_mapping[t]."""
+    _cuda("key", key)
+    _cuda("key_cache", key_cache, key.dtype)
+    _cuda("slot_mapping", slot_mapping, torch.int32)
+    dv = 0
+    if value is not None:
+        _cuda("value", value, key.dtype)
+        _cuda("value_cache", value_cache, key.dtype)
+        dv = value.shape[-1]
+    NB, bs, H, dk = key_cache.shape
+    _check("kvc_reshape_and_cache", lib().kvc_reshape_and_cache(
+        key.data_ptr(), _ptr(value), key_cache.data_ptr(), _ptr(value_cache),
+        slot_mapping.data_ptr(), key.shape[0], H, dk, dv, bs, NB, _DT[key.dtype],
+        _flag(err_flag), _stream()))
+
+
+def decode_workspace_size(num_q_heads: int, num_kv_heads: int, head_dim: int,
+                          num_ctas: int = 0) -> int:
+    return int(lib().kvc_paged_decode_workspace_size(num_q_heads, num_kv_heads, head_dim,
+                                                     num_ctas))
+
+
+def paged_decode(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                 block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                 out: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                 workspace: Optional[torch.Tensor] = None,
+                 err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode attention of q [B, Hq, D] over the paged caches [NB, bs, Hkv, D]."""
+    _cuda("q", q)
+    _cuda("key_cache", key_cache, q.dtype)
+    _cuda("value_cache", value_cache, q.dtype)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("seq_lens", seq_lens, torch.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, q.dtype)
+    if workspace is None:
+        n = decode_workspace_size(Hq, Hkv, D, num_ctas)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    _cuda("workspace", workspace)
+    _check("kvc_paged_decode", lib().kvc_paged_decode(
+        q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(), block_table.data_ptr(),
+        seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, D, bs, block_table.shape[1], NB,
+        float(scale), _DT[q.dtype], num_ctas, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _flag(err_flag), _stream()))
+    return out

@@ -1,0 +1,193 @@
+// The library's C ABI (include/kvc.h): host-side validation, then launches.
+// Every check here runs before anything is enqueued, so a rejected call has
+// no effect on the device.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <mutex>
+
+#include "../../include/kvc.h"
+#include "kvc_host.h"
+
+namespace kvc {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int& c = cached[dev & 63];
+  if (c == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    c = n;
+  }
+  return c;
+}
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool encode_tmap_16bit(CUtensorMap* map, kvc_dtype dtype, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  const CUresult r = fn(map,
+                        dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace kvc
+
+using kvc::aligned16;
+using kvc::is_pow2;
+
+extern "C" {
+
+const char* kvc_status_string(kvc_status s) {
+  switch (s) {
+    case KVC_OK: return "KVC_OK";
+    case KVC_ERR_INVALID_ARG: return "KVC_ERR_INVALID_ARG";
+    case KVC_ERR_UNSUPPORTED: return "KVC_ERR_UNSUPPORTED";
+    case KVC_ERR_CUDA: return "KVC_ERR_CUDA";
+    case KVC_ERR_WORKSPACE: return "KVC_ERR_WORKSPACE";
+  }
+  return "KVC_UNKNOWN_STATUS";
+}
+
+int kvc_version(void) { return 100; }
+
+kvc_status kvc_build_slot_mapping(const int32_t* block_table, int max_blocks_per_seq,
+                                  const int32_t* cu_seqlens, const int32_t* start_pos,
+                                  int num_seqs, int num_tokens, int block_size, int num_blocks,
+                                  int32_t* slot_mapping, uint32_t* err_flag,
+                                  kvc_stream_t stream) {
+  if (num_seqs < 0 || num_tokens < 0 || block_size <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0)
+    return KVC_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return KVC_OK;
+  if (num_seqs == 0 || !block_table || !start_pos || !slot_mapping) return KVC_ERR_INVALID_ARG;
+  if (!cu_seqlens && num_tokens != num_seqs) return KVC_ERR_INVALID_ARG;
+  return kvc::launch_slot_mapping(block_table, max_blocks_per_seq, cu_seqlens, start_pos,
+                                  num_seqs, num_tokens, block_size, num_blocks, slot_mapping,
+                                  err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                 void* value_cache, const int32_t* slot_mapping, int num_tokens,
+                                 int num_kv_heads, int head_dim_k, int head_dim_v,
+                                 int block_size, int num_blocks, kvc_dtype dtype,
+                                 uint32_t* err_flag, kvc_stream_t stream) {
+  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim_k <= 0 || block_size <= 0 ||
+      num_blocks <= 0)
+    return KVC_ERR_INVALID_ARG;
+  if ((value == nullptr) != (value_cache == nullptr)) return KVC_ERR_INVALID_ARG;
+  if (value && head_dim_v <= 0) return KVC_ERR_INVALID_ARG;
+  if (head_dim_k % 8 || (value && head_dim_v % 8)) return KVC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return KVC_OK;
+  if (!key || !key_cache || !slot_mapping) return KVC_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(key_cache) || (value && (!aligned16(value) ||
+                                                             !aligned16(value_cache))))
+    return KVC_ERR_INVALID_ARG;
+  return kvc::launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
+                                       num_tokens, num_kv_heads, head_dim_k, head_dim_v,
+                                       block_size, num_blocks, err_flag,
+                                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kvc_paged_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
+                                       int num_ctas) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+  const int group = num_q_heads / num_kv_heads;
+  if (group > 16 || (head_dim != 64 && head_dim != 128)) return 0;
+  // Enough for either dtype: the automatic CTA count may differ between them.
+  const int c16 = kvc::paged_decode_num_ctas(group, head_dim, KVC_F16, num_ctas);
+  const int cbf = kvc::paged_decode_num_ctas(group, head_dim, KVC_BF16, num_ctas);
+  return kvc::paged_decode_workspace_bytes(group, head_dim, c16 > cbf ? c16 : cbf);
+}
+
+kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* value_cache,
+                            const int32_t* block_table, const int32_t* seq_lens, void* out,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                            kvc_dtype dtype, int num_ctas, void* workspace,
+                            size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream) {
+  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0 || num_blocks <= 0 || num_ctas < 0)
+    return KVC_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return KVC_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return KVC_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > 16) return KVC_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (!is_pow2(block_size) || block_size < 8) return KVC_ERR_UNSUPPORTED;
+  if (batch > 1024) return KVC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+    return KVC_ERR_UNSUPPORTED;
+  if (batch == 0) return KVC_OK;
+  if (!q || !key_cache || !value_cache || !block_table || !seq_lens || !out)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache))
+    return KVC_ERR_INVALID_ARG;
+  kvc::DecodeArgs a;
+  a.q = q;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.num_ctas = num_ctas;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err_flag = err_flag;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return kvc::launch_paged_decode(a);
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Host-side internals of the kvc library: argument checks, device queries,
+// TMA descriptor encoding and the per-kernel launchers the C ABI calls.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+inline int ilog2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+
+// SM count of the current device (cached per device ordinal).
+int device_sm_count();
+
+// Encode a tiled TMA descriptor over a 16-bit tensor of rank `rank`.
+// dims/strides follow cuTensorMapEncodeTiled (dims innermost first, strides
+// in bytes for dims 1..rank-1).  Returns false if the driver rejects it.
+bool encode_tmap_16bit(CUtensorMap* map, kvc_dtype dtype, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes,
+                       const uint32_t* box, bool swizzle128);
+
+kvc_status launch_slot_mapping(const int32_t* block_table, int max_blocks_per_seq,
+                               const int32_t* cu_seqlens, const int32_t* start_pos, int num_seqs,
+                               int num_tokens, int block_size, int num_blocks,
+                               int32_t* slot_mapping, uint32_t* err_flag, cudaStream_t stream);
+
+kvc_status launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                    void* value_cache, const int32_t* slot_mapping,
+                                    int num_tokens, int num_kv_heads, int head_dim_k,
+                                    int head_dim_v, int block_size, int num_blocks,
+                                    uint32_t* err_flag, cudaStream_t stream);
+
+struct DecodeArgs {
+  const void* q;
+  const void* key_cache;
+  const void* value_cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  void* out;
+  int batch, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks;
+  float scale;
+  kvc_dtype dtype;
+  int num_ctas;
+  void* workspace;
+  size_t workspace_bytes;
+  uint32_t* err_flag;
+  cudaStream_t stream;
+};
+
+// Persistent CTAs the decode kernel would use for this shape (num_ctas <= 0
+// means "auto").  Returns 0 for an unsupported shape.
+int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas);
+size_t paged_decode_workspace_bytes(int group, int head_dim, int ctas);
+kvc_status launch_paged_decode(const DecodeArgs& a);
+
+}  // namespace kvc

@@ -26,3 +26,16 @@ def golden():
             key, val = (x.strip() for x in line.split("=", 1))
             vals[key] = eval(val, {"__builtins__": {}}, {"range": range, "list": list})  # literals only
     return vals
+
+
+@pytest.fixture(scope="session")
+def kvc_lib():
+    """Build (if needed) and load the CUDA library; GPU tests fail loudly without it."""
+    import torch
+
+    import paged_kv_cache_135_gb300 as kvc
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test selected but no CUDA device is visible")
+    kvc.build()
+    kvc.lib()
+    return kvc
