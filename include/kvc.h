@@ -158,8 +158,13 @@ size_t kvc_paged_decode_workspace_size(int num_q_heads, int num_kv_heads, int he
  * Supported: head_dim 64 or 128; num_q_heads / num_kv_heads <= 16; block_size
  * a power of two >= 8; batch <= 1024.
  * Long sequences are split across CTAs (split-KV); the partial softmax states
- * go to `workspace` (device, >= kvc_paged_decode_workspace_size bytes, no
- * initialisation needed) and a second kernel merges them.  num_ctas = 0 picks
+ * go to `workspace` (device, >= kvc_paged_decode_workspace_size bytes) and
+ * the CTA that finishes a split sequence last merges them, inside the same
+ * kernel.  The workspace must be zero-filled before its first use (for
+ * example cudaMemsetAsync); every call leaves it zero-filled again, so it can
+ * be reused without clearing.  After a call that raised
+ * KVC_FLAG_WAIT_TIMEOUT, zero it again.  Calls that overlap on the GPU must
+ * not share a workspace.  num_ctas = 0 picks
  * the device's resident capacity; any positive value is valid (tests use it
  * to force 1..many splits).  Results do not depend on the physical block IDs
  * and are bitwise reproducible for a fixed num_ctas.

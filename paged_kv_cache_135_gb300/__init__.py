@@ -151,7 +151,11 @@ def paged_decode(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Te
                  out: Optional[torch.Tensor] = None, num_ctas: int = 0,
                  workspace: Optional[torch.Tensor] = None,
                  err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Decode attention of q [B, Hq, D] over the paged caches [NB, bs, Hkv, D]."""
+    """Decode attention of q [B, Hq, D] over the paged caches [NB, bs, Hkv, D].
+
+    ``workspace`` (uint8, >= decode_workspace_size bytes) must be zero-filled
+    before its first use; each call leaves it zero-filled.
+    """
     _cuda("q", q)
     _cuda("key_cache", key_cache, q.dtype)
     _cuda("value_cache", value_cache, q.dtype)
@@ -164,7 +168,7 @@ def paged_decode(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Te
     _cuda("out", out, q.dtype)
     if workspace is None:
         n = decode_workspace_size(Hq, Hkv, D, num_ctas)
-        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=q.device)
     _cuda("workspace", workspace)
     _check("kvc_paged_decode", lib().kvc_paged_decode(
         q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(), block_table.data_ptr(),

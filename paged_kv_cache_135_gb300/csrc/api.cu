@@ -164,7 +164,8 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
   if (batch == 0) return KVC_OK;
   if (!q || !key_cache || !value_cache || !block_table || !seq_lens || !out)
     return KVC_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache))
+  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      !aligned16(workspace))
     return KVC_ERR_INVALID_ARG;
   kvc::DecodeArgs a;
   a.q = q;

@@ -15,8 +15,9 @@
 //    ("stream-K" split-KV), so every SM streams the same number of bytes
 //    whatever the length mix.  A segment cut by a share boundary leaves
 //    per-CTA partial softmax states (m, l, unnormalised O) in the workspace;
-//    a second kernel merges them in a fixed order (deterministic, and
-//    independent of physical block IDs).
+//    the CTA that finishes its share last (an atomic arrival counter per
+//    split segment) merges them in a fixed order -- no second kernel, no
+//    spin-wait, deterministic and independent of physical block IDs.
 //  * One producer warp gathers tiles with TMA: per tile and per K/V half
 //    (64 head-dim elements = 128 B rows) one 4-D box {64, 1, min(bs,64), 1}
 //    per physical block at coordinate (d0, g, token-in-block, block id), into
@@ -52,12 +53,14 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 3;
 constexpr int kMaxBatch = 1024;
 constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a K or V tile
+constexpr int kMaxPieces = 62;           // split shares merged from a shared-memory list
 
 struct DecodeParams {
   const void* q;
   void* out;
   const int32_t* block_table;
   const int32_t* seq_lens;
+  int* ws_cnt;   // [P][2] arrival counters of split segments (zero between calls)
   float* ws_o;   // [P][2][G][D] unnormalised partial outputs
   float* ws_ml;  // [P][2][G][2] partial (max, sum) in the log2 domain
   uint32_t* err_flag;
@@ -66,24 +69,42 @@ struct DecodeParams {
   float scale_log2;
 };
 
+__host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// Dynamic shared memory of the decode kernel.  A stage holds the K tile, the
+// V tile and the query rows of the tile's (b, g) (all 128-byte swizzled, each
+// 1024-byte aligned as the TMA swizzle requires); every other region starts
+// on a 16-byte boundary.
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
   static constexpr int kKBytes = kHalves * kHalfBytes;
-  static constexpr int kStageBytes = 2 * kKBytes;  // K tile then V tile
-  static constexpr int kBarOff = kStages * kStageBytes;
-  static constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
-  static constexpr int kLensOff = kBarOff + 128;
-  // lens[batch], cum[batch + 1], then the cross-warp combine buffers.
-  __host__ __device__ static int cum_off(int batch) { return kLensOff + ((batch + 3) & ~3) * 4; }
-  __host__ __device__ static int cmb_off(int batch) {
-    return cum_off(batch) + ((batch + 1 + 3) & ~3) * 4;
-  }
-  static size_t bytes(int batch, int group) {
-    return 1024 /*alignment slack*/ + cmb_off(batch) +
-           static_cast<size_t>(kConsumerWarps) * group * (D + 2) * 4;
+  int q_half;   // bytes of one 64-wide half of the G query rows (1024-aligned)
+  int stage;    // K tile, V tile, query rows
+  int bar;      // full[kStages], empty[kStages]
+  int flags;    // abort, last, npieces
+  int pieces;   // int[kMaxPieces]
+  int lens;     // int[batch]
+  int cum;      // int[batch + 1]
+  int cmb;      // cross-warp combine: m[4G], l[4G], o[4G][D]
+  int total;    // bytes to request (with 1024 bytes of alignment slack)
+  __host__ __device__ Layout(int batch, int group) {
+    q_half = align_up(group * 128, 1024);
+    stage = 2 * kKBytes + kHalves * q_half;
+    bar = kStages * stage;
+    flags = bar + 2 * kStages * 8;
+    pieces = align_up(flags + 12, 16);
+    lens = align_up(pieces + kMaxPieces * 4, 16);
+    cum = align_up(lens + batch * 4, 16);
+    cmb = align_up(cum + (batch + 1) * 4, 16);
+    total = 1024 + cmb + kConsumerWarps * group * (D + 2) * 4;
   }
 };
+
+// Arrival counters at the head of the workspace, padded to 256 bytes.
+__host__ __device__ inline size_t counter_bytes(int ctas) {
+  return (static_cast<size_t>(ctas) * 2 * sizeof(int) + 255) & ~static_cast<size_t>(255);
+}
 
 __device__ __forceinline__ int clamp_len(int L, int cap, uint32_t* err_flag) {
   if (L < 0 || L > cap) {
@@ -129,34 +150,27 @@ struct Cursor {
   }
 };
 
-// Load the G query rows of (b, g) as mma A fragments (rows >= G are zero).
-template <typename T, int D>
-__device__ __forceinline__ void load_q(const T* __restrict__ q, const DecodeParams& p, int b,
-                                       int g, int lane, uint32_t (&qa)[D / 16][4]) {
-  const T* base = q + (static_cast<long long>(b) * p.num_q_heads + g * p.group) * D;
-  const int r0 = lane >> 2, c = 2 * (lane & 3);
-  const bool v0 = r0 < p.group, v1 = r0 + 8 < p.group;
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const int col = kk * 16 + c;
-    qa[kk][0] = v0 ? *reinterpret_cast<const uint32_t*>(base + r0 * D + col) : 0u;
-    qa[kk][1] = v1 ? *reinterpret_cast<const uint32_t*>(base + (r0 + 8) * D + col) : 0u;
-    qa[kk][2] = v0 ? *reinterpret_cast<const uint32_t*>(base + r0 * D + col + 8) : 0u;
-    qa[kk][3] = v1 ? *reinterpret_cast<const uint32_t*>(base + (r0 + 8) * D + col + 8) : 0u;
-  }
-}
-
 __device__ __forceinline__ uint32_t keep_rows(uint32_t x, int k, int valid) {
   const uint32_t lo = k < valid ? 0x0000FFFFu : 0u;
   const uint32_t hi = k + 1 < valid ? 0xFFFF0000u : 0u;
   return x & (lo | hi);
 }
 
+// out[0..3] = v * inv, rounded to T (one 8-byte store).
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float4 v, float inv) {
+  float a, b;
+  uint2 w;
+  w.x = Pack<T>::run(v.x * inv, v.y * inv, a, b);
+  w.y = Pack<T>::run(v.z * inv, v.w * inv, a, b);
+  *reinterpret_cast<uint2*>(dst) = w;
+}
+
 // One warp's 16 tokens of a stage: S = Q K^T, online softmax, O += P V.
 template <typename T, int D>
 __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int warp, int lane,
-                                          int valid, float scale_log2,
-                                          const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4],
+                                          int valid, float scale_log2, uint32_t qbase,
+                                          int q_half, int group, float (&o)[D / 8][4],
                                           float (&m)[2], float (&l)[2]) {
   const int mi = lane >> 3, rr = lane & 7;
   float s[2][4];
@@ -166,13 +180,17 @@ __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int wa
     for (int e = 0; e < 4; ++e) s[i][e] = 0.f;
   {
     const int tok = warp * 16 + (mi >> 1) * 8 + rr;
+    // Query rows >= G are padding: they read row 0 and their results are dropped.
+    const int qr = (mi & 1) * 8 + rr < group ? (mi & 1) * 8 + rr : 0;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int dcol = kk * 16 + (mi & 1) * 8;
-      uint32_t b0, b1, b2, b3;
+      uint32_t a[4], b0, b1, b2, b3;
+      ldsm_x4(qbase + (kk >> 2) * q_half + swz128(qr, (kk & 3) * 2 + (mi >> 1)), a[0], a[1],
+              a[2], a[3]);
       ldsm_x4(kbase + (dcol >> 6) * kHalfBytes + swz128(tok, (dcol & 63) >> 3), b0, b1, b2, b3);
-      MmaOp<T>::run(s[0], qa[kk], b0, b1);
-      MmaOp<T>::run(s[1], qa[kk], b2, b3);
+      MmaOp<T>::run(s[0], a, b0, b1);
+      MmaOp<T>::run(s[1], a, b2, b3);
     }
   }
   const int c0 = 2 * (lane & 3);
@@ -229,20 +247,138 @@ __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int wa
   }
 }
 
+// The end of one segment share (cold path, kept out of line to spare the
+// main loop's registers): merge the four consumer warps' states held in
+// shared memory, then write the output (whole segment) or publish a partial
+// state; for a split segment the last-arriving CTA merges all partials.
+// Each thread handles four consecutive head-dim elements of one query row.
+template <typename T, int D>
+__device__ __noinline__ void finish_share(const DecodeParams& p, const float* cmb_m,
+                                          const float* cmb_l, float* cmb_o,
+                                          volatile int* last_flag, volatile int* npieces,
+                                          int* pieces, int ctid, int b, int g,
+                                          bool complete, int c, int slot, long long seg0,
+                                          int seg_tiles, long long N, int P) {
+  constexpr int kQuads = D / 4;
+  const int G = p.group;
+  T* out = static_cast<T*>(p.out);
+  const long long row0 = static_cast<long long>(b) * p.num_q_heads + g * G;
+  for (int e4 = ctid; e4 < G * kQuads; e4 += kConsumerWarps * 32) {
+    const int r = e4 / kQuads, d = (e4 - r * kQuads) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cmb_m[w * G + r]);
+    float Ls = 0.f;
+    float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = cmb_m[w * G + r];
+      const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+      Ls += f * cmb_l[w * G + r];
+      const float4 v = *reinterpret_cast<const float4*>(&cmb_o[(w * G + r) * D + d]);
+      Os.x += f * v.x; Os.y += f * v.y; Os.z += f * v.z; Os.w += f * v.w;
+    }
+    if (complete) {
+      store4<T>(out + (row0 + r) * D + d, Os, Ls > 0.f ? 1.f / Ls : 0.f);
+    } else {
+      const long long ws_row = (static_cast<long long>(c) * 2 + slot) * G + r;
+      *reinterpret_cast<float4*>(&p.ws_o[ws_row * D + d]) = Os;
+      if (d == 0) *reinterpret_cast<float2*>(&p.ws_ml[ws_row * 2]) = make_float2(M, Ls);
+    }
+  }
+  if (complete) return;
+
+  // Split segment: count arrivals with one acq_rel atomic per CTA (after a CTA
+  // barrier, so it releases every thread's partial writes); the CTA that
+  // arrives last merges all shares in ascending CTA order and resets the
+  // counter -- no second kernel and no waiting.
+  named_bar_sync(1, kConsumerWarps * 32);
+  const int cfirst = cta_of(seg0, N, P), clast = cta_of(seg0 + seg_tiles - 1, N, P);
+  const int slot0 = tile_begin(cfirst, N, P) == seg0 ? 0 : 1;
+  if (ctid == 0) {
+    // Workspace rows (cta * 2 + slot) of every non-empty share, in CTA order.
+    int n = 0;
+    long long tb = tile_begin(cfirst, N, P);
+    for (int cc = cfirst; cc <= clast; ++cc) {
+      const long long te = tile_begin(cc + 1, N, P);
+      if (tb < te) {
+        if (n < kMaxPieces) pieces[n] = cc * 2 + (cc == cfirst ? slot0 : 0);
+        ++n;
+      }
+      tb = te;
+    }
+    *npieces = n;
+    *last_flag = atomic_add_acq_rel(&p.ws_cnt[cfirst * 2 + slot0], 1) == n - 1 ? 1 : 0;
+  }
+  named_bar_sync(1, kConsumerWarps * 32);
+  if (!*last_flag) return;
+  const int n = *npieces;
+  if (n <= kMaxPieces) {
+    // (m, l) of every share and row, loaded in parallel into the (now free)
+    // combine buffer, then one float4 of each share per thread.
+    float2* ml = reinterpret_cast<float2*>(cmb_o);
+    for (int i = ctid; i < n * G; i += kConsumerWarps * 32)
+      ml[i] = __ldcg(reinterpret_cast<const float2*>(
+          &p.ws_ml[(static_cast<long long>(pieces[i / G]) * G + i % G) * 2]));
+    named_bar_sync(1, kConsumerWarps * 32);
+    for (int e4 = ctid; e4 < G * kQuads; e4 += kConsumerWarps * 32) {
+      const int r = e4 / kQuads, d = (e4 - r * kQuads) * 4;
+      float M = -INFINITY;
+      for (int i = 0; i < n; ++i) M = fmaxf(M, ml[i * G + r].x);
+      float Ls = 0.f;
+      float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int i = 0; i < n; ++i) {
+        const float f = fast_exp2(ml[i * G + r].x - M);
+        Ls += f * ml[i * G + r].y;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(
+            &p.ws_o[(static_cast<long long>(pieces[i]) * G + r) * D + d]));
+        Os.x += f * v.x; Os.y += f * v.y; Os.z += f * v.z; Os.w += f * v.w;
+      }
+      store4<T>(out + (row0 + r) * D + d, Os, Ls > 0.f ? 1.f / Ls : 0.f);
+    }
+  } else {
+    // Very many CTAs per segment (num_ctas far above the tile count).
+    for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
+      const int r = e / D, d = e - r * D;
+      float M = -INFINITY, Ls = 0.f, Os = 0.f;
+      for (int cc = cfirst; cc <= clast; ++cc) {
+        if (tile_begin(cc, N, P) == tile_begin(cc + 1, N, P)) continue;
+        const long long row = (static_cast<long long>(cc) * 2 + (cc == cfirst ? slot0 : 0)) * G + r;
+        M = fmaxf(M, __ldcg(&p.ws_ml[row * 2]));
+      }
+      for (int cc = cfirst; cc <= clast; ++cc) {
+        if (tile_begin(cc, N, P) == tile_begin(cc + 1, N, P)) continue;
+        const long long row = (static_cast<long long>(cc) * 2 + (cc == cfirst ? slot0 : 0)) * G + r;
+        const float f = fast_exp2(__ldcg(&p.ws_ml[row * 2]) - M);
+        Ls += f * __ldcg(&p.ws_ml[row * 2 + 1]);
+        Os += f * __ldcg(&p.ws_o[row * D + d]);
+      }
+      out[(row0 + r) * D + d] = Pack<T>::cvt(Ls > 0.f ? Os / Ls : 0.f);
+    }
+  }
+  if (ctid == 0) p.ws_cnt[cfirst * 2 + slot0] = 0;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-  using L = Layout<D>;
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ DecodeParams p) {
+  constexpr int kHalves = Layout<D>::kHalves;
+  constexpr int kKBytes = Layout<D>::kKBytes;
+  const Layout<D> L(p.batch, p.group);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar);
   uint64_t* empty = full + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbortOff);
-  int* lens = reinterpret_cast<int*>(smem + L::kLensOff);
-  int* cum = reinterpret_cast<int*>(smem + L::cum_off(p.batch));
-  float* cmb_m = reinterpret_cast<float*>(smem + L::cmb_off(p.batch));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
+  volatile int* last_flag = abort_flag + 1;
+  int* lens = reinterpret_cast<int*>(smem + L.lens);
+  int* cum = reinterpret_cast<int*>(smem + L.cum);
+  float* cmb_m = reinterpret_cast<float*>(smem + L.cmb);
   float* cmb_l = cmb_m + kConsumerWarps * p.group;
   float* cmb_o = cmb_l + kConsumerWarps * p.group;
 
@@ -261,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == kConsumerWarps && lane == 0) {
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_q);
   }
   // Plan: clamped lengths and the prefix sum of 64-token tiles per sequence.
   for (int i = tid; i < B; i += kThreads) lens[i] = clamp_len(p.seq_lens[i], cap, p.err_flag);
@@ -285,6 +422,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const long long N = static_cast<long long>(hkv) * cum[B];
   const int P = gridDim.x, c = blockIdx.x;
+  // Sequences with no cached token get a row of zeros (CTA b % P writes them).
+  {
+    T* out = static_cast<T*>(p.out);
+    const int row_elems = p.num_q_heads * D;
+    for (int b = c; b < B; b += P)
+      if (lens[b] == 0)
+        for (int e = tid; e < row_elems; e += kThreads)
+          out[static_cast<long long>(b) * row_elems + e] = Pack<T>::cvt(0.f);
+  }
   const long long t_begin = tile_begin(c, N, P), t_end = tile_begin(c + 1, N, P);
   if (t_begin >= t_end) return;
 
@@ -294,33 +440,45 @@ __global__ void __launch_bounds__(kThreads, 2)
     cur.locate(t_begin, cum, B, hkv);
     const int nsub = kTile / p.box_tokens;
     const uint32_t box_bytes = static_cast<uint32_t>(p.box_tokens) * 128u;
+    const uint32_t q_bytes = static_cast<uint32_t>(G) * 128u * kHalves;
     int it = 0;
     for (long long t = t_begin; t < t_end; ++t, ++it) {
       const int stage = it % kStages;
       const uint32_t phase = (it / kStages) & 1;
+      // Look up this tile's physical blocks first: the table load's latency
+      // overlaps the wait for a free stage.
+      const int Lb = lens[cur.b];
+      const int tok = cur.j * kTile + lane * p.box_tokens;
+      int pb = -1;
+      if (lane < nsub && tok < Lb)
+        pb = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks +
+                                  (tok >> p.log2_bs)]);
       bool ok = !*abort_flag && mbar_wait_bounded(&empty[stage], phase ^ 1, p.err_flag);
       if (!ok) {
         *abort_flag = 1;
       } else {
-        const int Lb = lens[cur.b];
-        const int tok = cur.j * kTile + lane * p.box_tokens;
         bool valid = false;
-        int pb = 0;
         if (lane < nsub && tok < Lb) {
-          pb = p.block_table[static_cast<long long>(cur.b) * p.max_blocks + (tok >> p.log2_bs)];
           if (pb < 0 || pb >= p.num_blocks) set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
           else valid = true;
         }
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], nvalid * box_bytes * L::kHalves * 2);
+        uint8_t* st = smem + stage * L.stage;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], nvalid * box_bytes * kHalves * 2 + q_bytes);
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h)
+            tma_load_3d(st + 2 * kKBytes + h * L.q_half, &tm_q, &full[stage], h * 64, cur.g * G,
+                        cur.b);
+        }
         __syncwarp();
         if (valid) {
-          uint8_t* kdst = smem + stage * L::kStageBytes + lane * box_bytes;
+          uint8_t* kdst = st + lane * box_bytes;
           const int in_blk = tok & (p.block_size - 1);
 #pragma unroll
-          for (int h = 0; h < L::kHalves; ++h) {
+          for (int h = 0; h < kHalves; ++h) {
             tma_load_4d(kdst + h * kHalfBytes, &tm_k, &full[stage], h * 64, cur.g, in_blk, pb);
-            tma_load_4d(kdst + L::kKBytes + h * kHalfBytes, &tm_v, &full[stage], h * 64, cur.g,
+            tma_load_4d(kdst + kKBytes + h * kHalfBytes, &tm_v, &full[stage], h * 64, cur.g,
                         in_blk, pb);
           }
         }
@@ -338,11 +496,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // -------------------------------------------------------------- consumers
-  const T* q = static_cast<const T*>(p.q);
-  T* out = static_cast<T*>(p.out);
   Cursor cur;
   cur.locate(t_begin, cum, B, hkv);
-  uint32_t qa[D / 16][4];
+  const int ctid = warp * 32 + lane;
   float o[D / 8][4], m[2], l[2];
   auto reset = [&]() {
 #pragma unroll
@@ -352,7 +508,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
   };
-  load_q<T, D>(q, p, cur.b, cur.g, lane, qa);
   reset();
   int seg_first_j = cur.j;
   int slot = 0;  // 0 for the first segment this CTA touches, 1 afterwards
@@ -365,8 +520,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!ok) *abort_flag = 1;
     const int valid = min(16, lens[cur.b] - cur.j * kTile - warp * 16);
     if (ok && valid > 0) {
-      const uint32_t kb = sbase + stage * L::kStageBytes;
-      attend_16<T, D>(kb, kb + L::kKBytes, warp, lane, valid, p.scale_log2, qa, o, m, l);
+      const uint32_t kb = sbase + stage * L.stage;
+      attend_16<T, D>(kb, kb + kKBytes, warp, lane, valid, p.scale_log2, kb + 2 * kKBytes,
+                      L.q_half, G, o, m, l);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -395,107 +551,20 @@ __global__ void __launch_bounds__(kThreads, 2)
               make_float2(o[n][2], o[n][3]);
       }
       named_bar_sync(1, kConsumerWarps * 32);
-      const int ctid = warp * 32 + lane;
-      const long long row0 = static_cast<long long>(cur.b) * p.num_q_heads + cur.g * G;
-      for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
-        const int r = e / D, d = e - r * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cmb_m[w * G + r]);
-        float Ls = 0.f, Os = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float mw = cmb_m[w * G + r];
-          const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-          Ls += f * cmb_l[w * G + r];
-          Os += f * cmb_o[(w * G + r) * D + d];
-        }
-        if (complete) {
-          out[(row0 + r) * D + d] = Pack<T>::cvt(Ls > 0.f ? Os / Ls : 0.f);
-        } else {
-          const long long ws_row = (static_cast<long long>(c) * 2 + slot) * G + r;
-          p.ws_o[ws_row * D + d] = Os;
-          if (d == 0) {
-            p.ws_ml[ws_row * 2] = M;
-            p.ws_ml[ws_row * 2 + 1] = Ls;
-          }
-        }
-      }
+      finish_share<T, D>(p, cmb_m, cmb_l, cmb_o, last_flag, abort_flag + 2,
+                         reinterpret_cast<int*>(smem + L.pieces), ctid, cur.b, cur.g,
+                         complete, c, slot,
+                         static_cast<long long>(hkv) * cum[cur.b] +
+                             static_cast<long long>(cur.g) * cur.n,
+                         cur.n, N, P);
       named_bar_sync(1, kConsumerWarps * 32);
       slot = 1;
       cur.advance(cum, B, hkv);
-      if (t + 1 < t_end) {
-        load_q<T, D>(q, p, cur.b, cur.g, lane, qa);
-        reset();
-        seg_first_j = cur.j;
-      }
+      reset();
+      seg_first_j = cur.j;
     } else {
       cur.advance(cum, B, hkv);
     }
-  }
-}
-
-// Merge the per-CTA partial states of segments that were split, write zeros
-// for empty sequences.  One CTA per (b, g).
-template <typename T>
-__global__ void __launch_bounds__(128)
-    paged_decode_merge_kernel(const DecodeParams p, int P) {
-  const int b = blockIdx.x / p.num_kv_heads, g = blockIdx.x - b * p.num_kv_heads;
-  const int G = p.group, D = p.head_dim;
-  const int cap = p.max_blocks * p.block_size;
-  __shared__ long long s_before, s_total;
-  __shared__ long long red[2][4];
-  long long before = 0, total = 0;
-  for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
-    int L = p.seq_lens[i];
-    L = L < 0 ? 0 : (L > cap ? cap : L);
-    const long long n = (L + kTile - 1) / kTile;
-    total += n;
-    if (i < b) before += n;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, off);
-    total += __shfl_xor_sync(0xffffffffu, total, off);
-  }
-  if ((threadIdx.x & 31) == 0) {
-    red[0][threadIdx.x >> 5] = before;
-    red[1][threadIdx.x >> 5] = total;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    s_before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-    s_total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  }
-  __syncthreads();
-  int Lb = p.seq_lens[b];
-  Lb = Lb < 0 ? 0 : (Lb > cap ? cap : Lb);
-  T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * p.num_q_heads + g * G) * D;
-  if (Lb == 0) {
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x) out[e] = Pack<T>::cvt(0.f);
-    return;
-  }
-  const long long nb = (Lb + kTile - 1) / kTile;
-  const long long N = static_cast<long long>(p.num_kv_heads) * s_total;
-  const long long seg0 = static_cast<long long>(p.num_kv_heads) * s_before + g * nb;
-  const int c0 = cta_of(seg0, N, P), c1 = cta_of(seg0 + nb - 1, N, P);
-  if (c0 == c1) return;  // written directly by the main kernel
-  const int slot0 = tile_begin(c0, N, P) == seg0 ? 0 : 1;
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-    const int r = e / D, d = e - r * D;
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) {
-      const long long row = (static_cast<long long>(c) * 2 + (c == c0 ? slot0 : 0)) * G + r;
-      M = fmaxf(M, p.ws_ml[row * 2]);
-    }
-    float Ls = 0.f, Os = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-      const long long row = (static_cast<long long>(c) * 2 + (c == c0 ? slot0 : 0)) * G + r;
-      const float f = fast_exp2(p.ws_ml[row * 2] - M);
-      Ls += f * p.ws_ml[row * 2 + 1];
-      Os += f * p.ws_o[row * D + d];
-    }
-    out[e] = Pack<T>::cvt(Ls > 0.f ? Os / Ls : 0.f);
   }
 }
 
@@ -512,7 +581,7 @@ struct DecodeKernel {
     auto it = cache.find({dev, smem});
     if (it != cache.end()) return it->second;
     cudaFuncSetAttribute(paged_decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(Layout<D>::bytes(kMaxBatch, 16)));
+                         Layout<D>(kMaxBatch, 16).total);
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<T, D>, kThreads,
                                                       smem) != cudaSuccess || occ < 1)
@@ -525,7 +594,7 @@ struct DecodeKernel {
 template <typename T, int D>
 kvc_status run_decode(const DecodeArgs& a) {
   const int G = a.num_q_heads / a.num_kv_heads;
-  const size_t smem = Layout<D>::bytes(a.batch, G);
+  const size_t smem = Layout<D>(a.batch, G).total;
   const int occ = DecodeKernel<T, D>::occupancy(smem);  // also sets the smem limit
   const int P = a.num_ctas > 0 ? a.num_ctas : device_sm_count() * occ;
   if (a.workspace_bytes < paged_decode_workspace_bytes(G, D, P) || a.workspace == nullptr)
@@ -540,8 +609,16 @@ kvc_status run_decode(const DecodeArgs& a) {
                                static_cast<uint64_t>(a.num_kv_heads) * D * 2,
                                static_cast<uint64_t>(a.block_size) * a.num_kv_heads * D * 2};
   const uint32_t box[4] = {64, 1, static_cast<uint32_t>(box_tokens), 1};
+  // Query [B, Hq, D]: one box = the G rows of a query group, 64 elements wide.
+  CUtensorMap tq;
+  const uint64_t qdims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_q_heads),
+                             static_cast<uint64_t>(a.batch)};
+  const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 2,
+                                static_cast<uint64_t>(a.num_q_heads) * D * 2};
+  const uint32_t qbox[3] = {64, static_cast<uint32_t>(G), 1};
   if (!encode_tmap_16bit(&tk, a.dtype, 4, a.key_cache, dims, strides, box, true) ||
-      !encode_tmap_16bit(&tv, a.dtype, 4, a.value_cache, dims, strides, box, true))
+      !encode_tmap_16bit(&tv, a.dtype, 4, a.value_cache, dims, strides, box, true) ||
+      !encode_tmap_16bit(&tq, a.dtype, 3, a.q, qdims, qstrides, qbox, true))
     return KVC_ERR_CUDA;
 
   DecodeParams p;
@@ -549,7 +626,8 @@ kvc_status run_decode(const DecodeArgs& a) {
   p.out = a.out;
   p.block_table = a.block_table;
   p.seq_lens = a.seq_lens;
-  p.ws_o = static_cast<float*>(a.workspace);
+  p.ws_cnt = static_cast<int*>(a.workspace);
+  p.ws_o = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + counter_bytes(P));
   p.ws_ml = p.ws_o + static_cast<size_t>(P) * 2 * G * D;
   p.err_flag = a.err_flag;
   p.batch = a.batch;
@@ -564,17 +642,14 @@ kvc_status run_decode(const DecodeArgs& a) {
   p.box_tokens = box_tokens;
   p.scale_log2 = a.scale * 1.4426950408889634f;
 
-  paged_decode_kernel<T, D><<<P, kThreads, smem, a.stream>>>(tk, tv, p);
-  if (cudaGetLastError() != cudaSuccess) return KVC_ERR_CUDA;
-  paged_decode_merge_kernel<T><<<a.batch * a.num_kv_heads, 128, 0, a.stream>>>(p, P);
-  if (cudaGetLastError() != cudaSuccess) return KVC_ERR_CUDA;
-  return KVC_OK;
+  paged_decode_kernel<T, D><<<P, kThreads, smem, a.stream>>>(tk, tv, tq, p);
+  return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
 }  // namespace
 
 size_t paged_decode_workspace_bytes(int group, int head_dim, int ctas) {
-  return static_cast<size_t>(ctas) * 2 * group * (head_dim + 2) * sizeof(float);
+  return counter_bytes(ctas) + static_cast<size_t>(ctas) * 2 * group * (head_dim + 2) * sizeof(float);
 }
 
 int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas) {
@@ -583,12 +658,12 @@ int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas
   if (sms <= 0) return 0;
   // The smallest batch needs the least shared memory, hence the most CTAs.
   if (head_dim == 64) {
-    const size_t smem = Layout<64>::bytes(1, group);
+    const size_t smem = Layout<64>(1, group).total;
     return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 64>::occupancy(smem)
                                     : DecodeKernel<__half, 64>::occupancy(smem));
   }
   if (head_dim == 128) {
-    const size_t smem = Layout<128>::bytes(1, group);
+    const size_t smem = Layout<128>(1, group).total;
     return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 128>::occupancy(smem)
                                     : DecodeKernel<__half, 128>::occupancy(smem));
   }

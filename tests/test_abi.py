@@ -100,4 +100,5 @@ def test_workspace_query_rejects_bad_shapes(lib):
     assert lib.kvc_paged_decode_workspace_size(6, 4, 128, 10) == 0
     assert lib.kvc_paged_decode_workspace_size(8, 2, 96, 10) == 0
     # explicit CTA count: no device query needed
-    assert lib.kvc_paged_decode_workspace_size(8, 2, 128, 10) == 10 * 2 * 4 * 130 * 4
+    # 10 CTAs: counters (padded to 256 B) + 2 shares x 4 rows x (128 + 2) floats each
+    assert lib.kvc_paged_decode_workspace_size(8, 2, 128, 10) == 256 + 10 * 2 * 4 * 130 * 4
