@@ -176,6 +176,41 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
                             kvc_dtype dtype, int num_ctas, void* workspace,
                             size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream);
 
+/*
+ * kvc_paged_decode_no_alloc -- kvc_paged_decode for callers that cannot
+ * allocate device memory.  The source pages have no counterpart to this entry
+ * point; it exists for callers such as a host application that gives this
+ * library a fixed memory budget and forbids later allocations, a serving loop
+ * that has already reserved the whole device for its KV-cache pool, or code
+ * that launches kernels from a thread where no device allocator is
+ * available.  They cannot provide the split-KV workspace kvc_paged_decode
+ * asks for.
+ *
+ * Arguments and results are those of kvc_paged_decode without `workspace` and
+ * `workspace_bytes`.  The scratch is a library-owned device array of
+ * KVC_NO_ALLOC_SCRATCH_BYTES (8 MiB) that every GPU which loads the library
+ * holds until the process exits; nothing is allocated or freed (no cudaMalloc,
+ * no cudaFree, no allocating library call).  If the shape needs more scratch
+ * than that (kvc_paged_decode_workspace_size(...) > 8 MiB: too many CTAs or
+ * too wide a query group), the call returns KVC_ERR_WORKSPACE and launches
+ * nothing.
+ *
+ * The first call on each device looks up the array's device address once
+ * (cudaGetSymbolAddress); make that first call before any stream capture on
+ * that device.  Each call first clears, on `stream`, the part of the array it
+ * uses (the array keeps the previous call's contents), then runs the decode.
+ * All calls on a device share the one array: calls that overlap on the GPU
+ * (for example on two streams) race, so the caller must serialise them.
+ */
+#define KVC_NO_ALLOC_SCRATCH_BYTES (8u << 20)
+kvc_status kvc_paged_decode_no_alloc(const void* q, const void* key_cache,
+                                     const void* value_cache, const int32_t* block_table,
+                                     const int32_t* seq_lens, void* out, int batch,
+                                     int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int max_blocks_per_seq, int num_blocks,
+                                     float scale, kvc_dtype dtype, int num_ctas,
+                                     uint32_t* err_flag, kvc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

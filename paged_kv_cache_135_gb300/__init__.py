@@ -176,3 +176,34 @@ def paged_decode(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Te
         float(scale), _DT[q.dtype], num_ctas, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _flag(err_flag), _stream()))
     return out
+
+
+def paged_decode_no_alloc(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                          block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                          out: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                          err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """paged_decode without a workspace, for callers that cannot allocate device memory.
+
+    The split-KV scratch is a fixed 8 MiB device array owned by the library
+    (one per GPU, held until exit); calls on one device share it, so calls
+    that overlap on the GPU race.  ``out`` must be given by such callers; if
+    it is None it is allocated here for convenience.
+    """
+    f = lib().kvc_paged_decode_no_alloc
+    f.restype = _I
+    f.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P]
+    _cuda("q", q)
+    _cuda("key_cache", key_cache, q.dtype)
+    _cuda("value_cache", value_cache, q.dtype)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("seq_lens", seq_lens, torch.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, q.dtype)
+    _check("kvc_paged_decode_no_alloc", f(
+        q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(), block_table.data_ptr(),
+        seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, D, bs, block_table.shape[1], NB,
+        float(scale), _DT[q.dtype], num_ctas, _flag(err_flag), _stream()))
+    return out
