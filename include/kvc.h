@@ -177,6 +177,43 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
                             size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream);
 
 /*
+ * kvc_varlen_prefill_paged -- packed variable-length causal prefill that
+ * writes its own K/V into the paged cache and attends through it.
+ * [NOTES] 3.1 (cu_seqlens / seq_offset, per-sequence positions), 3.2 (causal
+ * within a sequence only), 3.3 (packed token -> request and offset ->
+ * logical block -> physical block); [SKILL] 3.6 (each layer writes its cache,
+ * then FA reads it) and Appendix C (sparse_mode 3, causal); [ATB] 4.2 (the
+ * cache write).
+ *
+ *   sequence s owns packed tokens cu_seqlens[s] .. cu_seqlens[s+1]-1; token i
+ *   of it sits at position p = context_lens[s] + i.
+ *   1. key[t], value[t] are copied to their caches at slot_mapping[t] (as
+ *      kvc_reshape_and_cache; slot_mapping as kvc_build_slot_mapping's packed
+ *      form with start_pos = context_lens).
+ *   2. out[t][h] = sum_{j <= p} softmax_j(scale * q[t][h] . K_s[j][g]) V_s[j][g]
+ *      over positions 0..p of sequence s only (the diagonal included),
+ *      K_s/V_s read through block_table[s]; g = h / (num_q_heads/num_kv_heads).
+ *
+ * q, out: [num_tokens, num_q_heads, head_dim]; key, value: [num_tokens,
+ * num_kv_heads, head_dim]; cu_seqlens: int32 [num_seqs + 1] (leading 0);
+ * context_lens: int32 [num_seqs] cached tokens before this chunk, or NULL for
+ * none; slot_mapping: int32 [num_tokens]; block_table: int32 [num_seqs,
+ * max_blocks_per_seq]; caches: [num_blocks, block_size, num_kv_heads,
+ * head_dim].  max_seqlen_q is informational (the longest chunk).
+ * Supported: head_dim 64 or 128; block_size a power of two >= 8.  A sequence
+ * whose context_lens + length exceeds max_blocks_per_seq * block_size gets
+ * no output and sets KVC_FLAG_LEN_RANGE.
+ */
+kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* value,
+                                    const int32_t* cu_seqlens, const int32_t* context_lens,
+                                    const int32_t* slot_mapping, const int32_t* block_table,
+                                    void* key_cache, void* value_cache, void* out, int num_seqs,
+                                    int num_tokens, int max_seqlen_q, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int num_blocks, float scale,
+                                    kvc_dtype dtype, uint32_t* err_flag, kvc_stream_t stream);
+
+/*
  * kvc_paged_decode_no_alloc -- kvc_paged_decode for callers that cannot
  * allocate device memory.  The source pages have no counterpart to this entry
  * point; it exists for callers such as a host application that gives this

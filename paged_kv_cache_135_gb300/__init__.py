@@ -33,6 +33,8 @@ _SIGS = {
     "kvc_build_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "kvc_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
+    "kvc_varlen_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                      _I, _I, _I, _I, _F, _I, _P, _P]),
     "kvc_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                               _P, _S, _P, _P]),
 }
@@ -175,6 +177,43 @@ def paged_decode(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Te
         seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, D, bs, block_table.shape[1], NB,
         float(scale), _DT[q.dtype], num_ctas, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _flag(err_flag), _stream()))
+    return out
+
+
+def varlen_prefill_paged(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                        cu_seqlens: torch.Tensor, slot_mapping: torch.Tensor,
+                        block_table: torch.Tensor, key_cache: torch.Tensor,
+                        value_cache: torch.Tensor, scale: float, max_seqlen_q: int,
+                        context_lens: Optional[torch.Tensor] = None,
+                        out: Optional[torch.Tensor] = None,
+                        err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Packed causal prefill: write key/value at slot_mapping, attend through the cache.
+
+    q [T, Hq, D]; key, value [T, Hkv, D]; cu_seqlens int32 [S+1] with a
+    leading 0; context_lens int32 [S] (tokens cached before this chunk) or
+    None; caches [NB, bs, Hkv, D] (updated in place).
+    """
+    _cuda("q", q)
+    _cuda("key", key, q.dtype)
+    _cuda("value", value, q.dtype)
+    _cuda("cu_seqlens", cu_seqlens, torch.int32)
+    _cuda("slot_mapping", slot_mapping, torch.int32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("key_cache", key_cache, q.dtype)
+    _cuda("value_cache", value_cache, q.dtype)
+    if context_lens is not None:
+        _cuda("context_lens", context_lens, torch.int32)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, q.dtype)
+    _check("kvc_varlen_prefill_paged", lib().kvc_varlen_prefill_paged(
+        q.data_ptr(), key.data_ptr(), value.data_ptr(), cu_seqlens.data_ptr(),
+        _ptr(context_lens), slot_mapping.data_ptr(), block_table.data_ptr(),
+        key_cache.data_ptr(), value_cache.data_ptr(), out.data_ptr(), cu_seqlens.numel() - 1, T,
+        int(max_seqlen_q), Hq, Hkv, D, bs, block_table.shape[1], NB, float(scale),
+        _DT[q.dtype], _flag(err_flag), _stream()))
     return out
 
 

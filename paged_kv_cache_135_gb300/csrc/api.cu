@@ -191,4 +191,58 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
   return kvc::launch_paged_decode(a);
 }
 
+kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* value,
+                                    const int32_t* cu_seqlens, const int32_t* context_lens,
+                                    const int32_t* slot_mapping, const int32_t* block_table,
+                                    void* key_cache, void* value_cache, void* out, int num_seqs,
+                                    int num_tokens, int max_seqlen_q, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int num_blocks, float scale,
+                                    kvc_dtype dtype, uint32_t* err_flag, kvc_stream_t stream) {
+  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_tokens < 0 || max_seqlen_q < 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
+      num_blocks <= 0)
+    return KVC_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return KVC_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return KVC_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (!is_pow2(block_size) || block_size < 8) return KVC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL ||
+      static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+    return KVC_ERR_UNSUPPORTED;
+  if (num_tokens == 0 || num_seqs == 0) return KVC_OK;
+  if (!q || !key || !value || !cu_seqlens || !slot_mapping || !block_table || !key_cache ||
+      !value_cache || !out)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(key) || !aligned16(value) || !aligned16(key_cache) ||
+      !aligned16(value_cache) || !aligned16(out))
+    return KVC_ERR_INVALID_ARG;
+  kvc::PrefillArgs a;
+  a.q = q;
+  a.key = key;
+  a.value = value;
+  a.cu_seqlens = cu_seqlens;
+  a.context_lens = context_lens;
+  a.slot_mapping = slot_mapping;
+  a.block_table = block_table;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.out = out;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.max_seqlen_q = max_seqlen_q;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.err_flag = err_flag;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return kvc::launch_varlen_prefill(a);
+}
+
 }  // extern "C"

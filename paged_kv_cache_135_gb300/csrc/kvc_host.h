@@ -63,4 +63,26 @@ int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas
 size_t paged_decode_workspace_bytes(int group, int head_dim, int ctas);
 kvc_status launch_paged_decode(const DecodeArgs& a);
 
+struct PrefillArgs {
+  const void* q;
+  const void* key;
+  const void* value;
+  const int32_t* cu_seqlens;
+  const int32_t* context_lens;
+  const int32_t* slot_mapping;
+  const int32_t* block_table;
+  void* key_cache;
+  void* value_cache;
+  void* out;
+  int num_seqs, num_tokens, max_seqlen_q, num_q_heads, num_kv_heads, head_dim;
+  int block_size, max_blocks_per_seq, num_blocks;
+  float scale;
+  kvc_dtype dtype;
+  uint32_t* err_flag;
+  cudaStream_t stream;
+};
+
+// Cache write of the chunk's K/V rows, then the causal attention kernel.
+kvc_status launch_varlen_prefill(const PrefillArgs& a);
+
 }  // namespace kvc
