@@ -238,6 +238,98 @@ def run_reference(args):
     }), flush=True)
 
 
+def time_graphs(graphs, steps):
+    """Replay each graph in turn `steps` times; events around each replay.
+
+    Returns (total ms, {name: mean ms per replay})."""
+    stream = torch.cuda.current_stream()
+    evs = {n: [] for n, _ in graphs}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        for n, g in graphs:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            evs[n].append((a, b))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), {n: statistics.mean(a.elapsed_time(b) for a, b in v)
+                                 for n, v in evs.items()}
+
+
+def capture(fn):
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+    torch.cuda.current_stream().wait_stream(cap)
+    return g
+
+
+def prefill_flops(lens, ctx, Hq, D):
+    """Causal attention FLOPs: 4 * Hq * D per (query, visible key) pair."""
+    pairs = sum(c * n + n * (n + 1) // 2 for n, c in zip(lens, ctx))
+    return 4 * Hq * D * pairs
+
+
+def run_mixed(args, kvc, dev, rank):
+    """Mixed packed batch: 16 packed prefills, then a 128-sequence decode step."""
+    pre, dec = make_config("mixed_packed", seed=rank, value_device=str(dev))
+    m = pre.meta
+    Hq, Hkv, D, bs = m["num_q_heads"], m["num_kv_heads"], m["head_dim"], pre.block_size
+    P = {k: getattr(pre, k).to(dev) for k in ("q", "key", "value", "cu_seqlens", "context_lens",
+                                               "block_table")}
+    kc, vc = pre.key_cache, pre.value_cache          # one pool shared by both halves
+    T = pre.q.shape[0]
+    pslots = torch.empty(T, dtype=torch.int32, device=dev)
+    pout = torch.empty_like(P["q"])
+    dec.key_cache, dec.value_cache = kc, vc
+    step = DecodeStep(kvc, dec, dev)
+
+    def prefill():
+        kvc.build_slot_mapping(P["block_table"], bs, P["context_lens"], kc.shape[0],
+                               cu_seqlens=P["cu_seqlens"], num_tokens=T, out=pslots)
+        kvc.varlen_prefill_paged(P["q"], P["key"], P["value"], P["cu_seqlens"], pslots,
+                                 P["block_table"], kc, vc, pre.scale, pre.max_seqlen_q,
+                                 context_lens=P["context_lens"], out=pout)
+
+    for _ in range(args.warmup):
+        prefill()
+        step.write()
+        step.decode()
+    torch.cuda.synchronize()
+    graphs = [("prefill", capture(prefill)), ("decode_write", capture(step.write)),
+              ("decode", capture(step.decode))]
+    for _ in range(args.warmup):
+        for _, g in graphs:
+            g.replay()
+    steps = max(3, args.steps // 4)
+    with ClockSampler(dev.index or 0) as clk:
+        total_ms, per = time_graphs(graphs, steps)
+    lens = pre.meta["lens"]
+    flops = prefill_flops(lens, [0] * len(lens), Hq, D)
+    d_lens = dec.seq_lens.tolist()
+    d_bytes = decode_bytes(d_lens, Hq, Hkv, D, bs)
+    peak, kind = peaks()
+    ms_step = total_ms / steps
+    print(json.dumps({
+        "workload": CONFIGS["mixed_packed"]["about"], "steps": steps,
+        "ms_per_step": ms_step,
+        "prefill": {"ms": per["prefill"], "tokens": T, "attention_tflops": flops / per["prefill"]
+                    / 1e9, "tokens_per_s": T / (per["prefill"] * 1e-3)},
+        "decode": {"ms": per["decode"], "write_ms": per["decode_write"],
+                   "achieved_gbs": d_bytes / (per["decode"] * 1e-3) / 1e9,
+                   "frac_of_" + kind: d_bytes / (per["decode"] * 1e-3) / 1e9 / peak},
+        "clocks": clk.summary(),
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -248,6 +340,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--profile", action="store_true",
                     help="short run for ncu: no CPU baseline, few e2e steps")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(CONFIGS),
+                    help="the timed workload (default: the headline GQA 8B-shape decode)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -268,7 +362,9 @@ def main():
     kvc.build()
     kvc.lib()
 
-    case = make_config(WORKLOAD, seed=rank, value_device=str(dev))
+    if CONFIGS[args.workload]["kind"] == "mixed":
+        return run_mixed(args, kvc, dev, rank)
+    case = make_config(args.workload, seed=rank, value_device=str(dev))
     m = case.meta
     step = DecodeStep(kvc, case, dev)
     B = case.q.shape[0]
@@ -371,7 +467,8 @@ def main():
     dec_avg_ms = statistics.mean(dec_ms)
     achieved = d_bytes / (dec_avg_ms * 1e-3) / 1e9
     digest = kernel_source_digest()
-    traffic = recorded_traffic("paged_decode_gqa8b.md", digest)
+    traffic = (recorded_traffic("paged_decode_gqa8b.md", digest)
+               if args.workload == WORKLOAD else None)
 
     if rank == 0:
         res = {
@@ -385,10 +482,10 @@ def main():
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": case.dtype,
             "data": "synthetic",
             "config": {
-                "workload": CONFIGS[WORKLOAD]["about"],
+                "workload": CONFIGS[args.workload]["about"],
                 "batch": B, "num_q_heads": m["num_q_heads"], "num_kv_heads": m["num_kv_heads"],
                 "head_dim": m["head_dim"], "block_size": case.block_size,
                 "kv_tokens": int(sum(lens)), "step": "slot mapping + cache write + paged decode "

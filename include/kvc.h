@@ -214,6 +214,44 @@ kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* 
                                     kvc_dtype dtype, uint32_t* err_flag, kvc_stream_t stream);
 
 /*
+ * Bytes of workspace kvc_mla_paged_decode needs with `num_ctas` CTAs (0 = one
+ * CTA per SM of the current device; an odd count is rounded down to pairs).
+ * Returns 0 for an unsupported shape.
+ */
+size_t kvc_mla_paged_decode_workspace_size(int num_heads, int d_nope, int d_rope, int num_ctas);
+
+/*
+ * kvc_mla_paged_decode -- MLA (absorbed) decode over the latent paged cache.
+ * [SKILL] Mode 3: the cache stores cache_nope (kv_lora_rank wide) and
+ * cache_rope (qk_rope_head_dim wide) per token; FA takes key = value =
+ * cache_nope and query_rope / key_rope separately; query_rope and key_rope
+ * come together or not at all, rope D must be 64, query D 512.  Paging as in
+ * Mode 2.
+ *
+ *   s_j    = scale * (q_nope[b][h] . nope_j + q_rope[b][h] . rope_j)
+ *   out[b][h] = sum_{j < seq_lens[b]} softmax_j(s) nope_j
+ *   nope_j = cache_nope[block_table[b][j / block_size]][j % block_size][0]
+ *
+ * q_nope: [batch, 128, 512]; q_rope: [batch, 128, 64]; cache_nope:
+ * [num_blocks, block_size, 1, 512]; cache_rope: [num_blocks, block_size, 1,
+ * 64]; out: [batch, 128, 512]; block_table int32 [batch, max_blocks_per_seq];
+ * seq_lens int32 [batch].  Supported: num_heads 128, d_nope 512, d_rope 64,
+ * block_size a power of two >= 8, batch <= 1024; fp16 or bf16.
+ * Runs on CTA pairs (thread-block clusters of 2); long sequences are split
+ * over the pairs and merged inside the kernel.  workspace: device,
+ * >= kvc_mla_paged_decode_workspace_size bytes, zero-filled before first use
+ * and left zero-filled by every call (re-zero after KVC_FLAG_WAIT_TIMEOUT);
+ * calls that overlap on the GPU must not share it.
+ */
+kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
+                                const void* cache_rope, const int32_t* block_table,
+                                const int32_t* seq_lens, void* out, int batch, int num_heads,
+                                int d_nope, int d_rope, int block_size, int max_blocks_per_seq,
+                                int num_blocks, float scale, kvc_dtype dtype, int num_ctas,
+                                void* workspace, size_t workspace_bytes, uint32_t* err_flag,
+                                kvc_stream_t stream);
+
+/*
  * kvc_paged_decode_no_alloc -- kvc_paged_decode for callers that cannot
  * allocate device memory.  The source pages have no counterpart to this entry
  * point; it exists for callers such as a host application that gives this

@@ -33,6 +33,9 @@ _SIGS = {
     "kvc_build_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "kvc_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
+    "kvc_mla_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
+    "kvc_mla_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                  _I, _P, _S, _P, _P]),
     "kvc_varlen_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _I, _I, _F, _I, _P, _P]),
     "kvc_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
@@ -214,6 +217,44 @@ def varlen_prefill_paged(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor
         key_cache.data_ptr(), value_cache.data_ptr(), out.data_ptr(), cu_seqlens.numel() - 1, T,
         int(max_seqlen_q), Hq, Hkv, D, bs, block_table.shape[1], NB, float(scale),
         _DT[q.dtype], _flag(err_flag), _stream()))
+    return out
+
+
+def mla_workspace_size(num_ctas: int = 0) -> int:
+    return int(lib().kvc_mla_paged_decode_workspace_size(128, 512, 64, num_ctas))
+
+
+def mla_paged_decode(q_nope: torch.Tensor, q_rope: torch.Tensor, cache_nope: torch.Tensor,
+                     cache_rope: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                     scale: float, out: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                     workspace: Optional[torch.Tensor] = None,
+                     err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """MLA decode: q_nope [B, 128, 512], q_rope [B, 128, 64] over the latent caches.
+
+    ``workspace`` (uint8, >= mla_workspace_size bytes) must be zero-filled
+    before its first use; each call leaves it zero-filled.
+    """
+    _cuda("q_nope", q_nope)
+    _cuda("q_rope", q_rope, q_nope.dtype)
+    _cuda("cache_nope", cache_nope, q_nope.dtype)
+    _cuda("cache_rope", cache_rope, q_nope.dtype)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("seq_lens", seq_lens, torch.int32)
+    B, H, dn = q_nope.shape
+    NB, bs = cache_nope.shape[0], cache_nope.shape[1]
+    if out is None:
+        out = torch.empty_like(q_nope)
+    _cuda("out", out, q_nope.dtype)
+    if workspace is None:
+        workspace = torch.zeros(max(mla_workspace_size(num_ctas), 16), dtype=torch.uint8,
+                                device=q_nope.device)
+    _cuda("workspace", workspace)
+    _check("kvc_mla_paged_decode", lib().kvc_mla_paged_decode(
+        q_nope.data_ptr(), q_rope.data_ptr(), cache_nope.data_ptr(), cache_rope.data_ptr(),
+        block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(), B, H, dn, q_rope.shape[-1],
+        bs, block_table.shape[1], NB, float(scale), _DT[q_nope.dtype], num_ctas,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _flag(err_flag),
+        _stream()))
     return out
 
 

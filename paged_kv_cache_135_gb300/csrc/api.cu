@@ -245,4 +245,57 @@ kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* 
   return kvc::launch_varlen_prefill(a);
 }
 
+size_t kvc_mla_paged_decode_workspace_size(int num_heads, int d_nope, int d_rope, int num_ctas) {
+  if (num_heads != 128 || d_nope != 512 || d_rope != 64 || num_ctas < 0) return 0;
+  const int ctas = kvc::mla_decode_num_ctas(num_ctas);
+  return ctas >= 2 ? kvc::mla_decode_workspace_bytes(ctas) : 0;
+}
+
+kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
+                                const void* cache_rope, const int32_t* block_table,
+                                const int32_t* seq_lens, void* out, int batch, int num_heads,
+                                int d_nope, int d_rope, int block_size, int max_blocks_per_seq,
+                                int num_blocks, float scale, kvc_dtype dtype, int num_ctas,
+                                void* workspace, size_t workspace_bytes, uint32_t* err_flag,
+                                kvc_stream_t stream) {
+  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (batch < 0 || num_heads <= 0 || d_nope <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
+      num_blocks <= 0 || num_ctas < 0 || num_ctas == 1)
+    return KVC_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return KVC_ERR_INVALID_ARG;
+  // query_rope and key_rope come together or not at all; rope D must be 64.
+  if ((q_rope == nullptr) != (cache_rope == nullptr)) return KVC_ERR_INVALID_ARG;
+  if (q_rope == nullptr || d_rope != 64) return KVC_ERR_UNSUPPORTED;
+  if (num_heads != 128 || d_nope != 512) return KVC_ERR_UNSUPPORTED;
+  if (!is_pow2(block_size) || block_size < 8) return KVC_ERR_UNSUPPORTED;
+  if (batch > 1024) return KVC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+    return KVC_ERR_UNSUPPORTED;
+  if (batch == 0) return KVC_OK;
+  if (!q_nope || !cache_nope || !block_table || !seq_lens || !out) return KVC_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(cache_nope) ||
+      !aligned16(cache_rope) || !aligned16(out) || !aligned16(workspace))
+    return KVC_ERR_INVALID_ARG;
+  kvc::MlaArgs a;
+  a.q_nope = q_nope;
+  a.q_rope = q_rope;
+  a.cache_nope = cache_nope;
+  a.cache_rope = cache_rope;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.batch = batch;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.num_ctas = num_ctas;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err_flag = err_flag;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return kvc::launch_mla_decode(a);
+}
+
 }  // extern "C"

@@ -85,4 +85,27 @@ struct PrefillArgs {
 // Cache write of the chunk's K/V rows, then the causal attention kernel.
 kvc_status launch_varlen_prefill(const PrefillArgs& a);
 
+struct MlaArgs {
+  const void* q_nope;
+  const void* q_rope;
+  const void* cache_nope;
+  const void* cache_rope;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  void* out;
+  int batch, block_size, max_blocks_per_seq, num_blocks;
+  float scale;
+  kvc_dtype dtype;
+  int num_ctas;
+  void* workspace;
+  size_t workspace_bytes;
+  uint32_t* err_flag;
+  cudaStream_t stream;
+};
+
+// CTAs (an even number: pairs) the MLA kernel runs with (num_ctas <= 0: auto).
+int mla_decode_num_ctas(int num_ctas);
+size_t mla_decode_workspace_bytes(int ctas);
+kvc_status launch_mla_decode(const MlaArgs& a);
+
 }  // namespace kvc

@@ -1,0 +1,145 @@
+"""GPU parity of the tcgen05 MLA decode against the oracle (key = [nope | rope], value = nope).
+
+Attention outputs must be within max-abs 2e-3 (fp16) / 1e-2 (bf16) of the
+fp64 oracle; the latent cache write is bit-exact.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL, bits, to_cuda
+from oracle import kvc_oracle as O
+from synth import make_config, mla_case
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_mla(kvc, c, num_ctas=0, err=None, caches=None):
+    d = {k: to_cuda(getattr(c, k)) for k in ("q_nope", "q_rope", "cache_nope", "cache_rope",
+                                             "block_table", "seq_lens")}
+    if caches is not None:
+        d["cache_nope"], d["cache_rope"] = caches
+    out = kvc.mla_paged_decode(d["q_nope"], d["q_rope"], d["cache_nope"], d["cache_rope"],
+                               d["block_table"], d["seq_lens"], c.scale, num_ctas=num_ctas,
+                               err_flag=err)
+    torch.cuda.synchronize()
+    return d, out
+
+
+def oracle_mla(c):
+    return O.mla_paged_decode(c.q_nope.double().numpy(), c.q_rope.double().numpy(),
+                              c.cache_nope.double().numpy(), c.cache_rope.double().numpy(),
+                              c.block_table.numpy(), c.seq_lens.numpy(), c.scale)
+
+
+CASES = [
+    # (lens, block_size, dtype)
+    ([1, 5], 16, "bf16"),
+    ([63, 64, 65], 64, "bf16"),
+    ([200, 7, 129], 128, "f16"),
+    ([700], 8, "bf16"),
+    ([0, 130, 0, 1], 32, "bf16"),
+]
+
+
+@pytest.mark.parametrize("lens,bs,dtype", CASES)
+@pytest.mark.parametrize("num_ctas", [0, 2, 6])
+def test_mla_matches_oracle(kvc_lib, lens, bs, dtype, num_ctas):
+    c = mla_case(41, len(lens), lens, block_size=bs, dtype=dtype)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, out = gpu_mla(kvc_lib, c, num_ctas, err)
+    assert int(err.item()) == 0
+    ref = oracle_mla(c)
+    e = float(np.abs(out.double().cpu().numpy() - ref).max())
+    assert e <= TOL[dtype], e
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(out[b]).item() == 0
+
+
+def test_mla_many_splits(kvc_lib):
+    c = mla_case(42, 3, [3000, 40, 1500], block_size=64, dtype="bf16")
+    ref = oracle_mla(c)
+    for ctas in (2, 10, 64, 300):
+        _, out = gpu_mla(kvc_lib, c, ctas)
+        e = float(np.abs(out.double().cpu().numpy() - ref).max())
+        assert e <= TOL["bf16"], (ctas, e)
+
+
+def test_mla_deterministic_permutation_invariant_and_poison_safe(kvc_lib):
+    lens = [300, 77, 513]
+    c = mla_case(43, 3, lens, block_size=16, dtype="bf16", num_blocks=80)
+    _, a = gpu_mla(kvc_lib, c, 8)
+    a = a.clone()
+    _, b = gpu_mla(kvc_lib, c, 8)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    g = torch.Generator().manual_seed(5)
+    perm = torch.randperm(80, generator=g)
+    inv = torch.argsort(perm)
+    c2 = mla_case(43, 3, lens, block_size=16, dtype="bf16", num_blocks=80)
+    c2.cache_nope = c2.cache_nope[perm].contiguous()
+    c2.cache_rope = c2.cache_rope[perm].contiguous()
+    c2.block_table = inv[c2.block_table.long()].to(torch.int32)
+    _, p = gpu_mla(kvc_lib, c2, 8)
+    assert torch.equal(a.view(torch.int16), p.view(torch.int16))
+    bt = c.block_table.numpy()
+    owned = np.zeros(80 * 16, dtype=bool)
+    for s, L in enumerate(lens):
+        for pos in range(L):
+            owned[bt[s, pos // 16] * 16 + pos % 16] = True
+    mask = torch.from_numpy(~owned).view(80, 16)
+    c3 = mla_case(43, 3, lens, block_size=16, dtype="bf16", num_blocks=80)
+    c3.cache_nope[mask] = float("nan")
+    c3.cache_rope[mask] = float("nan")
+    _, z = gpu_mla(kvc_lib, c3, 8)
+    assert torch.isfinite(z).all()
+    assert torch.equal(a.view(torch.int16), z.view(torch.int16))
+
+
+def test_mla_rejects_missing_rope_and_odd_shapes(kvc_lib):
+    lib = kvc_lib.lib()
+    P = 0x1000
+    f = lib.kvc_mla_paged_decode
+    args = [P, P, P, P, P, P, P, 2, 128, 512, 64, 64, 4, 8, 0.04, 1, 0, P, 1 << 30, None, None]
+    bad = list(args)
+    bad[1] = None                       # query_rope without key_rope
+    assert f(*bad) == kvc_lib.KVC_ERR_INVALID_ARG
+    bad = list(args)
+    bad[10] = 32                        # rope D must be 64
+    assert f(*bad) == kvc_lib.KVC_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[9] = 128                        # query D 512 only in this build
+    assert f(*bad) == kvc_lib.KVC_ERR_UNSUPPORTED
+
+
+def test_full_size_mla_step_sampled(kvc_lib):
+    """MLA workload: 1-token latent write, then decode; 12 sequences checked in full."""
+    c = make_config("mla_decode", seed=0, value_device="cuda")
+    cn0, cr0 = c.cache_nope.clone(), c.cache_rope.clone()
+    d = {k: to_cuda(getattr(c, k)) for k in ("block_table", "seq_lens", "write_pos")}
+    slots = kvc_lib.build_slot_mapping(d["block_table"], c.block_size, d["write_pos"],
+                                       c.cache_nope.shape[0])
+    kvc_lib.reshape_and_cache(c.new_nope, c.new_rope, c.cache_nope, c.cache_rope, slots)
+    out = kvc_lib.mla_paged_decode(c.q_nope, c.q_rope, c.cache_nope, c.cache_rope,
+                                   d["block_table"], d["seq_lens"], c.scale)
+    torch.cuda.synchronize()
+    ref_slots = O.slot_mapping(c.block_table.numpy(), c.block_size, c.write_pos.numpy())
+    assert slots.cpu().numpy().tolist() == ref_slots.tolist()
+    bs = c.block_size
+    worst = 0.0
+    for b in range(0, 64, 6):
+        L = int(c.seq_lens[b])
+        nblk = -(-L // bs)
+        ids = c.block_table[b, :nblk].long().cuda()
+        cn = cn0[ids].double().cpu().numpy()
+        cr = cr0[ids].double().cpu().numpy()
+        table = np.arange(nblk)[None]
+        sm = O.slot_mapping(table, bs, [L - 1])
+        cn, cr = O.reshape_and_cache(c.new_nope[b:b + 1].double().cpu().numpy(),
+                                     c.new_rope[b:b + 1].double().cpu().numpy(), cn, cr, sm)
+        ref = O.mla_paged_decode(c.q_nope[b:b + 1].double().cpu().numpy(),
+                                 c.q_rope[b:b + 1].double().cpu().numpy(), cn, cr, table, [L],
+                                 c.scale)[0]
+        worst = max(worst, float(np.abs(out[b].double().cpu().numpy() - ref).max()))
+    assert worst <= TOL["bf16"], worst
