@@ -330,6 +330,53 @@ def run_mixed(args, kvc, dev, rank):
     }), flush=True)
 
 
+def run_mla(args, kvc, dev, rank):
+    """MLA decode step: latent write of the new token, then MLA decode."""
+    c = make_config("mla_decode", seed=rank, value_device=str(dev))
+    d = {k: getattr(c, k).to(dev) for k in ("q_nope", "q_rope", "cache_nope", "cache_rope",
+                                             "block_table", "seq_lens", "new_nope", "new_rope",
+                                             "write_pos")}
+    B = c.q_nope.shape[0]
+    slots = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q_nope"])
+    ws = torch.zeros(max(kvc.mla_workspace_size(), 16), dtype=torch.uint8, device=dev)
+    nb = d["cache_nope"].shape[0]
+
+    def write():
+        kvc.build_slot_mapping(d["block_table"], c.block_size, d["write_pos"], nb, out=slots)
+        kvc.reshape_and_cache(d["new_nope"], d["new_rope"], d["cache_nope"], d["cache_rope"],
+                              slots)
+
+    def decode():
+        kvc.mla_paged_decode(d["q_nope"], d["q_rope"], d["cache_nope"], d["cache_rope"],
+                             d["block_table"], d["seq_lens"], c.scale, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        write()
+        decode()
+    torch.cuda.synchronize()
+    graphs = [("write", capture(write)), ("decode", capture(decode))]
+    for _ in range(args.warmup):
+        for _, g in graphs:
+            g.replay()
+    with ClockSampler(dev.index or 0) as clk:
+        total_ms, per = time_graphs(graphs, args.steps)
+    lens = c.seq_lens.tolist()
+    toks = sum(lens)
+    by = toks * 576 * 2 + B * 128 * (576 + 512) * 2 + 4 * sum(-(-x // c.block_size) for x in lens) + 4 * B
+    flops = toks * 128 * (2 * 576 + 2 * 512)
+    peak, kind = peaks()
+    ms = per["decode"]
+    print(json.dumps({
+        "workload": CONFIGS["mla_decode"]["about"], "steps": args.steps,
+        "ms_per_step": total_ms / args.steps, "decode_ms": ms, "write_ms": per["write"],
+        "algorithmic_bytes": by, "achieved_gbs": by / (ms * 1e-3) / 1e9,
+        "frac_of_" + kind + "_hbm": by / (ms * 1e-3) / 1e9 / peak,
+        "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": B / (total_ms / args.steps * 1e-3),
+        "clocks": clk.summary(),
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -364,6 +411,8 @@ def main():
 
     if CONFIGS[args.workload]["kind"] == "mixed":
         return run_mixed(args, kvc, dev, rank)
+    if CONFIGS[args.workload]["kind"] == "mla":
+        return run_mla(args, kvc, dev, rank)
     case = make_config(args.workload, seed=rank, value_device=str(dev))
     m = case.meta
     step = DecodeStep(kvc, case, dev)

@@ -49,6 +49,28 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// The same with the accumulate flag as an immediate: D = A*B (fresh) or
+// D += A*B (acc).  Issue loops built from these, with descriptors advanced by
+// constant offsets, keep the single issuing thread off the critical path.
+__device__ __forceinline__ void umma_f16_fresh(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+__device__ __forceinline__ void umma_f16_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+
+// Descriptor of the same operand `bytes` further on in shared memory (the
+// start-address field holds address / 16 and never overflows its 14 bits).
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {

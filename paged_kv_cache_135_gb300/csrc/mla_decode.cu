@@ -171,6 +171,20 @@ __device__ __forceinline__ void mla_producer(const MlaParams& p, const CUtensorM
 }
 
 // --------------------------------------------------------------- tcgen05
+// S = Q K^T over NQ 64-wide chunks, fully unrolled from two base descriptors.
+template <int NQ>
+__device__ __forceinline__ void mla_issue_s(uint32_t d, uint64_t q0, uint64_t k0, uint32_t idesc) {
+#pragma unroll
+  for (int c = 0; c < NQ; ++c)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t a = desc_advance(q0, c * kQChunkBytes + kk * 32);
+      const uint64_t b = desc_advance(k0, c * kKChunkBytes + kk * 32);
+      if (c == 0 && kk == 0) umma_f16_fresh(d, a, b, idesc);
+      else umma_f16_acc(d, a, b, idesc);
+    }
+}
+
 // One thread.  S(t+1) = Q K(t+1)^T is issued before O += P(t) V(t), so the
 // tensor core computes the next scores while the softmax works on P(t).
 template <bool kBf16>
@@ -178,11 +192,13 @@ __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint6
                                         volatile int* abort_flag, const int* cum, uint32_t tmem,
                                         long long tb, long long te, int rank) {
   using L = MlaLayout;
-  const int nq = rank ? 5 : 4;
   const uint32_t idesc_s = umma_idesc_f16(kBf16, kH, kTok, 0, 0);
   const uint32_t idesc_o = umma_idesc_f16(kBf16, kH, kOutCols, 0, 1);
-  const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK);
-  const uint32_t sP = smem_u32(smem + L::kP);
+  const uint64_t q0 = umma_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+  const uint64_t k0 = umma_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
+  const uint64_t p0 = umma_desc_sw128(smem_u32(smem + L::kP), 16, 1024);
+  // V = the first four chunks of a stage, MN-major: next 64 columns 8 KB on.
+  const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kK), kKChunkBytes, 1024);
   const int n_it = static_cast<int>(te - tb);
   sched::Cursor cs;  // tile whose S is issued next
   cs.locate(tb, cum, p.batch, 1);
@@ -200,13 +216,9 @@ __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint6
     if (!wait_cta(&bars[kQFull], seg_s & 1, abort_flag, p.err_flag)) return false;
     tc_fence_after();
     const uint32_t d = tmem + (stage ? kTmemS1 : kTmemS0);
-    const uint32_t kst = sK + stage * L::kStageBytes;
-    for (int c = 0; c < nq; ++c)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_f16(d, umma_desc_sw128(sQ + c * kQChunkBytes + kk * 32, 16, 1024),
-                 umma_desc_sw128(kst + c * kKChunkBytes + kk * 32, 16, 1024), idesc_s,
-                 (c | kk) != 0);
+    const uint64_t k_st = desc_advance(k0, stage * L::kStageBytes);
+    if (rank) mla_issue_s<5>(d, q0, k_st, idesc_s);
+    else mla_issue_s<4>(d, q0, k_st, idesc_s);
     umma_commit(&bars[kSFull0 + stage]);
     if (last) umma_commit(&bars[kQFree]);
     cs.advance(cum, p.batch, 1);
@@ -215,13 +227,13 @@ __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint6
   auto issue_pv = [&](int it) -> bool {
     if (!wait_cta(&bars[kPFull], it & 1, abort_flag, p.err_flag)) return false;
     tc_fence_after();
-    const uint32_t kst = sK + (it & 1) * L::kStageBytes;
-    const bool first = first_flags[it & 1];
+    const uint64_t v_st = desc_advance(v0, (it & 1) * L::kStageBytes);
+    if (first_flags[it & 1]) umma_f16_fresh(tmem + kTmemO, p0, v_st, idesc_o);
+    else umma_f16_acc(tmem + kTmemO, p0, v_st, idesc_o);
 #pragma unroll
-    for (int ks = 0; ks < kTok / 16; ++ks)
-      umma_f16(tmem + kTmemO, umma_desc_sw128(sP + ks * 32, 16, 1024),
-               umma_desc_sw128(kst + ks * 16 * 128, kKChunkBytes, 1024), idesc_o,
-               !(first && ks == 0));
+    for (int ks = 1; ks < kTok / 16; ++ks)
+      umma_f16_acc(tmem + kTmemO, desc_advance(p0, ks * 32), desc_advance(v_st, ks * 16 * 128),
+                   idesc_o);
     umma_commit(&bars[kPVDone]);
     umma_commit(&bars[kKEmpty0 + (it & 1)]);
     return true;
@@ -389,12 +401,15 @@ __device__ __forceinline__ void mla_softmax(const MlaParams& p, uint8_t* smem, u
     mbar_arrive(&bars[kSFree0 + stage]);
 
     // 2. Exchange partial scores with the other CTA of the pair and sum them.
+    //    One elected thread signals after a CTA barrier: its cluster-scope
+    //    release covers every thread's remote stores before it.
     wait_peer(&bars[kXEmpty], (it & 1) ^ 1, abort_flag, p.err_flag);
 #pragma unroll
     for (int q = 0; q < kTok / 4; ++q)
       st_cluster_v4(x_peer + (q * kH + row) * 16,
                     make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]));
-    mbar_arrive_cluster(xfull_peer);
+    named_bar_sync(2, kSoftmaxThreads);
+    if (row == 0) mbar_arrive_cluster(xfull_peer);
     wait_peer(&bars[kXFull], it & 1, abort_flag, p.err_flag);
 #pragma unroll
     for (int q = 0; q < kTok / 4; ++q) {
@@ -404,7 +419,8 @@ __device__ __forceinline__ void mla_softmax(const MlaParams& p, uint8_t* smem, u
       s[4 * q + 2] += v.z;
       s[4 * q + 3] += v.w;
     }
-    mbar_arrive_cluster(xempty_peer);
+    named_bar_sync(2, kSoftmaxThreads);
+    if (row == 0) mbar_arrive_cluster(xempty_peer);
 
     // 3. Online softmax in the log2 domain; O is rescaled only when the
     //    running max grows by more than 2^kRescaleThreshold.
@@ -511,8 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     const uint32_t counts[L::kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, kSoftmaxThreads,
-                                          kSoftmaxThreads, kSoftmaxThreads, 1, kSoftmaxThreads,
-                                          kSoftmaxThreads, 1};
+                                          kSoftmaxThreads, kSoftmaxThreads, 1, 1, 1, 1};
     for (int i = 0; i < L::kNumBars; ++i) mbar_init(&bars[i], counts[i]);
     *abort_flag = 0;
     fence_barrier_init();
