@@ -84,6 +84,8 @@ struct PrefillArgs {
 
 // Cache write of the chunk's K/V rows, then the causal attention kernel.
 kvc_status launch_varlen_prefill(const PrefillArgs& a);
+// The causal attention part alone (tcgen05 kernel).
+kvc_status launch_prefill_attention_tc(const PrefillArgs& a);
 
 struct MlaArgs {
   const void* q_nope;
