@@ -13,7 +13,8 @@
 // of tcgen05.mma; K/V tiles are 128 tokens (N of S = Q K^T, K of O += P V),
 // so every MMA is M128 x N128 (or N = head_dim) and runs near the tensor
 // core's peak.  Roles: a TMA producer warp (query tile once, then K and V
-// tiles through block_table into a 2-stage ring), one thread issuing the
+// tiles through block_table into 2-stage K and V rings, K released as soon
+// as its S is computed), one thread issuing the
 // MMAs (S of the next tile is issued before P V of the current one, S
 // double-buffered in tensor memory, O accumulated in tensor memory), and
 // eight softmax warps, two threads per query row (64 columns each) that
@@ -61,18 +62,19 @@ template <int D>
 struct TcLayout {
   static constexpr int kHalves = D / 64;
   static constexpr int kQ = 0;                                 // kHalves chunks
-  static constexpr int kK = kQ + kHalves * kChunk;             // stages: K chunks then V chunks
-  static constexpr int kStageBytes = 2 * kHalves * kChunk;
-  static constexpr int kP = kK + kStages * kStageBytes;        // 2 chunks (128 tokens)
+  static constexpr int kStageBytes = kHalves * kChunk;         // one K or one V tile
+  static constexpr int kK = kQ + kHalves * kChunk;             // K ring
+  static constexpr int kV = kK + kStages * kStageBytes;        // V ring
+  static constexpr int kP = kV + kStages * kStageBytes;        // 2 chunks (128 tokens)
   static constexpr int kRed = kP + 2 * kChunk;                 // float[2 tiles][2 halves][128]
   static constexpr int kBar = kRed + 2 * 2 * kBM * 4;
-  static constexpr int kNumBars = 12;
+  static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBar + kNumBars * 8;            // tmem slot, abort, info[4]
   static constexpr int kTotal = 1024 + kMisc + 64;
 };
 
 enum Bar { kQFull = 0, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kSFull0, kSFull1, kSFree0, kSFree1,
-           kPFull, kPVDone, kDrain };
+           kPFull, kPVDone, kDrain, kVFull0, kVFull1, kVEmpty0, kVEmpty1 };
 
 __device__ __forceinline__ bool wait_tc(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                         uint32_t* err) {
@@ -143,30 +145,34 @@ __device__ __forceinline__ void tc_producer(const TcPrefillParams& p, const CUte
     int pb = -1;
     if (lane < nsub && tok < kv_len)
       pb = __ldg(&p.block_table[static_cast<long long>(s) * p.max_blocks + (tok >> p.log2_bs)]);
-    const bool ok = wait_tc(&bars[kKEmpty0 + stage], ((j >> 1) & 1) ^ 1, abort_flag, p.err_flag);
     bool valid = false;
     if (lane < nsub && tok < kv_len) {
       if (pb < 0 || pb >= p.num_blocks) set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
-      else valid = ok;
+      else valid = true;
     }
-    const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-    if (lane == 0)
-      mbar_arrive_expect_tx(&bars[kKFull0 + stage], nvalid * box_bytes * L::kHalves * 2);
-    __syncwarp();
-    if (valid) {
-      uint8_t* dst = smem + L::kK + stage * L::kStageBytes + lane * box_bytes;
-      const int in_blk = tok & (p.block_size - 1);
+    const int in_blk = tok & (p.block_size - 1);
+    // K(j) as soon as S(j-2) has consumed its stage, V(j) once P V(j-2) has.
+    for (int part = 0; part < 2; ++part) {
+      const int empty = part ? kVEmpty0 : kKEmpty0, full = part ? kVFull0 : kKFull0;
+      const bool ok = wait_tc(&bars[empty + stage], ((j >> 1) & 1) ^ 1, abort_flag, p.err_flag);
+      const bool go = valid && ok;
+      const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, go));
+      if (lane == 0) mbar_arrive_expect_tx(&bars[full + stage], nvalid * box_bytes * L::kHalves);
+      __syncwarp();
+      if (go) {
+        uint8_t* dst = smem + (part ? L::kV : L::kK) + stage * L::kStageBytes + lane * box_bytes;
 #pragma unroll
-      for (int c = 0; c < L::kHalves; ++c) {
-        tma_load_4d(dst + c * kChunk, tm_k, &bars[kKFull0 + stage], c * 64, g, in_blk, pb);
-        tma_load_4d(dst + (L::kHalves + c) * kChunk, tm_v, &bars[kKFull0 + stage], c * 64, g,
-                    in_blk, pb);
+        for (int c = 0; c < L::kHalves; ++c)
+          tma_load_4d(dst + c * kChunk, part ? tm_v : tm_k, &bars[full + stage], c * 64, g, in_blk,
+                      pb);
       }
     }
   }
   // Every copy issued must land before shared memory can be released.
-  for (int j = n_tiles > kStages ? n_tiles - kStages : 0; j < n_tiles; ++j)
+  for (int j = n_tiles > kStages ? n_tiles - kStages : 0; j < n_tiles; ++j) {
     mbar_wait_bounded(&bars[kKFull0 + (j & 1)], (j >> 1) & 1, p.err_flag);
+    mbar_wait_bounded(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, p.err_flag);
+  }
 }
 
 // One thread issues every MMA: S(j+1) before P(j) V(j).
@@ -178,7 +184,7 @@ __device__ __forceinline__ void tc_mma(const TcPrefillParams& p, uint8_t* smem, 
   constexpr uint32_t idesc_o = umma_idesc_f16(kBf16, kBM, D, 0, 1);
   const uint64_t q0 = umma_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
   const uint64_t k0 = umma_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
-  const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kK + L::kHalves * kChunk), kChunk, 1024);
+  const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kV), kChunk, 1024);
   const uint64_t p0 = umma_desc_sw128(smem_u32(smem + L::kP), 16, 1024);
   if (!wait_tc(&bars[kQFull], 0, abort_flag, p.err_flag)) return;
 
@@ -199,9 +205,11 @@ __device__ __forceinline__ void tc_mma(const TcPrefillParams& p, uint8_t* smem, 
         else umma_f16_acc(d, a, b, idesc_s);
       }
     umma_commit(&bars[kSFull0 + stage]);
+    umma_commit(&bars[kKEmpty0 + stage]);
     return true;
   };
   auto issue_pv = [&](int j) -> bool {
+    if (!wait_tc(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, abort_flag, p.err_flag)) return false;
     if (!wait_tc(&bars[kPFull], j & 1, abort_flag, p.err_flag)) return false;
     tc_fence_after();
     const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
@@ -213,7 +221,7 @@ __device__ __forceinline__ void tc_mma(const TcPrefillParams& p, uint8_t* smem, 
       else umma_f16_acc(tmem + kTmemO, a, b, idesc_o);
     }
     umma_commit(&bars[kPVDone]);
-    umma_commit(&bars[kKEmpty0 + (j & 1)]);
+    umma_commit(&bars[kVEmpty0 + (j & 1)]);
     return true;
   };
   if (!issue_s(0)) return;
@@ -319,7 +327,8 @@ __device__ __forceinline__ void tc_softmax(const TcPrefillParams& p, uint8_t* sm
     // cannot reach P V.
     const int valid = kv_len - j * kBN;
     if (valid < kBN) {
-      uint8_t* vst = smem + L::kK + stage * L::kStageBytes + L::kHalves * kChunk;
+      wait_tc(&bars[kVFull0 + stage], (j >> 1) & 1, abort_flag, p.err_flag);
+      uint8_t* vst = smem + L::kV + stage * L::kStageBytes;
       const int n16 = (kBN - valid) * L::kHalves * 8;
       for (int e = t; e < n16; e += kSmxThreads) {
         const int r = valid + e / (L::kHalves * 8), c = (e / 8) % L::kHalves, q = e % 8;
@@ -385,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       info[2] = ctx;
       info[3] = len;
       const uint32_t counts[L::kNumBars] = {1, 1, 1, 1, 1, 1, 1, kSmxThreads, kSmxThreads,
-                                            kSmxThreads, 1, 1};
+                                            kSmxThreads, 1, 1, 1, 1, 1, 1};
       for (int i = 0; i < L::kNumBars; ++i) mbar_init(&bars[i], counts[i]);
       *abort_flag = 0;
       fence_barrier_init();
