@@ -65,6 +65,22 @@ __device__ __forceinline__ void umma_f16_acc(uint32_t d_tmem, uint64_t a_desc, u
                : "memory");
 }
 
+// The same with A read from tensor memory: M rows in lanes 0..M-1, two 16-bit
+// K elements per 32-bit column (element 2c in the low half of column c), so
+// one 16-wide K step is 8 columns on from the previous one.
+__device__ __forceinline__ void umma_f16_ts_fresh(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
+               "r"(a_tmem), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+__device__ __forceinline__ void umma_f16_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+               "r"(a_tmem), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+
 // Descriptor of the same operand `bytes` further on in shared memory (the
 // start-address field holds address / 16 and never overflows its 14 bits).
 __device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
@@ -137,6 +153,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -168,6 +193,25 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(v.x),
                "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory that completes
+// 16 bytes of the transaction count of that CTA's mbarrier `cbar` (both
+// addresses from map_to_rank).  The receiver's wait on the barrier (acquire,
+// cluster scope) makes the data visible; no fence is needed on this side.
+__device__ __forceinline__ void st_async_cluster_v4(uint32_t caddr, float4 v, uint32_t cbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          caddr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cbar)
+      : "memory");
+}
+
+// Arrive (no memory ordering) on an mbarrier of another CTA of the cluster:
+// for "buffer free" signals after reads whose values have been consumed.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
                : "memory");
 }
 

@@ -15,20 +15,27 @@
 //   * rank 0 owns key columns nope[0:256] and output columns 0..255, rank 1
 //     owns nope[256:512] + rope[0:64] and output columns 256..511; each CTA
 //     loads only its own columns of every cached token (the pair reads each
-//     token once) and the query columns that go with them;
-//   * each CTA computes a partial S = Q_own K_own^T (M 128, N 64 tokens) into
-//     tensor memory; the two partials are exchanged through distributed
-//     shared memory and summed, so both CTAs hold the full S;
-//   * both run the same online softmax (one query row per thread, log2
-//     domain, rescaling of O only when the running max grows by more than
-//     2^8), write P (bf16, 128-byte swizzled) to shared memory and compute
-//     O_own += P V_own with V = their nope columns, straight from the K tile
-//     (MN-major operand), accumulating in tensor memory.
+//     token once);
+//   * the CTA's 256 nope query columns live in tensor memory (the A operand
+//     of S = Q K^T), which leaves shared memory for a 4-stage key ring;
+//     rank 1's rope query columns stay in shared memory;
+//   * each CTA computes a partial S (M 128, N 64 tokens) into tensor memory;
+//     the partials are exchanged through distributed shared memory and
+//     summed, so both CTAs hold the full S;
+//   * both run the same online softmax (two threads per query row, log2
+//     domain, O rescaled only when the running max grows by more than 2^8),
+//     write P (bf16/fp16, 128-byte swizzled) to shared memory and compute
+//     O_own += P V_own with V = their nope columns straight from the key
+//     tile (MN-major operand), accumulating in tensor memory.
+// The softmax runs one tile behind the exchange: while tile t's partial
+// scores travel to the other CTA, the softmax of tile t-1 runs, and the
+// tensor core computes S two tiles ahead of P V.
 // Work: 64-token tiles of all sequences in one linear order, split evenly
 // over the clusters (stream-K split-KV); the cluster that finishes a split
 // sequence last merges the partial states (per rank), as in the GQA decode.
-// Roles per CTA: warps 0-3 softmax / epilogue (one TMEM lane per thread),
-// warp 4 TMA producer, warp 5 tcgen05 issuer (one thread) and TMEM owner.
+// Roles per CTA: warps 0-7 softmax / epilogue (warp w reads TMEM lanes
+// 32*(w%4).., column half w/4), warp 8 TMA producer, warp 9 tcgen05 issuer
+// (one thread) and TMEM owner.
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -47,23 +54,28 @@ namespace {
 constexpr int kH = 128;             // query heads = MMA M
 constexpr int kTok = 64;            // tokens per tile = N of QK, K of PV
 constexpr int kNope = 512, kRope = 64;
-constexpr int kOutCols = 256;       // output columns per CTA
-constexpr int kMaxChunks = 5;       // 64-wide key chunks per CTA (rank 1: 4 nope + rope)
+constexpr int kOutCols = 256;       // output (and nope key) columns per CTA
 constexpr int kQChunkBytes = kH * 128;     // [128 heads][64 elements]
 constexpr int kKChunkBytes = kTok * 128;   // [64 tokens][64 elements]
-constexpr int kStages = 2;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = kSoftmaxThreads + 64;  // + producer warp + MMA warp
+constexpr int kStageChunks = 5;            // rank 1: 4 nope + rope
+constexpr int kStageBytes = kStageChunks * kKChunkBytes;
+constexpr int kStages = 4;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = kSoftmaxThreads + 64;
 constexpr int kMaxBatch = 1024;
 constexpr int kMaxPieces = 62;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
-// TMEM columns: O (256 fp32) then two S buffers (64 fp32 each).
+// TMEM columns: O (256 fp32), two S buffers (64 fp32 each), then the CTA's
+// 256 nope query columns as packed 16-bit pairs (128 columns).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0, kTmemS0 = 256, kTmemS1 = 320;
+constexpr uint32_t kTmemO = 0, kTmemS0 = 256, kTmemS1 = 320, kTmemQ = 384;
 
 struct MlaParams {
   void* out;
+  const void* q_nope;
   const int32_t* block_table;
   const int32_t* seq_lens;
   int* ws_cnt;    // [clusters][2 slots][2 ranks]
@@ -74,27 +86,72 @@ struct MlaParams {
   float scale_log2;
 };
 
-// Shared memory (1024-aligned base).  Regions sized for rank 1 (5 chunks).
+constexpr int align_up_c(int x, int a) { return (x + a - 1) / a * a; }
+
+// Shared memory (1024-aligned base), regions sized for rank 1.  The per-
+// sequence plan (clamped lengths, prefix sums of tiles) is built in the P
+// region at start and read only until every thread has found its first
+// tile.
 struct MlaLayout {
-  static constexpr int kQ = 0;                                       // 5 x 16 KB
-  static constexpr int kK = kQ + kMaxChunks * kQChunkBytes;          // 2 x 5 x 8 KB
-  static constexpr int kStageBytes = kMaxChunks * kKChunkBytes;
-  static constexpr int kP = kK + kStages * kStageBytes;              // 16 KB
-  static constexpr int kX = kP + kH * 128;                           // 32 KB
-  static constexpr int kBar = kX + kH * kTok * 4;
-  // barriers: q_full, q_free, k_full[2], k_empty[2], s_full[2], s_free[2],
-  //           p_full, pv_done, x_full, x_empty
-  static constexpr int kNumBars = 15;
-  static constexpr int kMisc = kBar + kNumBars * 8;                  // tmem slot, flags
+  static constexpr int kQr = 0;                                    // 16 KB
+  static constexpr int kK = kQr + kQChunkBytes;                    // 4 x 40 KB
+  static constexpr int kP = kK + kStages * kStageBytes;            // 16 KB
+  static constexpr int kX = kP + kH * 128;                         // 32 KB
+  static constexpr int kRed = kX + kH * kTok * 4;                  // [2][128] fp32
+  static constexpr int kBar = kRed + 2 * kH * 4;
+  static constexpr int kMisc = align_up_c(kBar + 19 * 8, 16);      // tmem slot, flags
   static constexpr int kPieces = kMisc + 32;
-  static constexpr int kLens = kPieces + kMaxPieces * 4 + 8;         // 16-aligned below
-  __host__ __device__ static int lens_off() { return (kLens + 15) & ~15; }
-  __host__ __device__ static int cum_off(int batch) { return lens_off() + ((batch + 3) & ~3) * 4; }
-  static size_t bytes(int batch) { return 1024 + cum_off(batch) + (batch + 1) * 4 + 16; }
+  static constexpr int kEnd = kPieces + kMaxPieces * 4;
+  static constexpr size_t kBytes = 1024 + static_cast<size_t>(kEnd);
+  static constexpr int kPlanLens = kP;                             // lens[batch]
+  static constexpr int kPlanCum = kP + kMaxBatch * 4;              // cum[batch + 1]
+  static_assert(2 * kMaxBatch * 4 + 4 <= kH * 128, "plan fits the P region");
+  static_assert(kBytes <= 232448, "fits the opt-in shared memory of one SM");
 };
 
-enum Bar { kQFull = 0, kQFree, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kSFull0, kSFull1,
-           kSFree0, kSFree1, kPFull, kPVDone, kXFull, kXEmpty, kDrain };
+// q_full, q_free, k_full[4], k_empty[4], s_full[2], s_free[2], p_full,
+// pv_done, x_full, x_empty, drain
+enum Bar {
+  kQFull = 0, kQFree = 1, kKFull0 = 2, kKEmpty0 = kKFull0 + kStages,
+  kSFull0 = kKEmpty0 + kStages, kSFree0 = kSFull0 + 2, kPFull = kSFree0 + 2, kPVDone,
+  kXFull, kXEmpty, kDrain, kNumBars
+};
+static_assert(kNumBars == 19, "barrier count used by the layout");
+
+// Walks the linear tile order (b, j); len = clamped length of b, base = its
+// first tile.  Past the first tile only the global lengths are read.
+struct MlaCursor {
+  int b, j, n, len;
+  long long base;
+  __device__ __forceinline__ void locate(long long t, const int* cum, const int* lens, int B) {
+    int lo = 0, hi = B - 1;  // largest b with cum[b] <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    base = cum[b];
+    n = cum[b + 1] - cum[b];
+    len = lens[b];
+    j = static_cast<int>(t - base);
+  }
+  __device__ __forceinline__ void advance(const int32_t* seq_lens, int cap, int B) {
+    if (++j < n) return;
+    j = 0;
+    base += n;
+    int L = 0;
+    do {
+      ++b;
+      if (b < B) {
+        L = __ldg(&seq_lens[b]);
+        L = L < 0 ? 0 : (L > cap ? cap : L);
+      }
+    } while (b < B && L == 0);
+    len = L;
+    n = (L + kTok - 1) / kTok;
+  }
+  __device__ __forceinline__ bool last() const { return j == n - 1; }
+};
 
 // Bounded wait that also gives up at once after another role aborted.
 __device__ __forceinline__ bool wait_cta(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -113,45 +170,42 @@ __device__ __forceinline__ bool wait_peer(uint64_t* bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------- producer
-// TMA loads: at each new sequence the CTA's query columns (after the tensor
-// core has finished with the previous ones), then every tile's own key
-// columns, one box per physical block per 64-wide chunk.
-__device__ __forceinline__ void mla_producer(const MlaParams& p, const CUtensorMap* tm_qn,
-                                             const CUtensorMap* tm_qr, const CUtensorMap* tm_cn,
-                                             const CUtensorMap* tm_cr, uint8_t* smem,
-                                             uint64_t* bars, volatile int* abort_flag,
-                                             const int* lens, const int* cum, long long tb,
-                                             long long te, int rank, int lane) {
+// TMA loads: at each new sequence rank 1's rope query columns (after the
+// tensor core has finished with the previous ones), then every tile's own
+// key columns, one box per physical block per 64-wide chunk.
+__device__ __forceinline__ void mla_producer(const MlaParams& p, const CUtensorMap* tm_qr,
+                                             const CUtensorMap* tm_cn, const CUtensorMap* tm_cr,
+                                             uint8_t* smem, uint64_t* bars,
+                                             volatile int* abort_flag, MlaCursor cur, int n_it,
+                                             int rank, int lane) {
   using L = MlaLayout;
   const int nq = rank ? 5 : 4;
-  const int B = p.batch;
-  sched::Cursor cur;
-  cur.locate(tb, cum, B, 1);
+  const int cap = p.max_blocks * p.block_size;
   const int nsub = kTok / p.box_tokens;
   const uint32_t box_bytes = static_cast<uint32_t>(p.box_tokens) * 128u;
   int seg = 0;
-  for (long long t = tb; t < te; ++t) {
-    const int it = static_cast<int>(t - tb);
+  for (int it = 0; it < n_it; ++it) {
     if (it == 0 || cur.j == 0) {
       const bool q_ok = seg == 0 || wait_cta(&bars[kQFree], (seg - 1) & 1, abort_flag, p.err_flag);
-      if (lane == 0 && q_ok) {
-        mbar_arrive_expect_tx(&bars[kQFull], nq * kQChunkBytes);
-        for (int c = 0; c < 4; ++c)
-          tma_load_3d(smem + L::kQ + c * kQChunkBytes, tm_qn, &bars[kQFull], (rank * 4 + c) * 64,
-                      0, cur.b);
-        if (rank) tma_load_3d(smem + L::kQ + 4 * kQChunkBytes, tm_qr, &bars[kQFull], 0, 0, cur.b);
+      if (lane == 0) {
+        if (rank && q_ok) {
+          mbar_arrive_expect_tx(&bars[kQFull], kQChunkBytes);
+          tma_load_3d(smem + L::kQr, tm_qr, &bars[kQFull], 0, 0, cur.b);
+        } else {
+          mbar_arrive(&bars[kQFull]);
+        }
       }
       ++seg;
     }
-    const int stage = it & 1;
-    const int Lb = lens[cur.b];
+    const int stage = it % kStages;
+    const uint32_t phase = static_cast<uint32_t>(it / kStages) & 1u;
     const int tok = cur.j * kTok + lane * p.box_tokens;
     int pb = -1;
-    if (lane < nsub && tok < Lb)
+    if (lane < nsub && tok < cur.len)
       pb = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks + (tok >> p.log2_bs)]);
-    const bool ok = wait_cta(&bars[kKEmpty0 + stage], ((it >> 1) & 1) ^ 1, abort_flag, p.err_flag);
+    const bool ok = wait_cta(&bars[kKEmpty0 + stage], phase ^ 1u, abort_flag, p.err_flag);
     bool valid = false;
-    if (lane < nsub && tok < Lb) {
+    if (lane < nsub && tok < cur.len) {
       if (pb < 0 || pb >= p.num_blocks) set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
       else valid = ok;
     }
@@ -159,107 +213,122 @@ __device__ __forceinline__ void mla_producer(const MlaParams& p, const CUtensorM
     if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull0 + stage], nvalid * box_bytes * nq);
     __syncwarp();
     if (valid) {
-      uint8_t* dst = smem + L::kK + stage * L::kStageBytes + lane * box_bytes;
+      uint8_t* dst = smem + L::kK + stage * kStageBytes + lane * box_bytes;
       const int in_blk = tok & (p.block_size - 1);
       for (int c = 0; c < 4; ++c)
         tma_load_3d(dst + c * kKChunkBytes, tm_cn, &bars[kKFull0 + stage], (rank * 4 + c) * 64,
                     in_blk, pb);
       if (rank) tma_load_3d(dst + 4 * kKChunkBytes, tm_cr, &bars[kKFull0 + stage], 0, in_blk, pb);
     }
-    cur.advance(cum, B, 1);
+    cur.advance(p.seq_lens, cap, p.batch);
   }
 }
 
 // --------------------------------------------------------------- tcgen05
-// S = Q K^T over NQ 64-wide chunks, fully unrolled from two base descriptors.
-template <int NQ>
-__device__ __forceinline__ void mla_issue_s(uint32_t d, uint64_t q0, uint64_t k0, uint32_t idesc) {
+// S = Q K^T for one tile: 16 K-steps over the nope columns with A (the
+// query) in tensor memory, then on rank 1 four K-steps over the rope
+// columns with A in shared memory.  Fully unrolled from base descriptors.
+template <bool kWithRope>
+__device__ __forceinline__ void mla_issue_s(uint32_t d, uint32_t q_tmem, uint64_t qr0, uint64_t k0,
+                                            uint32_t idesc) {
 #pragma unroll
-  for (int c = 0; c < NQ; ++c)
+  for (int k = 0; k < 16; ++k) {
+    const uint64_t b = desc_advance(k0, (k >> 2) * kKChunkBytes + (k & 3) * 32);
+    if (k == 0) umma_f16_ts_fresh(d, q_tmem, b, idesc);
+    else umma_f16_ts_acc(d, q_tmem + k * 8, b, idesc);
+  }
+  if (kWithRope) {
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t a = desc_advance(q0, c * kQChunkBytes + kk * 32);
-      const uint64_t b = desc_advance(k0, c * kKChunkBytes + kk * 32);
-      if (c == 0 && kk == 0) umma_f16_fresh(d, a, b, idesc);
-      else umma_f16_acc(d, a, b, idesc);
-    }
+    for (int kk = 0; kk < 4; ++kk)
+      umma_f16_acc(d, desc_advance(qr0, kk * 32), desc_advance(k0, 4 * kKChunkBytes + kk * 32),
+                   idesc);
+  }
 }
 
-// One thread.  S(t+1) = Q K(t+1)^T is issued before O += P(t) V(t), so the
-// tensor core computes the next scores while the softmax works on P(t).
+// One thread.  Order: S(0), S(1), then per tile t: S(t+2), P V(t).  S runs
+// two tiles ahead so the scores of the next tile are ready when the softmax
+// finishes the exchange of the current one.
 template <bool kBf16>
 __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint64_t* bars,
-                                        volatile int* abort_flag, const int* cum, uint32_t tmem,
-                                        long long tb, long long te, int rank) {
+                                        volatile int* abort_flag, uint32_t tmem, MlaCursor cs,
+                                        int n_it, int rank) {
   using L = MlaLayout;
+  const int cap = p.max_blocks * p.block_size;
   const uint32_t idesc_s = umma_idesc_f16(kBf16, kH, kTok, 0, 0);
   const uint32_t idesc_o = umma_idesc_f16(kBf16, kH, kOutCols, 0, 1);
-  const uint64_t q0 = umma_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+  const uint64_t qr0 = umma_desc_sw128(smem_u32(smem + L::kQr), 16, 1024);
   const uint64_t k0 = umma_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
   const uint64_t p0 = umma_desc_sw128(smem_u32(smem + L::kP), 16, 1024);
   // V = the first four chunks of a stage, MN-major: next 64 columns 8 KB on.
   const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kK), kKChunkBytes, 1024);
-  const int n_it = static_cast<int>(te - tb);
-  sched::Cursor cs;  // tile whose S is issued next
-  cs.locate(tb, cum, p.batch, 1);
   int seg_s = -1;
-  bool first_flags[2] = {false, false};
+  uint32_t first_bits = 0;  // bit (t & 3): tile t starts a sequence's share
 
   auto issue_s = [&](int it) -> bool {
     const bool first = it == 0 || cs.j == 0;
-    const bool last = it == n_it - 1 || cs.j == cs.n - 1;
+    const bool last = it == n_it - 1 || cs.last();
     if (first) ++seg_s;
-    first_flags[it & 1] = first;
-    const int stage = it & 1;
-    if (!wait_cta(&bars[kKFull0 + stage], (it >> 1) & 1, abort_flag, p.err_flag)) return false;
-    if (!wait_cta(&bars[kSFree0 + stage], ((it >> 1) & 1) ^ 1, abort_flag, p.err_flag)) return false;
+    first_bits = (first_bits & ~(1u << (it & 3))) | (first ? 1u << (it & 3) : 0u);
+    const int stage = it % kStages, sb = it & 1;
+    if (!wait_cta(&bars[kKFull0 + stage], static_cast<uint32_t>(it / kStages) & 1u, abort_flag,
+                  p.err_flag))
+      return false;
+    if (!wait_cta(&bars[kSFree0 + sb], ((it >> 1) & 1) ^ 1, abort_flag, p.err_flag)) return false;
     if (!wait_cta(&bars[kQFull], seg_s & 1, abort_flag, p.err_flag)) return false;
     tc_fence_after();
-    const uint32_t d = tmem + (stage ? kTmemS1 : kTmemS0);
-    const uint64_t k_st = desc_advance(k0, stage * L::kStageBytes);
-    if (rank) mla_issue_s<5>(d, q0, k_st, idesc_s);
-    else mla_issue_s<4>(d, q0, k_st, idesc_s);
-    umma_commit(&bars[kSFull0 + stage]);
+    const uint32_t d = tmem + (sb ? kTmemS1 : kTmemS0);
+    const uint64_t k_st = desc_advance(k0, stage * kStageBytes);
+    if (rank) mla_issue_s<true>(d, tmem + kTmemQ, qr0, k_st, idesc_s);
+    else mla_issue_s<false>(d, tmem + kTmemQ, qr0, k_st, idesc_s);
+    umma_commit(&bars[kSFull0 + sb]);
     if (last) umma_commit(&bars[kQFree]);
-    cs.advance(cum, p.batch, 1);
+    cs.advance(p.seq_lens, cap, p.batch);
     return true;
   };
   auto issue_pv = [&](int it) -> bool {
     if (!wait_cta(&bars[kPFull], it & 1, abort_flag, p.err_flag)) return false;
     tc_fence_after();
-    const uint64_t v_st = desc_advance(v0, (it & 1) * L::kStageBytes);
-    if (first_flags[it & 1]) umma_f16_fresh(tmem + kTmemO, p0, v_st, idesc_o);
+    const int stage = it % kStages;
+    const uint64_t v_st = desc_advance(v0, stage * kStageBytes);
+    if ((first_bits >> (it & 3)) & 1u) umma_f16_fresh(tmem + kTmemO, p0, v_st, idesc_o);
     else umma_f16_acc(tmem + kTmemO, p0, v_st, idesc_o);
 #pragma unroll
     for (int ks = 1; ks < kTok / 16; ++ks)
       umma_f16_acc(tmem + kTmemO, desc_advance(p0, ks * 32), desc_advance(v_st, ks * 16 * 128),
                    idesc_o);
     umma_commit(&bars[kPVDone]);
-    umma_commit(&bars[kKEmpty0 + (it & 1)]);
+    umma_commit(&bars[kKEmpty0 + stage]);
     return true;
   };
 
-  if (n_it > 0 && !issue_s(0)) return;
+  for (int it = 0; it < n_it && it < 2; ++it)
+    if (!issue_s(it)) return;
   for (int it = 0; it < n_it; ++it) {
-    if (it + 1 < n_it && !issue_s(it + 1)) return;
+    if (it + 2 < n_it && !issue_s(it + 2)) return;
     if (!issue_pv(it)) return;
   }
 }
 
 // ----------------------------------------------------------- epilogue
-// End of one sequence's share for query row `row` (one thread): write the
-// normalised output columns of this rank, or publish a partial state; the
-// cluster arriving last at a split sequence merges every share (per rank).
+// End of one sequence's share for query row `row`, column half `h` (128 of
+// this rank's 256 output columns): write the normalised output, or publish a
+// partial state; the cluster arriving last at a split sequence merges every
+// share (per rank).  The two halves' partial sums l are added first.
 template <typename T>
-__device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, int row, int b,
-                                        bool complete, int cl, int slot, long long seg0,
+__device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, int row, int h,
+                                        int b, bool complete, int cl, int slot, long long seg0,
                                         int seg_tiles, long long N, int P, int rank, float m_used,
-                                        float l, volatile int* last_flag, volatile int* npieces,
-                                        int* pieces) {
-  T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * kH + row) * kNope + rank * kOutCols;
+                                        float l_half, float* red, volatile int* last_flag,
+                                        volatile int* npieces, int* pieces) {
+  named_bar_sync(1, kSoftmaxThreads);
+  red[h * kH + row] = l_half;
+  named_bar_sync(1, kSoftmaxThreads);
+  const float l = red[row] + red[kH + row];
+  const int col0 = rank * kOutCols + h * 128;
+  T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * kH + row) * kNope + col0;
   if (complete) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    for (int c = 0; c < kOutCols / 16; ++c) {
+    for (int c = 0; c < 8; ++c) {
       float v[16];
       tmem_ld16(o_taddr + c * 16, v);
       tmem_wait_ld();
@@ -273,19 +342,19 @@ __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, in
     return;
   }
   const long long wrow = ((static_cast<long long>(cl) * 2 + slot) * 2 + rank) * kH + row;
-  for (int c = 0; c < kOutCols / 16; ++c) {
+  for (int c = 0; c < 8; ++c) {
     float v[16];
     tmem_ld16(o_taddr + c * 16, v);
     tmem_wait_ld();
-    float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * kOutCols + c * 16);
+    float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * kOutCols + h * 128 + c * 16);
 #pragma unroll
     for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
   }
-  *reinterpret_cast<float2*>(p.ws_ml + wrow * 2) = make_float2(m_used, l);
+  if (h == 0) *reinterpret_cast<float2*>(p.ws_ml + wrow * 2) = make_float2(m_used, l);
   named_bar_sync(1, kSoftmaxThreads);
   const int cfirst = sched::share_of(seg0, N, P), clast = sched::share_of(seg0 + seg_tiles - 1, N, P);
   const int slot0 = sched::share_begin(cfirst, N, P) == seg0 ? 0 : 1;
-  if (row == 0) {
+  if (row == 0 && h == 0) {
     int n = 0;
     long long tb = sched::share_begin(cfirst, N, P);
     for (int cc = cfirst; cc <= clast; ++cc) {
@@ -326,7 +395,7 @@ __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, in
       Ls += fast_exp2(__ldcg(p.ws_ml + r * 2) - M) * __ldcg(p.ws_ml + r * 2 + 1);
     }
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    for (int c = 0; c < kOutCols / 16; ++c) {
+    for (int c = 0; c < 8; ++c) {
       float acc[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) acc[k] = 0.f;
@@ -334,7 +403,7 @@ __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, in
       for (int i = 0; i < n; ++i) {
         const long long r = next_row(i);
         const float f = fast_exp2(__ldcg(p.ws_ml + r * 2) - M);
-        const float4* src = reinterpret_cast<const float4*>(p.ws_o + r * kOutCols + c * 16);
+        const float4* src = reinterpret_cast<const float4*>(p.ws_o + r * kOutCols + h * 128 + c * 16);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float4 v = __ldcg(src + k);
@@ -351,159 +420,211 @@ __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, in
       *reinterpret_cast<uint4*>(out + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4*>(out + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
     }
-    if (row == 0) p.ws_cnt[(cfirst * 2 + slot0) * 2 + rank] = 0;
   }
   named_bar_sync(1, kSoftmaxThreads);
+  if (*last_flag && row == 0 && h == 0) p.ws_cnt[(cfirst * 2 + slot0) * 2 + rank] = 0;
 }
 
 // --------------------------------------------------------------- softmax
-// Warps 0-3; thread `row` owns query head `row` (TMEM lane `row`).
+// This CTA's 256 nope query columns of sequence b, row `row`, half `h`
+// (128 columns = 64 packed TMEM columns) -> tensor memory.
+template <typename T>
+__device__ __forceinline__ void mla_load_q(const MlaParams& p, uint32_t lane_base, int b, int row,
+                                           int h, int rank) {
+  const uint4* src = reinterpret_cast<const uint4*>(
+      static_cast<const T*>(p.q_nope) + (static_cast<long long>(b) * kH + row) * kNope +
+      rank * kOutCols + h * 128);
+  uint4 v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __ldg(src + i);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    tmem_st16_u32(lane_base + kTmemQ + h * 64 + c * 16, reinterpret_cast<const uint32_t*>(v + 4 * c));
+  tmem_wait_st();
+}
+
+// Warps 0-7: thread (row, h) owns query head `row` (TMEM lane `row`) and
+// tokens / output columns of half h.  Iteration `it` (1) sends this CTA's
+// partial scores of tile `it` to the other CTA straight from TMEM, (2) runs
+// the softmax of tile `it-1` and hands its P to the tensor core, and (3)
+// completes the exchange of tile `it`, so the round trip through distributed
+// shared memory overlaps the softmax math.  The scores travel as st.async
+// stores that complete the receiver's x_full transaction count (no fence on
+// the sender); x_empty is a relaxed arrive after the reads are consumed.
 template <typename T>
 __device__ __forceinline__ void mla_softmax(const MlaParams& p, uint8_t* smem, uint64_t* bars,
                                             volatile int* abort_flag, volatile int* last_flag,
-                                            volatile int* npieces, int* pieces, const int* lens,
-                                            const int* cum, uint32_t tmem, long long tb,
-                                            long long te, long long N, int P, int cl, int rank,
-                                            int row) {
+                                            volatile int* npieces, int* pieces, uint32_t tmem,
+                                            MlaCursor cx, int n_it, long long N, int P, int cl,
+                                            int rank, int row, int h) {
   using L = MlaLayout;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>((row >> 5) * 32) << 16);
+  const int cap = p.max_blocks * p.block_size;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(row & ~31) << 16);
   const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
   const uint32_t x_peer = map_to_rank(smem_u32(smem + L::kX), peer);
   const uint32_t xfull_peer = map_to_rank(smem_u32(&bars[kXFull]), peer);
   const uint32_t xempty_peer = map_to_rank(smem_u32(&bars[kXEmpty]), peer);
   const float4* x_mine = reinterpret_cast<const float4*>(smem + L::kX);
-  sched::Cursor cur;
-  cur.locate(tb, cum, p.batch, 1);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
+  const bool elected = row == 0 && h == 0;
+  MlaCursor cm = cx;  // tile whose softmax runs next (one behind the exchange)
   float m_used = -INFINITY, l = 0.f;
-  int seg_first_j = cur.j, slot = 0;
-  for (long long t = tb; t < te; ++t) {
-    const int it = static_cast<int>(t - tb);
-    const bool first = it == 0 || cur.j == 0;
-    const bool last = t == te - 1 || cur.j == cur.n - 1;
-    if (first) {
-      m_used = -INFINITY;
-      l = 0.f;
-      seg_first_j = cur.j;
-    }
-    const int stage = it & 1;
-    const int valid = min(kTok, lens[cur.b] - cur.j * kTok);
+  int seg_first_j = cm.j, slot = 0, seg_x = 0;
+  float sp[32];  // summed scores of tile it-1, this thread's 32 tokens
 
-    // 1. This CTA's partial scores (the collective TMEM reads run even after
-    //    an abort; only the waits give up).
-    float s[kTok];
-    wait_cta(&bars[kSFull0 + stage], (it >> 1) & 1, abort_flag, p.err_flag);
-    tc_fence_after();
-#pragma unroll
-    for (int c = 0; c < kTok / 16; ++c)
-      tmem_ld16(lane_base + (stage ? kTmemS1 : kTmemS0) + c * 16, s + c * 16);
-    tmem_wait_ld();
-    tc_fence_before();
-    mbar_arrive(&bars[kSFree0 + stage]);
+  // Query of the first sequence (tensor memory is fresh).
+  mla_load_q<T>(p, lane_base, cx.b, row, h, rank);
+  tc_fence_before();
+  mbar_arrive(&bars[kQFull]);
 
-    // 2. Exchange partial scores with the other CTA of the pair and sum them.
-    //    One elected thread signals after a CTA barrier: its cluster-scope
-    //    release covers every thread's remote stores before it.
-    wait_peer(&bars[kXEmpty], (it & 1) ^ 1, abort_flag, p.err_flag);
-#pragma unroll
-    for (int q = 0; q < kTok / 4; ++q)
-      st_cluster_v4(x_peer + (q * kH + row) * 16,
-                    make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]));
-    named_bar_sync(2, kSoftmaxThreads);
-    if (row == 0) mbar_arrive_cluster(xfull_peer);
-    wait_peer(&bars[kXFull], it & 1, abort_flag, p.err_flag);
-#pragma unroll
-    for (int q = 0; q < kTok / 4; ++q) {
-      const float4 v = x_mine[q * kH + row];
-      s[4 * q] += v.x;
-      s[4 * q + 1] += v.y;
-      s[4 * q + 2] += v.z;
-      s[4 * q + 3] += v.w;
-    }
-    named_bar_sync(2, kSoftmaxThreads);
-    if (row == 0) mbar_arrive_cluster(xempty_peer);
-
-    // 3. Online softmax in the log2 domain; O is rescaled only when the
-    //    running max grows by more than 2^kRescaleThreshold.
-    float mx = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kTok; ++k) {
-      s[k] = k < valid ? s[k] * p.scale_log2 : -INFINITY;
-      mx = fmaxf(mx, s[k]);
-    }
-    float corr = 1.f;
-    bool rescale = false;
-    if (m_used == -INFINITY) {
-      m_used = mx;
-      corr = 0.f;
-    } else if (mx > m_used + kRescaleThreshold) {
-      corr = fast_exp2(m_used - mx);
-      m_used = mx;
-      rescale = true;
-    }
-    uint32_t pk[kTok / 2];
-    float ps = 0.f, ra, rb;
-#pragma unroll
-    for (int k = 0; k < kTok / 2; ++k) {
-      pk[k] = Pack<T>::run(fast_exp2(s[2 * k] - m_used), fast_exp2(s[2 * k + 1] - m_used), ra, rb);
-      ps += ra + rb;
-    }
-    l = l * corr + ps;
-
-    // 4. The previous P V must be finished before P and O are touched.
-    if (it > 0) {
-      wait_cta(&bars[kPVDone], (it - 1) & 1, abort_flag, p.err_flag);
+  for (int it = 0; it <= n_it; ++it) {
+    const int sb = it & 1;
+    if (it < n_it) {
+      // (1) Own partial scores of tile `it` -> the other CTA.
+      wait_cta(&bars[kSFull0 + sb], (it >> 1) & 1, abort_flag, p.err_flag);
       tc_fence_after();
-    }
-    if (__any_sync(0xffffffffu, rescale)) {
-      for (int c = 0; c < kOutCols / 16; ++c) {
+      wait_peer(&bars[kXEmpty], (it & 1) ^ 1, abort_flag, p.err_flag);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
         float v[16];
-        tmem_ld16(lane_base + kTmemO + c * 16, v);
+        tmem_ld16(lane_base + (sb ? kTmemS1 : kTmemS0) + h * 32 + c * 16, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] *= corr;
-        tmem_st16(lane_base + kTmemO + c * 16, v);
+        for (int q = 0; q < 4; ++q)
+          st_async_cluster_v4(x_peer + ((h * 8 + c * 4 + q) * kH + row) * 16,
+                              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]),
+                              xfull_peer);
       }
-      tmem_wait_st();
+      // Tile it+1 starts the next sequence: its query replaces this one once
+      // the tensor core is done with it (S(it) complete => all its S done).
+      if (it + 1 < n_it && cx.last()) {
+        wait_cta(&bars[kQFree], seg_x & 1, abort_flag, p.err_flag);
+        tc_fence_after();
+        MlaCursor nx = cx;
+        nx.advance(p.seq_lens, cap, p.batch);
+        mla_load_q<T>(p, lane_base, nx.b, row, h, rank);
+        tc_fence_before();
+        mbar_arrive(&bars[kQFull]);
+        ++seg_x;
+      }
+      cx.advance(p.seq_lens, cap, p.batch);
     }
-
-    // 5. P row -> shared memory (K-major, 128-byte swizzle); zero the value
-    //    rows past the sequence so stale cache contents cannot reach P V.
-    uint8_t* sp = smem + L::kP;
+    if (it > 0) {
+      // (2) Softmax of tile it-1 (log2 domain; O rescaled only when the
+      //     running max grows by more than 2^kRescaleThreshold).
+      const int pit = it - 1;
+      const bool first = pit == 0 || cm.j == 0;
+      const bool last = pit == n_it - 1 || cm.last();
+      if (first) {
+        m_used = -INFINITY;
+        l = 0.f;
+        seg_first_j = cm.j;
+      }
+      const int valid = min(kTok, cm.len - cm.j * kTok) - h * 32;  // of this thread's 32
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-      *reinterpret_cast<uint4*>(sp + swz128(row, ch)) =
-          make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-    if (valid < kTok) {
-      uint8_t* kst = smem + L::kK + stage * L::kStageBytes;
-      const int n16 = (kTok - valid) * 4 * 8;
-      for (int e = row; e < n16; e += kSoftmaxThreads) {
-        const int r = valid + e / 32, c = (e % 32) / 8, q = e % 8;
-        *reinterpret_cast<uint4*>(kst + c * kKChunkBytes + r * 128 + q * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
+      for (int k = 0; k < 32; ++k) {
+        sp[k] = k < valid ? sp[k] * p.scale_log2 : -INFINITY;
+        mx4[k & 3] = fmaxf(mx4[k & 3], sp[k]);
+      }
+      red[h * kH + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      named_bar_sync(3, kSoftmaxThreads);
+      const float mx = fmaxf(red[row], red[kH + row]);  // same order in both halves
+      float corr = 1.f;
+      bool rescale = false;
+      if (m_used == -INFINITY) {
+        m_used = mx;
+        corr = 0.f;
+      } else if (mx > m_used + kRescaleThreshold) {
+        corr = fast_exp2(m_used - mx);
+        m_used = mx;
+        rescale = true;
+      }
+      uint32_t pk[16];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f}, ra, rb;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        pk[k] = Pack<T>::run(fast_exp2(sp[2 * k] - m_used), fast_exp2(sp[2 * k + 1] - m_used), ra, rb);
+        ps[k & 3] += ra + rb;
+      }
+      l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      if (pit > 0) {  // P V of tile it-2 must be done before P and O are touched
+        wait_cta(&bars[kPVDone], (pit - 1) & 1, abort_flag, p.err_flag);
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        for (int c = 0; c < 8; ++c) {
+          float v[16];
+          tmem_ld16(lane_base + kTmemO + h * 128 + c * 16, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] *= corr;
+          tmem_st16(lane_base + kTmemO + h * 128 + c * 16, v);
+        }
+        tmem_wait_st();
+      }
+      // P row half -> shared memory (K-major, 128-byte swizzle); the value
+      // rows past the sequence are zeroed so stale contents cannot reach P V.
+      uint8_t* pptr = smem + L::kP;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4*>(pptr + swz128(row, h * 4 + ch)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      const int tile_valid = min(kTok, cm.len - cm.j * kTok);
+      if (tile_valid < kTok) {
+        uint8_t* kst = smem + L::kK + (pit % kStages) * kStageBytes;
+        const int n16 = (kTok - tile_valid) * 4 * 8;
+        for (int e = h * kH + row; e < n16; e += kSoftmaxThreads) {
+          const int r = tile_valid + e / 32, c = (e % 32) / 8, q = e % 8;
+          *reinterpret_cast<uint4*>(kst + c * kKChunkBytes + r * 128 + q * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[kPFull]);
+      if (last) {  // end of this sequence's share
+        wait_cta(&bars[kPVDone], pit & 1, abort_flag, p.err_flag);
+        tc_fence_after();
+        mla_finish<T>(p, lane_base + kTmemO + h * 128, row, h, cm.b,
+                      seg_first_j == 0 && cm.last(), cl, slot, cm.base, cm.n, N, P, rank, m_used,
+                      l, red, last_flag, npieces, pieces);
+        tc_fence_before();
+        slot = 1;
+      }
+      cm.advance(p.seq_lens, cap, p.batch);
+    }
+    if (it < n_it) {
+      // (3) Complete the exchange of tile `it`: own partial (re-read from
+      //     TMEM) + the other CTA's, then free both buffers.
+      wait_peer(&bars[kXFull], it & 1, abort_flag, p.err_flag);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        tmem_ld16(lane_base + (sb ? kTmemS1 : kTmemS0) + h * 32 + c * 16, sp + c * 16);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars[kSFree0 + sb]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 v = x_mine[(h * 8 + q) * kH + row];
+        sp[4 * q] += v.x;
+        sp[4 * q + 1] += v.y;
+        sp[4 * q + 2] += v.z;
+        sp[4 * q + 3] += v.w;
+      }
+      named_bar_sync(2, kSoftmaxThreads);
+      if (elected) {
+        // Next tile's scores arrive as 32 KB of transactions on x_full.
+        if (it + 1 < n_it) mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 4);
+        mbar_arrive_cluster_relaxed(xempty_peer);
       }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    mbar_arrive(&bars[kPFull]);
-
-    // 6. End of this sequence's share.
-    if (last) {
-      wait_cta(&bars[kPVDone], it & 1, abort_flag, p.err_flag);
-      tc_fence_after();
-      mla_finish<T>(p, lane_base + kTmemO, row, cur.b, seg_first_j == 0 && cur.j == cur.n - 1, cl,
-                    slot, static_cast<long long>(cum[cur.b]), cur.n, N, P, rank, m_used, l,
-                    last_flag, npieces, pieces);
-      tc_fence_before();
-      slot = 1;
-    }
-    cur.advance(cum, p.batch, 1);
   }
 }
 
 template <typename T, bool kBf16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_qn,
-                      const __grid_constant__ CUtensorMap tm_qr,
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_qr,
                       const __grid_constant__ CUtensorMap tm_cn,
                       const __grid_constant__ CUtensorMap tm_cr,
                       const __grid_constant__ MlaParams p) {
@@ -517,8 +638,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* last_flag = abort_flag + 1;
   volatile int* npieces = abort_flag + 2;
   int* pieces = reinterpret_cast<int*>(smem + L::kPieces);
-  int* lens = reinterpret_cast<int*>(smem + L::lens_off());
-  int* cum = reinterpret_cast<int*>(smem + L::cum_off(p.batch));
+  int* lens = reinterpret_cast<int*>(smem + L::kPlanLens);
+  int* cum = reinterpret_cast<int*>(smem + L::kPlanCum);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = static_cast<int>(cluster_ctarank());
@@ -526,15 +647,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int B = p.batch, cap = p.max_blocks * p.block_size;
 
   if (tid == 0) {
-    const uint32_t counts[L::kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, kSoftmaxThreads,
-                                          kSoftmaxThreads, kSoftmaxThreads, 1, 1, 1, 1};
-    for (int i = 0; i < L::kNumBars; ++i) mbar_init(&bars[i], counts[i]);
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t c = 1;
+      if (i == kQFull) c = 1 + kSoftmaxThreads;
+      if (i == kSFree0 || i == kSFree0 + 1 || i == kPFull) c = kSoftmaxThreads;
+      mbar_init(&bars[i], c);
+    }
     *abort_flag = 0;
     fence_barrier_init();
+    // The first tile's scores from the other CTA arrive as 32 KB of
+    // transactions on x_full (harmless if this cluster has no tile).
+    mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 4);
   }
-  if (warp == 5) tmem_alloc(tslot, kTmemCols);
-  if (warp == 4 && lane == 0) {
-    prefetch_tmap(&tm_qn);
+  if (warp == kMmaWarp) tmem_alloc(tslot, kTmemCols);
+  if (warp == kProducerWarp && lane == 0) {
     prefetch_tmap(&tm_qr);
     prefetch_tmap(&tm_cn);
     prefetch_tmap(&tm_cr);
@@ -558,31 +684,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           out[(static_cast<long long>(b) * kH + e / kOutCols) * kNope + rank * kOutCols +
               e % kOutCols] = Pack<T>::cvt(0.f);
   }
-  if (tb < te) {
-    if (warp < 4) {
-      mla_softmax<T>(p, smem, bars, abort_flag, last_flag, npieces, pieces, lens, cum, tmem, tb, te,
-                     N, P, cl, rank, tid);
-    } else if (warp == 4) {
-      mla_producer(p, &tm_qn, &tm_qr, &tm_cn, &tm_cr, smem, bars, abort_flag, lens, cum, tb, te,
-                   rank, lane);
+  MlaCursor cur;
+  if (tb < te) cur.locate(tb, cum, lens, B);
+  __syncthreads();  // the plan (in the P region) is not read past this point
+  const int n_it = static_cast<int>(te - tb);
+  if (n_it > 0) {
+    if (warp < kSoftmaxWarps) {
+      mla_softmax<T>(p, smem, bars, abort_flag, last_flag, npieces, pieces, tmem, cur, n_it, N, P,
+                     cl, rank, (warp & 3) * 32 + lane, warp >> 2);
+    } else if (warp == kProducerWarp) {
+      mla_producer(p, &tm_qr, &tm_cn, &tm_cr, smem, bars, abort_flag, cur, n_it, rank, lane);
       // Every copy issued must land before shared memory can be released.
-      const int n_it = static_cast<int>(te - tb);
       for (int it = max(0, n_it - kStages); it < n_it; ++it)
-        mbar_wait_bounded(&bars[kKFull0 + (it & 1)], (it >> 1) & 1, p.err_flag);
+        mbar_wait_bounded(&bars[kKFull0 + it % kStages], static_cast<uint32_t>(it / kStages) & 1u,
+                          p.err_flag);
     } else if (lane == 0) {
-      mla_mma<kBf16>(p, smem, bars, abort_flag, cum, tmem, tb, te, rank);
+      mla_mma<kBf16>(p, smem, bars, abort_flag, tmem, cur, n_it, rank);
     }
   }
   // Teardown: all tensor-core work done, TMEM freed, and neither CTA leaves
   // while its partner may still write into its shared memory.
-  if (warp == 5 && lane == 0) {
+  if (warp == kMmaWarp && lane == 0) {
     umma_commit(&bars[kDrain]);
     mbar_wait_bounded(&bars[kDrain], 0, p.err_flag);
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -602,12 +731,10 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(mla_decode_kernel<T, kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(MlaLayout::bytes(kMaxBatch)));
+                         static_cast<int>(MlaLayout::kBytes));
   });
   const int box_tokens = a.block_size < kTok ? a.block_size : kTok;
-  CUtensorMap qn, qr, cn, cr;
-  const uint64_t qn_dims[3] = {kNope, kH, static_cast<uint64_t>(a.batch)};
-  const uint64_t qn_str[2] = {kNope * 2, static_cast<uint64_t>(kH) * kNope * 2};
+  CUtensorMap qr, cn, cr;
   const uint64_t qr_dims[3] = {kRope, kH, static_cast<uint64_t>(a.batch)};
   const uint64_t qr_str[2] = {kRope * 2, static_cast<uint64_t>(kH) * kRope * 2};
   const uint32_t qbox[3] = {64, kH, 1};
@@ -618,13 +745,13 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
                                static_cast<uint64_t>(a.num_blocks)};
   const uint64_t cr_str[2] = {kRope * 2, static_cast<uint64_t>(a.block_size) * kRope * 2};
   const uint32_t cbox[3] = {64, static_cast<uint32_t>(box_tokens), 1};
-  if (!encode_tmap_16bit(&qn, a.dtype, 3, a.q_nope, qn_dims, qn_str, qbox, true) ||
-      !encode_tmap_16bit(&qr, a.dtype, 3, a.q_rope, qr_dims, qr_str, qbox, true) ||
+  if (!encode_tmap_16bit(&qr, a.dtype, 3, a.q_rope, qr_dims, qr_str, qbox, true) ||
       !encode_tmap_16bit(&cn, a.dtype, 3, a.cache_nope, cn_dims, cn_str, cbox, true) ||
       !encode_tmap_16bit(&cr, a.dtype, 3, a.cache_rope, cr_dims, cr_str, cbox, true))
     return KVC_ERR_CUDA;
   MlaParams p;
   p.out = a.out;
+  p.q_nope = a.q_nope;
   p.block_table = a.block_table;
   p.seq_lens = a.seq_lens;
   p.ws_cnt = static_cast<int*>(a.workspace);
@@ -638,8 +765,8 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
   p.num_blocks = a.num_blocks;
   p.box_tokens = box_tokens;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  mla_decode_kernel<T, kBf16><<<2 * clusters, kThreads, MlaLayout::bytes(a.batch), a.stream>>>(
-      qn, qr, cn, cr, p);
+  mla_decode_kernel<T, kBf16><<<2 * clusters, kThreads, MlaLayout::kBytes, a.stream>>>(qr, cn, cr,
+                                                                                       p);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
