@@ -214,8 +214,9 @@ kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* 
                                     kvc_dtype dtype, uint32_t* err_flag, kvc_stream_t stream);
 
 /*
- * Bytes of workspace kvc_mla_paged_decode needs with `num_ctas` CTAs (0 = one
- * CTA per SM of the current device; an odd count is rounded down to pairs).
+ * Bytes of workspace kvc_mla_paged_decode needs with `num_ctas` CTAs (0 = as
+ * many CTA pairs as the current device holds resident at once, at most one
+ * CTA per SM; an odd count is rounded down to pairs).
  * Returns 0 for an unsupported shape.
  */
 size_t kvc_mla_paged_decode_workspace_size(int num_heads, int d_nope, int d_rope, int num_ctas);
@@ -238,10 +239,9 @@ size_t kvc_mla_paged_decode_workspace_size(int num_heads, int d_nope, int d_rope
  * seq_lens int32 [batch].  Supported: num_heads 128, d_nope 512, d_rope 64,
  * block_size a power of two >= 8, batch <= 1024; fp16 or bf16.
  * Runs on CTA pairs (thread-block clusters of 2); long sequences are split
- * over the pairs and merged inside the kernel.  workspace: device,
- * >= kvc_mla_paged_decode_workspace_size bytes, zero-filled before first use
- * and left zero-filled by every call (re-zero after KVC_FLAG_WAIT_TIMEOUT);
- * calls that overlap on the GPU must not share it.
+ * over the pairs, and a second kernel on the same stream merges the pieces.
+ * workspace: device, >= kvc_mla_paged_decode_workspace_size bytes, needs no
+ * initialisation; calls that overlap on the GPU must not share it.
  */
 kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
                                 const void* cache_rope, const int32_t* block_table,

@@ -231,8 +231,7 @@ def mla_paged_decode(q_nope: torch.Tensor, q_rope: torch.Tensor, cache_nope: tor
                      err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
     """MLA decode: q_nope [B, 128, 512], q_rope [B, 128, 64] over the latent caches.
 
-    ``workspace`` (uint8, >= mla_workspace_size bytes) must be zero-filled
-    before its first use; each call leaves it zero-filled.
+    ``workspace`` (uint8, >= mla_workspace_size bytes) needs no initialisation.
     """
     _cuda("q_nope", q_nope)
     _cuda("q_rope", q_rope, q_nope.dtype)
@@ -246,7 +245,7 @@ def mla_paged_decode(q_nope: torch.Tensor, q_rope: torch.Tensor, cache_nope: tor
         out = torch.empty_like(q_nope)
     _cuda("out", out, q_nope.dtype)
     if workspace is None:
-        workspace = torch.zeros(max(mla_workspace_size(num_ctas), 16), dtype=torch.uint8,
+        workspace = torch.empty(max(mla_workspace_size(num_ctas), 16), dtype=torch.uint8,
                                 device=q_nope.device)
     _cuda("workspace", workspace)
     _check("kvc_mla_paged_decode", lib().kvc_mla_paged_decode(

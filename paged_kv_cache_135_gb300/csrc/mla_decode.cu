@@ -31,8 +31,8 @@
 // scores travel to the other CTA, the softmax of tile t-1 runs, and the
 // tensor core computes S two tiles ahead of P V.
 // Work: 64-token tiles of all sequences in one linear order, split evenly
-// over the clusters (stream-K split-KV); the cluster that finishes a split
-// sequence last merges the partial states (per rank), as in the GQA decode.
+// over the clusters (stream-K split-KV); pieces of split sequences leave
+// partial states that a small second kernel (mla_merge_kernel) combines.
 // Roles per CTA: warps 0-7 softmax / epilogue (warp w reads TMEM lanes
 // 32*(w%4).., column half w/4), warp 8 TMA producer, warp 9 tcgen05 issuer
 // (one thread) and TMEM owner.
@@ -65,7 +65,6 @@ constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kThreads = kSoftmaxThreads + 64;
 constexpr int kMaxBatch = 1024;
-constexpr int kMaxPieces = 62;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
 // TMEM columns: O (256 fp32), two S buffers (64 fp32 each), then the CTA's
@@ -78,7 +77,7 @@ struct MlaParams {
   const void* q_nope;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  int* ws_cnt;    // [clusters][2 slots][2 ranks]
+  int* ws_plan;   // [batch + 1] tiles before each sequence (written by CTA 0)
   float* ws_o;    // [clusters][2][2][128][256]
   float* ws_ml;   // [clusters][2][2][128][2]
   uint32_t* err_flag;
@@ -100,8 +99,7 @@ struct MlaLayout {
   static constexpr int kRed = kX + kH * kTok * 4;                  // [2][128] fp32
   static constexpr int kBar = kRed + 2 * kH * 4;
   static constexpr int kMisc = align_up_c(kBar + 19 * 8, 16);      // tmem slot, flags
-  static constexpr int kPieces = kMisc + 32;
-  static constexpr int kEnd = kPieces + kMaxPieces * 4;
+  static constexpr int kEnd = kMisc + 32;
   static constexpr size_t kBytes = 1024 + static_cast<size_t>(kEnd);
   static constexpr int kPlanLens = kP;                             // lens[batch]
   static constexpr int kPlanCum = kP + kMaxBatch * 4;              // cum[batch + 1]
@@ -311,22 +309,21 @@ __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint6
 
 // ----------------------------------------------------------- epilogue
 // End of one sequence's share for query row `row`, column half `h` (128 of
-// this rank's 256 output columns): write the normalised output, or publish a
-// partial state; the cluster arriving last at a split sequence merges every
-// share (per rank).  The two halves' partial sums l are added first.
+// this rank's 256 output columns).  The two halves' partial sums l are added
+// first.  A sequence the share holds whole is normalised and written out; a
+// piece of a split sequence publishes its partial state (m, l, unnormalised
+// O) in workspace slot (cluster, slot, rank) for mla_merge_kernel.
 template <typename T>
 __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, int row, int h,
-                                        int b, bool complete, int cl, int slot, long long seg0,
-                                        int seg_tiles, long long N, int P, int rank, float m_used,
-                                        float l_half, float* red, volatile int* last_flag,
-                                        volatile int* npieces, int* pieces) {
+                                        int b, bool complete, int cl, int slot, int rank,
+                                        float m_used, float l_half, float* red) {
   named_bar_sync(1, kSoftmaxThreads);
   red[h * kH + row] = l_half;
   named_bar_sync(1, kSoftmaxThreads);
   const float l = red[row] + red[kH + row];
-  const int col0 = rank * kOutCols + h * 128;
-  T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * kH + row) * kNope + col0;
   if (complete) {
+    T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * kH + row) * kNope +
+             rank * kOutCols + h * 128;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     for (int c = 0; c < 8; ++c) {
       float v[16];
@@ -351,78 +348,6 @@ __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, in
     for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
   }
   if (h == 0) *reinterpret_cast<float2*>(p.ws_ml + wrow * 2) = make_float2(m_used, l);
-  named_bar_sync(1, kSoftmaxThreads);
-  const int cfirst = sched::share_of(seg0, N, P), clast = sched::share_of(seg0 + seg_tiles - 1, N, P);
-  const int slot0 = sched::share_begin(cfirst, N, P) == seg0 ? 0 : 1;
-  if (row == 0 && h == 0) {
-    int n = 0;
-    long long tb = sched::share_begin(cfirst, N, P);
-    for (int cc = cfirst; cc <= clast; ++cc) {
-      const long long te = sched::share_begin(cc + 1, N, P);
-      if (tb < te) {
-        if (n < kMaxPieces) pieces[n] = cc * 2 + (cc == cfirst ? slot0 : 0);
-        ++n;
-      }
-      tb = te;
-    }
-    *npieces = n;
-    *last_flag =
-        atomic_add_acq_rel(&p.ws_cnt[(cfirst * 2 + slot0) * 2 + rank], 1) == n - 1 ? 1 : 0;
-  }
-  named_bar_sync(1, kSoftmaxThreads);
-  if (*last_flag) {
-    __threadfence();
-    const int n = *npieces;
-    // Workspace row of every share in CTA order: from the shared-memory list,
-    // or (very many shares) by walking the cluster range again.
-    const bool listed = n <= kMaxPieces;
-    int cc = cfirst;
-    auto next_row = [&](int i) -> long long {
-      if (listed) return (static_cast<long long>(pieces[i]) * 2 + rank) * kH + row;
-      while (sched::share_begin(cc, N, P) == sched::share_begin(cc + 1, N, P)) ++cc;
-      const long long r =
-          ((static_cast<long long>(cc) * 2 + (cc == cfirst ? slot0 : 0)) * 2 + rank) * kH + row;
-      ++cc;
-      return r;
-    };
-    float M = -INFINITY;
-    cc = cfirst;
-    for (int i = 0; i < n; ++i) M = fmaxf(M, __ldcg(p.ws_ml + next_row(i) * 2));
-    float Ls = 0.f;
-    cc = cfirst;
-    for (int i = 0; i < n; ++i) {
-      const long long r = next_row(i);
-      Ls += fast_exp2(__ldcg(p.ws_ml + r * 2) - M) * __ldcg(p.ws_ml + r * 2 + 1);
-    }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    for (int c = 0; c < 8; ++c) {
-      float acc[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-      cc = cfirst;
-      for (int i = 0; i < n; ++i) {
-        const long long r = next_row(i);
-        const float f = fast_exp2(__ldcg(p.ws_ml + r * 2) - M);
-        const float4* src = reinterpret_cast<const float4*>(p.ws_o + r * kOutCols + h * 128 + c * 16);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 v = __ldcg(src + k);
-          acc[4 * k] += f * v.x;
-          acc[4 * k + 1] += f * v.y;
-          acc[4 * k + 2] += f * v.z;
-          acc[4 * k + 3] += f * v.w;
-        }
-      }
-      uint32_t w[8];
-      float ra, rb;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) w[k] = Pack<T>::run(acc[2 * k] * inv, acc[2 * k + 1] * inv, ra, rb);
-      *reinterpret_cast<uint4*>(out + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(out + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-  }
-  named_bar_sync(1, kSoftmaxThreads);
-  if (*last_flag && row == 0 && h == 0) p.ws_cnt[(cfirst * 2 + slot0) * 2 + rank] = 0;
 }
 
 // --------------------------------------------------------------- softmax
@@ -453,10 +378,8 @@ __device__ __forceinline__ void mla_load_q(const MlaParams& p, uint32_t lane_bas
 // the sender); x_empty is a relaxed arrive after the reads are consumed.
 template <typename T>
 __device__ __forceinline__ void mla_softmax(const MlaParams& p, uint8_t* smem, uint64_t* bars,
-                                            volatile int* abort_flag, volatile int* last_flag,
-                                            volatile int* npieces, int* pieces, uint32_t tmem,
-                                            MlaCursor cx, int n_it, long long N, int P, int cl,
-                                            int rank, int row, int h) {
+                                            volatile int* abort_flag, uint32_t tmem, MlaCursor cx,
+                                            int n_it, int cl, int rank, int row, int h) {
   using L = MlaLayout;
   const int cap = p.max_blocks * p.block_size;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(row & ~31) << 16);
@@ -587,8 +510,7 @@ __device__ __forceinline__ void mla_softmax(const MlaParams& p, uint8_t* smem, u
         wait_cta(&bars[kPVDone], pit & 1, abort_flag, p.err_flag);
         tc_fence_after();
         mla_finish<T>(p, lane_base + kTmemO + h * 128, row, h, cm.b,
-                      seg_first_j == 0 && cm.last(), cl, slot, cm.base, cm.n, N, P, rank, m_used,
-                      l, red, last_flag, npieces, pieces);
+                      seg_first_j == 0 && cm.last(), cl, slot, rank, m_used, l, red);
         tc_fence_before();
         slot = 1;
       }
@@ -635,9 +557,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-  volatile int* last_flag = abort_flag + 1;
-  volatile int* npieces = abort_flag + 2;
-  int* pieces = reinterpret_cast<int*>(smem + L::kPieces);
   int* lens = reinterpret_cast<int*>(smem + L::kPlanLens);
   int* cum = reinterpret_cast<int*>(smem + L::kPlanCum);
 
@@ -670,6 +589,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) sched::plan_tiles(lens, cum, B, kTok, lane);
   tc_fence_before();
   __syncthreads();
+  if (blockIdx.x == 0)  // the plan, for the merge of split sequences
+    for (int i = tid; i <= B; i += kThreads) p.ws_plan[i] = cum[i];
   tc_fence_after();
   cluster_sync();  // both CTAs' barriers exist before any remote arrive
 
@@ -690,8 +611,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int n_it = static_cast<int>(te - tb);
   if (n_it > 0) {
     if (warp < kSoftmaxWarps) {
-      mla_softmax<T>(p, smem, bars, abort_flag, last_flag, npieces, pieces, tmem, cur, n_it, N, P,
-                     cl, rank, (warp & 3) * 32 + lane, warp >> 2);
+      mla_softmax<T>(p, smem, bars, abort_flag, tmem, cur, n_it, cl, rank, (warp & 3) * 32 + lane,
+                     warp >> 2);
     } else if (warp == kProducerWarp) {
       mla_producer(p, &tm_qr, &tm_cn, &tm_cr, smem, bars, abort_flag, cur, n_it, rank, lane);
       // Every copy issued must land before shared memory can be released.
@@ -718,21 +639,128 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
 }
 
+// ------------------------------------------------------- split merge
+// One CTA per (sequence, 128 output columns), one thread per query head:
+// sequences split over several clusters combine their partial states,
+//   out = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i,   M = max_i m_i,
+// reading the pieces in cluster order (deterministic).  Sequences held whole
+// by one cluster were written by the decode kernel and are skipped.
+struct MlaMergeParams {
+  void* out;
+  const int* plan;
+  const float* ws_o;
+  const float* ws_ml;
+  int batch, clusters;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ MlaMergeParams m) {
+  const int b = blockIdx.x, q = blockIdx.y, row = threadIdx.x;
+  const int rank = q >> 1, col0 = (q & 1) * 128;
+  const long long seg0 = m.plan[b], n = m.plan[b + 1] - seg0;
+  if (n <= 0) return;
+  const long long N = m.plan[m.batch];
+  const int P = m.clusters;
+  const int cfirst = sched::share_of(seg0, N, P), clast = sched::share_of(seg0 + n - 1, N, P);
+  if (cfirst == clast) return;
+  const int slot0 = sched::share_begin(cfirst, N, P) == seg0 ? 0 : 1;
+  auto piece_row = [&](int cc) -> long long {
+    return ((static_cast<long long>(cc) * 2 + (cc == cfirst ? slot0 : 0)) * 2 + rank) * kH + row;
+  };
+  auto non_empty = [&](int cc) {
+    return sched::share_begin(cc, N, P) < sched::share_begin(cc + 1, N, P);
+  };
+  float M = -INFINITY;
+  for (int cc = cfirst; cc <= clast; ++cc)
+    if (non_empty(cc)) M = fmaxf(M, __ldcg(m.ws_ml + piece_row(cc) * 2));
+  float Ls = 0.f;
+  for (int cc = cfirst; cc <= clast; ++cc)
+    if (non_empty(cc)) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(m.ws_ml + piece_row(cc) * 2));
+      Ls += fast_exp2(ml.x - M) * ml.y;
+    }
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  T* out = static_cast<T*>(m.out) + (static_cast<long long>(b) * kH + row) * kNope +
+           rank * kOutCols + col0;
+  for (int c = 0; c < 4; ++c) {  // 32 columns at a time
+    float acc[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+    for (int cc = cfirst; cc <= clast; ++cc) {
+      if (!non_empty(cc)) continue;
+      const long long r = piece_row(cc);
+      const float f = fast_exp2(__ldcg(m.ws_ml + r * 2) - M);
+      const float4* src = reinterpret_cast<const float4*>(m.ws_o + r * kOutCols + col0 + c * 32);
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __ldcg(src + k);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc[4 * k] += f * v[k].x;
+        acc[4 * k + 1] += f * v[k].y;
+        acc[4 * k + 2] += f * v[k].z;
+        acc[4 * k + 3] += f * v[k].w;
+      }
+    }
+    uint32_t w[16];
+    float ra, rb;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k] = Pack<T>::run(acc[2 * k] * inv, acc[2 * k + 1] * inv, ra, rb);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint4*>(out + c * 32 + k * 8) =
+          make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+}
+
 }  // namespace
 
 namespace {
 
-size_t mla_counter_bytes(int clusters) {
-  return (static_cast<size_t>(clusters) * 4 * sizeof(int) + 255) & ~static_cast<size_t>(255);
-}
+// Workspace: the plan ([kMaxBatch + 1] int, padded to 256 B), then the
+// partial states of [clusters][2 slots][2 ranks] pieces.
+constexpr size_t kPlanBytes = ((kMaxBatch + 1) * sizeof(int) + 255) & ~static_cast<size_t>(255);
 
 template <typename T, bool kBf16>
-kvc_status run_mla(const MlaArgs& a, int clusters) {
+void mla_set_smem_attr() {
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(mla_decode_kernel<T, kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(MlaLayout::kBytes));
   });
+}
+
+// Clusters of two CTAs that can be resident at once on the current device.
+// A GPC with an odd number of free SMs leaves one idle, so this can be below
+// SMs / 2; launching more would run the extra clusters as a second wave.
+int mla_resident_clusters() {
+  static std::mutex mu;
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] > 0) return cache[dev];
+  const int sms = device_sm_count();
+  mla_set_smem_attr<__nv_bfloat16, true>();
+  mla_set_smem_attr<__half, false>();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = MlaLayout::kBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<__nv_bfloat16, true>, &cfg) !=
+          cudaSuccess ||
+      n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  cache[dev] = n < sms / 2 ? n : sms / 2;
+  return cache[dev];
+}
+
+template <typename T, bool kBf16>
+kvc_status run_mla(const MlaArgs& a, int clusters) {
+  mla_set_smem_attr<T, kBf16>();
   const int box_tokens = a.block_size < kTok ? a.block_size : kTok;
   CUtensorMap qr, cn, cr;
   const uint64_t qr_dims[3] = {kRope, kH, static_cast<uint64_t>(a.batch)};
@@ -754,8 +782,8 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
   p.q_nope = a.q_nope;
   p.block_table = a.block_table;
   p.seq_lens = a.seq_lens;
-  p.ws_cnt = static_cast<int*>(a.workspace);
-  p.ws_o = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + mla_counter_bytes(clusters));
+  p.ws_plan = static_cast<int*>(a.workspace);
+  p.ws_o = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + kPlanBytes);
   p.ws_ml = p.ws_o + static_cast<size_t>(clusters) * 4 * kH * kOutCols;
   p.err_flag = a.err_flag;
   p.batch = a.batch;
@@ -767,6 +795,15 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   mla_decode_kernel<T, kBf16><<<2 * clusters, kThreads, MlaLayout::kBytes, a.stream>>>(qr, cn, cr,
                                                                                        p);
+  if (cudaGetLastError() != cudaSuccess) return KVC_ERR_CUDA;
+  MlaMergeParams mp;
+  mp.out = a.out;
+  mp.plan = p.ws_plan;
+  mp.ws_o = p.ws_o;
+  mp.ws_ml = p.ws_ml;
+  mp.batch = a.batch;
+  mp.clusters = clusters;
+  mla_merge_kernel<T><<<dim3(a.batch, 4), kH, 0, a.stream>>>(mp);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
@@ -774,14 +811,12 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
 
 int mla_decode_num_ctas(int num_ctas) {
   if (num_ctas > 0) return num_ctas & ~1;
-  const int sms = device_sm_count();
-  return sms > 1 ? sms & ~1 : 0;  // one CTA per SM, pairs
+  return 2 * mla_resident_clusters();  // one CTA per SM, pairs, all resident
 }
 
 size_t mla_decode_workspace_bytes(int ctas) {
   const int clusters = ctas / 2;
-  return mla_counter_bytes(clusters) +
-         static_cast<size_t>(clusters) * 4 * kH * (kOutCols + 2) * sizeof(float);
+  return kPlanBytes + static_cast<size_t>(clusters) * 4 * kH * (kOutCols + 2) * sizeof(float);
 }
 
 kvc_status launch_mla_decode(const MlaArgs& a) {

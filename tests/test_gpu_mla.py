@@ -67,6 +67,25 @@ def test_mla_many_splits(kvc_lib):
         assert e <= TOL["bf16"], (ctas, e)
 
 
+def test_mla_workspace_needs_no_zeroing(kvc_lib):
+    """A workspace full of NaN bit patterns gives the same output as the oracle, twice in a row."""
+    c = mla_case(43, 4, [900, 33, 2048, 5], block_size=32, dtype="bf16")
+    d = {k: to_cuda(getattr(c, k)) for k in ("q_nope", "q_rope", "cache_nope", "cache_rope",
+                                             "block_table", "seq_lens")}
+    ref = oracle_mla(c)
+    ws = torch.full((kvc_lib.mla_workspace_size(10),), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        out = kvc_lib.mla_paged_decode(d["q_nope"], d["q_rope"], d["cache_nope"], d["cache_rope"],
+                                       d["block_table"], d["seq_lens"], c.scale, num_ctas=10,
+                                       workspace=ws)
+        torch.cuda.synchronize()
+        e = float(np.abs(out.double().cpu().numpy() - ref).max())
+        assert e <= TOL["bf16"], e
+        outs.append(out.clone())
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_mla_deterministic_permutation_invariant_and_poison_safe(kvc_lib):
     lens = [300, 77, 513]
     c = mla_case(43, 3, lens, block_size=16, dtype="bf16", num_blocks=80)
