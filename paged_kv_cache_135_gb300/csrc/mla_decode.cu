@@ -640,11 +640,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------- split merge
-// One CTA per (sequence, 128 output columns), one thread per query head:
+// One CTA per (sequence, 32 output columns), one thread per query head:
 // sequences split over several clusters combine their partial states,
 //   out = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i,   M = max_i m_i,
-// reading the pieces in cluster order (deterministic).  Sequences held whole
-// by one cluster were written by the decode kernel and are skipped.
+// over the pieces in cluster order (deterministic).  Up to four pieces are
+// loaded at once (one memory round trip); more go through a loop.  Sequences
+// held whole by one cluster were written by the decode kernel and are skipped.
 struct MlaMergeParams {
   void* out;
   const int* plan;
@@ -653,10 +654,13 @@ struct MlaMergeParams {
   int batch, clusters;
 };
 
+constexpr int kMergeCols = 32;
+constexpr int kMergeFast = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ MlaMergeParams m) {
   const int b = blockIdx.x, q = blockIdx.y, row = threadIdx.x;
-  const int rank = q >> 1, col0 = (q & 1) * 128;
+  const int rank = q / (kOutCols / kMergeCols), col0 = (q % (kOutCols / kMergeCols)) * kMergeCols;
   const long long seg0 = m.plan[b], n = m.plan[b + 1] - seg0;
   if (n <= 0) return;
   const long long N = m.plan[m.batch];
@@ -667,50 +671,84 @@ __global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ M
   auto piece_row = [&](int cc) -> long long {
     return ((static_cast<long long>(cc) * 2 + (cc == cfirst ? slot0 : 0)) * 2 + rank) * kH + row;
   };
-  auto non_empty = [&](int cc) {
-    return sched::share_begin(cc, N, P) < sched::share_begin(cc + 1, N, P);
-  };
-  float M = -INFINITY;
+  long long rows[kMergeFast];
+  int np = 0;
   for (int cc = cfirst; cc <= clast; ++cc)
-    if (non_empty(cc)) M = fmaxf(M, __ldcg(m.ws_ml + piece_row(cc) * 2));
-  float Ls = 0.f;
-  for (int cc = cfirst; cc <= clast; ++cc)
-    if (non_empty(cc)) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(m.ws_ml + piece_row(cc) * 2));
-      Ls += fast_exp2(ml.x - M) * ml.y;
+    if (sched::share_begin(cc, N, P) < sched::share_begin(cc + 1, N, P)) {
+      if (np < kMergeFast) rows[np] = piece_row(cc);
+      ++np;
     }
+  float acc[kMergeCols];
+  float Ls = 0.f;
+  if (np <= kMergeFast) {
+    float2 ml[kMergeFast];
+    float4 v[kMergeFast][kMergeCols / 4];
+#pragma unroll
+    for (int i = 0; i < kMergeFast; ++i) {
+      if (i < np) {
+        ml[i] = __ldcg(reinterpret_cast<const float2*>(m.ws_ml + rows[i] * 2));
+        const float4* src = reinterpret_cast<const float4*>(m.ws_o + rows[i] * kOutCols + col0);
+#pragma unroll
+        for (int k = 0; k < kMergeCols / 4; ++k) v[i][k] = __ldcg(src + k);
+      } else {
+        ml[i] = make_float2(-INFINITY, 0.f);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMergeFast; ++i) M = fmaxf(M, ml[i].x);
+#pragma unroll
+    for (int k = 0; k < kMergeCols; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMergeFast; ++i) {
+      if (i < np) {
+        const float f = fast_exp2(ml[i].x - M);
+        Ls += f * ml[i].y;
+#pragma unroll
+        for (int k = 0; k < kMergeCols / 4; ++k) {
+          acc[4 * k] += f * v[i][k].x;
+          acc[4 * k + 1] += f * v[i][k].y;
+          acc[4 * k + 2] += f * v[i][k].z;
+          acc[4 * k + 3] += f * v[i][k].w;
+        }
+      }
+    }
+  } else {  // many pieces: one at a time
+    float M = -INFINITY;
+    for (int cc = cfirst; cc <= clast; ++cc)
+      if (sched::share_begin(cc, N, P) < sched::share_begin(cc + 1, N, P))
+        M = fmaxf(M, __ldcg(m.ws_ml + piece_row(cc) * 2));
+#pragma unroll
+    for (int k = 0; k < kMergeCols; ++k) acc[k] = 0.f;
+    for (int cc = cfirst; cc <= clast; ++cc) {
+      if (sched::share_begin(cc, N, P) >= sched::share_begin(cc + 1, N, P)) continue;
+      const long long r = piece_row(cc);
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(m.ws_ml + r * 2));
+      const float f = fast_exp2(ml.x - M);
+      Ls += f * ml.y;
+      const float4* src = reinterpret_cast<const float4*>(m.ws_o + r * kOutCols + col0);
+#pragma unroll
+      for (int k = 0; k < kMergeCols / 4; ++k) {
+        const float4 x = __ldcg(src + k);
+        acc[4 * k] += f * x.x;
+        acc[4 * k + 1] += f * x.y;
+        acc[4 * k + 2] += f * x.z;
+        acc[4 * k + 3] += f * x.w;
+      }
+    }
+  }
   const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
   T* out = static_cast<T*>(m.out) + (static_cast<long long>(b) * kH + row) * kNope +
            rank * kOutCols + col0;
-  for (int c = 0; c < 4; ++c) {  // 32 columns at a time
-    float acc[32];
+  uint32_t w[kMergeCols / 2];
+  float ra, rb;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-    for (int cc = cfirst; cc <= clast; ++cc) {
-      if (!non_empty(cc)) continue;
-      const long long r = piece_row(cc);
-      const float f = fast_exp2(__ldcg(m.ws_ml + r * 2) - M);
-      const float4* src = reinterpret_cast<const float4*>(m.ws_o + r * kOutCols + col0 + c * 32);
-      float4 v[8];
+  for (int k = 0; k < kMergeCols / 2; ++k)
+    w[k] = Pack<T>::run(acc[2 * k] * inv, acc[2 * k + 1] * inv, ra, rb);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = __ldcg(src + k);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        acc[4 * k] += f * v[k].x;
-        acc[4 * k + 1] += f * v[k].y;
-        acc[4 * k + 2] += f * v[k].z;
-        acc[4 * k + 3] += f * v[k].w;
-      }
-    }
-    uint32_t w[16];
-    float ra, rb;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) w[k] = Pack<T>::run(acc[2 * k] * inv, acc[2 * k + 1] * inv, ra, rb);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      *reinterpret_cast<uint4*>(out + c * 32 + k * 8) =
-          make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-  }
+  for (int k = 0; k < kMergeCols / 8; ++k)
+    *reinterpret_cast<uint4*>(out + k * 8) =
+        make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
 }  // namespace
@@ -803,7 +841,7 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
   mp.ws_ml = p.ws_ml;
   mp.batch = a.batch;
   mp.clusters = clusters;
-  mla_merge_kernel<T><<<dim3(a.batch, 4), kH, 0, a.stream>>>(mp);
+  mla_merge_kernel<T><<<dim3(a.batch, 2 * kOutCols / kMergeCols), kH, 0, a.stream>>>(mp);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
