@@ -33,9 +33,10 @@
 // Work: 64-token tiles of all sequences in one linear order, split evenly
 // over the clusters (stream-K split-KV); pieces of split sequences leave
 // partial states that a small second kernel (mla_merge_kernel) combines.
-// Roles per CTA: warps 0-7 softmax / epilogue (warp w reads TMEM lanes
-// 32*(w%4).., column half w/4), warp 8 TMA producer, warp 9 tcgen05 issuer
-// (one thread) and TMEM owner.
+// Roles per CTA: warps 0-3 exchange the partial scores (one thread per
+// query row), warps 4-11 run the softmax and the epilogue (two threads per
+// row), warp 12 is the TMA producer, warp 13 the tcgen05 issuer (one thread)
+// and TMEM owner.  Warp w reads TMEM lanes 32*(w%4)...
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -60,10 +61,10 @@ constexpr int kKChunkBytes = kTok * 128;   // [64 tokens][64 elements]
 constexpr int kStageChunks = 5;            // rank 1: 4 nope + rope
 constexpr int kStageBytes = kStageChunks * kKChunkBytes;
 constexpr int kStages = 4;
-constexpr int kSoftmaxWarps = 8;
-constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kExchangeThreads = 128;   // warps 0-3
+constexpr int kMathThreads = 256;       // warps 4-11, two threads per query row
+constexpr int kProducerWarp = 12, kMmaWarp = 13;
+constexpr int kThreads = kExchangeThreads + kMathThreads + 64;
 constexpr int kMaxBatch = 1024;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
@@ -243,9 +244,11 @@ __device__ __forceinline__ void mla_issue_s(uint32_t d, uint32_t q_tmem, uint64_
   }
 }
 
-// One thread.  Order: S(0), S(1), then per tile t: S(t+2), P V(t).  S runs
-// two tiles ahead so the scores of the next tile are ready when the softmax
-// finishes the exchange of the current one.
+// One thread.  S(t) and P V(t) are issued as soon as their inputs are ready,
+// whichever comes first (P V first when both are): S(t) needs its key stage,
+// a free S buffer and the sequence's query; P V(t) needs P(t).  So a key tile
+// still in flight never holds back the P V of an earlier tile.  A stall of
+// kWaitLimitNs without progress sets KVC_FLAG_WAIT_TIMEOUT and aborts.
 template <bool kBf16>
 __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint64_t* bars,
                                         volatile int* abort_flag, uint32_t tmem, MlaCursor cs,
@@ -259,51 +262,64 @@ __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint6
   const uint64_t p0 = umma_desc_sw128(smem_u32(smem + L::kP), 16, 1024);
   // V = the first four chunks of a stage, MN-major: next 64 columns 8 KB on.
   const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kK), kKChunkBytes, 1024);
-  int seg_s = -1;
+  int seg_s = -1, ns = 0, npv = 0;
   uint32_t first_bits = 0;  // bit (t & 3): tile t starts a sequence's share
-
-  auto issue_s = [&](int it) -> bool {
-    const bool first = it == 0 || cs.j == 0;
-    const bool last = it == n_it - 1 || cs.last();
-    if (first) ++seg_s;
-    first_bits = (first_bits & ~(1u << (it & 3))) | (first ? 1u << (it & 3) : 0u);
-    const int stage = it % kStages, sb = it & 1;
-    if (!wait_cta(&bars[kKFull0 + stage], static_cast<uint32_t>(it / kStages) & 1u, abort_flag,
-                  p.err_flag))
-      return false;
-    if (!wait_cta(&bars[kSFree0 + sb], ((it >> 1) & 1) ^ 1, abort_flag, p.err_flag)) return false;
-    if (!wait_cta(&bars[kQFull], seg_s & 1, abort_flag, p.err_flag)) return false;
-    tc_fence_after();
-    const uint32_t d = tmem + (sb ? kTmemS1 : kTmemS0);
-    const uint64_t k_st = desc_advance(k0, stage * kStageBytes);
-    if (rank) mla_issue_s<true>(d, tmem + kTmemQ, qr0, k_st, idesc_s);
-    else mla_issue_s<false>(d, tmem + kTmemQ, qr0, k_st, idesc_s);
-    umma_commit(&bars[kSFull0 + sb]);
-    if (last) umma_commit(&bars[kQFree]);
-    cs.advance(p.seq_lens, cap, p.batch);
-    return true;
-  };
-  auto issue_pv = [&](int it) -> bool {
-    if (!wait_cta(&bars[kPFull], it & 1, abort_flag, p.err_flag)) return false;
-    tc_fence_after();
-    const int stage = it % kStages;
-    const uint64_t v_st = desc_advance(v0, stage * kStageBytes);
-    if ((first_bits >> (it & 3)) & 1u) umma_f16_fresh(tmem + kTmemO, p0, v_st, idesc_o);
-    else umma_f16_acc(tmem + kTmemO, p0, v_st, idesc_o);
+  unsigned long long t_prog = global_timer_ns();
+  int idle = 0;
+  while (npv < n_it) {
+    if (*abort_flag) return;
+    bool progress = false;
+    if (npv < ns && mbar_test_wait(&bars[kPFull], npv & 1)) {
+      tc_fence_after();
+      const int stage = npv % kStages;
+      const uint64_t v_st = desc_advance(v0, stage * kStageBytes);
+      if ((first_bits >> (npv & 3)) & 1u) umma_f16_fresh(tmem + kTmemO, p0, v_st, idesc_o);
+      else umma_f16_acc(tmem + kTmemO, p0, v_st, idesc_o);
 #pragma unroll
-    for (int ks = 1; ks < kTok / 16; ++ks)
-      umma_f16_acc(tmem + kTmemO, desc_advance(p0, ks * 32), desc_advance(v_st, ks * 16 * 128),
-                   idesc_o);
-    umma_commit(&bars[kPVDone]);
-    umma_commit(&bars[kKEmpty0 + stage]);
-    return true;
-  };
-
-  for (int it = 0; it < n_it && it < 2; ++it)
-    if (!issue_s(it)) return;
-  for (int it = 0; it < n_it; ++it) {
-    if (it + 2 < n_it && !issue_s(it + 2)) return;
-    if (!issue_pv(it)) return;
+      for (int ks = 1; ks < kTok / 16; ++ks)
+        umma_f16_acc(tmem + kTmemO, desc_advance(p0, ks * 32), desc_advance(v_st, ks * 16 * 128),
+                     idesc_o);
+      umma_commit(&bars[kPVDone]);
+      umma_commit(&bars[kKEmpty0 + stage]);
+      ++npv;
+      progress = true;
+    }
+    if (ns < n_it && ns < npv + 4) {
+      const bool first = ns == 0 || cs.j == 0;
+      const int seg = first ? seg_s + 1 : seg_s;
+      const int stage = ns % kStages, sb = ns & 1;
+      if (mbar_test_wait(&bars[kKFull0 + stage], static_cast<uint32_t>(ns / kStages) & 1u) &&
+          mbar_test_wait(&bars[kSFree0 + sb], ((ns >> 1) & 1) ^ 1) &&
+          mbar_test_wait(&bars[kQFull], seg & 1)) {
+        tc_fence_after();
+        const bool last = ns == n_it - 1 || cs.last();
+        seg_s = seg;
+        first_bits = (first_bits & ~(1u << (ns & 3))) | (first ? 1u << (ns & 3) : 0u);
+        const uint32_t d = tmem + (sb ? kTmemS1 : kTmemS0);
+        const uint64_t k_st = desc_advance(k0, stage * kStageBytes);
+        if (rank) mla_issue_s<true>(d, tmem + kTmemQ, qr0, k_st, idesc_s);
+        else mla_issue_s<false>(d, tmem + kTmemQ, qr0, k_st, idesc_s);
+        umma_commit(&bars[kSFull0 + sb]);
+        if (last) umma_commit(&bars[kQFree]);
+        cs.advance(p.seq_lens, cap, p.batch);
+        ++ns;
+        progress = true;
+      }
+    }
+    if (progress) {
+      idle = 0;
+      t_prog = 0;
+    } else if (++idle >= 64) {
+      idle = 0;
+      const unsigned long long now = global_timer_ns();
+      if (t_prog == 0) {
+        t_prog = now;
+      } else if (now - t_prog > kWaitLimitNs) {
+        set_flag(p.err_flag, KVC_FLAG_WAIT_TIMEOUT);
+        *abort_flag = 1;
+        return;
+      }
+    }
   }
 }
 
@@ -317,9 +333,9 @@ template <typename T>
 __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, int row, int h,
                                         int b, bool complete, int cl, int slot, int rank,
                                         float m_used, float l_half, float* red) {
-  named_bar_sync(1, kSoftmaxThreads);
+  named_bar_sync(1, kMathThreads);
   red[h * kH + row] = l_half;
-  named_bar_sync(1, kSoftmaxThreads);
+  named_bar_sync(1, kMathThreads);
   const float l = red[row] + red[kH + row];
   if (complete) {
     T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * kH + row) * kNope +
@@ -350,197 +366,206 @@ __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, in
   if (h == 0) *reinterpret_cast<float2*>(p.ws_ml + wrow * 2) = make_float2(m_used, l);
 }
 
-// --------------------------------------------------------------- softmax
-// This CTA's 256 nope query columns of sequence b, row `row`, half `h`
-// (128 columns = 64 packed TMEM columns) -> tensor memory.
+// ------------------------------------------------------------- exchange
+// This CTA's 256 nope query columns of sequence b, row `row` (128 packed
+// TMEM columns), loaded in two halves.
 template <typename T>
 __device__ __forceinline__ void mla_load_q(const MlaParams& p, uint32_t lane_base, int b, int row,
-                                           int h, int rank) {
+                                           int rank) {
   const uint4* src = reinterpret_cast<const uint4*>(
       static_cast<const T*>(p.q_nope) + (static_cast<long long>(b) * kH + row) * kNope +
-      rank * kOutCols + h * 128);
-  uint4 v[16];
+      rank * kOutCols);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __ldg(src + i);
+  for (int half = 0; half < 2; ++half) {
+    uint4 v[16];
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
-    tmem_st16_u32(lane_base + kTmemQ + h * 64 + c * 16, reinterpret_cast<const uint32_t*>(v + 4 * c));
+    for (int i = 0; i < 16; ++i) v[i] = __ldg(src + half * 16 + i);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      tmem_st16_u32(lane_base + kTmemQ + half * 64 + c * 16,
+                    reinterpret_cast<const uint32_t*>(v + 4 * c));
+  }
   tmem_wait_st();
 }
 
-// Warps 0-7: thread (row, h) owns query head `row` (TMEM lane `row`) and
-// tokens / output columns of half h.  Iteration `it` (1) sends this CTA's
-// partial scores of tile `it` to the other CTA straight from TMEM, (2) runs
-// the softmax of tile `it-1` and hands its P to the tensor core, and (3)
-// completes the exchange of tile `it`, so the round trip through distributed
-// shared memory overlaps the softmax math.  The scores travel as st.async
-// stores that complete the receiver's x_full transaction count (no fence on
-// the sender); x_empty is a relaxed arrive after the reads are consumed.
+// Warps 0-3, thread `row` = query head.  Per tile: this CTA's partial scores
+// (TMEM) go to the other CTA as st.async stores that complete its x_full
+// transaction count, once the other CTA has freed its X buffer (x_empty, a
+// relaxed arrive from its math warps).  These warps also load each
+// sequence's query into TMEM.
 template <typename T>
-__device__ __forceinline__ void mla_softmax(const MlaParams& p, uint8_t* smem, uint64_t* bars,
-                                            volatile int* abort_flag, uint32_t tmem, MlaCursor cx,
-                                            int n_it, int cl, int rank, int row, int h) {
+__device__ __forceinline__ void mla_exchange(const MlaParams& p, uint8_t* smem, uint64_t* bars,
+                                             volatile int* abort_flag, uint32_t tmem, MlaCursor cx,
+                                             int n_it, int rank, int row) {
   using L = MlaLayout;
   const int cap = p.max_blocks * p.block_size;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(row & ~31) << 16);
   const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
   const uint32_t x_peer = map_to_rank(smem_u32(smem + L::kX), peer);
   const uint32_t xfull_peer = map_to_rank(smem_u32(&bars[kXFull]), peer);
-  const uint32_t xempty_peer = map_to_rank(smem_u32(&bars[kXEmpty]), peer);
-  const float4* x_mine = reinterpret_cast<const float4*>(smem + L::kX);
-  float* red = reinterpret_cast<float*>(smem + L::kRed);
-  const bool elected = row == 0 && h == 0;
-  MlaCursor cm = cx;  // tile whose softmax runs next (one behind the exchange)
-  float m_used = -INFINITY, l = 0.f;
-  int seg_first_j = cm.j, slot = 0, seg_x = 0;
-  float sp[32];  // summed scores of tile it-1, this thread's 32 tokens
+  int seg_x = 0;
 
-  // Query of the first sequence (tensor memory is fresh).
-  mla_load_q<T>(p, lane_base, cx.b, row, h, rank);
+  mla_load_q<T>(p, lane_base, cx.b, row, rank);  // tensor memory is fresh
   tc_fence_before();
   mbar_arrive(&bars[kQFull]);
 
-  for (int it = 0; it <= n_it; ++it) {
+  for (int it = 0; it < n_it; ++it) {
     const int sb = it & 1;
-    if (it < n_it) {
-      // (1) Own partial scores of tile `it` -> the other CTA.
-      wait_cta(&bars[kSFull0 + sb], (it >> 1) & 1, abort_flag, p.err_flag);
-      tc_fence_after();
-      wait_peer(&bars[kXEmpty], (it & 1) ^ 1, abort_flag, p.err_flag);
+    const uint32_t s_col = lane_base + (sb ? kTmemS1 : kTmemS0);
+    float so[kTok];
+    wait_cta(&bars[kSFull0 + sb], (it >> 1) & 1, abort_flag, p.err_flag);
+    tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < kTok / 16; ++c) tmem_ld16(s_col + c * 16, so + c * 16);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&bars[kSFree0 + sb]);
+    wait_peer(&bars[kXEmpty], (it & 1) ^ 1, abort_flag, p.err_flag);
+#pragma unroll
+    for (int q = 0; q < kTok / 4; ++q)
+      st_async_cluster_v4(x_peer + (q * kH + row) * 16,
+                          make_float4(so[4 * q], so[4 * q + 1], so[4 * q + 2], so[4 * q + 3]),
+                          xfull_peer);
+    // Tile it+1 starts the next sequence: its query replaces this one (S(it)
+    // complete => every S of this sequence is done).
+    if (it + 1 < n_it && cx.last()) {
+      wait_cta(&bars[kQFree], seg_x & 1, abort_flag, p.err_flag);
+      tc_fence_after();
+      MlaCursor nx = cx;
+      nx.advance(p.seq_lens, cap, p.batch);
+      mla_load_q<T>(p, lane_base, nx.b, row, rank);
+      tc_fence_before();
+      mbar_arrive(&bars[kQFull]);
+      ++seg_x;
+    }
+    cx.advance(p.seq_lens, cap, p.batch);
+  }
+}
+
+// ----------------------------------------------------------------- math
+// Warps 4-11, thread (row, h) = query head `row`, tokens and output columns
+// of half h: online softmax in the log2 domain (O rescaled only when the
+// running max grows by more than 2^kRescaleThreshold; the two halves of a
+// row share their maxima through shared memory), P (bf16/fp16, K-major,
+// 128-byte swizzle) to shared memory, then the end-of-share epilogue.
+template <typename T>
+__device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint64_t* bars,
+                                         volatile int* abort_flag, uint32_t tmem, MlaCursor cm,
+                                         int n_it, int cl, int rank, int row, int h) {
+  using L = MlaLayout;
+  const int cap = p.max_blocks * p.block_size;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(row & ~31) << 16);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
+  const float4* x_mine = reinterpret_cast<const float4*>(smem + L::kX);
+  const uint32_t xempty_peer = map_to_rank(smem_u32(&bars[kXEmpty]), static_cast<uint32_t>(rank ^ 1));
+  const bool elected = row == 0 && h == 0;
+  float m_used = -INFINITY, l = 0.f;
+  int seg_first_j = cm.j, slot = 0;
+  for (int it = 0; it < n_it; ++it) {
+    const int sb = it & 1;
+    const bool first = it == 0 || cm.j == 0;
+    const bool last = it == n_it - 1 || cm.last();
+    if (first) {
+      m_used = -INFINITY;
+      l = 0.f;
+      seg_first_j = cm.j;
+    }
+    // Scores of this thread's 32 tokens: own partial (TMEM) + the other
+    // CTA's (X); then both buffers are released.
+    float s[32];
+    wait_cta(&bars[kSFull0 + sb], (it >> 1) & 1, abort_flag, p.err_flag);
+    tc_fence_after();
+    tmem_ld16(lane_base + (sb ? kTmemS1 : kTmemS0) + h * 32, s);
+    tmem_ld16(lane_base + (sb ? kTmemS1 : kTmemS0) + h * 32 + 16, s + 16);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&bars[kSFree0 + sb]);
+    wait_peer(&bars[kXFull], it & 1, abort_flag, p.err_flag);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = x_mine[(h * 8 + q) * kH + row];
+      s[4 * q] += v.x;
+      s[4 * q + 1] += v.y;
+      s[4 * q + 2] += v.z;
+      s[4 * q + 3] += v.w;
+    }
+    const int tile_valid = min(kTok, cm.len - cm.j * kTok);
+    const int valid = tile_valid - h * 32;  // of this thread's 32 tokens
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      s[k] = k < valid ? s[k] * p.scale_log2 : -INFINITY;
+      mx4[k & 3] = fmaxf(mx4[k & 3], s[k]);
+    }
+    red[h * kH + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    named_bar_sync(3, kMathThreads);  // also: every thread has read X
+    if (elected) {
+      // The next tile's scores arrive as 32 KB of transactions on x_full.
+      if (it + 1 < n_it) mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 4);
+      mbar_arrive_cluster_relaxed(xempty_peer);
+    }
+    const float mx = fmaxf(red[row], red[kH + row]);  // same order in both halves
+    float corr = 1.f;
+    bool rescale = false;
+    if (m_used == -INFINITY) {
+      m_used = mx;
+      corr = 0.f;
+    } else if (mx > m_used + kRescaleThreshold) {
+      corr = fast_exp2(m_used - mx);
+      m_used = mx;
+      rescale = true;
+    }
+    uint32_t pk[16];
+    float ps[4] = {0.f, 0.f, 0.f, 0.f}, ra, rb;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      pk[k] = Pack<T>::run(fast_exp2(s[2 * k] - m_used), fast_exp2(s[2 * k + 1] - m_used), ra, rb);
+      ps[k & 3] += ra + rb;
+    }
+    l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+    if (it > 0) {  // P V of the previous tile must be done before P and O are touched
+      wait_cta(&bars[kPVDone], (it - 1) & 1, abort_flag, p.err_flag);
+      tc_fence_after();
+    }
+    if (__any_sync(0xffffffffu, rescale)) {
+      for (int c = 0; c < 8; ++c) {
         float v[16];
-        tmem_ld16(lane_base + (sb ? kTmemS1 : kTmemS0) + h * 32 + c * 16, v);
+        tmem_ld16(lane_base + kTmemO + h * 128 + c * 16, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_async_cluster_v4(x_peer + ((h * 8 + c * 4 + q) * kH + row) * 16,
-                              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]),
-                              xfull_peer);
+        for (int k = 0; k < 16; ++k) v[k] *= corr;
+        tmem_st16(lane_base + kTmemO + h * 128 + c * 16, v);
       }
-      // Tile it+1 starts the next sequence: its query replaces this one once
-      // the tensor core is done with it (S(it) complete => all its S done).
-      if (it + 1 < n_it && cx.last()) {
-        wait_cta(&bars[kQFree], seg_x & 1, abort_flag, p.err_flag);
-        tc_fence_after();
-        MlaCursor nx = cx;
-        nx.advance(p.seq_lens, cap, p.batch);
-        mla_load_q<T>(p, lane_base, nx.b, row, h, rank);
-        tc_fence_before();
-        mbar_arrive(&bars[kQFull]);
-        ++seg_x;
-      }
-      cx.advance(p.seq_lens, cap, p.batch);
+      tmem_wait_st();
     }
-    if (it > 0) {
-      // (2) Softmax of tile it-1 (log2 domain; O rescaled only when the
-      //     running max grows by more than 2^kRescaleThreshold).
-      const int pit = it - 1;
-      const bool first = pit == 0 || cm.j == 0;
-      const bool last = pit == n_it - 1 || cm.last();
-      if (first) {
-        m_used = -INFINITY;
-        l = 0.f;
-        seg_first_j = cm.j;
-      }
-      const int valid = min(kTok, cm.len - cm.j * kTok) - h * 32;  // of this thread's 32
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    // P row half -> shared memory; the value rows past the sequence are
+    // zeroed so stale contents cannot reach P V.
+    uint8_t* pptr = smem + L::kP;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        sp[k] = k < valid ? sp[k] * p.scale_log2 : -INFINITY;
-        mx4[k & 3] = fmaxf(mx4[k & 3], sp[k]);
+    for (int ch = 0; ch < 4; ++ch)
+      *reinterpret_cast<uint4*>(pptr + swz128(row, h * 4 + ch)) =
+          make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+    if (tile_valid < kTok) {
+      uint8_t* kst = smem + L::kK + (it % kStages) * kStageBytes;
+      const int n16 = (kTok - tile_valid) * 4 * 8;
+      for (int e = h * kH + row; e < n16; e += kMathThreads) {
+        const int r = tile_valid + e / 32, c = (e % 32) / 8, q = e % 8;
+        *reinterpret_cast<uint4*>(kst + c * kKChunkBytes + r * 128 + q * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
       }
-      red[h * kH + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      named_bar_sync(3, kSoftmaxThreads);
-      const float mx = fmaxf(red[row], red[kH + row]);  // same order in both halves
-      float corr = 1.f;
-      bool rescale = false;
-      if (m_used == -INFINITY) {
-        m_used = mx;
-        corr = 0.f;
-      } else if (mx > m_used + kRescaleThreshold) {
-        corr = fast_exp2(m_used - mx);
-        m_used = mx;
-        rescale = true;
-      }
-      uint32_t pk[16];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f}, ra, rb;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        pk[k] = Pack<T>::run(fast_exp2(sp[2 * k] - m_used), fast_exp2(sp[2 * k + 1] - m_used), ra, rb);
-        ps[k & 3] += ra + rb;
-      }
-      l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      if (pit > 0) {  // P V of tile it-2 must be done before P and O are touched
-        wait_cta(&bars[kPVDone], (pit - 1) & 1, abort_flag, p.err_flag);
-        tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        for (int c = 0; c < 8; ++c) {
-          float v[16];
-          tmem_ld16(lane_base + kTmemO + h * 128 + c * 16, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] *= corr;
-          tmem_st16(lane_base + kTmemO + h * 128 + c * 16, v);
-        }
-        tmem_wait_st();
-      }
-      // P row half -> shared memory (K-major, 128-byte swizzle); the value
-      // rows past the sequence are zeroed so stale contents cannot reach P V.
-      uint8_t* pptr = smem + L::kP;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4*>(pptr + swz128(row, h * 4 + ch)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      const int tile_valid = min(kTok, cm.len - cm.j * kTok);
-      if (tile_valid < kTok) {
-        uint8_t* kst = smem + L::kK + (pit % kStages) * kStageBytes;
-        const int n16 = (kTok - tile_valid) * 4 * 8;
-        for (int e = h * kH + row; e < n16; e += kSoftmaxThreads) {
-          const int r = tile_valid + e / 32, c = (e % 32) / 8, q = e % 8;
-          *reinterpret_cast<uint4*>(kst + c * kKChunkBytes + r * 128 + q * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      fence_proxy_async_smem();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(&bars[kPFull]);
+    if (last) {  // end of this sequence's share
+      wait_cta(&bars[kPVDone], it & 1, abort_flag, p.err_flag);
+      tc_fence_after();
+      mla_finish<T>(p, lane_base + kTmemO + h * 128, row, h, cm.b, seg_first_j == 0 && cm.last(),
+                    cl, slot, rank, m_used, l, red);
       tc_fence_before();
-      mbar_arrive(&bars[kPFull]);
-      if (last) {  // end of this sequence's share
-        wait_cta(&bars[kPVDone], pit & 1, abort_flag, p.err_flag);
-        tc_fence_after();
-        mla_finish<T>(p, lane_base + kTmemO + h * 128, row, h, cm.b,
-                      seg_first_j == 0 && cm.last(), cl, slot, rank, m_used, l, red);
-        tc_fence_before();
-        slot = 1;
-      }
-      cm.advance(p.seq_lens, cap, p.batch);
+      slot = 1;
     }
-    if (it < n_it) {
-      // (3) Complete the exchange of tile `it`: own partial (re-read from
-      //     TMEM) + the other CTA's, then free both buffers.
-      wait_peer(&bars[kXFull], it & 1, abort_flag, p.err_flag);
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-        tmem_ld16(lane_base + (sb ? kTmemS1 : kTmemS0) + h * 32 + c * 16, sp + c * 16);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars[kSFree0 + sb]);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 v = x_mine[(h * 8 + q) * kH + row];
-        sp[4 * q] += v.x;
-        sp[4 * q + 1] += v.y;
-        sp[4 * q + 2] += v.z;
-        sp[4 * q + 3] += v.w;
-      }
-      named_bar_sync(2, kSoftmaxThreads);
-      if (elected) {
-        // Next tile's scores arrive as 32 KB of transactions on x_full.
-        if (it + 1 < n_it) mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 4);
-        mbar_arrive_cluster_relaxed(xempty_peer);
-      }
-    }
+    cm.advance(p.seq_lens, cap, p.batch);
   }
 }
 
@@ -568,8 +593,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t c = 1;
-      if (i == kQFull) c = 1 + kSoftmaxThreads;
-      if (i == kSFree0 || i == kSFree0 + 1 || i == kPFull) c = kSoftmaxThreads;
+      if (i == kQFull) c = 1 + kExchangeThreads;
+      if (i == kSFree0 || i == kSFree0 + 1) c = kExchangeThreads + kMathThreads;
+      if (i == kPFull) c = kMathThreads;
       mbar_init(&bars[i], c);
     }
     *abort_flag = 0;
@@ -610,9 +636,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();  // the plan (in the P region) is not read past this point
   const int n_it = static_cast<int>(te - tb);
   if (n_it > 0) {
-    if (warp < kSoftmaxWarps) {
-      mla_softmax<T>(p, smem, bars, abort_flag, tmem, cur, n_it, cl, rank, (warp & 3) * 32 + lane,
-                     warp >> 2);
+    if (warp < 4) {
+      mla_exchange<T>(p, smem, bars, abort_flag, tmem, cur, n_it, rank, tid);
+    } else if (warp < 12) {
+      mla_math<T>(p, smem, bars, abort_flag, tmem, cur, n_it, cl, rank, (warp & 3) * 32 + lane,
+                  (warp - 4) >> 2);
     } else if (warp == kProducerWarp) {
       mla_producer(p, &tm_qr, &tm_cn, &tm_cr, smem, bars, abort_flag, cur, n_it, rank, lane);
       // Every copy issued must land before shared memory can be released.
