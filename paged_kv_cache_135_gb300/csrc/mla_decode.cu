@@ -668,8 +668,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------- split merge
-// One CTA per (sequence, 32 output columns), one thread per query head:
-// sequences split over several clusters combine their partial states,
+// One CTA per (sequence, rank, 16 query heads); 16 threads per head, each
+// owning 16 adjacent output columns, so a warp reads and writes whole rows.
+// Sequences split over several clusters combine their partial states,
 //   out = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i,   M = max_i m_i,
 // over the pieces in cluster order (deterministic).  Up to four pieces are
 // loaded at once (one memory round trip); more go through a loop.  Sequences
@@ -682,13 +683,17 @@ struct MlaMergeParams {
   int batch, clusters;
 };
 
-constexpr int kMergeCols = 32;
+constexpr int kMergeRows = 16;                       // query heads per CTA
+constexpr int kMergeThreads = kMergeRows * 16;       // 16 threads per head
 constexpr int kMergeFast = 4;
 
 template <typename T>
-__global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ MlaMergeParams m) {
-  const int b = blockIdx.x, q = blockIdx.y, row = threadIdx.x;
-  const int rank = q / (kOutCols / kMergeCols), col0 = (q % (kOutCols / kMergeCols)) * kMergeCols;
+__global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
+    const __grid_constant__ MlaMergeParams m) {
+  const int b = blockIdx.x;
+  const int rank = blockIdx.y / (kH / kMergeRows);
+  const int row = (blockIdx.y % (kH / kMergeRows)) * kMergeRows + threadIdx.x / 16;
+  const int col0 = (threadIdx.x % 16) * 16;
   const long long seg0 = m.plan[b], n = m.plan[b + 1] - seg0;
   if (n <= 0) return;
   const long long N = m.plan[m.batch];
@@ -706,18 +711,20 @@ __global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ M
       if (np < kMergeFast) rows[np] = piece_row(cc);
       ++np;
     }
-  float acc[kMergeCols];
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
   float Ls = 0.f;
   if (np <= kMergeFast) {
     float2 ml[kMergeFast];
-    float4 v[kMergeFast][kMergeCols / 4];
+    float4 v[kMergeFast][4];
 #pragma unroll
     for (int i = 0; i < kMergeFast; ++i) {
       if (i < np) {
         ml[i] = __ldcg(reinterpret_cast<const float2*>(m.ws_ml + rows[i] * 2));
         const float4* src = reinterpret_cast<const float4*>(m.ws_o + rows[i] * kOutCols + col0);
 #pragma unroll
-        for (int k = 0; k < kMergeCols / 4; ++k) v[i][k] = __ldcg(src + k);
+        for (int k = 0; k < 4; ++k) v[i][k] = __ldcg(src + k);
       } else {
         ml[i] = make_float2(-INFINITY, 0.f);
       }
@@ -726,14 +733,12 @@ __global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ M
 #pragma unroll
     for (int i = 0; i < kMergeFast; ++i) M = fmaxf(M, ml[i].x);
 #pragma unroll
-    for (int k = 0; k < kMergeCols; ++k) acc[k] = 0.f;
-#pragma unroll
     for (int i = 0; i < kMergeFast; ++i) {
       if (i < np) {
         const float f = fast_exp2(ml[i].x - M);
         Ls += f * ml[i].y;
 #pragma unroll
-        for (int k = 0; k < kMergeCols / 4; ++k) {
+        for (int k = 0; k < 4; ++k) {
           acc[4 * k] += f * v[i][k].x;
           acc[4 * k + 1] += f * v[i][k].y;
           acc[4 * k + 2] += f * v[i][k].z;
@@ -746,8 +751,6 @@ __global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ M
     for (int cc = cfirst; cc <= clast; ++cc)
       if (sched::share_begin(cc, N, P) < sched::share_begin(cc + 1, N, P))
         M = fmaxf(M, __ldcg(m.ws_ml + piece_row(cc) * 2));
-#pragma unroll
-    for (int k = 0; k < kMergeCols; ++k) acc[k] = 0.f;
     for (int cc = cfirst; cc <= clast; ++cc) {
       if (sched::share_begin(cc, N, P) >= sched::share_begin(cc + 1, N, P)) continue;
       const long long r = piece_row(cc);
@@ -756,7 +759,7 @@ __global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ M
       Ls += f * ml.y;
       const float4* src = reinterpret_cast<const float4*>(m.ws_o + r * kOutCols + col0);
 #pragma unroll
-      for (int k = 0; k < kMergeCols / 4; ++k) {
+      for (int k = 0; k < 4; ++k) {
         const float4 x = __ldcg(src + k);
         acc[4 * k] += f * x.x;
         acc[4 * k + 1] += f * x.y;
@@ -768,15 +771,12 @@ __global__ void __launch_bounds__(kH) mla_merge_kernel(const __grid_constant__ M
   const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
   T* out = static_cast<T*>(m.out) + (static_cast<long long>(b) * kH + row) * kNope +
            rank * kOutCols + col0;
-  uint32_t w[kMergeCols / 2];
+  uint32_t w[8];
   float ra, rb;
 #pragma unroll
-  for (int k = 0; k < kMergeCols / 2; ++k)
-    w[k] = Pack<T>::run(acc[2 * k] * inv, acc[2 * k + 1] * inv, ra, rb);
-#pragma unroll
-  for (int k = 0; k < kMergeCols / 8; ++k)
-    *reinterpret_cast<uint4*>(out + k * 8) =
-        make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  for (int k = 0; k < 8; ++k) w[k] = Pack<T>::run(acc[2 * k] * inv, acc[2 * k + 1] * inv, ra, rb);
+  *reinterpret_cast<uint4*>(out) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(out + 8) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 }  // namespace
@@ -869,7 +869,7 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
   mp.ws_ml = p.ws_ml;
   mp.batch = a.batch;
   mp.clusters = clusters;
-  mla_merge_kernel<T><<<dim3(a.batch, 2 * kOutCols / kMergeCols), kH, 0, a.stream>>>(mp);
+  mla_merge_kernel<T><<<dim3(a.batch, 2 * (kH / kMergeRows)), kMergeThreads, 0, a.stream>>>(mp);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
