@@ -86,6 +86,8 @@ struct PrefillArgs {
 kvc_status launch_varlen_prefill(const PrefillArgs& a);
 // The causal attention part alone (tcgen05 kernel).
 kvc_status launch_prefill_attention_tc(const PrefillArgs& a);
+// Two query heads per CTA; requires an even GQA group size.
+kvc_status launch_prefill_attention_tc2(const PrefillArgs& a);
 
 struct MlaArgs {
   const void* q_nope;

@@ -1,0 +1,557 @@
+// Packed-varlen causal prefill over the paged cache on the tcgen05 tensor
+// cores, two query heads of one GQA group per CTA (row a5 of the hot path,
+// attention part, used when the group size is even).
+//
+// What it computes: the hotelren.com notes "Paged KV Cache + Packed
+// Sequence" 3.1-3.3 -- packed sequences delimited by cu_seqlens, each token
+// attending causally (diagonal included) to its own sequence's tokens only,
+// read back from the paged cache through the sequence's block_table;
+// "external-cannbot-model-model-infer-kvcache" Appendix C sparse_mode 3.
+//
+// GB300 design.  One CTA per (sequence, 128-query tile, pair of query heads
+// sharing a KV head), heaviest tiles first.  Both heads' 128-row query
+// tiles stay in shared memory and share one stream of 128-token K and V
+// tiles (TMA through block_table, 2-stage rings), so every K/V byte feeds
+// two heads.  Tensor memory holds O and S for each head (4 x 128 columns).
+// Each head has its own softmax warpgroup, one thread per query row and all
+// 128 columns of the tile: the thread pulls its S row into registers and
+// frees the S buffer at once, so the tensor core computes the head's next S
+// while the thread runs the exponentials; no cross-thread reduction is
+// needed.  The two heads alternate on one P buffer (bf16/fp16, 128-byte
+// swizzled shared memory).  One thread issues the MMAs in whatever order
+// their inputs become ready (S of either head, P V in alternating order).
+// Online softmax in the log2 domain; O is rescaled only when a row's max
+// grows by more than 2^8.
+#include <cuda_runtime.h>
+
+#include <math.h>
+
+#include <mutex>
+
+#include "kvc_device.cuh"
+#include "kvc_host.h"
+#include "kvc_tcgen05.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kBM = 128;                    // query rows per head = MMA M
+constexpr int kBN = 128;                    // kv tokens per tile
+constexpr int kHeadThreads = 128;           // softmax threads per head
+constexpr int kSmxThreads = 2 * kHeadThreads;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = kSmxThreads + 64;
+constexpr int kStages = 2;
+constexpr int kChunk = 128 * 128;           // one [128 rows][64 elements] swizzled region
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns of head x: O at 128x, S at 256 + 128x.
+__host__ __device__ constexpr uint32_t tmem_o(int x) { return 128u * x; }
+__host__ __device__ constexpr uint32_t tmem_s(int x) { return 256u + 128u * x; }
+
+struct Tc2Params {
+  void* out;
+  const int32_t* cu_seqlens;
+  const int32_t* context_lens;
+  const int32_t* block_table;
+  uint32_t* err_flag;
+  int num_seqs, num_q_heads, group;
+  int block_size, log2_bs, max_blocks, num_blocks, box_tokens;
+  float scale_log2;
+};
+
+template <int D>
+struct Tc2Layout {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kStageBytes = kHalves * kChunk;         // one K or one V tile
+  static constexpr int kQ = 0;                                 // head A then head B
+  static constexpr int kK = kQ + 2 * kStageBytes;
+  static constexpr int kV = kK + kStages * kStageBytes;
+  static constexpr int kP = kV + kStages * kStageBytes;        // 2 chunks (128 tokens)
+  static constexpr int kBar = kP + 2 * kChunk;
+  static constexpr int kNumBars = 19;
+  static constexpr int kMisc = kBar + kNumBars * 8;            // tmem slot, abort, info[4]
+  static constexpr int kTotal = 1024 + kMisc + 64;
+  static_assert(kTotal <= 232448, "fits the opt-in shared memory of one SM");
+};
+
+// pv_done[h]: one completion per P V of head h.  The P buffer passes A(0),
+// B(0), A(1), B(1), ...: head A writes P(j) after pv_done[B] completion j-1,
+// head B after pv_done[A] completion j.  Each of those waits is at most one
+// phase behind its barrier, so the parity is unambiguous (one barrier shared
+// by both heads would be two phases apart between a head's waits).
+// o_done[h]: the last P V of head h has completed (the epilogue's wait).
+enum Bar {
+  kQFull = 0, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
+  kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kPVDone0, kPVDone1, kODone0, kODone1, kDrain
+};
+
+__device__ __forceinline__ bool wait_t2(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        uint32_t* err) {
+  if (*abort_flag) return false;
+  if (mbar_wait_bounded(bar, parity, err)) return true;
+  *abort_flag = 1;
+  return false;
+}
+
+// Work item -> (sequence, query tile), the tiles of each sequence from its
+// last (heaviest under the causal mask) to its first; one warp scans
+// cu_seqlens 32 sequences at a time.
+__device__ __forceinline__ bool tc2_locate(const Tc2Params& p, int item, int lane, int& s,
+                                           int& tile, int& ctx, int& len) {
+  int before = 0;
+  for (int base = 0; base < p.num_seqs; base += 32) {
+    const int i = base + lane;
+    int n = 0, L = 0;
+    if (i < p.num_seqs) {
+      L = p.cu_seqlens[i + 1] - p.cu_seqlens[i];
+      n = L > 0 ? (L + kBM - 1) / kBM : 0;
+    }
+    int x = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    const int lo = before + x - n;
+    const unsigned hit = __ballot_sync(0xffffffffu, i < p.num_seqs && item >= lo && item < lo + n);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      s = base + src;
+      tile = __shfl_sync(0xffffffffu, n, src) - 1 - (item - __shfl_sync(0xffffffffu, lo, src));
+      len = __shfl_sync(0xffffffffu, L, src);
+      ctx = p.context_lens ? p.context_lens[s] : 0;
+      return true;
+    }
+    before += __shfl_sync(0xffffffffu, x, 31);
+  }
+  return false;
+}
+
+// TMA producer (one warp): both heads' query tiles once, then each 128-token
+// K and V tile, one box per physical block per 64-wide chunk.
+template <int D>
+__device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorMap* tm_q,
+                                             const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                             uint8_t* smem, uint64_t* bars,
+                                             volatile int* abort_flag, int s, int h0, int g,
+                                             int tok0, int kv_len, int n_tiles, int lane) {
+  using L = Tc2Layout<D>;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kStageBytes);
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+#pragma unroll
+      for (int c = 0; c < L::kHalves; ++c)
+        tma_load_3d(smem + L::kQ + x * L::kStageBytes + c * kChunk, tm_q, &bars[kQFull], c * 64,
+                    h0 + x, tok0);
+  }
+  const int nsub = kBN / p.box_tokens;
+  const uint32_t box_bytes = static_cast<uint32_t>(p.box_tokens) * 128u;
+  for (int j = 0; j < n_tiles; ++j) {
+    const int stage = j & 1;
+    const int tok = j * kBN + lane * p.box_tokens;
+    int pb = -1;
+    if (lane < nsub && tok < kv_len)
+      pb = __ldg(&p.block_table[static_cast<long long>(s) * p.max_blocks + (tok >> p.log2_bs)]);
+    bool valid = false;
+    if (lane < nsub && tok < kv_len) {
+      if (pb < 0 || pb >= p.num_blocks) set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
+      else valid = true;
+    }
+    const int in_blk = tok & (p.block_size - 1);
+    // K(j) once both heads' S(j-2) have consumed its stage, V(j) once both
+    // heads' P V(j-2) have.
+    for (int part = 0; part < 2; ++part) {
+      const int empty = part ? kVEmpty0 : kKEmpty0, full = part ? kVFull0 : kKFull0;
+      const bool ok = wait_t2(&bars[empty + stage], ((j >> 1) & 1) ^ 1, abort_flag, p.err_flag);
+      const bool go = valid && ok;
+      const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, go));
+      if (lane == 0) mbar_arrive_expect_tx(&bars[full + stage], nvalid * box_bytes * L::kHalves);
+      __syncwarp();
+      if (go) {
+        uint8_t* dst = smem + (part ? L::kV : L::kK) + stage * L::kStageBytes + lane * box_bytes;
+#pragma unroll
+        for (int c = 0; c < L::kHalves; ++c)
+          tma_load_4d(dst + c * kChunk, part ? tm_v : tm_k, &bars[full + stage], c * 64, g, in_blk,
+                      pb);
+      }
+    }
+  }
+  // Every copy issued must land before shared memory can be released.
+  for (int j = n_tiles > kStages ? n_tiles - kStages : 0; j < n_tiles; ++j) {
+    mbar_wait_bounded(&bars[kKFull0 + (j & 1)], (j >> 1) & 1, p.err_flag);
+    mbar_wait_bounded(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, p.err_flag);
+  }
+}
+
+// One thread.  Streams: S_A(j), S_B(j) (S_B never ahead of S_A, so the
+// commit after S_B(j) releases K(j) for both) and P V in use order
+// u = 2j + head.  Whatever is ready is issued, P V first.  A stall of
+// kWaitLimitNs without progress sets KVC_FLAG_WAIT_TIMEOUT and aborts.
+template <int D, bool kBf16>
+__device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
+                                        volatile int* abort_flag, uint32_t tmem, int n_tiles) {
+  using L = Tc2Layout<D>;
+  constexpr uint32_t idesc_s = umma_idesc_f16(kBf16, kBM, kBN, 0, 0);
+  constexpr uint32_t idesc_o = umma_idesc_f16(kBf16, kBM, D, 0, 1);
+  const uint64_t q0 = umma_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+  const uint64_t k0 = umma_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
+  const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kV), kChunk, 1024);
+  const uint64_t p0 = umma_desc_sw128(smem_u32(smem + L::kP), 16, 1024);
+  if (!wait_t2(&bars[kQFull], 0, abort_flag, p.err_flag)) return;
+  int ns[2] = {0, 0}, u = 0;
+  const int n_use = 2 * n_tiles;
+  unsigned long long t_prog = 0;
+  int idle = 0;
+  while (u < n_use) {
+    if (*abort_flag) return;
+    bool progress = false;
+    {  // P V of use u
+      const int j = u >> 1, x = u & 1;
+      if (j < ns[x] && mbar_test_wait(&bars[kVFull0 + (j & 1)], (j >> 1) & 1) &&
+          mbar_test_wait(&bars[kPFull], u & 1)) {
+        tc_fence_after();
+        const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
+        const uint32_t d = tmem + tmem_o(x);
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t a = desc_advance(p0, (ks >> 2) * kChunk + (ks & 3) * 32);
+          const uint64_t b = desc_advance(v_st, ks * 16 * 128);
+          if (j == 0 && ks == 0) umma_f16_fresh(d, a, b, idesc_o);
+          else umma_f16_acc(d, a, b, idesc_o);
+        }
+        umma_commit(&bars[kPVDone0 + x]);
+        if (x == 1) umma_commit(&bars[kVEmpty0 + (j & 1)]);
+        if (j == n_tiles - 1) umma_commit(&bars[kODone0 + x]);
+        ++u;
+        progress = true;
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {  // S of head x
+      const int j = ns[x];
+      if (j >= n_tiles || (x == 1 && j >= ns[0])) continue;
+      if (mbar_test_wait(&bars[kKFull0 + (j & 1)], (j >> 1) & 1) &&
+          mbar_test_wait(&bars[kSFree0 + x], (j & 1) ^ 1)) {
+        tc_fence_after();
+        const uint32_t d = tmem + tmem_s(x);
+        const uint64_t qx = desc_advance(q0, x * L::kStageBytes);
+        const uint64_t k_st = desc_advance(k0, (j & 1) * L::kStageBytes);
+#pragma unroll
+        for (int c = 0; c < L::kHalves; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = desc_advance(qx, c * kChunk + kk * 32);
+            const uint64_t b = desc_advance(k_st, c * kChunk + kk * 32);
+            if (c == 0 && kk == 0) umma_f16_fresh(d, a, b, idesc_s);
+            else umma_f16_acc(d, a, b, idesc_s);
+          }
+        umma_commit(&bars[kSFull0 + x]);
+        if (x == 1) umma_commit(&bars[kKEmpty0 + (j & 1)]);
+        ++ns[x];
+        progress = true;
+      }
+    }
+    if (progress) {
+      idle = 0;
+      t_prog = 0;
+    } else if (++idle >= 64) {
+      idle = 0;
+      const unsigned long long now = global_timer_ns();
+      if (t_prog == 0) {
+        t_prog = now;
+      } else if (now - t_prog > kWaitLimitNs) {
+        set_flag(p.err_flag, KVC_FLAG_WAIT_TIMEOUT);
+        *abort_flag = 1;
+        return;
+      }
+    }
+  }
+}
+
+// Softmax warpgroup of head x (threads x*128 .. +127): thread owns query row
+// `row`, all 128 columns of each tile.
+template <typename T, int D>
+__device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
+                                            volatile int* abort_flag, uint32_t tmem, int x,
+                                            int row, int n_tiles, int q0, int ctx, int kv_len,
+                                            int q_rows, int tok0, int h) {
+  using L = Tc2Layout<D>;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(row & ~31) << 16);
+  const int pos = ctx + q0 + row;
+  float m_used = -INFINITY, l = 0.f;
+  for (int j = 0; j < n_tiles; ++j) {
+    wait_t2(&bars[kSFull0 + x], j & 1, abort_flag, p.err_flag);
+    tc_fence_after();
+    float s[kBN];
+#pragma unroll
+    for (int c = 0; c < kBN / 16; ++c) tmem_ld16(lane_base + tmem_s(x) + c * 16, s + c * 16);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&bars[kSFree0 + x]);
+
+    // Row max of the raw scores (the scale is positive, so it commutes with
+    // the max and is folded into the exponent below).  Causal + length mask:
+    // token k of the tile is visible iff k < lim; only tiles that reach past
+    // this row take the masked path.
+    const int kv0 = j * kBN;
+    const int lim = min(pos + 1, kv_len) - kv0;
+    float mx8[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
+    if (lim >= kBN) {
+#pragma unroll
+      for (int k = 0; k < kBN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kBN; ++k) {
+        s[k] = k < lim ? s[k] : -INFINITY;
+        mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
+      }
+    }
+    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                     p.scale_log2;
+    float corr = 1.f;
+    bool rescale = false;
+    if (m_used == -INFINITY) {
+      m_used = mx;
+      corr = 0.f;
+    } else if (mx > m_used + kRescaleThreshold) {
+      corr = fast_exp2(m_used - mx);
+      m_used = mx;
+      rescale = true;
+    }
+    // p = 2^(s * scale_log2 - m_used); a row with nothing visible yet keeps
+    // m_used = -inf and all its scores at -inf, so its p are 0.
+    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+    const float sc = p.scale_log2;
+    uint32_t pk[kBN / 2];
+    float ps[4] = {0.f, 0.f, 0.f, 0.f}, ra, rb;
+#pragma unroll
+    for (int k = 0; k < kBN / 2; ++k) {
+      pk[k] = Pack<T>::run(fast_exp2(fmaf(s[2 * k], sc, neg_m)),
+                           fast_exp2(fmaf(s[2 * k + 1], sc, neg_m)), ra, rb);
+      ps[k & 3] += ra + rb;
+    }
+    l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+
+    // The P buffer's previous user: head B of tile j-1 (for head A) or head
+    // A of tile j (for head B); that also means this head's previous P V is
+    // done, so O may be rescaled.
+    if (x == 1 || j > 0) {
+      const int prev_j = x == 1 ? j : j - 1;
+      wait_t2(&bars[kPVDone0 + (x ^ 1)], prev_j & 1, abort_flag, p.err_flag);
+      tc_fence_after();
+    }
+    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        float v[16];
+        const uint32_t a = lane_base + tmem_o(x) + c * 16;
+        tmem_ld16(a, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] *= corr;
+        tmem_st16(a, v);
+      }
+      tmem_wait_st();
+    }
+    // P row -> shared memory: chunk c holds tokens 64c .. 64c+63.
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint8_t* pc = smem + L::kP + c * kChunk;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(pc + swz128(row, ch)) =
+            make_uint4(pk[32 * c + 4 * ch], pk[32 * c + 4 * ch + 1], pk[32 * c + 4 * ch + 2],
+                       pk[32 * c + 4 * ch + 3]);
+    }
+    // Before the first P V of tile j (head 0's), value rows past the cached
+    // tokens are zeroed so stale cache contents cannot reach P V.
+    const int valid = kv_len - j * kBN;
+    if (x == 0 && valid < kBN) {
+      wait_t2(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, abort_flag, p.err_flag);
+      uint8_t* vst = smem + L::kV + (j & 1) * L::kStageBytes;
+      const int n16 = (kBN - valid) * L::kHalves * 8;
+      for (int e = row; e < n16; e += kHeadThreads) {
+        const int r = valid + e / (L::kHalves * 8), c = (e / 8) % L::kHalves, q = e % 8;
+        *reinterpret_cast<uint4*>(vst + c * kChunk + r * 128 + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(&bars[kPFull]);
+  }
+
+  // Epilogue: normalise and write this head's row.
+  wait_t2(&bars[kODone0 + x], 0, abort_flag, p.err_flag);
+  tc_fence_after();
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  T* o = static_cast<T*>(p.out) + (static_cast<long long>(tok0) + row) * p.num_q_heads * D + h * D;
+#pragma unroll
+  for (int c = 0; c < D / 16; ++c) {
+    float v[16];
+    tmem_ld16(lane_base + tmem_o(x) + c * 16, v);
+    tmem_wait_ld();
+    if (row < q_rows) {
+      uint32_t w[8];
+      float a, b;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, a, b);
+      *reinterpret_cast<uint4*>(o + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(o + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+  tc_fence_before();
+}
+
+template <typename T, int D, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ Tc2Params p) {
+  using L = Tc2Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  int* info = reinterpret_cast<int*>(smem + L::kMisc + 16);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pairs = p.num_q_heads / 2;
+  const int h0 = 2 * (blockIdx.x % pairs);
+  const int item = blockIdx.x / pairs;
+
+  if (warp == 0) {
+    int s = 0, tile = 0, ctx = 0, len = 0;
+    const bool found = tc2_locate(p, item, lane, s, tile, ctx, len);
+    if (lane == 0) {
+      info[0] = found ? s : -1;
+      info[1] = tile;
+      info[2] = ctx;
+      info[3] = len;
+      for (int i = 0; i < L::kNumBars; ++i) {
+        uint32_t c = 1;
+        if (i == kSFree0 || i == kSFree1 || i == kPFull) c = kHeadThreads;
+        mbar_init(&bars[i], c);
+      }
+      *abort_flag = 0;
+      fence_barrier_init();
+    }
+  }
+  __syncthreads();
+  const int s = info[0];
+  if (s < 0) return;  // grid slots beyond the real number of tiles
+  const int q0 = info[1] * kBM, ctx = info[2], len = info[3];
+  const int q_rows = min(kBM, len - q0);
+  const int kv_len = ctx + len;
+  if (kv_len > p.max_blocks * p.block_size) {  // table too short: flag, write nothing
+    if (tid == 0) set_flag(p.err_flag, KVC_FLAG_LEN_RANGE);
+    return;
+  }
+  const int n_tiles = (ctx + q0 + q_rows - 1) / kBN + 1;
+  const int tok0 = p.cu_seqlens[s] + q0;
+
+  if (warp == kMmaWarp) tmem_alloc(tslot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp < kProducerWarp) {
+    const int x = tid / kHeadThreads;
+    tc2_softmax<T, D>(p, smem, bars, abort_flag, tmem, x, tid % kHeadThreads, n_tiles, q0, ctx,
+                      kv_len, q_rows, tok0, h0 + x);
+  } else if (warp == kProducerWarp) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+    }
+    tc2_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, s, h0, h0 / p.group, tok0,
+                    kv_len, n_tiles, lane);
+  } else if (lane == 0) {
+    tc2_mma<D, kBf16>(p, smem, bars, abort_flag, tmem, n_tiles);
+  }
+  // Teardown: all tensor-core work done before TMEM is freed.
+  if (warp == kMmaWarp && lane == 0) {
+    umma_commit(&bars[kDrain]);
+    mbar_wait_bounded(&bars[kDrain], 0, p.err_flag);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <typename T, int D, bool kBf16>
+kvc_status run_prefill_tc2(const PrefillArgs& a) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(prefill_tc2_kernel<T, D, kBf16>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Layout<D>::kTotal);
+  });
+  CUtensorMap tq, tk, tv;
+  const uint64_t qdims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_q_heads),
+                             static_cast<uint64_t>(a.num_tokens)};
+  const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 2,
+                                static_cast<uint64_t>(a.num_q_heads) * D * 2};
+  const uint32_t qbox[3] = {64, 1, kBM};
+  const int box_tokens = a.block_size < kBN ? a.block_size : kBN;
+  const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_kv_heads),
+                            static_cast<uint64_t>(a.block_size),
+                            static_cast<uint64_t>(a.num_blocks)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2,
+                               static_cast<uint64_t>(a.num_kv_heads) * D * 2,
+                               static_cast<uint64_t>(a.block_size) * a.num_kv_heads * D * 2};
+  const uint32_t box[4] = {64, 1, static_cast<uint32_t>(box_tokens), 1};
+  if (!encode_tmap_16bit(&tq, a.dtype, 3, a.q, qdims, qstrides, qbox, true) ||
+      !encode_tmap_16bit(&tk, a.dtype, 4, a.key_cache, dims, strides, box, true) ||
+      !encode_tmap_16bit(&tv, a.dtype, 4, a.value_cache, dims, strides, box, true))
+    return KVC_ERR_CUDA;
+  Tc2Params p;
+  p.out = a.out;
+  p.cu_seqlens = a.cu_seqlens;
+  p.context_lens = a.context_lens;
+  p.block_table = a.block_table;
+  p.err_flag = a.err_flag;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.log2_bs = ilog2(a.block_size);
+  p.max_blocks = a.max_blocks_per_seq;
+  p.num_blocks = a.num_blocks;
+  p.box_tokens = box_tokens;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  // Upper bound of query tiles: sum ceil(L_s / BM) <= T / BM + S.
+  const long long grid =
+      (static_cast<long long>(a.num_tokens) / kBM + a.num_seqs) * (a.num_q_heads / 2);
+  if (grid > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+  prefill_tc2_kernel<T, D, kBf16><<<static_cast<unsigned>(grid), kThreads, Tc2Layout<D>::kTotal,
+                                    a.stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+}  // namespace
+
+// Two heads per CTA; the caller checks that the GQA group size is even.
+kvc_status launch_prefill_attention_tc2(const PrefillArgs& a) {
+  if (a.head_dim == 64)
+    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 64, true>(a)
+                               : run_prefill_tc2<__half, 64, false>(a);
+  if (a.head_dim == 128)
+    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 128, true>(a)
+                               : run_prefill_tc2<__half, 128, false>(a);
+  return KVC_ERR_UNSUPPORTED;
+}
+
+}  // namespace kvc

@@ -2,7 +2,8 @@
 // paged cache at slot_mapping (ai6s.net KVCache article 4.2: each layer
 // writes its cache, then FA reads it -- "external-cannbot-model-model-infer-
 // kvcache" 3.6), then every packed token attends causally to its own
-// sequence through the cache (prefill_tc.cu).
+// sequence through the cache (prefill_tc2.cu for an even GQA group size --
+// two heads per CTA sharing the K/V stream -- else prefill_tc.cu).
 #include <cuda_runtime.h>
 
 #include "kvc_device.cuh"
@@ -18,6 +19,7 @@ kvc_status launch_varlen_prefill(const PrefillArgs& a) {
                                            a.err_flag, a.stream);
   if (st != KVC_OK) return st;
   // 2. Causal attention of every packed token over its sequence's cache.
+  if ((a.num_q_heads / a.num_kv_heads) % 2 == 0) return launch_prefill_attention_tc2(a);
   return launch_prefill_attention_tc(a);
 }
 

@@ -176,3 +176,26 @@ def test_full_size_mixed_prefill_sampled(kvc_lib):
                 ref = O.softmax_attention(qrow[h], K[:i + 1, gg], V[:i + 1, gg], pre.scale)
                 worst = max(worst, float(np.abs(out[t, h].double().cpu().numpy() - ref).max()))
     assert worst <= TOL["bf16"], worst
+
+
+def test_prefill_head_pairs_repeatable_at_tile_boundaries(kvc_lib):
+    """Two heads per CTA share one P buffer: lengths that end one row into a new tile, repeated.
+
+    Repeats must match the oracle and each other bit for bit (a premature reuse of
+    the shared P buffer shows up as a timing-dependent error in one head).
+    """
+    lens = [1, 127, 128, 129, 255, 257, 3]
+    for Hq, Hkv in ((8, 2), (4, 2), (16, 8)):
+        c = prefill_case(36, lens, Hq, Hkv, 128, 16, context=[0] * len(lens), dtype="bf16")
+        _, ref = oracle_prefill(c)
+        first = None
+        for _ in range(4):
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
+            _, _, out = gpu_prefill(kvc_lib, c, err)
+            assert int(err.item()) == 0
+            e = float(np.abs(out.double().cpu().numpy() - ref).max())
+            assert e <= TOL["bf16"], (Hq, Hkv, e)
+            if first is None:
+                first = out.clone()
+            else:
+                assert torch.equal(out, first), (Hq, Hkv)
