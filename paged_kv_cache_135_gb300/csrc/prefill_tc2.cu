@@ -87,6 +87,36 @@ enum Bar {
   kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kPVDone0, kPVDone1, kODone0, kODone1, kDrain
 };
 
+// Paired fp32 arithmetic (one instruction for two lanes of a float2) and a
+// round-to-nearest pack of two floats into 16-bit pairs.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&r);
+}
+template <typename T>
+__device__ __forceinline__ uint32_t pack_pair(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack_pair<__nv_bfloat16>(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack_pair<__half>(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 __device__ __forceinline__ bool wait_t2(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                         uint32_t* err) {
   if (*abort_flag) return false;
@@ -326,17 +356,21 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     }
     // p = 2^(s * scale_log2 - m_used); a row with nothing visible yet keeps
     // m_used = -inf and all its scores at -inf, so its p are 0.
+    // The row sum l adds the exponentials before rounding (P itself is
+    // rounded to T for the tensor core).
     const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-    const float sc = p.scale_log2;
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
     uint32_t pk[kBN / 2];
-    float ps[4] = {0.f, 0.f, 0.f, 0.f}, ra, rb;
+    float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int k = 0; k < kBN / 2; ++k) {
-      pk[k] = Pack<T>::run(fast_exp2(fmaf(s[2 * k], sc, neg_m)),
-                           fast_exp2(fmaf(s[2 * k + 1], sc, neg_m)), ra, rb);
-      ps[k & 3] += ra + rb;
+      const float2 x = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc2, nm2);
+      const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      pk[k] = pack_pair<T>(e.x, e.y);
+      ps2[k & 1] = add2(ps2[k & 1], e);
     }
-    l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+    const float2 pst = add2(ps2[0], ps2[1]);
+    l = l * corr + (pst.x + pst.y);
 
     // The P buffer's previous user: head B of tile j-1 (for head A) or head
     // A of tile j (for head B); that also means this head's previous P V is
