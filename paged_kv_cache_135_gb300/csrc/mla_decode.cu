@@ -484,20 +484,29 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const float4 v = x_mine[(h * 8 + q) * kH + row];
-      s[4 * q] += v.x;
-      s[4 * q + 1] += v.y;
-      s[4 * q + 2] += v.z;
-      s[4 * q + 3] += v.w;
+      const float2 a = add2(make_float2(s[4 * q], s[4 * q + 1]), make_float2(v.x, v.y));
+      const float2 b = add2(make_float2(s[4 * q + 2], s[4 * q + 3]), make_float2(v.z, v.w));
+      s[4 * q] = a.x;
+      s[4 * q + 1] = a.y;
+      s[4 * q + 2] = b.x;
+      s[4 * q + 3] = b.y;
     }
     const int tile_valid = min(kTok, cm.len - cm.j * kTok);
     const int valid = tile_valid - h * 32;  // of this thread's 32 tokens
+    // Row max of the raw scores (the positive scale is folded into the
+    // exponent below); tokens past the sequence only in a tail tile.
     float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (valid >= 32) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      s[k] = k < valid ? s[k] * p.scale_log2 : -INFINITY;
-      mx4[k & 3] = fmaxf(mx4[k & 3], s[k]);
+      for (int k = 0; k < 32; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], s[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        s[k] = k < valid ? s[k] : -INFINITY;
+        mx4[k & 3] = fmaxf(mx4[k & 3], s[k]);
+      }
     }
-    red[h * kH + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    red[h * kH + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
     named_bar_sync(3, kMathThreads);  // also: every thread has read X
     if (elected) {
       // The next tile's scores arrive as 32 KB of transactions on x_full.
@@ -515,14 +524,21 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
       m_used = mx;
       rescale = true;
     }
+    // p = 2^(s * scale_log2 - m_used); l adds the exponentials before
+    // rounding (P itself is rounded to T for the tensor core).
+    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
     uint32_t pk[16];
-    float ps[4] = {0.f, 0.f, 0.f, 0.f}, ra, rb;
+    float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      pk[k] = Pack<T>::run(fast_exp2(s[2 * k] - m_used), fast_exp2(s[2 * k + 1] - m_used), ra, rb);
-      ps[k & 3] += ra + rb;
+      const float2 x = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc2, nm2);
+      const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      pk[k] = pack_pair<T>(e.x, e.y);
+      ps2[k & 1] = add2(ps2[k & 1], e);
     }
-    l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+    const float2 pst = add2(ps2[0], ps2[1]);
+    l = l * corr + (pst.x + pst.y);
     if (it > 0) {  // P V of the previous tile must be done before P and O are touched
       wait_cta(&bars[kPVDone], (it - 1) & 1, abort_flag, p.err_flag);
       tc_fence_after();

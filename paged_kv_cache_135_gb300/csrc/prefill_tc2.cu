@@ -87,36 +87,6 @@ enum Bar {
   kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kPVDone0, kPVDone1, kODone0, kODone1, kDrain
 };
 
-// Paired fp32 arithmetic (one instruction for two lanes of a float2) and a
-// round-to-nearest pack of two floats into 16-bit pairs.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(r)
-      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
-        "l"(*reinterpret_cast<const uint64_t*>(&c)));
-  return *reinterpret_cast<float2*>(&r);
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;"
-      : "=l"(r)
-      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
-  return *reinterpret_cast<float2*>(&r);
-}
-template <typename T>
-__device__ __forceinline__ uint32_t pack_pair(float a, float b);
-template <>
-__device__ __forceinline__ uint32_t pack_pair<__nv_bfloat16>(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-template <>
-__device__ __forceinline__ uint32_t pack_pair<__half>(float a, float b) {
-  __half2 v = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 __device__ __forceinline__ bool wait_t2(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                         uint32_t* err) {
   if (*abort_flag) return false;
