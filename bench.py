@@ -68,6 +68,29 @@ def write_bytes(B, Hkv, D, elt=2):
     return 2 * (2 * B * Hkv * D * elt) + 3 * 4 * B
 
 
+DECODE_METRIC = "paged decode achieved HBM GB/s (algorithmic bytes) and decode tokens/s"
+
+
+def decode_workload(name, case, ws):
+    """(config dict, decode bytes, step bytes) of a decode workload; both arms print this config."""
+    m = case.meta
+    B = case.q.shape[0]
+    lens = case.seq_lens.tolist()
+    d_bytes = decode_bytes(lens, m["num_q_heads"], m["num_kv_heads"], m["head_dim"],
+                           case.block_size)
+    step_bytes = d_bytes + write_bytes(B, m["num_kv_heads"], m["head_dim"])
+    config = {
+        "workload": CONFIGS[name]["about"],
+        "batch": B, "num_q_heads": m["num_q_heads"], "num_kv_heads": m["num_kv_heads"],
+        "head_dim": m["head_dim"], "block_size": case.block_size,
+        "kv_tokens": int(sum(lens)), "step": "slot mapping + cache write + paged decode "
+        "(split-KV, fused merge), replayed from CUDA graphs", "algorithmic_bytes_per_step": step_bytes,
+        "l2": "no flush: each step reads %.0f MB of K/V, more than the 129 MB L2" % (d_bytes / 1e6),
+        "parallelism": f"replicas x{ws}",
+    }
+    return config, d_bytes, step_bytes
+
+
 def kernel_source_digest():
     h = hashlib.sha256()
     for name in ("paged_decode.cu", "kvc_device.cuh"):
@@ -225,12 +248,12 @@ def run_reference(args):
     value = statistics.median(v[0] for v in vals)
     n_seq = vals[0][1]
     print(json.dumps({
-        "impl": "reference", "metric": "paged decode achieved HBM GB/s (algorithmic bytes)",
+        "impl": "reference", "metric": DECODE_METRIC,
         "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(v[2] for v in vals),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": CONFIGS[WORKLOAD]["about"]},
+        "config": decode_workload(WORKLOAD, case, ws)[0],
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"first {n_seq} of 64 sequences per step (fp64 NumPy oracle)"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -521,7 +544,7 @@ def main():
 
     if rank == 0:
         res = {
-            "metric": "paged decode achieved HBM GB/s (algorithmic bytes) and decode tokens/s",
+            "metric": DECODE_METRIC,
             "value": value,
             "unit": "GB/s",
             "n_gpus": ws,
@@ -533,16 +556,7 @@ def main():
             "vs_baseline": None,
             "dtype": case.dtype,
             "data": "synthetic",
-            "config": {
-                "workload": CONFIGS[args.workload]["about"],
-                "batch": B, "num_q_heads": m["num_q_heads"], "num_kv_heads": m["num_kv_heads"],
-                "head_dim": m["head_dim"], "block_size": case.block_size,
-                "kv_tokens": int(sum(lens)), "step": "slot mapping + cache write + paged decode "
-                "(split-KV, fused merge), replayed from CUDA graphs", "algorithmic_bytes_per_step": step_bytes,
-                "l2": "no flush: each step reads %.0f MB of K/V, more than the 129 MB L2"
-                      % (d_bytes / 1e6),
-                "parallelism": f"replicas x{ws}",
-            },
+            "config": decode_workload(args.workload, case, ws)[0],
             "decode_tokens_per_s": tokens_per_s,
             "pct_of_nominal_8tbps": 100.0 * value / NOMINAL_HBM_GBS,
             "roofline": {
