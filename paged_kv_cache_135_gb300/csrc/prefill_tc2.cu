@@ -14,14 +14,17 @@
 // tiles (TMA through block_table, 2-stage rings), so every K/V byte feeds
 // two heads.  Tensor memory holds O and S for each head (4 x 128 columns).
 // Each head has its own softmax warpgroup, one thread per query row and all
-// 128 columns of the tile: the thread pulls its S row into registers and
-// frees the S buffer at once, so the tensor core computes the head's next S
-// while the thread runs the exponentials; no cross-thread reduction is
-// needed.  The two heads alternate on one P buffer (bf16/fp16, 128-byte
-// swizzled shared memory).  One thread issues the MMAs in whatever order
-// their inputs become ready (S of either head, P V in alternating order).
-// Online softmax in the log2 domain; O is rescaled only when a row's max
-// grows by more than 2^8.
+// 128 columns of the tile (no cross-thread reduction).  P (bf16/fp16) is
+// written back into the head's S columns of tensor memory and read from
+// there as the A operand of P V, so each head runs S -> softmax -> P V ->
+// next S while the tensor core works on the other head.  The signal that S
+// of a tile is complete also means every earlier MMA of the issuing thread
+// is complete (tcgen05.commit tracks all of them), so P and O may be written
+// without a further wait; the next S of a head is issued after its P V, and
+// the tensor core performs one thread's MMAs in issue order.  One thread
+// issues the MMAs in whatever order their inputs become ready.  Online
+// softmax in the log2 domain; O is rescaled only when a row's max grows by
+// more than 2^8.
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -68,23 +71,18 @@ struct Tc2Layout {
   static constexpr int kQ = 0;                                 // head A then head B
   static constexpr int kK = kQ + 2 * kStageBytes;
   static constexpr int kV = kK + kStages * kStageBytes;
-  static constexpr int kP = kV + kStages * kStageBytes;        // 2 chunks (128 tokens)
-  static constexpr int kBar = kP + 2 * kChunk;
-  static constexpr int kNumBars = 19;
+  static constexpr int kBar = kV + kStages * kStageBytes;
+  static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBar + kNumBars * 8;            // tmem slot, abort, info[4]
   static constexpr int kTotal = 1024 + kMisc + 64;
   static_assert(kTotal <= 232448, "fits the opt-in shared memory of one SM");
 };
 
-// pv_done[h]: one completion per P V of head h.  The P buffer passes A(0),
-// B(0), A(1), B(1), ...: head A writes P(j) after pv_done[B] completion j-1,
-// head B after pv_done[A] completion j.  Each of those waits is at most one
-// phase behind its barrier, so the parity is unambiguous (one barrier shared
-// by both heads would be two phases apart between a head's waits).
-// o_done[h]: the last P V of head h has completed (the epilogue's wait).
+// k_empty / v_empty complete when both heads' S / P V of the tile are done
+// (count 2); s_full[h], p_full[h], o_done[h] are per head.
 enum Bar {
   kQFull = 0, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-  kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kPVDone0, kPVDone1, kODone0, kODone1, kDrain
+  kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kDrain
 };
 
 __device__ __forceinline__ bool wait_t2(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -186,10 +184,11 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
   }
 }
 
-// One thread.  Streams: S_A(j), S_B(j) (S_B never ahead of S_A, so the
-// commit after S_B(j) releases K(j) for both) and P V in use order
-// u = 2j + head.  Whatever is ready is issued, P V first.  A stall of
-// kWaitLimitNs without progress sets KVC_FLAG_WAIT_TIMEOUT and aborts.
+// One thread.  Per head x: S_x(0), P V_x(0), S_x(1), P V_x(1), ... (S of
+// the next tile once the head's P V is issued, so P in its S columns has
+// been read first); the two heads interleave in whatever order their inputs
+// become ready, P V first.  A stall of kWaitLimitNs without progress sets
+// KVC_FLAG_WAIT_TIMEOUT and aborts.
 template <int D, bool kBf16>
 __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
                                         volatile int* abort_flag, uint32_t tmem, int n_tiles) {
@@ -199,59 +198,55 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
   const uint64_t q0 = umma_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
   const uint64_t k0 = umma_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
   const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kV), kChunk, 1024);
-  const uint64_t p0 = umma_desc_sw128(smem_u32(smem + L::kP), 16, 1024);
   if (!wait_t2(&bars[kQFull], 0, abort_flag, p.err_flag)) return;
-  int ns[2] = {0, 0}, u = 0;
-  const int n_use = 2 * n_tiles;
+  int ns[2] = {0, 0}, npv[2] = {0, 0};
   unsigned long long t_prog = 0;
   int idle = 0;
-  while (u < n_use) {
+  while (npv[0] < n_tiles || npv[1] < n_tiles) {
     if (*abort_flag) return;
     bool progress = false;
-    {  // P V of use u
-      const int j = u >> 1, x = u & 1;
-      if (j < ns[x] && mbar_test_wait(&bars[kVFull0 + (j & 1)], (j >> 1) & 1) &&
-          mbar_test_wait(&bars[kPFull], u & 1)) {
-        tc_fence_after();
-        const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
-        const uint32_t d = tmem + tmem_o(x);
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t a = desc_advance(p0, (ks >> 2) * kChunk + (ks & 3) * 32);
-          const uint64_t b = desc_advance(v_st, ks * 16 * 128);
-          if (j == 0 && ks == 0) umma_f16_fresh(d, a, b, idesc_o);
-          else umma_f16_acc(d, a, b, idesc_o);
-        }
-        umma_commit(&bars[kPVDone0 + x]);
-        if (x == 1) umma_commit(&bars[kVEmpty0 + (j & 1)]);
-        if (j == n_tiles - 1) umma_commit(&bars[kODone0 + x]);
-        ++u;
-        progress = true;
-      }
-    }
+    for (int x = 0; x < 2; ++x) {
+      {  // P V_x of tile npv[x]: A = P in the head's S columns of tensor memory
+        const int j = npv[x];
+        if (j < ns[x] && mbar_test_wait(&bars[kVFull0 + (j & 1)], (j >> 1) & 1) &&
+            mbar_test_wait(&bars[kPFull0 + x], j & 1)) {
+          tc_fence_after();
+          const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
+          const uint32_t d = tmem + tmem_o(x), a0 = tmem + tmem_s(x);
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {  // S of head x
-      const int j = ns[x];
-      if (j >= n_tiles || (x == 1 && j >= ns[0])) continue;
-      if (mbar_test_wait(&bars[kKFull0 + (j & 1)], (j >> 1) & 1) &&
-          mbar_test_wait(&bars[kSFree0 + x], (j & 1) ^ 1)) {
-        tc_fence_after();
-        const uint32_t d = tmem + tmem_s(x);
-        const uint64_t qx = desc_advance(q0, x * L::kStageBytes);
-        const uint64_t k_st = desc_advance(k0, (j & 1) * L::kStageBytes);
-#pragma unroll
-        for (int c = 0; c < L::kHalves; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = desc_advance(qx, c * kChunk + kk * 32);
-            const uint64_t b = desc_advance(k_st, c * kChunk + kk * 32);
-            if (c == 0 && kk == 0) umma_f16_fresh(d, a, b, idesc_s);
-            else umma_f16_acc(d, a, b, idesc_s);
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            const uint64_t b = desc_advance(v_st, ks * 16 * 128);
+            if (j == 0 && ks == 0) umma_f16_ts_fresh(d, a0, b, idesc_o);
+            else umma_f16_ts_acc(d, a0 + ks * 8, b, idesc_o);
           }
-        umma_commit(&bars[kSFull0 + x]);
-        if (x == 1) umma_commit(&bars[kKEmpty0 + (j & 1)]);
-        ++ns[x];
-        progress = true;
+          umma_commit(&bars[kVEmpty0 + (j & 1)]);
+          if (j == n_tiles - 1) umma_commit(&bars[kODone0 + x]);
+          ++npv[x];
+          progress = true;
+        }
+      }
+      {  // S_x of tile ns[x], once the head's previous P V has been issued
+        const int j = ns[x];
+        if (j < n_tiles && j == npv[x] && mbar_test_wait(&bars[kKFull0 + (j & 1)], (j >> 1) & 1)) {
+          tc_fence_after();
+          const uint32_t d = tmem + tmem_s(x);
+          const uint64_t qx = desc_advance(q0, x * L::kStageBytes);
+          const uint64_t k_st = desc_advance(k0, (j & 1) * L::kStageBytes);
+#pragma unroll
+          for (int c = 0; c < L::kHalves; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = desc_advance(qx, c * kChunk + kk * 32);
+              const uint64_t b = desc_advance(k_st, c * kChunk + kk * 32);
+              if (c == 0 && kk == 0) umma_f16_fresh(d, a, b, idesc_s);
+              else umma_f16_acc(d, a, b, idesc_s);
+            }
+          umma_commit(&bars[kSFull0 + x]);
+          umma_commit(&bars[kKEmpty0 + (j & 1)]);
+          ++ns[x];
+          progress = true;
+        }
       }
     }
     if (progress) {
@@ -289,8 +284,6 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
 #pragma unroll
     for (int c = 0; c < kBN / 16; ++c) tmem_ld16(lane_base + tmem_s(x) + c * 16, s + c * 16);
     tmem_wait_ld();
-    tc_fence_before();
-    mbar_arrive(&bars[kSFree0 + x]);
 
     // Row max of the raw scores (the scale is positive, so it commutes with
     // the max and is folded into the exponent below).  Causal + length mask:
@@ -342,14 +335,8 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     const float2 pst = add2(ps2[0], ps2[1]);
     l = l * corr + (pst.x + pst.y);
 
-    // The P buffer's previous user: head B of tile j-1 (for head A) or head
-    // A of tile j (for head B); that also means this head's previous P V is
-    // done, so O may be rescaled.
-    if (x == 1 || j > 0) {
-      const int prev_j = x == 1 ? j : j - 1;
-      wait_t2(&bars[kPVDone0 + (x ^ 1)], prev_j & 1, abort_flag, p.err_flag);
-      tc_fence_after();
-    }
+    // S(j) complete means this head's P V(j-1) is complete too, so O may be
+    // rescaled and P written over the S columns now.
     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
@@ -361,22 +348,16 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
         for (int k = 0; k < 16; ++k) v[k] *= corr;
         tmem_st16(a, v);
       }
-      tmem_wait_st();
     }
-    // P row -> shared memory: chunk c holds tokens 64c .. 64c+63.
+    // P row -> the first 64 columns of the head's S (two 16-bit tokens per
+    // column, token 2c in the low half of column c).
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      uint8_t* pc = smem + L::kP + c * kChunk;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(pc + swz128(row, ch)) =
-            make_uint4(pk[32 * c + 4 * ch], pk[32 * c + 4 * ch + 1], pk[32 * c + 4 * ch + 2],
-                       pk[32 * c + 4 * ch + 3]);
-    }
-    // Before the first P V of tile j (head 0's), value rows past the cached
-    // tokens are zeroed so stale cache contents cannot reach P V.
+    for (int c = 0; c < kBN / 32; ++c) tmem_st16_u32(lane_base + tmem_s(x) + c * 16, pk + c * 16);
+    tmem_wait_st();
+    // Value rows past the cached tokens are zeroed (by both heads, before
+    // either head's P V of the tile) so stale contents cannot reach P V.
     const int valid = kv_len - j * kBN;
-    if (x == 0 && valid < kBN) {
+    if (valid < kBN) {
       wait_t2(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, abort_flag, p.err_flag);
       uint8_t* vst = smem + L::kV + (j & 1) * L::kStageBytes;
       const int n16 = (kBN - valid) * L::kHalves * 8;
@@ -384,10 +365,10 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
         const int r = valid + e / (L::kHalves * 8), c = (e / 8) % L::kHalves, q = e % 8;
         *reinterpret_cast<uint4*>(vst + c * kChunk + r * 128 + q * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
+      fence_proxy_async_smem();
     }
-    fence_proxy_async_smem();
     tc_fence_before();
-    mbar_arrive(&bars[kPFull]);
+    mbar_arrive(&bars[kPFull0 + x]);
   }
 
   // Epilogue: normalise and write this head's row.
@@ -441,7 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       info[3] = len;
       for (int i = 0; i < L::kNumBars; ++i) {
         uint32_t c = 1;
-        if (i == kSFree0 || i == kSFree1 || i == kPFull) c = kHeadThreads;
+        if (i == kPFull0 || i == kPFull1) c = kHeadThreads;
+        if (i == kKEmpty0 || i == kKEmpty1 || i == kVEmpty0 || i == kVEmpty1) c = 2;
         mbar_init(&bars[i], c);
       }
       *abort_flag = 0;
