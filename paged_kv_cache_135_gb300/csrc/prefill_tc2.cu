@@ -78,8 +78,9 @@ struct Tc2Layout {
   static_assert(kTotal <= 232448, "fits the opt-in shared memory of one SM");
 };
 
-// k_empty / v_empty complete when both heads' S / P V of the tile are done
-// (count 2); s_full[h], p_full[h], o_done[h] are per head.
+// k_empty / v_empty complete when both heads' S / P V of the tile are done:
+// one commit after head 1's, which the tensor core performs after head 0's;
+// s_full[h], p_full[h], o_done[h] are per head.
 enum Bar {
   kQFull = 0, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
   kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kDrain
@@ -184,85 +185,97 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
   }
 }
 
-// One thread.  Per head x: S_x(0), P V_x(0), S_x(1), P V_x(1), ... (S of
-// the next tile once the head's P V is issued, so P in its S columns has
-// been read first); the two heads interleave in whatever order their inputs
-// become ready, P V first.  A stall of kWaitLimitNs without progress sets
-// KVC_FLAG_WAIT_TIMEOUT and aborts.
+// One thread, in a fixed order: S_0(0), S_1(0), then for each tile j and
+// head x one block of P V_x(j) followed by S_x(j+1) (the head's P in its S
+// columns is read before S_x(j+1) overwrites them: one thread's MMAs run in
+// issue order).  The tensor core keeps only a short queue, so any latency
+// between two MMAs of this thread is idle tensor time.  Hence a block issues
+// its 16 MMAs with nothing between them but commits; the barriers the next
+// block needs are tested inside the instruction sequence of the block's last
+// two MMAs (their latency hides behind those issues), and the thread blocks
+// in a wait only when an input is really not ready yet.  A wait that runs
+// past kWaitLimitNs sets KVC_FLAG_WAIT_TIMEOUT and aborts.
 template <int D, bool kBf16>
 __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
                                         volatile int* abort_flag, uint32_t tmem, int n_tiles) {
   using L = Tc2Layout<D>;
+  constexpr int kSSteps = D / 16;   // K steps of S = Q K^T
+  constexpr int kPSteps = kBN / 16; // K steps of O += P V
   constexpr uint32_t idesc_s = umma_idesc_f16(kBf16, kBM, kBN, 0, 0);
   constexpr uint32_t idesc_o = umma_idesc_f16(kBf16, kBM, D, 0, 1);
   const uint64_t q0 = umma_desc_sw128(smem_u32(smem + L::kQ), 16, 1024);
   const uint64_t k0 = umma_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
   const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kV), kChunk, 1024);
+
+  // S_x(j).  The next block is P V_y(t) + S_y(t+1): it needs P_y(t), V(t)
+  // and K(kt) (kt = t+1, or any tile whose K has surely landed when no S
+  // follows); returns whether all three were there before the last MMA.
+  auto s_group = [&](int x, int j, int y, int t, int kt) -> bool {
+    const uint32_t d = tmem + tmem_s(x);
+    const uint64_t qx = desc_advance(q0, x * L::kStageBytes);
+    const uint64_t k_st = desc_advance(k0, (j & 1) * L::kStageBytes);
+    auto a_at = [&](int st) { return desc_advance(qx, (st / 4) * kChunk + (st % 4) * 32); };
+    auto b_at = [&](int st) { return desc_advance(k_st, (st / 4) * kChunk + (st % 4) * 32); };
+#pragma unroll
+    for (int st = 0; st < kSSteps - 2; ++st) {
+      if (st == 0) umma_f16_fresh(d, a_at(st), b_at(st), idesc_s);
+      else umma_f16_acc(d, a_at(st), b_at(st), idesc_s);
+    }
+    const bool ready = umma_f16_acc2_test3(
+        d, a_at(kSSteps - 2), b_at(kSSteps - 2), a_at(kSSteps - 1), b_at(kSSteps - 1), idesc_s,
+        &bars[kPFull0 + y], t & 1, &bars[kVFull0 + (t & 1)], (t >> 1) & 1,
+        &bars[kKFull0 + (kt & 1)], (kt >> 1) & 1);
+    umma_commit(&bars[kSFull0 + x]);
+    if (x == 1) umma_commit(&bars[kKEmpty0 + (j & 1)]);
+    return ready;
+  };
+  // P V_x(j), A = P in the head's S columns of tensor memory.  Only the
+  // last tile's P V ends a block; it tests P_y(t) and V(t) for the next one.
+  auto pv_group = [&](int x, int j) {
+    const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
+    const uint32_t d = tmem + tmem_o(x), a0 = tmem + tmem_s(x);
+#pragma unroll
+    for (int ks = 0; ks < kPSteps; ++ks) {
+      const uint64_t b = desc_advance(v_st, ks * 16 * 128);
+      if (ks == 0) umma_f16_ts(d, a0, b, idesc_o, j > 0);
+      else umma_f16_ts_acc(d, a0 + ks * 8, b, idesc_o);
+    }
+    if (x == 1) umma_commit(&bars[kVEmpty0 + (j & 1)]);
+    if (j == n_tiles - 1) umma_commit(&bars[kODone0 + x]);
+  };
+  auto wait_inputs = [&](int x, int j, bool with_k) -> bool {
+    return wait_t2(&bars[kPFull0 + x], j & 1, abort_flag, p.err_flag) &&
+           wait_t2(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, abort_flag, p.err_flag) &&
+           (!with_k ||
+            wait_t2(&bars[kKFull0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err_flag));
+  };
+
   if (!wait_t2(&bars[kQFull], 0, abort_flag, p.err_flag)) return;
-  int ns[2] = {0, 0}, npv[2] = {0, 0};
-  unsigned long long t_prog = 0;
-  int idle = 0;
-  while (npv[0] < n_tiles || npv[1] < n_tiles) {
-    if (*abort_flag) return;
-    bool progress = false;
+  if (!wait_t2(&bars[kKFull0], 0, abort_flag, p.err_flag)) return;
+  tc_fence_after();
+  s_group(0, 0, 0, 0, 0);
+  bool ready = s_group(1, 0, 0, 0, n_tiles > 1 ? 1 : 0);
+  for (int j = 0; j + 1 < n_tiles; ++j) {
+    // Block (0, j); the next block is (1, j), whose K(j+1) was waited for here.
+    if (!ready && !wait_inputs(0, j, true)) return;
+    tc_fence_after();
+    pv_group(0, j);
+    ready = s_group(0, j + 1, 1, j, j + 1);
+    // Block (1, j); the next block is (0, j+1), which needs K(j+2) unless it is
+    // the last tile's P V.
+    if (!ready && !wait_inputs(1, j, true)) return;
+    tc_fence_after();
+    pv_group(1, j);
+    ready = s_group(1, j + 1, 0, j + 1, j + 2 < n_tiles ? j + 2 : j + 1);
+  }
+  // The last tile: P V only.
+  const int j = n_tiles - 1;
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      {  // P V_x of tile npv[x]: A = P in the head's S columns of tensor memory
-        const int j = npv[x];
-        if (j < ns[x] && mbar_test_wait(&bars[kVFull0 + (j & 1)], (j >> 1) & 1) &&
-            mbar_test_wait(&bars[kPFull0 + x], j & 1)) {
-          tc_fence_after();
-          const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
-          const uint32_t d = tmem + tmem_o(x), a0 = tmem + tmem_s(x);
-#pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            const uint64_t b = desc_advance(v_st, ks * 16 * 128);
-            if (j == 0 && ks == 0) umma_f16_ts_fresh(d, a0, b, idesc_o);
-            else umma_f16_ts_acc(d, a0 + ks * 8, b, idesc_o);
-          }
-          umma_commit(&bars[kVEmpty0 + (j & 1)]);
-          if (j == n_tiles - 1) umma_commit(&bars[kODone0 + x]);
-          ++npv[x];
-          progress = true;
-        }
-      }
-      {  // S_x of tile ns[x], once the head's previous P V has been issued
-        const int j = ns[x];
-        if (j < n_tiles && j == npv[x] && mbar_test_wait(&bars[kKFull0 + (j & 1)], (j >> 1) & 1)) {
-          tc_fence_after();
-          const uint32_t d = tmem + tmem_s(x);
-          const uint64_t qx = desc_advance(q0, x * L::kStageBytes);
-          const uint64_t k_st = desc_advance(k0, (j & 1) * L::kStageBytes);
-#pragma unroll
-          for (int c = 0; c < L::kHalves; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = desc_advance(qx, c * kChunk + kk * 32);
-              const uint64_t b = desc_advance(k_st, c * kChunk + kk * 32);
-              if (c == 0 && kk == 0) umma_f16_fresh(d, a, b, idesc_s);
-              else umma_f16_acc(d, a, b, idesc_s);
-            }
-          umma_commit(&bars[kSFull0 + x]);
-          umma_commit(&bars[kKEmpty0 + (j & 1)]);
-          ++ns[x];
-          progress = true;
-        }
-      }
-    }
-    if (progress) {
-      idle = 0;
-      t_prog = 0;
-    } else if (++idle >= 64) {
-      idle = 0;
-      const unsigned long long now = global_timer_ns();
-      if (t_prog == 0) {
-        t_prog = now;
-      } else if (now - t_prog > kWaitLimitNs) {
-        set_flag(p.err_flag, KVC_FLAG_WAIT_TIMEOUT);
-        *abort_flag = 1;
-        return;
-      }
-    }
+  for (int x = 0; x < 2; ++x) {
+    if (!ready && !wait_inputs(x, j, false)) return;
+    tc_fence_after();
+    pv_group(x, j);
+    ready = false;
   }
 }
 
@@ -423,7 +436,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < L::kNumBars; ++i) {
         uint32_t c = 1;
         if (i == kPFull0 || i == kPFull1) c = kHeadThreads;
-        if (i == kKEmpty0 || i == kKEmpty1 || i == kVEmpty0 || i == kVEmpty1) c = 2;
         mbar_init(&bars[i], c);
       }
       *abort_flag = 0;
