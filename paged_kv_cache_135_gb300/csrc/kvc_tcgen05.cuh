@@ -185,6 +185,86 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------ warp-convergent issue
+//
+// The issuing warp runs its loop with all 32 lanes converged and predicates
+// each tcgen05.mma / commit on one elected lane.  Descriptors then stay
+// warp-uniform, and the issue keeps pace with the tensor core even when the
+// other warps on the same scheduler issue arithmetic every cycle (issued from
+// a lone diverged lane, the same MMAs slowed down several times over).
+
+// Whole warp: 1 in exactly one lane, 0 in the others.
+__device__ __forceinline__ uint32_t elect_one_sync() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 t;\n\t"
+      "elect.sync t|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(r));
+  return r;
+}
+
+// D (+)= A[smem] * B[smem] from the elected lane; `accumulate` at run time.
+__device__ __forceinline__ void umma_ss_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate, uint32_t leader) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 e, %5, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+// The same with A read from tensor memory.
+__device__ __forceinline__ void umma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate, uint32_t leader) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 e, %5, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+// tcgen05.commit from the elected lane.
+__device__ __forceinline__ void umma_commit_e(uint64_t* bar, uint32_t leader) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "setp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(leader)
+      : "memory");
+}
+// Two accumulating MMAs (A and B in shared memory) from the elected lane,
+// preceded in the same instruction sequence by every lane testing three
+// mbarrier phases the next group needs; the predicates are consumed only
+// after the MMAs are issued, so the tests' latency hides behind them.
+// Returns whether all three phases had completed.
+__device__ __forceinline__ bool umma_ss_acc2_test3_e(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                                     uint64_t a1, uint64_t b1, uint32_t idesc,
+                                                     uint64_t* bar0, uint32_t par0, uint64_t* bar1,
+                                                     uint32_t par1, uint64_t* bar2, uint32_t par2,
+                                                     uint32_t leader) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p, q, r, e;\n\t"
+      "setp.ne.b32 e, %13, 0;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%6], %7;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q, [%8], %9;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 r, [%10], %11;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %12, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], %4, %5, %12, 1;\n\t"
+      "and.pred p, p, q;\n\t"
+      "and.pred p, p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(d_tmem), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(smem_u32(bar0)), "r"(par0),
+        "r"(smem_u32(bar1)), "r"(par1), "r"(smem_u32(bar2)), "r"(par2), "r"(idesc), "r"(leader)
+      : "memory");
+  return ok != 0;
+}
+
 // ------------------------------------------------------------------ TMEM
 
 // Whole warp: allocate `ncols` (power of two, 32..512) TMEM columns; the base

@@ -185,19 +185,21 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
   }
 }
 
-// One thread, in a fixed order: S_0(0), S_1(0), then for each tile j and
-// head x one block of P V_x(j) followed by S_x(j+1) (the head's P in its S
-// columns is read before S_x(j+1) overwrites them: one thread's MMAs run in
-// issue order).  The tensor core keeps only a short queue, so any latency
-// between two MMAs of this thread is idle tensor time.  Hence a block issues
-// its 16 MMAs with nothing between them but commits; the barriers the next
-// block needs are tested inside the instruction sequence of the block's last
-// two MMAs (their latency hides behind those issues), and the thread blocks
-// in a wait only when an input is really not ready yet.  A wait that runs
-// past kWaitLimitNs sets KVC_FLAG_WAIT_TIMEOUT and aborts.
+// The MMA warp, all lanes converged (one elected lane issues; see
+// elect_one_sync), in a fixed order: S_0(0), S_1(0), then for each tile j
+// and head x one block of P V_x(j) followed by S_x(j+1) (the head's P in its
+// S columns is read before S_x(j+1) overwrites them: one thread's MMAs run
+// in issue order).  The tensor core keeps only a short queue, so any latency
+// between two MMAs is idle tensor time.  Hence a block issues its 16 MMAs
+// with nothing between them but commits; the barriers the next block needs
+// are tested inside the instruction sequence of the block's last two MMAs
+// (their latency hides behind those issues), and the warp blocks in a wait
+// only when an input is really not ready yet.  A wait that runs past
+// kWaitLimitNs sets KVC_FLAG_WAIT_TIMEOUT and aborts.
 template <int D, bool kBf16>
 __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
-                                        volatile int* abort_flag, uint32_t tmem, int n_tiles) {
+                                        volatile int* abort_flag, uint32_t tmem, int n_tiles,
+                                        uint32_t leader) {
   using L = Tc2Layout<D>;
   constexpr int kSSteps = D / 16;   // K steps of S = Q K^T
   constexpr int kPSteps = kBN / 16; // K steps of O += P V
@@ -217,31 +219,24 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
     auto a_at = [&](int st) { return desc_advance(qx, (st / 4) * kChunk + (st % 4) * 32); };
     auto b_at = [&](int st) { return desc_advance(k_st, (st / 4) * kChunk + (st % 4) * 32); };
 #pragma unroll
-    for (int st = 0; st < kSSteps - 2; ++st) {
-      if (st == 0) umma_f16_fresh(d, a_at(st), b_at(st), idesc_s);
-      else umma_f16_acc(d, a_at(st), b_at(st), idesc_s);
-    }
-    const bool ready = umma_f16_acc2_test3(
+    for (int st = 0; st < kSSteps - 2; ++st) umma_ss_e(d, a_at(st), b_at(st), idesc_s, st != 0, leader);
+    const bool ready = umma_ss_acc2_test3_e(
         d, a_at(kSSteps - 2), b_at(kSSteps - 2), a_at(kSSteps - 1), b_at(kSSteps - 1), idesc_s,
         &bars[kPFull0 + y], t & 1, &bars[kVFull0 + (t & 1)], (t >> 1) & 1,
-        &bars[kKFull0 + (kt & 1)], (kt >> 1) & 1);
-    umma_commit(&bars[kSFull0 + x]);
-    if (x == 1) umma_commit(&bars[kKEmpty0 + (j & 1)]);
+        &bars[kKFull0 + (kt & 1)], (kt >> 1) & 1, leader);
+    umma_commit_e(&bars[kSFull0 + x], leader);
+    if (x == 1) umma_commit_e(&bars[kKEmpty0 + (j & 1)], leader);
     return ready;
   };
-  // P V_x(j), A = P in the head's S columns of tensor memory.  Only the
-  // last tile's P V ends a block; it tests P_y(t) and V(t) for the next one.
+  // P V_x(j), A = P in the head's S columns of tensor memory.
   auto pv_group = [&](int x, int j) {
     const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
     const uint32_t d = tmem + tmem_o(x), a0 = tmem + tmem_s(x);
 #pragma unroll
-    for (int ks = 0; ks < kPSteps; ++ks) {
-      const uint64_t b = desc_advance(v_st, ks * 16 * 128);
-      if (ks == 0) umma_f16_ts(d, a0, b, idesc_o, j > 0);
-      else umma_f16_ts_acc(d, a0 + ks * 8, b, idesc_o);
-    }
-    if (x == 1) umma_commit(&bars[kVEmpty0 + (j & 1)]);
-    if (j == n_tiles - 1) umma_commit(&bars[kODone0 + x]);
+    for (int ks = 0; ks < kPSteps; ++ks)
+      umma_ts_e(d, a0 + ks * 8, desc_advance(v_st, ks * 16 * 128), idesc_o, ks > 0 || j > 0, leader);
+    if (x == 1) umma_commit_e(&bars[kVEmpty0 + (j & 1)], leader);
+    if (j == n_tiles - 1) umma_commit_e(&bars[kODone0 + x], leader);
   };
   auto wait_inputs = [&](int x, int j, bool with_k) -> bool {
     return wait_t2(&bars[kPFull0 + x], j & 1, abort_flag, p.err_flag) &&
@@ -307,18 +302,14 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     float mx8[8];
 #pragma unroll
     for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
-    if (lim >= kBN) {
+    if (lim < kBN) {
 #pragma unroll
-      for (int k = 0; k < kBN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < kBN; ++k) {
-        s[k] = k < lim ? s[k] : -INFINITY;
-        mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
-      }
+      for (int k = 0; k < kBN; ++k) s[k] = k < lim ? s[k] : -INFINITY;
     }
-    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+#pragma unroll
+    for (int k = 0; k < kBN; k += 2) mx8[(k / 2) & 7] = fmax3(mx8[(k / 2) & 7], s[k], s[k + 1]);
+    const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                           fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7])) *
                      p.scale_log2;
     float corr = 1.f;
     bool rescale = false;
@@ -340,8 +331,8 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int k = 0; k < kBN / 2; ++k) {
-      const float2 x = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc2, nm2);
-      const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      const float2 y = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc2, nm2);
+      const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
       pk[k] = pack_pair<T>(e.x, e.y);
       ps2[k & 1] = add2(ps2[k & 1], e);
     }
@@ -473,12 +464,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc2_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, s, h0, h0 / p.group, tok0,
                     kv_len, n_tiles, lane);
-  } else if (lane == 0) {
-    tc2_mma<D, kBf16>(p, smem, bars, abort_flag, tmem, n_tiles);
-  }
-  // Teardown: all tensor-core work done before TMEM is freed.
-  if (warp == kMmaWarp && lane == 0) {
-    umma_commit(&bars[kDrain]);
+  } else {
+    const uint32_t leader = elect_one_sync();
+    tc2_mma<D, kBf16>(p, smem, bars, abort_flag, tmem, n_tiles, leader);
+    // Teardown: all tensor-core work done before TMEM is freed.
+    __syncwarp();
+    umma_commit_e(&bars[kDrain], leader);
     mbar_wait_bounded(&bars[kDrain], 0, p.err_flag);
   }
   __syncwarp();
