@@ -229,22 +229,21 @@ __device__ __forceinline__ void mla_producer(const MlaParams& p, const CUtensorM
 // columns with A in shared memory.  Fully unrolled from base descriptors.
 template <bool kWithRope>
 __device__ __forceinline__ void mla_issue_s(uint32_t d, uint32_t q_tmem, uint64_t qr0, uint64_t k0,
-                                            uint32_t idesc) {
+                                            uint32_t idesc, uint32_t leader) {
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const uint64_t b = desc_advance(k0, (k >> 2) * kKChunkBytes + (k & 3) * 32);
-    if (k == 0) umma_f16_ts_fresh(d, q_tmem, b, idesc);
-    else umma_f16_ts_acc(d, q_tmem + k * 8, b, idesc);
-  }
+  for (int k = 0; k < 16; ++k)
+    umma_ts_e(d, q_tmem + k * 8, desc_advance(k0, (k >> 2) * kKChunkBytes + (k & 3) * 32), idesc,
+              k != 0, leader);
   if (kWithRope) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      umma_f16_acc(d, desc_advance(qr0, kk * 32), desc_advance(k0, 4 * kKChunkBytes + kk * 32),
-                   idesc);
+      umma_ss_e(d, desc_advance(qr0, kk * 32), desc_advance(k0, 4 * kKChunkBytes + kk * 32), idesc,
+                1u, leader);
   }
 }
 
-// One thread.  S(t) and P V(t) are issued as soon as their inputs are ready,
+// The MMA warp, all lanes converged (one elected lane issues; see
+// elect_one_sync).  S(t) and P V(t) are issued as soon as their inputs are ready,
 // whichever comes first (P V first when both are): S(t) needs its key stage,
 // a free S buffer and the sequence's query; P V(t) needs P(t).  So a key tile
 // still in flight never holds back the P V of an earlier tile.  A stall of
@@ -252,7 +251,7 @@ __device__ __forceinline__ void mla_issue_s(uint32_t d, uint32_t q_tmem, uint64_
 template <bool kBf16>
 __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint64_t* bars,
                                         volatile int* abort_flag, uint32_t tmem, MlaCursor cs,
-                                        int n_it, int rank) {
+                                        int n_it, int rank, uint32_t leader) {
   using L = MlaLayout;
   const int cap = p.max_blocks * p.block_size;
   const uint32_t idesc_s = umma_idesc_f16(kBf16, kH, kTok, 0, 0);
@@ -273,14 +272,13 @@ __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint6
       tc_fence_after();
       const int stage = npv % kStages;
       const uint64_t v_st = desc_advance(v0, stage * kStageBytes);
-      if ((first_bits >> (npv & 3)) & 1u) umma_f16_fresh(tmem + kTmemO, p0, v_st, idesc_o);
-      else umma_f16_acc(tmem + kTmemO, p0, v_st, idesc_o);
+      umma_ss_e(tmem + kTmemO, p0, v_st, idesc_o, ((first_bits >> (npv & 3)) & 1u) ^ 1u, leader);
 #pragma unroll
       for (int ks = 1; ks < kTok / 16; ++ks)
-        umma_f16_acc(tmem + kTmemO, desc_advance(p0, ks * 32), desc_advance(v_st, ks * 16 * 128),
-                     idesc_o);
-      umma_commit(&bars[kPVDone]);
-      umma_commit(&bars[kKEmpty0 + stage]);
+        umma_ss_e(tmem + kTmemO, desc_advance(p0, ks * 32), desc_advance(v_st, ks * 16 * 128),
+                  idesc_o, 1u, leader);
+      umma_commit_e(&bars[kPVDone], leader);
+      umma_commit_e(&bars[kKEmpty0 + stage], leader);
       ++npv;
       progress = true;
     }
@@ -297,10 +295,10 @@ __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint6
         first_bits = (first_bits & ~(1u << (ns & 3))) | (first ? 1u << (ns & 3) : 0u);
         const uint32_t d = tmem + (sb ? kTmemS1 : kTmemS0);
         const uint64_t k_st = desc_advance(k0, stage * kStageBytes);
-        if (rank) mla_issue_s<true>(d, tmem + kTmemQ, qr0, k_st, idesc_s);
-        else mla_issue_s<false>(d, tmem + kTmemQ, qr0, k_st, idesc_s);
-        umma_commit(&bars[kSFull0 + sb]);
-        if (last) umma_commit(&bars[kQFree]);
+        if (rank) mla_issue_s<true>(d, tmem + kTmemQ, qr0, k_st, idesc_s, leader);
+        else mla_issue_s<false>(d, tmem + kTmemQ, qr0, k_st, idesc_s, leader);
+        umma_commit_e(&bars[kSFull0 + sb], leader);
+        if (last) umma_commit_e(&bars[kQFree], leader);
         cs.advance(p.seq_lens, cap, p.batch);
         ++ns;
         progress = true;
@@ -620,7 +618,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // transactions on x_full (harmless if this cluster has no tile).
     mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 4);
   }
-  if (warp == kMmaWarp) tmem_alloc(tslot, kTmemCols);
+  uint32_t leader = 0;  // the MMA warp's issuing lane
+  if (warp == kMmaWarp) {
+    tmem_alloc(tslot, kTmemCols);
+    leader = elect_one_sync();
+  }
   if (warp == kProducerWarp && lane == 0) {
     prefetch_tmap(&tm_qr);
     prefetch_tmap(&tm_cn);
@@ -663,14 +665,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int it = max(0, n_it - kStages); it < n_it; ++it)
         mbar_wait_bounded(&bars[kKFull0 + it % kStages], static_cast<uint32_t>(it / kStages) & 1u,
                           p.err_flag);
-    } else if (lane == 0) {
-      mla_mma<kBf16>(p, smem, bars, abort_flag, tmem, cur, n_it, rank);
+    } else {
+      mla_mma<kBf16>(p, smem, bars, abort_flag, tmem, cur, n_it, rank, leader);
     }
   }
   // Teardown: all tensor-core work done, TMEM freed, and neither CTA leaves
   // while its partner may still write into its shared memory.
-  if (warp == kMmaWarp && lane == 0) {
-    umma_commit(&bars[kDrain]);
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    umma_commit_e(&bars[kDrain], leader);
     mbar_wait_bounded(&bars[kDrain], 0, p.err_flag);
   }
   __syncwarp();
