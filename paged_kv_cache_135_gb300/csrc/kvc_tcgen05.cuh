@@ -38,139 +38,10 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(bool bf16, int M, int N, i
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem], issued by one thread.
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
-}
-
-// The same with the accumulate flag as an immediate: D = A*B (fresh) or
-// D += A*B (acc).  Issue loops built from these, with descriptors advanced by
-// constant offsets, keep the single issuing thread off the critical path.
-__device__ __forceinline__ void umma_f16_fresh(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                               uint32_t idesc) {
-  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
-               "l"(a_desc), "l"(b_desc), "r"(idesc)
-               : "memory");
-}
-__device__ __forceinline__ void umma_f16_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc) {
-  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
-               "l"(a_desc), "l"(b_desc), "r"(idesc)
-               : "memory");
-}
-
-// The same with A read from tensor memory: M rows in lanes 0..M-1, two 16-bit
-// K elements per 32-bit column (element 2c in the low half of column c), so
-// one 16-wide K step is 8 columns on from the previous one.
-__device__ __forceinline__ void umma_f16_ts_fresh(uint32_t d_tmem, uint32_t a_tmem,
-                                                  uint64_t b_desc, uint32_t idesc) {
-  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
-               "r"(a_tmem), "l"(b_desc), "r"(idesc)
-               : "memory");
-}
-__device__ __forceinline__ void umma_f16_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                uint32_t idesc) {
-  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
-               "r"(a_tmem), "l"(b_desc), "r"(idesc)
-               : "memory");
-}
-
-// A from tensor memory with the accumulate flag taken at run time (a
-// predicate inside the instruction sequence, no branch in the issuing thread).
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
-}
-
-// The last two MMAs of a group (accumulating), preceded in the same
-// instruction sequence by tests of two mbarrier phases that the next group
-// needs; the predicates are consumed only after both MMAs are issued, so the
-// tests' latency overlaps the MMAs instead of stalling the issuing thread
-// while the tensor core runs dry.  Returns whether both phases completed.
-__device__ __forceinline__ bool umma_f16_acc2_test2(uint32_t d_tmem, uint64_t a0, uint64_t b0,
-                                                    uint64_t a1, uint64_t b1, uint32_t idesc,
-                                                    uint64_t* bar0, uint32_t par0, uint64_t* bar1,
-                                                    uint32_t par1) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%6], %7;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q, [%8], %9;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %10, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%1], %4, %5, %10, 1;\n\t"
-      "and.pred p, p, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(d_tmem), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(smem_u32(bar0)), "r"(par0),
-        "r"(smem_u32(bar1)), "r"(par1), "r"(idesc)
-      : "memory");
-  return ok != 0;
-}
-// The same with three phases tested.
-__device__ __forceinline__ bool umma_f16_acc2_test3(uint32_t d_tmem, uint64_t a0, uint64_t b0,
-                                                    uint64_t a1, uint64_t b1, uint32_t idesc,
-                                                    uint64_t* bar0, uint32_t par0, uint64_t* bar1,
-                                                    uint32_t par1, uint64_t* bar2,
-                                                    uint32_t par2) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p, q, r;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%6], %7;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q, [%8], %9;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 r, [%10], %11;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %12, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%1], %4, %5, %12, 1;\n\t"
-      "and.pred p, p, q;\n\t"
-      "and.pred p, p, r;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(d_tmem), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(smem_u32(bar0)), "r"(par0),
-        "r"(smem_u32(bar1)), "r"(par1), "r"(smem_u32(bar2)), "r"(par2), "r"(idesc)
-      : "memory");
-  return ok != 0;
-}
-// The same with A read from tensor memory and one phase tested.
-__device__ __forceinline__ bool umma_f16_ts_acc2_test(uint32_t d_tmem, uint32_t a0, uint64_t b0,
-                                                      uint32_t a1, uint64_t b1, uint32_t idesc,
-                                                      uint64_t* bar, uint32_t par) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%6], %7;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %8, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%4], %5, %8, 1;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(d_tmem), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(smem_u32(bar)), "r"(par),
-        "r"(idesc)
-      : "memory");
-  return ok != 0;
-}
-
 // Descriptor of the same operand `bytes` further on in shared memory (the
 // start-address field holds address / 16 and never overflows its 14 bits).
 __device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
   return desc + static_cast<uint64_t>(bytes >> 4);
-}
-
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {

@@ -175,10 +175,12 @@ __device__ __forceinline__ void tc_producer(const TcPrefillParams& p, const CUte
   }
 }
 
-// One thread issues every MMA: S(j+1) before P(j) V(j).
+// The MMA warp, all lanes converged (one elected lane issues; see
+// elect_one_sync), issues every MMA: S(j+1) before P(j) V(j).
 template <int D, bool kBf16>
 __device__ __forceinline__ void tc_mma(const TcPrefillParams& p, uint8_t* smem, uint64_t* bars,
-                                       volatile int* abort_flag, uint32_t tmem, int n_tiles) {
+                                       volatile int* abort_flag, uint32_t tmem, int n_tiles,
+                                       uint32_t leader) {
   using L = TcLayout<D>;
   constexpr uint32_t idesc_s = umma_idesc_f16(kBf16, kBM, kBN, 0, 0);
   constexpr uint32_t idesc_o = umma_idesc_f16(kBf16, kBM, D, 0, 1);
@@ -201,11 +203,10 @@ __device__ __forceinline__ void tc_mma(const TcPrefillParams& p, uint8_t* smem, 
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t a = desc_advance(q0, c * kChunk + kk * 32);
         const uint64_t b = desc_advance(k_st, c * kChunk + kk * 32);
-        if (c == 0 && kk == 0) umma_f16_fresh(d, a, b, idesc_s);
-        else umma_f16_acc(d, a, b, idesc_s);
+        umma_ss_e(d, a, b, idesc_s, c != 0 || kk != 0, leader);
       }
-    umma_commit(&bars[kSFull0 + stage]);
-    umma_commit(&bars[kKEmpty0 + stage]);
+    umma_commit_e(&bars[kSFull0 + stage], leader);
+    umma_commit_e(&bars[kKEmpty0 + stage], leader);
     return true;
   };
   auto issue_pv = [&](int j) -> bool {
@@ -217,11 +218,10 @@ __device__ __forceinline__ void tc_mma(const TcPrefillParams& p, uint8_t* smem, 
     for (int ks = 0; ks < kBN / 16; ++ks) {
       const uint64_t a = desc_advance(p0, (ks >> 2) * kChunk + (ks & 3) * 32);
       const uint64_t b = desc_advance(v_st, ks * 16 * 128);
-      if (j == 0 && ks == 0) umma_f16_fresh(tmem + kTmemO, a, b, idesc_o);
-      else umma_f16_acc(tmem + kTmemO, a, b, idesc_o);
+      umma_ss_e(tmem + kTmemO, a, b, idesc_o, j != 0 || ks != 0, leader);
     }
-    umma_commit(&bars[kPVDone]);
-    umma_commit(&bars[kVEmpty0 + (j & 1)]);
+    umma_commit_e(&bars[kPVDone], leader);
+    umma_commit_e(&bars[kVEmpty0 + (j & 1)], leader);
     return true;
   };
   if (!issue_s(0)) return;
@@ -413,7 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (ctx + q0 + q_rows - 1) / kBN + 1;
   const int tok0 = p.cu_seqlens[s] + q0;
 
-  if (warp == kMmaWarp) tmem_alloc(tslot, kTmemCols);
+  uint32_t leader = 0;  // the MMA warp's issuing lane
+  if (warp == kMmaWarp) {
+    tmem_alloc(tslot, kTmemCols);
+    leader = elect_one_sync();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -430,12 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, s, h, h / p.group, tok0, kv_len,
                    n_tiles, lane);
-  } else if (lane == 0) {
-    tc_mma<D, kBf16>(p, smem, bars, abort_flag, tmem, n_tiles);
+  } else {
+    tc_mma<D, kBf16>(p, smem, bars, abort_flag, tmem, n_tiles, leader);
   }
   // Teardown: all tensor-core work done before TMEM is freed.
-  if (warp == kMmaWarp && lane == 0) {
-    umma_commit(&bars[kDrain]);
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    umma_commit_e(&bars[kDrain], leader);
     mbar_wait_bounded(&bars[kDrain], 0, p.err_flag);
   }
   __syncwarp();
