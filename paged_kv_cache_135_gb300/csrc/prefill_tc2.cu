@@ -72,7 +72,7 @@ struct Tc2Layout {
   static constexpr int kK = kQ + 2 * kStageBytes;
   static constexpr int kV = kK + kStages * kStageBytes;
   static constexpr int kBar = kV + kStages * kStageBytes;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 18;
   static constexpr int kMisc = kBar + kNumBars * 8;            // tmem slot, abort, info[4]
   static constexpr int kTotal = 1024 + kMisc + 64;
   static_assert(kTotal <= 232448, "fits the opt-in shared memory of one SM");
@@ -83,7 +83,7 @@ struct Tc2Layout {
 // s_full[h], p_full[h], o_done[h] are per head.
 enum Bar {
   kQFull = 0, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-  kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kDrain
+  kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kDrain, kPHalf0, kPHalf1
 };
 
 __device__ __forceinline__ bool wait_t2(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -209,9 +209,10 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
   const uint64_t k0 = umma_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
   const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kV), kChunk, 1024);
 
-  // S_x(j).  The next block is P V_y(t) + S_y(t+1): it needs P_y(t), V(t)
-  // and K(kt) (kt = t+1, or any tile whose K has surely landed when no S
-  // follows); returns whether all three were there before the last MMA.
+  // S_x(j).  The next block is P V_y(t) + S_y(t+1): it starts on the first
+  // half of P_y(t) and needs V(t) and K(kt) (kt = t+1, or any tile whose K
+  // has surely landed when no S follows); returns whether all three were
+  // there before the last MMA.
   auto s_group = [&](int x, int j, int y, int t, int kt) -> bool {
     const uint32_t d = tmem + tmem_s(x);
     const uint64_t qx = desc_advance(q0, x * L::kStageBytes);
@@ -222,24 +223,31 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
     for (int st = 0; st < kSSteps - 2; ++st) umma_ss_e(d, a_at(st), b_at(st), idesc_s, st != 0, leader);
     const bool ready = umma_ss_acc2_test3_e(
         d, a_at(kSSteps - 2), b_at(kSSteps - 2), a_at(kSSteps - 1), b_at(kSSteps - 1), idesc_s,
-        &bars[kPFull0 + y], t & 1, &bars[kVFull0 + (t & 1)], (t >> 1) & 1,
+        &bars[kPHalf0 + y], t & 1, &bars[kVFull0 + (t & 1)], (t >> 1) & 1,
         &bars[kKFull0 + (kt & 1)], (kt >> 1) & 1, leader);
     umma_commit_e(&bars[kSFull0 + x], leader);
     if (x == 1) umma_commit_e(&bars[kKEmpty0 + (j & 1)], leader);
     return ready;
   };
-  // P V_x(j), A = P in the head's S columns of tensor memory.
-  auto pv_group = [&](int x, int j) {
+  // P V_x(j), A = P in the head's S columns of tensor memory: tokens 0-63
+  // (released by p_half), then, once the whole of P_x(j) is there, 64-127.
+  auto pv_group = [&](int x, int j) -> bool {
     const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
     const uint32_t d = tmem + tmem_o(x), a0 = tmem + tmem_s(x);
 #pragma unroll
-    for (int ks = 0; ks < kPSteps; ++ks)
+    for (int ks = 0; ks < kPSteps / 2; ++ks)
       umma_ts_e(d, a0 + ks * 8, desc_advance(v_st, ks * 16 * 128), idesc_o, ks > 0 || j > 0, leader);
+    if (!wait_t2(&bars[kPFull0 + x], j & 1, abort_flag, p.err_flag)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int ks = kPSteps / 2; ks < kPSteps; ++ks)
+      umma_ts_e(d, a0 + ks * 8, desc_advance(v_st, ks * 16 * 128), idesc_o, 1u, leader);
     if (x == 1) umma_commit_e(&bars[kVEmpty0 + (j & 1)], leader);
     if (j == n_tiles - 1) umma_commit_e(&bars[kODone0 + x], leader);
+    return true;
   };
   auto wait_inputs = [&](int x, int j, bool with_k) -> bool {
-    return wait_t2(&bars[kPFull0 + x], j & 1, abort_flag, p.err_flag) &&
+    return wait_t2(&bars[kPHalf0 + x], j & 1, abort_flag, p.err_flag) &&
            wait_t2(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, abort_flag, p.err_flag) &&
            (!with_k ||
             wait_t2(&bars[kKFull0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err_flag));
@@ -254,13 +262,13 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
     // Block (0, j); the next block is (1, j), whose K(j+1) was waited for here.
     if (!ready && !wait_inputs(0, j, true)) return;
     tc_fence_after();
-    pv_group(0, j);
+    if (!pv_group(0, j)) return;
     ready = s_group(0, j + 1, 1, j, j + 1);
     // Block (1, j); the next block is (0, j+1), which needs K(j+2) unless it is
     // the last tile's P V.
     if (!ready && !wait_inputs(1, j, true)) return;
     tc_fence_after();
-    pv_group(1, j);
+    if (!pv_group(1, j)) return;
     ready = s_group(1, j + 1, 0, j + 1, j + 2 < n_tiles ? j + 2 : j + 1);
   }
   // The last tile: P V only.
@@ -269,7 +277,7 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
   for (int x = 0; x < 2; ++x) {
     if (!ready && !wait_inputs(x, j, false)) return;
     tc_fence_after();
-    pv_group(x, j);
+    if (!pv_group(x, j)) return;
     ready = false;
   }
 }
@@ -288,26 +296,31 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
   for (int j = 0; j < n_tiles; ++j) {
     wait_t2(&bars[kSFull0 + x], j & 1, abort_flag, p.err_flag);
     tc_fence_after();
-    float s[kBN];
-#pragma unroll
-    for (int c = 0; c < kBN / 16; ++c) tmem_ld16(lane_base + tmem_s(x) + c * 16, s + c * 16);
-    tmem_wait_ld();
-
     // Row max of the raw scores (the scale is positive, so it commutes with
-    // the max and is folded into the exponent below).  Causal + length mask:
-    // token k of the tile is visible iff k < lim; only tiles that reach past
-    // this row take the masked path.
+    // the max and is folded into the exponent below), read in two halves of
+    // 64 columns to keep register pressure down; S stays in tensor memory
+    // and is read again for the exponentials.  Causal + length mask: token k
+    // of the tile is visible iff k < lim; only tiles that reach past this row
+    // take the masked path.
     const int kv0 = j * kBN;
     const int lim = min(pos + 1, kv_len) - kv0;
     float mx8[8];
 #pragma unroll
     for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
-    if (lim < kBN) {
 #pragma unroll
-      for (int k = 0; k < kBN; ++k) s[k] = k < lim ? s[k] : -INFINITY;
+    for (int hf = 0; hf < 2; ++hf) {
+      float s[kBN / 2];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c)
+        tmem_ld16(lane_base + tmem_s(x) + hf * (kBN / 2) + c * 16, s + c * 16);
+      tmem_wait_ld();
+      if (lim < kBN) {
+#pragma unroll
+        for (int k = 0; k < kBN / 2; ++k) s[k] = hf * (kBN / 2) + k < lim ? s[k] : -INFINITY;
+      }
+#pragma unroll
+      for (int k = 0; k < kBN / 2; k += 2) mx8[(k / 2) & 7] = fmax3(mx8[(k / 2) & 7], s[k], s[k + 1]);
     }
-#pragma unroll
-    for (int k = 0; k < kBN; k += 2) mx8[(k / 2) & 7] = fmax3(mx8[(k / 2) & 7], s[k], s[k + 1]);
     const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
                            fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7])) *
                      p.scale_log2;
@@ -321,24 +334,6 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
       m_used = mx;
       rescale = true;
     }
-    // p = 2^(s * scale_log2 - m_used); a row with nothing visible yet keeps
-    // m_used = -inf and all its scores at -inf, so its p are 0.
-    // The row sum l adds the exponentials before rounding (P itself is
-    // rounded to T for the tensor core).
-    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
-    uint32_t pk[kBN / 2];
-    float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-    for (int k = 0; k < kBN / 2; ++k) {
-      const float2 y = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc2, nm2);
-      const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-      pk[k] = pack_pair<T>(e.x, e.y);
-      ps2[k & 1] = add2(ps2[k & 1], e);
-    }
-    const float2 pst = add2(ps2[0], ps2[1]);
-    l = l * corr + (pst.x + pst.y);
-
     // S(j) complete means this head's P V(j-1) is complete too, so O may be
     // rescaled and P written over the S columns now.
     if (__any_sync(0xffffffffu, rescale)) {
@@ -353,11 +348,6 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
         tmem_st16(a, v);
       }
     }
-    // P row -> the first 64 columns of the head's S (two 16-bit tokens per
-    // column, token 2c in the low half of column c).
-#pragma unroll
-    for (int c = 0; c < kBN / 32; ++c) tmem_st16_u32(lane_base + tmem_s(x) + c * 16, pk + c * 16);
-    tmem_wait_st();
     // Value rows past the cached tokens are zeroed (by both heads, before
     // either head's P V of the tile) so stale contents cannot reach P V.
     const int valid = kv_len - j * kBN;
@@ -371,6 +361,47 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
       }
       fence_proxy_async_smem();
     }
+    // p = 2^(s * scale_log2 - m_used); a row with nothing visible yet keeps
+    // m_used = -inf and all its scores at -inf, so its p are 0.  The row sum
+    // l adds the exponentials before rounding (P itself is rounded to T for
+    // the tensor core).  P goes to the first 64 columns of the head's S (two
+    // 16-bit tokens per column, token 2c in the low half of column c) in two
+    // halves: tokens 0-63 are released (p_half) while 64-127 are computed,
+    // so the first half of P V overlaps the second half of the exponentials.
+    // Half h of P overwrites only scores of half 0, which are read before.
+    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
+    float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      float s[kBN / 2];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c)
+        tmem_ld16(lane_base + tmem_s(x) + hf * (kBN / 2) + c * 16, s + c * 16);
+      tmem_wait_ld();
+      if (lim < kBN) {
+#pragma unroll
+        for (int k = 0; k < kBN / 2; ++k) s[k] = hf * (kBN / 2) + k < lim ? s[k] : -INFINITY;
+      }
+      uint32_t pk[kBN / 4];
+#pragma unroll
+      for (int k = 0; k < kBN / 4; ++k) {
+        const float2 y = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc2, nm2);
+        const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+        pk[k] = pack_pair<T>(e.x, e.y);
+        ps2[k & 1] = add2(ps2[k & 1], e);
+      }
+#pragma unroll
+      for (int c = 0; c < kBN / 64; ++c)
+        tmem_st16_u32(lane_base + tmem_s(x) + hf * (kBN / 4) + c * 16, pk + c * 16);
+      tmem_wait_st();
+      if (hf == 0) {
+        tc_fence_before();
+        mbar_arrive(&bars[kPHalf0 + x]);
+      }
+    }
+    const float2 pst = add2(ps2[0], ps2[1]);
+    l = l * corr + (pst.x + pst.y);
     tc_fence_before();
     mbar_arrive(&bars[kPFull0 + x]);
   }
@@ -426,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       info[3] = len;
       for (int i = 0; i < L::kNumBars; ++i) {
         uint32_t c = 1;
-        if (i == kPFull0 || i == kPFull1) c = kHeadThreads;
+        if (i == kPFull0 || i == kPFull1 || i == kPHalf0 || i == kPHalf1) c = kHeadThreads;
         mbar_init(&bars[i], c);
       }
       *abort_flag = 0;
