@@ -96,8 +96,8 @@ struct MlaLayout {
   static constexpr int kQr = 0;                                    // 16 KB
   static constexpr int kK = kQr + kQChunkBytes;                    // 4 x 40 KB
   static constexpr int kP = kK + kStages * kStageBytes;            // 16 KB
-  static constexpr int kX = kP + kH * 128;                         // 32 KB
-  static constexpr int kRed = kX + kH * kTok * 4;                  // [2][128] fp32
+  static constexpr int kX = kP + kH * 128;                         // 16 KB
+  static constexpr int kRed = kX + kH * kTok * 2;                  // [2][128] fp32
   static constexpr int kBar = kRed + 2 * kH * 4;
   static constexpr int kMisc = align_up_c(kBar + 19 * 8, 16);      // tmem slot, flags
   static constexpr int kEnd = kMisc + 32;
@@ -387,10 +387,12 @@ __device__ __forceinline__ void mla_load_q(const MlaParams& p, uint32_t lane_bas
 }
 
 // Warps 0-3, thread `row` = query head.  Per tile: this CTA's partial scores
-// (TMEM) go to the other CTA as st.async stores that complete its x_full
+// (TMEM), scaled to the log2 domain and rounded to fp16 (their rounding error
+// is below 2^-11 of the scaled partial, far under the bf16/fp16 rounding of
+// P), go to the other CTA as st.async stores that complete its x_full
 // transaction count, once the other CTA has freed its X buffer (x_empty, a
-// relaxed arrive from its math warps).  These warps also load each
-// sequence's query into TMEM.
+// relaxed arrive from its math warps): 128 bytes per query head and tile.
+// These warps also load each sequence's query into TMEM.
 template <typename T>
 __device__ __forceinline__ void mla_exchange(const MlaParams& p, uint8_t* smem, uint64_t* bars,
                                              volatile int* abort_flag, uint32_t tmem, MlaCursor cx,
@@ -418,11 +420,16 @@ __device__ __forceinline__ void mla_exchange(const MlaParams& p, uint8_t* smem, 
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(&bars[kSFree0 + sb]);
+    uint32_t xh[kTok / 2];
+#pragma unroll
+    for (int k = 0; k < kTok / 2; ++k)
+      xh[k] = pack_pair<__half>(so[2 * k] * p.scale_log2, so[2 * k + 1] * p.scale_log2);
     wait_peer(&bars[kXEmpty], (it & 1) ^ 1, abort_flag, p.err_flag);
 #pragma unroll
-    for (int q = 0; q < kTok / 4; ++q)
+    for (int q = 0; q < kTok / 8; ++q)  // chunk q: tokens 8q .. 8q+7
       st_async_cluster_v4(x_peer + (q * kH + row) * 16,
-                          make_float4(so[4 * q], so[4 * q + 1], so[4 * q + 2], so[4 * q + 3]),
+                          make_float4(__uint_as_float(xh[4 * q]), __uint_as_float(xh[4 * q + 1]),
+                                      __uint_as_float(xh[4 * q + 2]), __uint_as_float(xh[4 * q + 3])),
                           xfull_peer);
     // Tile it+1 starts the next sequence: its query replaces this one (S(it)
     // complete => every S of this sequence is done).
@@ -454,7 +461,7 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
   const int cap = p.max_blocks * p.block_size;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(row & ~31) << 16);
   float* red = reinterpret_cast<float*>(smem + L::kRed);
-  const float4* x_mine = reinterpret_cast<const float4*>(smem + L::kX);
+  const uint4* x_mine = reinterpret_cast<const uint4*>(smem + L::kX);
   const uint32_t xempty_peer = map_to_rank(smem_u32(&bars[kXEmpty]), static_cast<uint32_t>(rank ^ 1));
   const bool elected = row == 0 && h == 0;
   float m_used = -INFINITY, l = 0.f;
@@ -468,8 +475,9 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
       l = 0.f;
       seg_first_j = cm.j;
     }
-    // Scores of this thread's 32 tokens: own partial (TMEM) + the other
-    // CTA's (X); then both buffers are released.
+    // Scores of this thread's 32 tokens in the log2 domain: own partial
+    // (TMEM, fp32) times scale_log2 plus the other CTA's (X, already scaled,
+    // fp16); then both buffers are released.
     float s[32];
     wait_cta(&bars[kSFull0 + sb], (it >> 1) & 1, abort_flag, p.err_flag);
     tc_fence_after();
@@ -479,20 +487,24 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
     tc_fence_before();
     mbar_arrive(&bars[kSFree0 + sb]);
     wait_peer(&bars[kXFull], it & 1, abort_flag, p.err_flag);
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 v = x_mine[(h * 8 + q) * kH + row];
-      const float2 a = add2(make_float2(s[4 * q], s[4 * q + 1]), make_float2(v.x, v.y));
-      const float2 b = add2(make_float2(s[4 * q + 2], s[4 * q + 3]), make_float2(v.z, v.w));
-      s[4 * q] = a.x;
-      s[4 * q + 1] = a.y;
-      s[4 * q + 2] = b.x;
-      s[4 * q + 3] = b.y;
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = x_mine[(h * 4 + q) * kH + row];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = 8 * q + 2 * i;
+        const float2 other = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        const float2 t = fma2(make_float2(s[k], s[k + 1]), sl2, other);
+        s[k] = t.x;
+        s[k + 1] = t.y;
+      }
     }
     const int tile_valid = min(kTok, cm.len - cm.j * kTok);
     const int valid = tile_valid - h * 32;  // of this thread's 32 tokens
-    // Row max of the raw scores (the positive scale is folded into the
-    // exponent below); tokens past the sequence only in a tail tile.
+    // Row max of the scaled scores; tokens past the sequence only in a tail
+    // tile.
     float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (valid >= 32) {
 #pragma unroll
@@ -504,11 +516,11 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
         mx4[k & 3] = fmaxf(mx4[k & 3], s[k]);
       }
     }
-    red[h * kH + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+    red[h * kH + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
     named_bar_sync(3, kMathThreads);  // also: every thread has read X
     if (elected) {
-      // The next tile's scores arrive as 32 KB of transactions on x_full.
-      if (it + 1 < n_it) mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 4);
+      // The next tile's scores arrive as 16 KB of transactions on x_full.
+      if (it + 1 < n_it) mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 2);
       mbar_arrive_cluster_relaxed(xempty_peer);
     }
     const float mx = fmaxf(red[row], red[kH + row]);  // same order in both halves
@@ -522,15 +534,15 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
       m_used = mx;
       rescale = true;
     }
-    // p = 2^(s * scale_log2 - m_used); l adds the exponentials before
+    // p = 2^(s - m_used) (s already scaled); l adds the exponentials before
     // rounding (P itself is rounded to T for the tensor core).
     const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
+    const float2 nm2 = make_float2(neg_m, neg_m);
     uint32_t pk[16];
     float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      const float2 x = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc2, nm2);
+      const float2 x = add2(make_float2(s[2 * k], s[2 * k + 1]), nm2);
       const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
       pk[k] = pack_pair<T>(e.x, e.y);
       ps2[k & 1] = add2(ps2[k & 1], e);
@@ -614,9 +626,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
-    // The first tile's scores from the other CTA arrive as 32 KB of
+    // The first tile's scores from the other CTA arrive as 16 KB of
     // transactions on x_full (harmless if this cluster has no tile).
-    mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 4);
+    mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 2);
   }
   uint32_t leader = 0;  // the MMA warp's issuing lane
   if (warp == kMmaWarp) {
