@@ -339,27 +339,31 @@ __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, in
     T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * kH + row) * kNope +
              rank * kOutCols + h * 128;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    for (int c = 0; c < 8; ++c) {
-      float v[16];
+    for (int c = 0; c < 8; c += 2) {  // two loads in flight per wait
+      float v[32];
       tmem_ld16(o_taddr + c * 16, v);
+      tmem_ld16(o_taddr + c * 16 + 16, v + 16);
       tmem_wait_ld();
-      uint32_t w[8];
+      uint32_t w[16];
       float ra, rb;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, ra, rb);
-      *reinterpret_cast<uint4*>(out + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(out + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+      for (int k = 0; k < 16; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, ra, rb);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(out + c * 16 + q * 8) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     }
     return;
   }
   const long long wrow = ((static_cast<long long>(cl) * 2 + slot) * 2 + rank) * kH + row;
-  for (int c = 0; c < 8; ++c) {
-    float v[16];
+  for (int c = 0; c < 8; c += 2) {  // two loads in flight per wait
+    float v[32];
     tmem_ld16(o_taddr + c * 16, v);
+    tmem_ld16(o_taddr + c * 16 + 16, v + 16);
     tmem_wait_ld();
     float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * kOutCols + h * 128 + c * 16);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
   }
   if (h == 0) *reinterpret_cast<float2*>(p.ws_ml + wrow * 2) = make_float2(m_used, l);
 }
@@ -432,8 +436,19 @@ __device__ __forceinline__ void mla_exchange(const MlaParams& p, uint8_t* smem, 
                                       __uint_as_float(xh[4 * q + 2]), __uint_as_float(xh[4 * q + 3])),
                           xfull_peer);
     // Tile it+1 starts the next sequence: its query replaces this one (S(it)
-    // complete => every S of this sequence is done).
+    // complete => every S of this sequence is done).  Its rows are first
+    // fetched into L2, so the load after q_free does not wait on HBM.
     if (it + 1 < n_it && cx.last()) {
+      {
+        MlaCursor nx = cx;
+        nx.advance(p.seq_lens, cap, p.batch);
+        const char* q = reinterpret_cast<const char*>(
+            static_cast<const T*>(p.q_nope) + (static_cast<long long>(nx.b) * kH + row) * kNope +
+            rank * kOutCols);
+#pragma unroll
+        for (int i = 0; i < kOutCols * static_cast<int>(sizeof(T)) / 128; ++i)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(q + i * 128));
+      }
       wait_cta(&bars[kQFree], seg_x & 1, abort_flag, p.err_flag);
       tc_fence_after();
       MlaCursor nx = cx;
