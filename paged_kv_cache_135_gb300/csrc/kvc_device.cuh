@@ -202,13 +202,6 @@ struct Pack<__half> {
 };
 
 // 2^x on the SFU (PTX ex2.approx.ftz.f32); ex2(-inf) = +0.
-// max(a, b, c) in one instruction (sm_100+); exact, like two fmaxf.
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -199,6 +199,13 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // --------------------------------------------------------- paired fp32
 
+// max(a, b, c) in one instruction (sm_100+); exact, like two fmaxf.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Paired fp32 arithmetic (one instruction for two lanes of a float2) and a
 // round-to-nearest pack of two floats into 16-bit pairs.
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
