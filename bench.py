@@ -84,7 +84,8 @@ def decode_workload(name, case, ws):
         "batch": B, "num_q_heads": m["num_q_heads"], "num_kv_heads": m["num_kv_heads"],
         "head_dim": m["head_dim"], "block_size": case.block_size,
         "kv_tokens": int(sum(lens)), "step": "slot mapping + cache write + paged decode "
-        "(split-KV, fused merge), replayed from CUDA graphs", "algorithmic_bytes_per_step": step_bytes,
+        "(split-KV, fused merge) in one launch (kvc_paged_decode_append), replayed from a "
+        "CUDA graph", "algorithmic_bytes_per_step": step_bytes,
         "l2": "no flush: each step reads %.0f MB of K/V, more than the 129 MB L2" % (d_bytes / 1e6),
         "parallelism": f"replicas x{ws}",
     }
@@ -199,7 +200,13 @@ class DecodeStep:
         self.kvc.paged_decode(self.q, self.kc, self.vc, self.bt, self.sl, self.case.scale,
                               out=self.out, workspace=self.ws)
 
-    LAUNCHES = 3  # slot mapping, cache write, paged decode (split-KV merge fused)
+    def step(self):
+        """The whole step in one launch: slot mapping, new-token write, decode."""
+        self.kvc.paged_decode_append(self.q, self.nk, self.nv, self.kc, self.vc, self.bt,
+                                     self.sl, self.case.scale, out=self.out,
+                                     slot_mapping=self.slots, workspace=self.ws)
+
+    LAUNCHES = 1  # kvc_paged_decode_append: slot mapping, cache write, decode, split merge
 
 
 def dist_info():
@@ -447,23 +454,19 @@ def main():
     step_bytes = d_bytes + w_bytes
 
     for _ in range(args.warmup):
-        step.write()
-        step.decode()
+        step.step()
     torch.cuda.synchronize()
 
-    # The step's launches are captured once into CUDA graphs (how a serving
-    # loop issues a decode step); replays keep the GPU fed without host gaps.
-    g_write, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    # The step's launch is captured once into a CUDA graph (how a serving loop
+    # issues a decode step); replays keep the GPU fed without host gaps.
+    g_dec = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(cap):
-        with torch.cuda.graph(g_write, stream=cap):
-            step.write()
         with torch.cuda.graph(g_dec, stream=cap):
-            step.decode()
+            step.step()
     torch.cuda.current_stream().wait_stream(cap)
     for _ in range(args.warmup):
-        g_write.replay()
         g_dec.replay()
     torch.cuda.synchronize()
 
@@ -482,7 +485,6 @@ def main():
         torch.cuda.synchronize()
         t_start.record(stream)
         for i in range(args.steps):
-            g_write.replay()
             ev[i][0].record(stream)
             g_dec.replay()
             ev[i][1].record(stream)
@@ -492,11 +494,11 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(b) for a, b in ev]
 
-    # Diagnostic: the same decode launched eagerly through the Python binding.
+    # Diagnostic: the same step launched eagerly through the Python binding.
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(20):
-        step.decode()
+        step.step()
     e1.record(stream)
     torch.cuda.synchronize()
     eager_ms = e0.elapsed_time(e1) / 20
@@ -511,7 +513,7 @@ def main():
     # End to end through the public API: per step, pinned host inputs -> device,
     # the step, device -> pinned host output, synchronised.
     h = {k: getattr(case, k).cpu().pin_memory() for k in
-         ("q", "new_key", "new_value", "block_table", "seq_lens", "write_pos")}
+         ("q", "new_key", "new_value", "block_table", "seq_lens")}
     h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = h_out.numel() * h_out.element_size()
@@ -524,9 +526,7 @@ def main():
         step.nv.copy_(h["new_value"], non_blocking=True)
         step.bt.copy_(h["block_table"], non_blocking=True)
         step.sl.copy_(h["seq_lens"], non_blocking=True)
-        step.wp.copy_(h["write_pos"], non_blocking=True)
-        step.write()
-        step.decode()
+        step.step()
         h_out.copy_(step.out, non_blocking=True)
         torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / max(1, args.e2e_steps)
@@ -537,7 +537,7 @@ def main():
 
     peak, peak_kind = peaks()
     dec_avg_ms = statistics.mean(dec_ms)
-    achieved = d_bytes / (dec_avg_ms * 1e-3) / 1e9
+    achieved = step_bytes / (dec_avg_ms * 1e-3) / 1e9
     digest = kernel_source_digest()
     traffic = (recorded_traffic("paged_decode_gqa8b.md", digest)
                if args.workload == WORKLOAD else None)
@@ -560,10 +560,11 @@ def main():
             "decode_tokens_per_s": tokens_per_s,
             "pct_of_nominal_8tbps": 100.0 * value / NOMINAL_HBM_GBS,
             "roofline": {
-                "kernel": "paged_decode_kernel (one kvc_paged_decode call, split-KV merge fused)",
+                "kernel": "paged_decode_kernel (one kvc_paged_decode_append call: new-token "
+                          "write, decode and split-KV merge fused)",
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                "algorithmic_bytes_per_launch": d_bytes, "avg_launch_ms": dec_avg_ms,
+                "algorithmic_bytes_per_launch": step_bytes, "avg_launch_ms": dec_avg_ms,
                 "eager_launch_ms": eager_ms,
                 "frac_of_nominal_8tbps": achieved / NOMINAL_HBM_GBS,
             },

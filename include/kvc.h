@@ -177,6 +177,37 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
                             size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream);
 
 /*
+ * kvc_paged_decode_append -- one decode step in one launch: rows a1 (slot
+ * mapping), a2 (cache write of the new token) and a3/a4 (paged decode with
+ * split-KV) fused.  Identical in effect to kvc_build_slot_mapping (start_pos =
+ * seq_lens - 1) + kvc_reshape_and_cache + kvc_paged_decode for every sequence
+ * with seq_lens[b] >= 1: the pages describe the cache write before the
+ * attention that reads it ([SKILL] 3.6, [ATB] 4.2).  Not a separate operation
+ * on the pages; it exists so a decode step costs one launch.
+ *
+ *   p = seq_lens[b] - 1 (seq_lens includes the new token);
+ *   slot = block_table[b][p / block_size] * block_size + p % block_size;
+ *   key_cache / value_cache row `slot` (all kv heads) <- new_key[b] / new_value[b];
+ *   slot_mapping[b] = slot (or -1 when seq_lens[b] == 0: nothing is written);
+ *   out = kvc_paged_decode over the updated cache.
+ *
+ * new_key, new_value: [batch, num_kv_heads, head_dim] (device, 16-byte
+ * aligned); slot_mapping: int32 [batch] output, may be NULL; every other
+ * argument, the workspace rules and the errors are those of kvc_paged_decode.
+ * The row of the new token is written by the CTA that then reads it, before it
+ * reads it, so no other ordering is needed.  A block_table entry outside
+ * [0, num_blocks) sets KVC_FLAG_BLOCK_ID_RANGE and that row is not written.
+ */
+kvc_status kvc_paged_decode_append(const void* q, const void* new_key, const void* new_value,
+                                   void* key_cache, void* value_cache, const int32_t* block_table,
+                                   const int32_t* seq_lens, int32_t* slot_mapping, void* out,
+                                   int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_blocks_per_seq, int num_blocks,
+                                   float scale, kvc_dtype dtype, int num_ctas, void* workspace,
+                                   size_t workspace_bytes, uint32_t* err_flag,
+                                   kvc_stream_t stream);
+
+/*
  * kvc_varlen_prefill_paged -- packed variable-length causal prefill that
  * writes its own K/V into the paged cache and attends through it.
  * [NOTES] 3.1 (cu_seqlens / seq_offset, per-sequence positions), 3.2 (causal

@@ -40,6 +40,8 @@ _SIGS = {
                                       _I, _I, _I, _I, _F, _I, _P, _P]),
     "kvc_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                               _P, _S, _P, _P]),
+    "kvc_paged_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                     _I, _F, _I, _I, _P, _S, _P, _P]),
 }
 
 
@@ -180,6 +182,46 @@ def paged_decode(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Te
         seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, D, bs, block_table.shape[1], NB,
         float(scale), _DT[q.dtype], num_ctas, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _flag(err_flag), _stream()))
+    return out
+
+
+def paged_decode_append(q: torch.Tensor, new_key: torch.Tensor, new_value: torch.Tensor,
+                        key_cache: torch.Tensor, value_cache: torch.Tensor,
+                        block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                        out: Optional[torch.Tensor] = None,
+                        slot_mapping: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                        workspace: Optional[torch.Tensor] = None,
+                        err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step in one launch: write new_key / new_value [B, Hkv, D] at
+    position seq_lens[b] - 1 of each sequence's cache (slot into slot_mapping,
+    -1 for an empty sequence), then decode as paged_decode over seq_lens."""
+    _cuda("q", q)
+    _cuda("new_key", new_key, q.dtype)
+    _cuda("new_value", new_value, q.dtype)
+    _cuda("key_cache", key_cache, q.dtype)
+    _cuda("value_cache", value_cache, q.dtype)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("seq_lens", seq_lens, torch.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    if tuple(new_key.shape) != (B, Hkv, D) or tuple(new_value.shape) != (B, Hkv, D):
+        raise ValueError("new_key / new_value must be [batch, num_kv_heads, head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, q.dtype)
+    if slot_mapping is not None:
+        _cuda("slot_mapping", slot_mapping, torch.int32)
+    if workspace is None:
+        n = decode_workspace_size(Hq, Hkv, D, num_ctas)
+        workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=q.device)
+    _cuda("workspace", workspace)
+    _check("kvc_paged_decode_append", lib().kvc_paged_decode_append(
+        q.data_ptr(), new_key.data_ptr(), new_value.data_ptr(), key_cache.data_ptr(),
+        value_cache.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+        slot_mapping.data_ptr() if slot_mapping is not None else None, out.data_ptr(),
+        B, Hq, Hkv, D, bs, block_table.shape[1], NB, float(scale), _DT[q.dtype], num_ctas,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _flag(err_flag),
+        _stream()))
     return out
 
 

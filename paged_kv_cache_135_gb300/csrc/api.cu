@@ -191,6 +191,61 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
   return kvc::launch_paged_decode(a);
 }
 
+kvc_status kvc_paged_decode_append(const void* q, const void* new_key, const void* new_value,
+                                   void* key_cache, void* value_cache, const int32_t* block_table,
+                                   const int32_t* seq_lens, int32_t* slot_mapping, void* out,
+                                   int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_blocks_per_seq, int num_blocks,
+                                   float scale, kvc_dtype dtype, int num_ctas, void* workspace,
+                                   size_t workspace_bytes, uint32_t* err_flag,
+                                   kvc_stream_t stream) {
+  if (batch > 0 && (!new_key || !new_value || !aligned16(new_key) || !aligned16(new_value)))
+    return KVC_ERR_INVALID_ARG;
+  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0 || num_blocks <= 0 || num_ctas < 0)
+    return KVC_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return KVC_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return KVC_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > 16) return KVC_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (!is_pow2(block_size) || block_size < 8) return KVC_ERR_UNSUPPORTED;
+  if (batch > 1024) return KVC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+    return KVC_ERR_UNSUPPORTED;
+  if (batch == 0) return KVC_OK;
+  if (!q || !key_cache || !value_cache || !block_table || !seq_lens || !out)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      !aligned16(workspace))
+    return KVC_ERR_INVALID_ARG;
+  kvc::DecodeArgs a;
+  a.q = q;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.num_ctas = num_ctas;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err_flag = err_flag;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.new_key = new_key;
+  a.new_value = new_value;
+  a.slot_out = slot_mapping;
+  return kvc::launch_paged_decode(a);
+}
+
 kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* value,
                                     const int32_t* cu_seqlens, const int32_t* context_lens,
                                     const int32_t* slot_mapping, const int32_t* block_table,

@@ -55,6 +55,10 @@ struct DecodeArgs {
   size_t workspace_bytes;
   uint32_t* err_flag;
   cudaStream_t stream;
+  // Appending decode (all null for plain decode): see kvc_paged_decode_append.
+  const void* new_key = nullptr;
+  const void* new_value = nullptr;
+  int32_t* slot_out = nullptr;
 };
 
 // Persistent CTAs the decode kernel would use for this shape (num_ctas <= 0

@@ -64,6 +64,15 @@ struct DecodeParams {
   float* ws_o;   // [P][2][G][D] unnormalised partial outputs
   float* ws_ml;  // [P][2][G][2] partial (max, sum) in the log2 domain
   uint32_t* err_flag;
+  // Appending variant (null = plain decode): the new token of sequence b sits
+  // at position seq_lens[b] - 1; its K/V rows come from new_k / new_v
+  // [B, Hkv, D] and are written into k_cache / v_cache by the CTA that loads
+  // that position, before it loads it; slot_out[b] (nullable) gets its slot.
+  const void* new_k;
+  const void* new_v;
+  void* k_cache;
+  void* v_cache;
+  int32_t* slot_out;
   int batch, num_q_heads, num_kv_heads, group, head_dim;
   int block_size, log2_bs, max_blocks, num_blocks, box_tokens;
   float scale_log2;
@@ -422,14 +431,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const long long N = static_cast<long long>(hkv) * cum[B];
   const int P = gridDim.x, c = blockIdx.x;
-  // Sequences with no cached token get a row of zeros (CTA b % P writes them).
+  // Sequences with no cached token get a row of zeros (CTA b % P writes them)
+  // and, when appending, no slot (-1): there is no new token to write.
   {
     T* out = static_cast<T*>(p.out);
     const int row_elems = p.num_q_heads * D;
     for (int b = c; b < B; b += P)
-      if (lens[b] == 0)
+      if (lens[b] == 0) {
         for (int e = tid; e < row_elems; e += kThreads)
           out[static_cast<long long>(b) * row_elems + e] = Pack<T>::cvt(0.f);
+        if (tid == 0 && p.slot_out) p.slot_out[b] = -1;
+      }
   }
   const long long t_begin = tile_begin(c, N, P), t_end = tile_begin(c + 1, N, P);
   if (t_begin >= t_end) return;
@@ -453,6 +465,38 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane < nsub && tok < Lb)
         pb = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks +
                                   (tok >> p.log2_bs)]);
+      if (p.new_k != nullptr && cur.j == cur.n - 1) {
+        // The last tile of segment (b, g) holds the new token: write its K/V
+        // rows for head g (16 bytes per lane), make the writes visible to the
+        // TMA unit, then load the tile as usual.  No other CTA reads them.
+        const int pos = Lb - 1;
+        const int pbn = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks +
+                                             (pos >> p.log2_bs)]);
+        constexpr int kChunks = D * 2 / 16;  // 16-byte pieces of one row
+        if (pbn >= 0 && pbn < p.num_blocks) {
+          if (lane < 2 * kChunks) {
+            const bool is_v = lane >= kChunks;
+            const int q16 = lane - (is_v ? kChunks : 0);
+            const long long src_row = static_cast<long long>(cur.b) * p.num_kv_heads + cur.g;
+            const long long dst_row =
+                (static_cast<long long>(pbn) * p.block_size + (pos & (p.block_size - 1))) *
+                    p.num_kv_heads + cur.g;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                                      static_cast<const T*>(is_v ? p.new_v : p.new_k) + src_row * D) +
+                                  q16);
+            *(reinterpret_cast<uint4*>(static_cast<T*>(is_v ? p.v_cache : p.k_cache) + dst_row * D) +
+              q16) = v;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+          if (lane == 0 && cur.g == 0 && p.slot_out)
+            p.slot_out[cur.b] = pbn * p.block_size + (pos & (p.block_size - 1));
+        } else if (lane == 0) {
+          set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
+          if (cur.g == 0 && p.slot_out) p.slot_out[cur.b] = -1;
+        }
+        __syncwarp();
+        if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
       bool ok = !*abort_flag && mbar_wait_bounded(&empty[stage], phase ^ 1, p.err_flag);
       if (!ok) {
         *abort_flag = 1;
@@ -630,6 +674,11 @@ kvc_status run_decode(const DecodeArgs& a) {
   p.ws_o = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + counter_bytes(P));
   p.ws_ml = p.ws_o + static_cast<size_t>(P) * 2 * G * D;
   p.err_flag = a.err_flag;
+  p.new_k = a.new_key;
+  p.new_v = a.new_value;
+  p.k_cache = const_cast<void*>(a.key_cache);
+  p.v_cache = const_cast<void*>(a.value_cache);
+  p.slot_out = a.slot_out;
   p.batch = a.batch;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
