@@ -412,17 +412,20 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
   const float inv = l > 0.f ? 1.f / l : 0.f;
   T* o = static_cast<T*>(p.out) + (static_cast<long long>(tok0) + row) * p.num_q_heads * D + h * D;
 #pragma unroll
-  for (int c = 0; c < D / 16; ++c) {
-    float v[16];
-    tmem_ld16(lane_base + tmem_o(x) + c * 16, v);
+  for (int c = 0; c < D / 32; ++c) {  // two TMEM loads in flight per wait
+    float v[32];
+    tmem_ld16(lane_base + tmem_o(x) + c * 32, v);
+    tmem_ld16(lane_base + tmem_o(x) + c * 32 + 16, v + 16);
     tmem_wait_ld();
     if (row < q_rows) {
-      uint32_t w[8];
+      uint32_t w[16];
       float a, b;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, a, b);
-      *reinterpret_cast<uint4*>(o + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(o + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+      for (int k = 0; k < 16; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, a, b);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(o + c * 32 + q * 8) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     }
   }
   tc_fence_before();
