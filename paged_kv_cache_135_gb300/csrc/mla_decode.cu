@@ -35,8 +35,8 @@
 // partial states that a small second kernel (mla_merge_kernel) combines.
 // Roles per CTA: warps 0-3 exchange the partial scores (one thread per
 // query row), warps 4-11 run the softmax and the epilogue (two threads per
-// row), warp 12 is the TMA producer, warp 13 the tcgen05 issuer (one thread)
-// and TMEM owner.  Warp w reads TMEM lanes 32*(w%4)...
+// row), warp 12 is the TMA producer, warp 13 the tcgen05 issuer (warp-
+// convergent, one elected lane) and TMEM owner.  Warp w reads TMEM lanes 32*(w%4)...
 #include <cuda_runtime.h>
 
 #include <math.h>

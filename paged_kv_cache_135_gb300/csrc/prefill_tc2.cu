@@ -21,10 +21,11 @@
 // of a tile is complete also means every earlier MMA of the issuing thread
 // is complete (tcgen05.commit tracks all of them), so P and O may be written
 // without a further wait; the next S of a head is issued after its P V, and
-// the tensor core performs one thread's MMAs in issue order.  One thread
-// issues the MMAs in whatever order their inputs become ready.  Online
-// softmax in the log2 domain; O is rescaled only when a row's max grows by
-// more than 2^8.
+// the tensor core performs one thread's MMAs in issue order.  The MMA warp
+// issues warp-convergent from one elected lane, in a fixed order (S of both
+// heads, then per tile and head P V followed by the next S), releasing P in
+// two halves so P V starts during the exponentials.  Online softmax in the
+// log2 domain; O is rescaled only when a row's max grows by more than 2^8.
 #include <cuda_runtime.h>
 
 #include <math.h>
