@@ -49,6 +49,8 @@ constexpr int kThreads = kSmxThreads + 64;
 constexpr int kStages = 2;
 constexpr int kChunk = 128 * 128;           // one [128 rows][64 elements] swizzled region
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kMaxN = 2048;      // distinct per-item tile counts the sorted schedule handles
+constexpr int kMaxSched = 512;   // items per CTA in the sorted schedule
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of head x: O at 128x, S at 256 + 128x.
 __host__ __device__ constexpr uint32_t tmem_o(int x) { return 128u * x; }
@@ -73,9 +75,11 @@ struct Tc2Layout {
   static constexpr int kK = kQ + 2 * kStageBytes;
   static constexpr int kV = kK + kStages * kStageBytes;
   static constexpr int kBar = kV + kStages * kStageBytes;
-  static constexpr int kNumBars = 18;
-  static constexpr int kMisc = kBar + kNumBars * 8;            // tmem slot, abort, info[4]
-  static constexpr int kTotal = 1024 + kMisc + 64;
+  static constexpr int kNumBars = 19;
+  static constexpr int kMisc = kBar + kNumBars * 8;            // tmem slot, abort, schedule ints
+  static constexpr int kHist = kMisc + 64;                     // int[kMaxN]
+  static constexpr int kList = kHist + kMaxN * 4;              // int2[kMaxSched]
+  static constexpr int kTotal = 1024 + kList + kMaxSched * 8;
   static_assert(kTotal <= 232448, "fits the opt-in shared memory of one SM");
 };
 
@@ -84,7 +88,7 @@ struct Tc2Layout {
 // s_full[h], p_full[h], o_done[h] are per head.
 enum Bar {
   kQFull = 0, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-  kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kDrain, kPHalf0, kPHalf1
+  kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kDrain, kPHalf0, kPHalf1, kQEmpty
 };
 
 __device__ __forceinline__ bool wait_t2(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -136,8 +140,12 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint8_t* smem, uint64_t* bars,
                                              volatile int* abort_flag, int s, int h0, int g,
-                                             int tok0, int kv_len, int n_tiles, int lane) {
+                                             int tok0, int kv_len, int n_tiles, int gj0, int kit,
+                                             int lane) {
   using L = Tc2Layout<D>;
+  // This item's query tiles replace the previous item's once its last S is
+  // done (q_empty).
+  if (kit > 0 && !wait_t2(&bars[kQEmpty], (kit - 1) & 1, abort_flag, p.err_flag)) return;
   if (lane == 0) {
     mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kStageBytes);
 #pragma unroll
@@ -150,7 +158,8 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
   const int nsub = kBN / p.box_tokens;
   const uint32_t box_bytes = static_cast<uint32_t>(p.box_tokens) * 128u;
   for (int j = 0; j < n_tiles; ++j) {
-    const int stage = j & 1;
+    const int gj = gj0 + j;  // the CTA's running tile count sets stage and phase
+    const int stage = gj & 1;
     const int tok = j * kBN + lane * p.box_tokens;
     int pb = -1;
     if (lane < nsub && tok < kv_len)
@@ -165,7 +174,7 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
     // heads' P V(j-2) have.
     for (int part = 0; part < 2; ++part) {
       const int empty = part ? kVEmpty0 : kKEmpty0, full = part ? kVFull0 : kKFull0;
-      const bool ok = wait_t2(&bars[empty + stage], ((j >> 1) & 1) ^ 1, abort_flag, p.err_flag);
+      const bool ok = wait_t2(&bars[empty + stage], ((gj >> 1) & 1) ^ 1, abort_flag, p.err_flag);
       const bool go = valid && ok;
       const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, go));
       if (lane == 0) mbar_arrive_expect_tx(&bars[full + stage], nvalid * box_bytes * L::kHalves);
@@ -178,11 +187,6 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
                       pb);
       }
     }
-  }
-  // Every copy issued must land before shared memory can be released.
-  for (int j = n_tiles > kStages ? n_tiles - kStages : 0; j < n_tiles; ++j) {
-    mbar_wait_bounded(&bars[kKFull0 + (j & 1)], (j >> 1) & 1, p.err_flag);
-    mbar_wait_bounded(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, p.err_flag);
   }
 }
 
@@ -200,7 +204,7 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
 template <int D, bool kBf16>
 __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
                                         volatile int* abort_flag, uint32_t tmem, int n_tiles,
-                                        uint32_t leader) {
+                                        int gj0, int kit, uint32_t leader) {
   using L = Tc2Layout<D>;
   constexpr int kSSteps = D / 16;   // K steps of S = Q K^T
   constexpr int kPSteps = kBN / 16; // K steps of O += P V
@@ -210,52 +214,58 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
   const uint64_t k0 = umma_desc_sw128(smem_u32(smem + L::kK), 16, 1024);
   const uint64_t v0 = umma_desc_sw128(smem_u32(smem + L::kV), kChunk, 1024);
 
+  // Tiles j, t, kt below are this item's; gj0 + j is the CTA's running tile
+  // count, which sets the ring stage and every barrier phase.
   // S_x(j).  The next block is P V_y(t) + S_y(t+1): it starts on the first
   // half of P_y(t) and needs V(t) and K(kt) (kt = t+1, or any tile whose K
   // has surely landed when no S follows); returns whether all three were
-  // there before the last MMA.
+  // there before the last MMA.  The item's last S releases its query tiles.
   auto s_group = [&](int x, int j, int y, int t, int kt) -> bool {
+    const int G = gj0 + j, T = gj0 + t, KT = gj0 + kt;
     const uint32_t d = tmem + tmem_s(x);
     const uint64_t qx = desc_advance(q0, x * L::kStageBytes);
-    const uint64_t k_st = desc_advance(k0, (j & 1) * L::kStageBytes);
+    const uint64_t k_st = desc_advance(k0, (G & 1) * L::kStageBytes);
     auto a_at = [&](int st) { return desc_advance(qx, (st / 4) * kChunk + (st % 4) * 32); };
     auto b_at = [&](int st) { return desc_advance(k_st, (st / 4) * kChunk + (st % 4) * 32); };
 #pragma unroll
     for (int st = 0; st < kSSteps - 2; ++st) umma_ss_e(d, a_at(st), b_at(st), idesc_s, st != 0, leader);
     const bool ready = umma_ss_acc2_test3_e(
         d, a_at(kSSteps - 2), b_at(kSSteps - 2), a_at(kSSteps - 1), b_at(kSSteps - 1), idesc_s,
-        &bars[kPHalf0 + y], t & 1, &bars[kVFull0 + (t & 1)], (t >> 1) & 1,
-        &bars[kKFull0 + (kt & 1)], (kt >> 1) & 1, leader);
+        &bars[kPHalf0 + y], T & 1, &bars[kVFull0 + (T & 1)], (T >> 1) & 1,
+        &bars[kKFull0 + (KT & 1)], (KT >> 1) & 1, leader);
     umma_commit_e(&bars[kSFull0 + x], leader);
-    if (x == 1) umma_commit_e(&bars[kKEmpty0 + (j & 1)], leader);
+    if (x == 1) umma_commit_e(&bars[kKEmpty0 + (G & 1)], leader);
+    if (x == 1 && j == n_tiles - 1) umma_commit_e(&bars[kQEmpty], leader);
     return ready;
   };
   // P V_x(j), A = P in the head's S columns of tensor memory: tokens 0-63
   // (released by p_half), then, once the whole of P_x(j) is there, 64-127.
   auto pv_group = [&](int x, int j) -> bool {
-    const uint64_t v_st = desc_advance(v0, (j & 1) * L::kStageBytes);
+    const int G = gj0 + j;
+    const uint64_t v_st = desc_advance(v0, (G & 1) * L::kStageBytes);
     const uint32_t d = tmem + tmem_o(x), a0 = tmem + tmem_s(x);
 #pragma unroll
     for (int ks = 0; ks < kPSteps / 2; ++ks)
       umma_ts_e(d, a0 + ks * 8, desc_advance(v_st, ks * 16 * 128), idesc_o, ks > 0 || j > 0, leader);
-    if (!wait_t2(&bars[kPFull0 + x], j & 1, abort_flag, p.err_flag)) return false;
+    if (!wait_t2(&bars[kPFull0 + x], G & 1, abort_flag, p.err_flag)) return false;
     tc_fence_after();
 #pragma unroll
     for (int ks = kPSteps / 2; ks < kPSteps; ++ks)
       umma_ts_e(d, a0 + ks * 8, desc_advance(v_st, ks * 16 * 128), idesc_o, 1u, leader);
-    if (x == 1) umma_commit_e(&bars[kVEmpty0 + (j & 1)], leader);
+    if (x == 1) umma_commit_e(&bars[kVEmpty0 + (G & 1)], leader);
     if (j == n_tiles - 1) umma_commit_e(&bars[kODone0 + x], leader);
     return true;
   };
   auto wait_inputs = [&](int x, int j, bool with_k) -> bool {
-    return wait_t2(&bars[kPHalf0 + x], j & 1, abort_flag, p.err_flag) &&
-           wait_t2(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, abort_flag, p.err_flag) &&
+    const int G = gj0 + j;
+    return wait_t2(&bars[kPHalf0 + x], G & 1, abort_flag, p.err_flag) &&
+           wait_t2(&bars[kVFull0 + (G & 1)], (G >> 1) & 1, abort_flag, p.err_flag) &&
            (!with_k ||
-            wait_t2(&bars[kKFull0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err_flag));
+            wait_t2(&bars[kKFull0 + ((G + 1) & 1)], ((G + 1) >> 1) & 1, abort_flag, p.err_flag));
   };
 
-  if (!wait_t2(&bars[kQFull], 0, abort_flag, p.err_flag)) return;
-  if (!wait_t2(&bars[kKFull0], 0, abort_flag, p.err_flag)) return;
+  if (!wait_t2(&bars[kQFull], kit & 1, abort_flag, p.err_flag)) return;
+  if (!wait_t2(&bars[kKFull0 + (gj0 & 1)], (gj0 >> 1) & 1, abort_flag, p.err_flag)) return;
   tc_fence_after();
   s_group(0, 0, 0, 0, 0);
   bool ready = s_group(1, 0, 0, 0, n_tiles > 1 ? 1 : 0);
@@ -289,13 +299,14 @@ template <typename T, int D>
 __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
                                             volatile int* abort_flag, uint32_t tmem, int x,
                                             int row, int n_tiles, int q0, int ctx, int kv_len,
-                                            int q_rows, int tok0, int h) {
+                                            int q_rows, int tok0, int h, int gj0, int kit) {
   using L = Tc2Layout<D>;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(row & ~31) << 16);
   const int pos = ctx + q0 + row;
   float m_used = -INFINITY, l = 0.f;
   for (int j = 0; j < n_tiles; ++j) {
-    wait_t2(&bars[kSFull0 + x], j & 1, abort_flag, p.err_flag);
+    const int gj = gj0 + j;  // the CTA's running tile count sets every phase
+    wait_t2(&bars[kSFull0 + x], gj & 1, abort_flag, p.err_flag);
     tc_fence_after();
     // Row max of the raw scores (the scale is positive, so it commutes with
     // the max and is folded into the exponent below), read in two halves of
@@ -353,8 +364,8 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     // either head's P V of the tile) so stale contents cannot reach P V.
     const int valid = kv_len - j * kBN;
     if (valid < kBN) {
-      wait_t2(&bars[kVFull0 + (j & 1)], (j >> 1) & 1, abort_flag, p.err_flag);
-      uint8_t* vst = smem + L::kV + (j & 1) * L::kStageBytes;
+      wait_t2(&bars[kVFull0 + (gj & 1)], (gj >> 1) & 1, abort_flag, p.err_flag);
+      uint8_t* vst = smem + L::kV + (gj & 1) * L::kStageBytes;
       const int n16 = (kBN - valid) * L::kHalves * 8;
       for (int e = row; e < n16; e += kHeadThreads) {
         const int r = valid + e / (L::kHalves * 8), c = (e / 8) % L::kHalves, q = e % 8;
@@ -408,7 +419,7 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
   }
 
   // Epilogue: normalise and write this head's row.
-  wait_t2(&bars[kODone0 + x], 0, abort_flag, p.err_flag);
+  wait_t2(&bars[kODone0 + x], kit & 1, abort_flag, p.err_flag);
   tc_fence_after();
   const float inv = l > 0.f ? 1.f / l : 0.f;
   T* o = static_cast<T*>(p.out) + (static_cast<long long>(tok0) + row) * p.num_q_heads * D + h * D;
@@ -432,6 +443,173 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
   tc_fence_before();
 }
 
+// One work item: (sequence, 128-query tile, pair of query heads); every
+// lane of the calling warp gets the same result.
+struct Tc2Item {
+  int s, h0, q0, q_rows, ctx, kv_len, n_tiles, tok0;
+  bool ok;  // kv_len fits the block table
+};
+__device__ __forceinline__ bool tc2_item(const Tc2Params& p, int w, int lane, Tc2Item& it) {
+  const int pairs = p.num_q_heads / 2;
+  int s = 0, tile = 0, ctx = 0, len = 0;
+  if (!tc2_locate(p, w / pairs, lane, s, tile, ctx, len)) return false;
+  it.s = s;
+  it.h0 = 2 * (w % pairs);
+  it.q0 = tile * kBM;
+  it.q_rows = min(kBM, len - it.q0);
+  it.ctx = ctx;
+  it.kv_len = ctx + len;
+  it.ok = it.kv_len <= p.max_blocks * p.block_size;
+  it.n_tiles = (ctx + it.q0 + it.q_rows - 1) / kBN + 1;
+  it.tok0 = p.cu_seqlens[s] + it.q0;
+  return true;
+}
+
+// The work item of query tile t of sequence s, head pair `pair`.
+__device__ __forceinline__ void tc2_item_at(const Tc2Params& p, int s, int t, int pair,
+                                            Tc2Item& it) {
+  const int len = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
+  it.s = s;
+  it.h0 = 2 * pair;
+  it.q0 = t * kBM;
+  it.q_rows = min(kBM, len - it.q0);
+  it.ctx = p.context_lens ? p.context_lens[s] : 0;
+  it.kv_len = it.ctx + len;
+  it.ok = it.kv_len <= p.max_blocks * p.block_size;
+  it.n_tiles = (it.ctx + it.q0 + it.q_rows - 1) / kBN + 1;
+  it.tok0 = p.cu_seqlens[s] + it.q0;
+}
+
+// Tiles attended by query tile t of a sequence with `ctx` cached tokens and
+// `len` new ones (its weight in the schedule).
+__device__ __forceinline__ int tc2_weight(int ctx, int len, int t) {
+  const int rows = min(kBM, len - kBM * t);
+  return (ctx + kBM * t + rows - 1) / kBN + 1;
+}
+
+// Sorted schedule, built by every CTA in its prologue (all threads): the work
+// items ordered by weight (tiles attended) from heaviest, then sequence,
+// tile and head pair, dealt to the CTAs in a serpentine (CTA c takes
+// positions c, 2G-1-c, 2G+c, ...), so every CTA gets a similar total.  A
+// query tile's weight is c0 + t + 1 (c0 = ceil(ctx / 128)) except that the
+// last tile of a sequence may share its predecessor's, so the tile of a
+// given weight in a sequence is found in closed form.  Returns the number
+// of items of this CTA, written as (s, t << 8 | pair) to `list`, or -1 when
+// the bounds are exceeded (then the CTA walks items c, c + G, ... unsorted).
+__device__ __forceinline__ int tc2_tiles_of_weight(const Tc2Params& p, int s, int n, int* t_out) {
+  const int len = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
+  const int ctx = p.context_lens ? p.context_lens[s] : 0;
+  const int nq = len > 0 ? (len + kBM - 1) / kBM : 0;
+  int cnt = 0;
+  const int t1 = n - 1 - (ctx + kBN - 1) / kBN;
+  if (t1 >= 0 && t1 < nq - 1) t_out[cnt++] = t1;
+  if (nq > 0 && tc2_weight(ctx, len, nq - 1) == n) t_out[cnt++] = nq - 1;
+  return cnt;
+}
+template <int D>
+__device__ int tc2_build_schedule(const Tc2Params& p, uint8_t* smem, int tid, int warp, int lane,
+                                  int c, int G) {
+  using L = Tc2Layout<D>;
+  int* hist = reinterpret_cast<int*>(smem + L::kHist);
+  int2* list = reinterpret_cast<int2*>(smem + L::kList);
+  volatile int* misc = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);  // qtot, bad, nsched
+  const int pairs = p.num_q_heads / 2;
+  for (int i = tid; i < kMaxN; i += kThreads) hist[i] = 0;
+  if (tid == 0) {
+    misc[0] = 0;
+    misc[1] = pairs > 255 ? 1 : 0;
+  }
+  __syncthreads();
+  for (int s = tid; s < p.num_seqs; s += kThreads) {
+    const int len = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
+    const int ctx = p.context_lens ? p.context_lens[s] : 0;
+    const int nq = len > 0 ? (len + kBM - 1) / kBM : 0;
+    for (int t = 0; t < nq; ++t) {
+      const int n = tc2_weight(ctx, len, t);
+      if (n < kMaxN) atomicAdd(&hist[n], 1);
+      else misc[1] = 1;
+    }
+    if (nq) atomicAdd(const_cast<int*>(&misc[0]), nq);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int nsched = -1;
+    if (misc[1] == 0) {
+      // hist[n] -> tiles with weight > n (suffix sums, 32 entries at a time).
+      int carry = 0;
+      for (int base = kMaxN - 32; base >= 0; base -= 32) {
+        const int v = hist[base + lane];
+        int x = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_down_sync(0xffffffffu, x, off);
+          if (lane + off < 32) x += y;
+        }
+        hist[base + lane] = carry + x - v;
+        carry += __shfl_sync(0xffffffffu, x, 0);
+      }
+      __syncwarp();
+      const long long items = static_cast<long long>(misc[0]) * pairs;
+      nsched = 0;
+      for (int k = 0;; ++k) {
+        const long long i = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+        if (i >= items) break;
+        if (k >= kMaxSched) {
+          nsched = -1;
+          break;
+        }
+        const int qi = static_cast<int>(i / pairs), pair = static_cast<int>(i % pairs);
+        int lo = 1, hi = kMaxN - 1;  // smallest n with (tiles heavier than n) <= qi
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (hist[mid] <= qi) hi = mid; else lo = mid + 1;
+        }
+        const int n = lo;
+        int r = qi - hist[n];  // rank among the tiles of weight n, in (s, t) order
+        int found_s = -1, found_t = 0;
+        for (int base = 0; base < p.num_seqs && found_s < 0; base += 32) {
+          const int sq = base + lane;
+          int ts[2] = {0, 0};
+          const int cnt = sq < p.num_seqs ? tc2_tiles_of_weight(p, sq, n, ts) : 0;
+          int x = cnt;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+          }
+          const unsigned hit = __ballot_sync(0xffffffffu, x > r && x - cnt <= r);
+          if (hit) {
+            const int src = __ffs(hit) - 1;
+            const int before = __shfl_sync(0xffffffffu, x - cnt, src);
+            const int t0 = __shfl_sync(0xffffffffu, ts[0], src);
+            const int t1 = __shfl_sync(0xffffffffu, ts[1], src);
+            found_s = base + src;
+            found_t = (r - before) == 0 ? t0 : t1;
+          } else {
+            r -= __shfl_sync(0xffffffffu, x, 31);
+          }
+        }
+        if (found_s < 0) {  // inconsistent counts: walk the items unsorted instead
+          nsched = -1;
+          break;
+        }
+        if (lane == 0) list[k] = make_int2(found_s, (found_t << 8) | pair);
+        nsched = k + 1;
+      }
+    }
+    if (lane == 0) misc[2] = nsched;
+  }
+  __syncthreads();
+  return misc[2];
+}
+
+// Persistent: CTA c takes its items from the sorted schedule (or c, c + G,
+// ... when that does not fit).  Every role walks the same items; the ring
+// stages and barrier phases follow
+// the CTA's running tile count (gj0) and item count (ni), so the next item's
+// queries, K/V tiles and first S are loaded and computed while the softmax
+// warps finish the previous item's epilogue.  An item whose sequence does not
+// fit the block table is skipped (KVC_FLAG_LEN_RANGE, nothing written).
 template <typename T, int D, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -445,63 +623,84 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-  int* info = reinterpret_cast<int*>(smem + L::kMisc + 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pairs = p.num_q_heads / 2;
-  const int h0 = 2 * (blockIdx.x % pairs);
-  const int item = blockIdx.x / pairs;
+  const int c = blockIdx.x, G = gridDim.x;
 
-  if (warp == 0) {
-    int s = 0, tile = 0, ctx = 0, len = 0;
-    const bool found = tc2_locate(p, item, lane, s, tile, ctx, len);
-    if (lane == 0) {
-      info[0] = found ? s : -1;
-      info[1] = tile;
-      info[2] = ctx;
-      info[3] = len;
-      for (int i = 0; i < L::kNumBars; ++i) {
-        uint32_t c = 1;
-        if (i == kPFull0 || i == kPFull1 || i == kPHalf0 || i == kPHalf1) c = kHeadThreads;
-        mbar_init(&bars[i], c);
-      }
-      *abort_flag = 0;
-      fence_barrier_init();
+  if (tid == 0) {
+    for (int i = 0; i < L::kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == kPFull0 || i == kPFull1 || i == kPHalf0 || i == kPHalf1) cnt = kHeadThreads;
+      mbar_init(&bars[i], cnt);
     }
+    *abort_flag = 0;
+    fence_barrier_init();
   }
-  __syncthreads();
-  const int s = info[0];
-  if (s < 0) return;  // grid slots beyond the real number of tiles
-  const int q0 = info[1] * kBM, ctx = info[2], len = info[3];
-  const int q_rows = min(kBM, len - q0);
-  const int kv_len = ctx + len;
-  if (kv_len > p.max_blocks * p.block_size) {  // table too short: flag, write nothing
-    if (tid == 0) set_flag(p.err_flag, KVC_FLAG_LEN_RANGE);
-    return;
-  }
-  const int n_tiles = (ctx + q0 + q_rows - 1) / kBN + 1;
-  const int tok0 = p.cu_seqlens[s] + q0;
-
   if (warp == kMmaWarp) tmem_alloc(tslot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  const int nsched = tc2_build_schedule<D>(p, smem, tid, warp, lane, c, G);
+  const int2* list = reinterpret_cast<const int2*>(smem + L::kList);
+  // The k-th item of this CTA: from the sorted schedule, or items c + k*G.
+  auto next_item = [&](int k, Tc2Item& it) -> bool {
+    if (nsched >= 0) {
+      if (k >= nsched) return false;
+      const int2 e = list[k];
+      tc2_item_at(p, e.x, e.y >> 8, e.y & 255, it);
+      return true;
+    }
+    return tc2_item(p, c + k * G, lane, it);
+  };
 
+  int gj0 = 0, ni = 0;
   if (warp < kProducerWarp) {
     const int x = tid / kHeadThreads;
-    tc2_softmax<T, D>(p, smem, bars, abort_flag, tmem, x, tid % kHeadThreads, n_tiles, q0, ctx,
-                      kv_len, q_rows, tok0, h0 + x);
+    for (int k = 0;; ++k) {
+      Tc2Item it;
+      if (!next_item(k, it)) break;
+      if (!it.ok) continue;
+      tc2_softmax<T, D>(p, smem, bars, abort_flag, tmem, x, tid % kHeadThreads, it.n_tiles, it.q0,
+                        it.ctx, it.kv_len, it.q_rows, it.tok0, it.h0 + x, gj0, ni);
+      gj0 += it.n_tiles;
+      ++ni;
+      if (*abort_flag) break;
+    }
   } else if (warp == kProducerWarp) {
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
     }
-    tc2_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, s, h0, h0 / p.group, tok0,
-                    kv_len, n_tiles, lane);
+    for (int k = 0;; ++k) {
+      Tc2Item it;
+      if (!next_item(k, it)) break;
+      if (!it.ok) {
+        if (lane == 0) set_flag(p.err_flag, KVC_FLAG_LEN_RANGE);
+        continue;
+      }
+      tc2_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, it.s, it.h0,
+                      it.h0 / p.group, it.tok0, it.kv_len, it.n_tiles, gj0, ni, lane);
+      gj0 += it.n_tiles;
+      ++ni;
+      if (*abort_flag) break;
+    }
+    // Every copy issued must land before shared memory can be released.
+    for (int gj = gj0 > kStages ? gj0 - kStages : 0; gj < gj0; ++gj) {
+      mbar_wait_bounded(&bars[kKFull0 + (gj & 1)], (gj >> 1) & 1, p.err_flag);
+      mbar_wait_bounded(&bars[kVFull0 + (gj & 1)], (gj >> 1) & 1, p.err_flag);
+    }
   } else {
     const uint32_t leader = elect_one_sync();
-    tc2_mma<D, kBf16>(p, smem, bars, abort_flag, tmem, n_tiles, leader);
+    for (int k = 0;; ++k) {
+      Tc2Item it;
+      if (!next_item(k, it)) break;
+      if (!it.ok) continue;
+      tc2_mma<D, kBf16>(p, smem, bars, abort_flag, tmem, it.n_tiles, gj0, ni, leader);
+      gj0 += it.n_tiles;
+      ++ni;
+      if (*abort_flag) break;
+    }
     // Teardown: all tensor-core work done before TMEM is freed.
     __syncwarp();
     umma_commit_e(&bars[kDrain], leader);
@@ -556,10 +755,15 @@ kvc_status run_prefill_tc2(const PrefillArgs& a) {
   p.num_blocks = a.num_blocks;
   p.box_tokens = box_tokens;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  // Upper bound of query tiles: sum ceil(L_s / BM) <= T / BM + S.
-  const long long grid =
+  // Work items: (query tile, head pair); query tiles <= T / BM + S.  One
+  // persistent CTA per SM, or fewer when there are fewer items.
+  const long long items =
       (static_cast<long long>(a.num_tokens) / kBM + a.num_seqs) * (a.num_q_heads / 2);
-  if (grid > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+  if (items > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+  const int sms = device_sm_count();
+  if (sms <= 0) return KVC_ERR_CUDA;
+  const long long grid = items < sms ? items : sms;
+  if (grid <= 0) return KVC_OK;
   prefill_tc2_kernel<T, D, kBf16><<<static_cast<unsigned>(grid), kThreads, Tc2Layout<D>::kTotal,
                                     a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
