@@ -52,6 +52,11 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr int kMaxN = 2048;      // distinct per-item tile counts the sorted schedule handles
 constexpr int kMaxSched = 512;   // items per CTA in the sorted schedule
 constexpr uint32_t kTmemCols = 512;
+// Epilogue staging of one softmax warp: 32 rows of 32 output elements
+// (64 bytes), rows 80 bytes apart so that 16-byte accesses of 8 consecutive
+// rows fall in distinct banks.
+constexpr int kStgRow = 80;
+constexpr int kStgWarpBytes = 32 * kStgRow;
 // TMEM columns of head x: O at 128x, S at 256 + 128x.
 __host__ __device__ constexpr uint32_t tmem_o(int x) { return 128u * x; }
 __host__ __device__ constexpr uint32_t tmem_s(int x) { return 256u + 128u * x; }
@@ -79,7 +84,8 @@ struct Tc2Layout {
   static constexpr int kMisc = kBar + kNumBars * 8;            // tmem slot, abort, schedule ints
   static constexpr int kHist = kMisc + 64;                     // int[kMaxN]
   static constexpr int kList = kHist + kMaxN * 4;              // int2[kMaxSched]
-  static constexpr int kTotal = 1024 + kList + kMaxSched * 8;
+  static constexpr int kStg = (kList + kMaxSched * 8 + 15) & ~15;  // epilogue staging, per warp
+  static constexpr int kTotal = 1024 + kStg + (kSmxThreads / 32) * kStgWarpBytes;
   static_assert(kTotal <= 232448, "fits the opt-in shared memory of one SM");
 };
 
@@ -418,27 +424,39 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     mbar_arrive(&bars[kPFull0 + x]);
   }
 
-  // Epilogue: normalise and write this head's row.
+  // Epilogue: normalise and write this head's rows, 32 columns at a time.
+  // Each warp passes its 32 rows through shared memory so that a store
+  // instruction writes 8 rows x 64 contiguous bytes (8 lines) rather than
+  // 32 rows x 16 bytes (32 lines).
   wait_t2(&bars[kODone0 + x], kit & 1, abort_flag, p.err_flag);
   tc_fence_after();
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  T* o = static_cast<T*>(p.out) + (static_cast<long long>(tok0) + row) * p.num_q_heads * D + h * D;
+  const int lane = row & 31, wrow0 = row & ~31;
+  uint8_t* stg = smem + L::kStg + (x * 4 + (row >> 5)) * kStgWarpBytes;
+  const long long ostride = static_cast<long long>(p.num_q_heads) * D;
+  T* obase = static_cast<T*>(p.out) + (static_cast<long long>(tok0) + wrow0) * ostride + h * D;
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {  // two TMEM loads in flight per wait
     float v[32];
     tmem_ld16(lane_base + tmem_o(x) + c * 32, v);
     tmem_ld16(lane_base + tmem_o(x) + c * 32 + 16, v + 16);
     tmem_wait_ld();
-    if (row < q_rows) {
-      uint32_t w[16];
-      float a, b;
+    uint32_t w[16];
+    float a, b;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, a, b);
+    for (int k = 0; k < 16; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, a, b);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(o + c * 32 + q * 8) =
-            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(stg + lane * kStgRow + q * 16) =
+          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 8 + (lane >> 2), q = lane & 3;
+      const uint4 val = *reinterpret_cast<const uint4*>(stg + r * kStgRow + q * 16);
+      if (wrow0 + r < q_rows) *reinterpret_cast<uint4*>(obase + r * ostride + c * 32 + q * 8) = val;
     }
+    __syncwarp();
   }
   tc_fence_before();
 }
