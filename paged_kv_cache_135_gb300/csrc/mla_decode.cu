@@ -326,17 +326,36 @@ __device__ __forceinline__ void mla_mma(const MlaParams& p, uint8_t* smem, uint6
 // this rank's 256 output columns).  The two halves' partial sums l are added
 // first.  A sequence the share holds whole is normalised and written out; a
 // piece of a split sequence publishes its partial state (m, l, unnormalised
-// O) in workspace slot (cluster, slot, rank) for mla_merge_kernel.
+// O) in workspace slot (cluster, slot, rank) for mla_merge_kernel.  Each
+// warp passes its 32 rows through `stg` (2 KB of shared memory: 32 rows of
+// 64 bytes, 16-byte chunk q of row r at r*64 + (q ^ ((r >> 1) & 3))*16, so
+// neither the row-wise writes nor the chunk-wise reads conflict), so that a
+// store instruction writes 8 rows x 64 contiguous bytes rather than 32 rows
+// x 16 bytes.
 template <typename T>
 __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, int row, int h,
                                         int b, bool complete, int cl, int slot, int rank,
-                                        float m_used, float l_half, float* red) {
+                                        float m_used, float l_half, float* red, uint8_t* stg) {
   named_bar_sync(1, kMathThreads);
   red[h * kH + row] = l_half;
   named_bar_sync(1, kMathThreads);
   const float l = red[row] + red[kH + row];
+  const int lane = row & 31, wrow0 = row & ~31;
+  // This thread's 64 bytes -> its staging row; then chunk i of the read-back
+  // pattern (row i*8 + lane/4, 16-byte piece lane%4).
+  auto put = [&](const uint32_t* w) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) * 16)) =
+          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    __syncwarp();
+  };
+  auto get = [&](int i) -> uint4 {
+    const int r = i * 8 + (lane >> 2), q = lane & 3;
+    return *reinterpret_cast<const uint4*>(stg + r * 64 + ((q ^ ((r >> 1) & 3)) * 16));
+  };
   if (complete) {
-    T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * kH + row) * kNope +
+    T* out = static_cast<T*>(p.out) + (static_cast<long long>(b) * kH + wrow0) * kNope +
              rank * kOutCols + h * 128;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     for (int c = 0; c < 8; c += 2) {  // two loads in flight per wait
@@ -348,24 +367,39 @@ __device__ __noinline__ void mla_finish(const MlaParams& p, uint32_t o_taddr, in
       float ra, rb;
 #pragma unroll
       for (int k = 0; k < 16; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, ra, rb);
+      put(w);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(out + c * 16 + q * 8) =
-            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      for (int i = 0; i < 4; ++i) {
+        const int r = i * 8 + (lane >> 2), q = lane & 3;
+        *reinterpret_cast<uint4*>(out + r * kNope + c * 16 + q * 8) = get(i);
+      }
+      __syncwarp();
     }
     return;
   }
-  const long long wrow = ((static_cast<long long>(cl) * 2 + slot) * 2 + rank) * kH + row;
+  float* wbase = p.ws_o +
+                 (((static_cast<long long>(cl) * 2 + slot) * 2 + rank) * kH + wrow0) * kOutCols +
+                 h * 128;
   for (int c = 0; c < 8; c += 2) {  // two loads in flight per wait
     float v[32];
     tmem_ld16(o_taddr + c * 16, v);
     tmem_ld16(o_taddr + c * 16 + 16, v + 16);
     tmem_wait_ld();
-    float4* dst = reinterpret_cast<float4*>(p.ws_o + wrow * kOutCols + h * 128 + c * 16);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    for (int hf = 0; hf < 2; ++hf) {  // 16 fp32 columns = 64 bytes per row
+      put(reinterpret_cast<const uint32_t*>(v + hf * 16));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = i * 8 + (lane >> 2), q = lane & 3;
+        *reinterpret_cast<uint4*>(wbase + r * kOutCols + c * 16 + hf * 16 + q * 4) = get(i);
+      }
+      __syncwarp();
+    }
   }
-  if (h == 0) *reinterpret_cast<float2*>(p.ws_ml + wrow * 2) = make_float2(m_used, l);
+  if (h == 0) {
+    const long long wrow = ((static_cast<long long>(cl) * 2 + slot) * 2 + rank) * kH + row;
+    *reinterpret_cast<float2*>(p.ws_ml + wrow * 2) = make_float2(m_used, l);
+  }
 }
 
 // ------------------------------------------------------------- exchange
@@ -601,8 +635,9 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
     if (last) {  // end of this sequence's share
       wait_cta(&bars[kPVDone], it & 1, abort_flag, p.err_flag);
       tc_fence_after();
+      // P V is done, so the P buffer is free: 2 KB of it stage each warp's rows.
       mla_finish<T>(p, lane_base + kTmemO + h * 128, row, h, cm.b, seg_first_j == 0 && cm.last(),
-                    cl, slot, rank, m_used, l, red);
+                    cl, slot, rank, m_used, l, red, smem + L::kP + (h * 4 + (row >> 5)) * 2048);
       tc_fence_before();
       slot = 1;
     }

@@ -341,6 +341,11 @@ __device__ __forceinline__ void tc_softmax(const TcPrefillParams& p, uint8_t* sm
   }
 
   // Epilogue: combine the pair's row sums, normalise, write this row's half.
+  // The P buffer is no longer read once the last P V is done: 2 KB of it per
+  // warp stage the warp's 32 rows, 32 columns at a time (16-byte chunk q of
+  // row r at r*64 + (q ^ ((r >> 1) & 3))*16: no bank conflicts either way),
+  // so that a store instruction writes 8 rows x 64 contiguous bytes rather
+  // than 32 rows x 16 bytes.
   wait_tc(&bars[kPVDone], (n_tiles - 1) & 1, abort_flag, p.err_flag);
   tc_fence_after();
   const int rb = n_tiles & 1;  // the reduction buffer not used by the last tile
@@ -348,21 +353,34 @@ __device__ __forceinline__ void tc_softmax(const TcPrefillParams& p, uint8_t* sm
   named_bar_sync(1, kSmxThreads);
   const float lt = l + red[(rb * 2 + (half ^ 1)) * kBM + row];
   const float inv = lt > 0.f ? 1.f / lt : 0.f;
-  T* o = static_cast<T*>(p.out) + (static_cast<long long>(tok0) + row) * p.num_q_heads * D +
-         h * D + half * (D / 2);
+  uint8_t* stg = smem + L::kP + warp * 2048;
+  const int wrow0 = quad * 32;
+  const long long ostride = static_cast<long long>(p.num_q_heads) * D;
+  T* obase = static_cast<T*>(p.out) + (static_cast<long long>(tok0) + wrow0) * ostride + h * D +
+             half * (D / 2);
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    float v[16];
-    tmem_ld16(lane_base + kTmemO + half * (D / 2) + c * 16, v);
+  for (int c = 0; c < D / 64; ++c) {  // two TMEM loads in flight per wait
+    float v[32];
+    tmem_ld16(lane_base + kTmemO + half * (D / 2) + c * 32, v);
+    tmem_ld16(lane_base + kTmemO + half * (D / 2) + c * 32 + 16, v + 16);
     tmem_wait_ld();
-    if (row < q_rows) {
-      uint32_t w[8];
-      float a, b;
+    uint32_t w[16];
+    float a, b;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, a, b);
-      *reinterpret_cast<uint4*>(o + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(o + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+    for (int k = 0; k < 16; ++k) w[k] = Pack<T>::run(v[2 * k] * inv, v[2 * k + 1] * inv, a, b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) * 16)) =
+          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 8 + (lane >> 2), q = lane & 3;
+      const uint4 val =
+          *reinterpret_cast<const uint4*>(stg + r * 64 + ((q ^ ((r >> 1) & 3)) * 16));
+      if (wrow0 + r < q_rows) *reinterpret_cast<uint4*>(obase + r * ostride + c * 32 + q * 8) = val;
     }
+    __syncwarp();
   }
   tc_fence_before();
 }
