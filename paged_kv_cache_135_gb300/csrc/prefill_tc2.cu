@@ -315,19 +315,21 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     wait_t2(&bars[kSFull0 + x], gj & 1, abort_flag, p.err_flag);
     tc_fence_after();
     // Row max of the raw scores (the scale is positive, so it commutes with
-    // the max and is folded into the exponent below), read in two halves of
-    // 64 columns to keep register pressure down; S stays in tensor memory
-    // and is read again for the exponentials.  Causal + length mask: token k
-    // of the tile is visible iff k < lim; only tiles that reach past this row
-    // take the masked path.
+    // the max and is folded into the exponent below).  The scores stay in
+    // tensor memory and are read in halves of 64 columns to keep register
+    // pressure down: half 1 first (for its max only), then half 0, which is
+    // kept in registers for its exponentials, so the first half of P is
+    // released after two rounds of loads, not three.  Causal + length mask:
+    // token k of the tile is visible iff k < lim; only tiles that reach past
+    // this row take the masked path.
     const int kv0 = j * kBN;
     const int lim = min(pos + 1, kv_len) - kv0;
     float mx8[8];
 #pragma unroll
     for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
+    float s[kBN / 2];
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      float s[kBN / 2];
+    for (int hf = 1; hf >= 0; --hf) {
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c)
         tmem_ld16(lane_base + tmem_s(x) + hf * (kBN / 2) + c * 16, s + c * 16);
@@ -365,6 +367,15 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
         for (int k = 0; k < 16; ++k) v[k] *= corr;
         tmem_st16(a, v);
       }
+      // Half 0 of the scores is read again (S is untouched until P is
+      // written), so it need not stay in registers across this rare path.
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) tmem_ld16(lane_base + tmem_s(x) + c * 16, s + c * 16);
+      tmem_wait_ld();
+      if (lim < kBN) {
+#pragma unroll
+        for (int k = 0; k < kBN / 2; ++k) s[k] = k < lim ? s[k] : -INFINITY;
+      }
     }
     // Value rows past the cached tokens are zeroed (by both heads, before
     // either head's P V of the tile) so stale contents cannot reach P V.
@@ -384,22 +395,24 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     // l adds the exponentials before rounding (P itself is rounded to T for
     // the tensor core).  P goes to the first 64 columns of the head's S (two
     // 16-bit tokens per column, token 2c in the low half of column c) in two
-    // halves: tokens 0-63 are released (p_half) while 64-127 are computed,
-    // so the first half of P V overlaps the second half of the exponentials.
-    // Half h of P overwrites only scores of half 0, which are read before.
+    // halves: tokens 0-63 (already in registers) are released (p_half) before
+    // tokens 64-127 are read again and computed, so the first half of P V
+    // overlaps the second half of the exponentials.  Half h of P overwrites
+    // only scores of half 0, which are read before.
     const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
     float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
-      float s[kBN / 2];
+      if (hf == 1) {
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld16(lane_base + tmem_s(x) + hf * (kBN / 2) + c * 16, s + c * 16);
-      tmem_wait_ld();
-      if (lim < kBN) {
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld16(lane_base + tmem_s(x) + (kBN / 2) + c * 16, s + c * 16);
+        tmem_wait_ld();
+        if (lim < kBN) {
 #pragma unroll
-        for (int k = 0; k < kBN / 2; ++k) s[k] = hf * (kBN / 2) + k < lim ? s[k] : -INFINITY;
+          for (int k = 0; k < kBN / 2; ++k) s[k] = (kBN / 2) + k < lim ? s[k] : -INFINITY;
+        }
       }
       uint32_t pk[kBN / 4];
 #pragma unroll
