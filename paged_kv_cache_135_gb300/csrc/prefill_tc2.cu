@@ -8,11 +8,14 @@
 // read back from the paged cache through the sequence's block_table;
 // "external-cannbot-model-model-infer-kvcache" Appendix C sparse_mode 3.
 //
-// GB300 design.  One CTA per (sequence, 128-query tile, pair of query heads
-// sharing a KV head), heaviest tiles first.  Both heads' 128-row query
-// tiles stay in shared memory and share one stream of 128-token K and V
-// tiles (TMA through block_table, 2-stage rings), so every K/V byte feeds
-// two heads.  Tensor memory holds O and S for each head (4 x 128 columns).
+// GB300 design.  A work item is (sequence, 128-query tile, pair of query
+// heads sharing a KV head).  The CTAs are persistent, one per SM; each takes
+// its items from a schedule sorted by weight (tiles attended) and dealt in a
+// serpentine, and loads the next item's queries, K/V and first S while the
+// previous item's epilogue runs.  Both heads' 128-row query tiles stay in
+// shared memory and share one stream of 128-token K and V tiles (TMA
+// through block_table, 2-stage rings), so every K/V byte feeds two heads.
+// Tensor memory holds O and S for each head (4 x 128 columns).
 // Each head has its own softmax warpgroup, one thread per query row and all
 // 128 columns of the tile (no cross-thread reduction).  P (bf16/fp16) is
 // written back into the head's S columns of tensor memory and read from
@@ -26,6 +29,8 @@
 // heads, then per tile and head P V followed by the next S), releasing P in
 // two halves so P V starts during the exponentials.  Online softmax in the
 // log2 domain; O is rescaled only when a row's max grows by more than 2^8.
+// The epilogue passes each warp's output rows through shared memory so that
+// every store instruction writes whole 64-byte row segments.
 #include <cuda_runtime.h>
 
 #include <math.h>
