@@ -216,6 +216,17 @@ def dist_info():
     return ws, rank, local
 
 
+def max_over_ranks(x, device):
+    """The largest x over all ranks of the job (x itself on one rank): every timing
+    is the slowest replica's."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def cpu_oracle_rate(case, budget_s=10.0):
     """Time the oracle on the workload's sequences, in order and wrapping around, until
     about budget_s of oracle time has elapsed."""
@@ -513,10 +524,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     eager_ms = e0.elapsed_time(e1) / 20
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
     value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
     tokens_per_s = ws * B / (ms_per_step * 1e-3)
@@ -552,10 +560,7 @@ def main():
         h_out.copy_(step.out, non_blocking=True)
         torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / max(1, args.e2e_steps)
-    if ws > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dev)
 
     peak, peak_kind = peaks()
     dec_avg_ms = statistics.mean(dec_ms)
