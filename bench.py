@@ -318,6 +318,12 @@ def capture(fn):
     return g
 
 
+def steps_per_graph(steps, cap=10):
+    """Steps captured per CUDA graph replay: the largest divisor of `steps` up to `cap`,
+    so the timed region is exactly `steps` steps."""
+    return max(d for d in range(1, cap + 1) if steps % d == 0)
+
+
 def prefill_flops(lens, ctx, Hq, D):
     """Causal attention FLOPs: 4 * Hq * D per (query, visible key) pair."""
     pairs = sum(c * n + n * (n + 1) // 2 for n, c in zip(lens, ctx))
@@ -478,7 +484,7 @@ def main():
     # launch over the whole cache) per replay, so no host or graph-launch gap
     # sits between steps.  The K/V read per step (far above L2) is the same
     # whatever the grouping.
-    per_graph = max(d for d in range(1, 11) if args.steps % d == 0)
+    per_graph = steps_per_graph(args.steps)
     g_dec = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())

@@ -1,0 +1,58 @@
+"""Host arithmetic of bench.py: the algorithmic bytes and FLOPs behind every roofline
+figure, the grouping of timed steps into CUDA graph replays, and the rule that a
+committed ncu traffic figure is reported only for the kernel source it was taken on."""
+
+import math
+
+import numpy as np
+
+import bench
+
+
+def test_decode_bytes_matches_its_definition():
+    # K and V rows attended, Q and O rows, one int32 table entry per block touched,
+    # one int32 length per sequence (bf16/fp16 elements).
+    lens, Hq, Hkv, D, bs = [37, 5, 16, 0], 4, 2, 64, 16
+    want = 0
+    for L in lens:
+        want += L * Hkv * D * 2 * 2          # K and V
+        want += 2 * Hq * D * 2               # q and out rows of the sequence
+        want += 4 * math.ceil(L / bs) + 4    # table entries, length
+    assert bench.decode_bytes(lens, Hq, Hkv, D, bs) == want
+    assert bench.decode_bytes([37, 5], 4, 2, 64, 16) == 21504 + 2048 + 16 + 8
+
+
+def test_write_bytes_matches_its_definition():
+    B, Hkv, D = 64, 8, 128
+    rows = 2 * B * Hkv * D * 2                # new K and V rows, bf16
+    assert bench.write_bytes(B, Hkv, D) == 2 * rows + 3 * 4 * B
+
+
+def test_prefill_flops_counts_visible_pairs_by_brute_force():
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        S = int(rng.integers(1, 5))
+        lens = [int(x) for x in rng.integers(0, 40, S)]
+        ctx = [int(x) for x in rng.integers(0, 30, S)]
+        pairs = 0
+        for n, c in zip(lens, ctx):
+            for i in range(n):                # query i sees cached keys and keys 0..i
+                for k in range(c + n):
+                    pairs += k <= c + i
+        assert bench.prefill_flops(lens, ctx, 32, 128) == 4 * 32 * 128 * pairs
+
+
+def test_steps_per_graph_divides_the_timed_steps():
+    for steps, want in [(200, 10), (3, 3), (7, 7), (13, 1), (24, 8), (1, 1), (30, 10)]:
+        got = bench.steps_per_graph(steps)
+        assert got == want and steps % got == 0
+
+
+def test_recorded_traffic_needs_the_matching_source_digest(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "p.md").write_text(
+        "kernel_source_digest: 0123456789abcdef\ntraffic_bytes_per_launch_full_size: 598906624\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("p.md", "0123456789abcdef") == 598906624.0
+    assert bench.recorded_traffic("p.md", "fedcba9876543210") is None
+    assert bench.recorded_traffic("missing.md", "0123456789abcdef") is None
