@@ -45,6 +45,8 @@
  *   KVC_ERR_UNSUPPORTED (a legal shape this build does not implement).
  * - KVC_ERR_WORKSPACE: the workspace is smaller than the size query says.
  * - KVC_ERR_CUDA: a launch failed (cudaGetLastError after launch).
+ * - KVC_ERR_OUT_OF_BLOCKS: the host block manager has no free block left
+ *   (the call changed nothing).
  * - Data errors found on the device never trap.  The kernel skips the bad
  *   access and, if `err_flag` (a device uint32, may be NULL) is given, ORs
  *   one of the KVC_FLAG_* bits into it.  The caller reads it after syncing.
@@ -68,7 +70,8 @@ typedef enum {
   KVC_ERR_INVALID_ARG = 1,
   KVC_ERR_UNSUPPORTED = 2,
   KVC_ERR_CUDA = 3,
-  KVC_ERR_WORKSPACE = 4
+  KVC_ERR_WORKSPACE = 4,
+  KVC_ERR_OUT_OF_BLOCKS = 5
 } kvc_status;
 
 typedef enum { KVC_F16 = 0, KVC_BF16 = 1 } kvc_dtype;
@@ -316,6 +319,82 @@ kvc_status kvc_paged_decode_no_alloc(const void* q, const void* key_cache,
                                      int block_size, int max_blocks_per_seq, int num_blocks,
                                      float scale, kvc_dtype dtype, int num_ctas,
                                      uint32_t* err_flag, kvc_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Host block manager: the allocator of the cache pool's physical blocks.
+ *
+ * What it follows: the hotelren.com notes "Paged KV Cache + Packed Sequence"
+ * 2.1 (fixed-size physical blocks taken from a free list, a reference count
+ * per block, per sequence its physical blocks in logical order), 2.2 (a decode
+ * step allocates a block only when the token it writes opens one; the token's
+ * slot is block * block_size + position % block_size) and 5.2 (sequences that
+ * share a prefix share its blocks; a block returns to the free list only when
+ * its count reaches 0).  Where the notes are silent: appending into a shared,
+ * partly filled last block first gives the sequence a private copy of it.
+ *
+ * Host memory only: no call here touches the GPU.  One manager is used by one
+ * thread at a time.  A sequence is an int64 id; its length counts the tokens
+ * that have slots.  Blocks are taken from the end of the free list (initially
+ * 0 .. num_blocks-1) and returned to its end.  Every call either succeeds or
+ * changes nothing.  The tables it produces are the `block_table` / `seq_lens`
+ * arguments of the attention calls above (copied to the device by the caller).
+ */
+typedef struct kvc_block_manager kvc_block_manager;
+
+/* A manager of blocks 0 .. num_blocks-1 holding block_size tokens each; one
+ * sequence holds at most max_blocks_per_seq blocks.  *out receives the handle,
+ * which the caller owns and releases with kvc_bm_destroy.  KVC_ERR_INVALID_ARG
+ * for a non-positive size, num_blocks * block_size above INT32_MAX, or NULL out. */
+kvc_status kvc_bm_create(int num_blocks, int block_size, int max_blocks_per_seq,
+                         kvc_block_manager** out);
+/* Releases the manager (NULL: nothing happens). */
+void kvc_bm_destroy(kvc_block_manager* bm);
+
+/* Blocks on the free list (-1 for NULL bm). */
+int kvc_bm_num_free(const kvc_block_manager* bm);
+/* Reference count of `block` (-1 if it is outside the pool). */
+int kvc_bm_ref_count(const kvc_block_manager* bm, int block);
+/* Length of sequence seq_id in tokens (-1 if there is no such sequence). */
+int kvc_bm_seq_len(const kvc_block_manager* bm, int64_t seq_id);
+
+/* A new sequence of num_tokens (>= 0) tokens, e.g. a prompt: it gets
+ * ceil(num_tokens / block_size) blocks with count 1.  slot_mapping (host,
+ * num_tokens int32, may be NULL) receives the slots of tokens 0 .. num_tokens-1,
+ * for the prompt's cache write.  KVC_ERR_INVALID_ARG: seq_id exists,
+ * num_tokens < 0, or more than max_blocks_per_seq blocks would be needed.
+ * KVC_ERR_OUT_OF_BLOCKS: fewer free blocks than needed. */
+kvc_status kvc_bm_add(kvc_block_manager* bm, int64_t seq_id, int num_tokens,
+                      int32_t* slot_mapping);
+
+/* A new sequence `child` sharing every block of `parent` (each count + 1) and
+ * its length: a shared prefix, as in beam search or parallel sampling.
+ * KVC_ERR_INVALID_ARG: parent unknown, child exists, or parent == child. */
+kvc_status kvc_bm_fork(kvc_block_manager* bm, int64_t parent, int64_t child);
+
+/* Room for one more token at position p = the sequence's length, which then
+ * grows by one; *slot (required) receives the token's slot.  If p is a
+ * multiple of block_size, a free block is appended to the sequence.  Otherwise
+ * the token goes into the sequence's last block; if that block is shared
+ * (count > 1) a free block replaces it in this sequence first (the shared
+ * block loses one count), and *cow_src / *cow_dst receive the shared and the
+ * new block: the caller copies rows 0 .. p % block_size - 1 of block cow_src to
+ * block cow_dst in each cache before writing the token.  Otherwise both are -1
+ * (each may be NULL).  KVC_ERR_INVALID_ARG: unknown sequence, NULL slot, or a
+ * new block beyond max_blocks_per_seq.  KVC_ERR_OUT_OF_BLOCKS: no free block. */
+kvc_status kvc_bm_append(kvc_block_manager* bm, int64_t seq_id, int32_t* slot,
+                         int32_t* cow_src, int32_t* cow_dst);
+
+/* Ends sequence seq_id: each of its blocks loses one count, and a block whose
+ * count reaches 0 returns to the free list.  KVC_ERR_INVALID_ARG: unknown id. */
+kvc_status kvc_bm_free(kvc_block_manager* bm, int64_t seq_id);
+
+/* Row i of block_table (host int32 [n][max_blocks_per_seq]) receives the blocks
+ * of sequence seq_ids[i] in logical order, then `pad` in the unused entries;
+ * seq_lens (host int32 [n], may be NULL) receives the lengths.
+ * KVC_ERR_INVALID_ARG: an unknown id, n < 0, or a NULL array for n > 0
+ * (nothing is written). */
+kvc_status kvc_bm_tables(const kvc_block_manager* bm, const int64_t* seq_ids, int n,
+                         int32_t pad, int32_t* block_table, int32_t* seq_lens);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,8 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libkvc.so")
 
-KVC_OK, KVC_ERR_INVALID_ARG, KVC_ERR_UNSUPPORTED, KVC_ERR_CUDA, KVC_ERR_WORKSPACE = range(5)
+(KVC_OK, KVC_ERR_INVALID_ARG, KVC_ERR_UNSUPPORTED, KVC_ERR_CUDA, KVC_ERR_WORKSPACE,
+ KVC_ERR_OUT_OF_BLOCKS) = range(6)
 KVC_F16, KVC_BF16 = 0, 1
 FLAG_BLOCK_ID_RANGE, FLAG_SLOT_RANGE, FLAG_LEN_RANGE, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
 
@@ -42,6 +43,16 @@ _SIGS = {
                               _P, _S, _P, _P]),
     "kvc_paged_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                      _I, _F, _I, _I, _P, _S, _P, _P]),
+    "kvc_bm_create": (_I, [_I, _I, _I, _P]),
+    "kvc_bm_destroy": (None, [_P]),
+    "kvc_bm_num_free": (_I, [_P]),
+    "kvc_bm_ref_count": (_I, [_P, _I]),
+    "kvc_bm_seq_len": (_I, [_P, ctypes.c_int64]),
+    "kvc_bm_add": (_I, [_P, ctypes.c_int64, _I, _P]),
+    "kvc_bm_fork": (_I, [_P, ctypes.c_int64, ctypes.c_int64]),
+    "kvc_bm_append": (_I, [_P, ctypes.c_int64, _P, _P, _P]),
+    "kvc_bm_free": (_I, [_P, ctypes.c_int64]),
+    "kvc_bm_tables": (_I, [_P, _P, _I, ctypes.c_int32, _P, _P]),
 }
 
 
@@ -328,3 +339,67 @@ def paged_decode_no_alloc(q: torch.Tensor, key_cache: torch.Tensor, value_cache:
         seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, D, bs, block_table.shape[1], NB,
         float(scale), _DT[q.dtype], num_ctas, _flag(err_flag), _stream()))
     return out
+
+
+class BlockManager:
+    """The library's host block manager (``kvc_bm_*`` in ``include/kvc.h``): physical
+    blocks of the cache pool handed to sequences, reference-counted so that sequences
+    can share a prefix.  Host memory only; the tables it returns are the ``block_table``
+    / ``seq_lens`` arguments of the attention calls once copied to the device."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int):
+        h = ctypes.c_void_p()
+        _check("kvc_bm_create", lib().kvc_bm_create(num_blocks, block_size,
+                                                     max_blocks_per_seq, ctypes.byref(h)))
+        self._h = h
+        self.num_blocks, self.block_size = num_blocks, block_size
+        self.max_blocks_per_seq = max_blocks_per_seq
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value is not None and _lib is not None:
+            _lib.kvc_bm_destroy(h)
+            self._h = None
+
+    @property
+    def num_free(self) -> int:
+        return int(lib().kvc_bm_num_free(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return int(lib().kvc_bm_ref_count(self._h, block))
+
+    def seq_len(self, seq_id: int) -> int:
+        return int(lib().kvc_bm_seq_len(self._h, seq_id))
+
+    def add(self, seq_id: int, num_tokens: int) -> torch.Tensor:
+        """A new sequence of num_tokens tokens; returns their slots (int32, host)."""
+        slots = torch.empty(max(num_tokens, 0), dtype=torch.int32)
+        _check("kvc_bm_add", lib().kvc_bm_add(self._h, seq_id, num_tokens,
+                                               slots.data_ptr() if num_tokens > 0 else None))
+        return slots
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("kvc_bm_fork", lib().kvc_bm_fork(self._h, parent, child))
+
+    def append(self, seq_id: int):
+        """Room for one more token: (slot, cow_src, cow_dst), the last two -1 unless the
+        caller must first copy a shared block's rows into the sequence's new block."""
+        v = (ctypes.c_int32 * 3)()
+        _check("kvc_bm_append", lib().kvc_bm_append(
+            self._h, seq_id, ctypes.addressof(v), ctypes.addressof(v) + 4,
+            ctypes.addressof(v) + 8))
+        return int(v[0]), int(v[1]), int(v[2])
+
+    def free(self, seq_id: int) -> None:
+        _check("kvc_bm_free", lib().kvc_bm_free(self._h, seq_id))
+
+    def tables(self, seq_ids, pad: int = 0):
+        """(block_table int32 [n, max_blocks_per_seq], seq_lens int32 [n]), host tensors."""
+        ids = torch.tensor(list(seq_ids), dtype=torch.int64)
+        n = ids.numel()
+        table = torch.empty(n, self.max_blocks_per_seq, dtype=torch.int32)
+        lens = torch.empty(n, dtype=torch.int32)
+        _check("kvc_bm_tables", lib().kvc_bm_tables(
+            self._h, ids.data_ptr() if n else None, n, pad, table.data_ptr() if n else None,
+            lens.data_ptr() if n else None))
+        return table, lens

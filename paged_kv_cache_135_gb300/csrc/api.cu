@@ -85,6 +85,7 @@ const char* kvc_status_string(kvc_status s) {
     case KVC_ERR_UNSUPPORTED: return "KVC_ERR_UNSUPPORTED";
     case KVC_ERR_CUDA: return "KVC_ERR_CUDA";
     case KVC_ERR_WORKSPACE: return "KVC_ERR_WORKSPACE";
+    case KVC_ERR_OUT_OF_BLOCKS: return "KVC_ERR_OUT_OF_BLOCKS";
   }
   return "KVC_UNKNOWN_STATUS";
 }
