@@ -18,13 +18,16 @@ definitions on the source pages, with no blocking, fusion or reordering:
   blocks).
 * MLA -- KVCache skill Mode 3: key = value = cache_nope, plus a separate rope
   part for query and key.
+* Band attention -- KVCache skill Appendix C sparse_mode 4 (sliding window)
+  and ai6s.net article 3 (4) (keep the most recent N tokens).
 
 Readings where the pages are silent (each listed in the design doc):
   - q head h uses kv head h // (Hq / Hkv) (contiguous GQA groups);
   - causal attention includes the query's own position;
   - seq_lens counts cached tokens including the one written this step;
   - a sequence with no visible key returns exact zeros;
-  - a negative slot in slot_mapping means "do not write".
+  - a negative slot in slot_mapping means "do not write";
+  - a band of `window` positions ends at the query's own position.
 
 All floating-point work is float64.  Inputs given as fp16/bf16 values must be
 converted to float64 by the caller (the conversion is exact).
@@ -290,6 +293,70 @@ def varlen_prefill_paged(q, key, value, cu_seqlens, context_lens, slots, block_t
                 g = kv_head_of(h, Hq, Hkv)
                 out[cu[s] + i, h] = softmax_attention(q[cu[s] + i, h], K[:visible, g, :],
                                                       V[:visible, g, :], scale)
+    return out, kc, vc
+
+
+# ---------------------------------------------------------------------------
+# Band (sliding-window) attention (KVCache skill Appendix C, sparse_mode 4;
+# ai6s.net article 3 (4): keep only the most recent N tokens)
+# ---------------------------------------------------------------------------
+
+
+def window_start(pos: int, window: int) -> int:
+    """First key position visible from query position `pos` under a band of `window`.
+
+    The skill's sparse_mode 4 names a band for sliding-window models and the
+    article keeps the most recent N tokens; neither fixes the edges.  Reading:
+    the band ends at the query's own position and holds `window` positions,
+    pos - window + 1 .. pos.
+    """
+    if window < 1:
+        raise ValueError("window must be >= 1")
+    return max(0, pos - window + 1)
+
+
+def windowed_paged_decode(q, key_cache, value_cache, block_table, seq_lens, scale: float,
+                          window: int):
+    """paged_decode restricted to each sequence's last `window` cached tokens."""
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, _ = q.shape
+    Hkv = key_cache.shape[2]
+    out = np.zeros((B, Hq, value_cache.shape[3]), dtype=np.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        lo = window_start(L - 1, window)
+        K = gather_sequence(key_cache, block_table[b], L).astype(np.float64)
+        V = gather_sequence(value_cache, block_table[b], L).astype(np.float64)
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            out[b, h] = softmax_attention(q[b, h], K[lo:, g, :], V[lo:, g, :], scale)
+    return out
+
+
+def windowed_varlen_prefill_paged(q, key, value, cu_seqlens, context_lens, slots, block_table,
+                                  key_cache, value_cache, scale: float, window: int):
+    """varlen_prefill_paged with each query seeing only the band of `window` positions
+    ending at its own (causal inside the band)."""
+    kc, vc = reshape_and_cache(key, value, key_cache, value_cache, slots)
+    q = np.asarray(q, dtype=np.float64)
+    T, Hq, _ = q.shape
+    Hkv = kc.shape[2]
+    out = np.zeros((T, Hq, vc.shape[3]), dtype=np.float64)
+    cu = [int(x) for x in cu_seqlens]
+    for s in range(len(cu) - 1):
+        ctx = 0 if context_lens is None else int(context_lens[s])
+        n = cu[s + 1] - cu[s]
+        K = gather_sequence(kc, block_table[s], ctx + n).astype(np.float64)
+        V = gather_sequence(vc, block_table[s], ctx + n).astype(np.float64)
+        for i in range(n):
+            pos = ctx + i
+            lo = window_start(pos, window)
+            for h in range(Hq):
+                g = kv_head_of(h, Hq, Hkv)
+                out[cu[s] + i, h] = softmax_attention(q[cu[s] + i, h], K[lo:pos + 1, g, :],
+                                                      V[lo:pos + 1, g, :], scale)
     return out, kc, vc
 
 
