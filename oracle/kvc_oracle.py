@@ -20,6 +20,8 @@ definitions on the source pages, with no blocking, fusion or reordering:
   part for query and key.
 * Band attention -- KVCache skill Appendix C sparse_mode 4 (sliding window)
   and ai6s.net article 3 (4) (keep the most recent N tokens).
+* INT8 KV cache -- KVCache skill 4 (quantized KV: antiquant / dequant scales)
+  and its INT8 KVCache Quantization note; ai6s.net article 3 (FP16 -> INT8).
 
 Readings where the pages are silent (each listed in the design doc):
   - q head h uses kv head h // (Hq / Hkv) (contiguous GQA groups);
@@ -27,7 +29,9 @@ Readings where the pages are silent (each listed in the design doc):
   - seq_lens counts cached tokens including the one written this step;
   - a sequence with no visible key returns exact zeros;
   - a negative slot in slot_mapping means "do not write";
-  - a band of `window` positions ends at the query's own position.
+  - a band of `window` positions ends at the query's own position;
+  - an INT8 cache row carries one fp32 scale per (token, kv head), its codes
+    decided in fp32 (quantize_rows_int8).
 
 All floating-point work is float64.  Inputs given as fp16/bf16 values must be
 converted to float64 by the caller (the conversion is exact).
@@ -358,6 +362,65 @@ def windowed_varlen_prefill_paged(q, key, value, cu_seqlens, context_lens, slots
                 out[cu[s] + i, h] = softmax_attention(q[cu[s] + i, h], K[lo:pos + 1, g, :],
                                                       V[lo:pos + 1, g, :], scale)
     return out, kc, vc
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV cache (KVCache skill 4 "Quantized KV" antiquant_scale /
+# dequant_scale_key/value and "KVCache Quantization: INT8"; ai6s.net article
+# 3 (FP16 -> INT8 halves the bytes per element))
+# ---------------------------------------------------------------------------
+
+
+def quantize_rows_int8(x):
+    """Symmetric INT8 codes of each row (last axis) of x, one fp32 scale per row.
+
+    The pages name INT8 KV caches and their dequantisation scales but no
+    scheme.  Reading: one scale per written row (token, kv head), so a decode
+    write never re-quantises earlier tokens.  The code is an integer decided
+    by floating point, so it is fixed in fp32, the precision a kernel uses:
+    amax = max|x|; inv = 127 / amax and scale = amax / 127 (fp32 divisions,
+    round to nearest); code = x * inv (fp32 product) rounded half to even and
+    clamped to [-127, 127].  A row of zeros has scale 0 and codes 0.
+    Returns (codes int8, scales float32 [...]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1)
+    safe = np.where(amax > 0, amax, np.float32(1))
+    inv = np.where(amax > 0, np.float32(127) / safe, np.float32(0)).astype(np.float32)
+    scale = (amax / np.float32(127)).astype(np.float32)
+    prod = (x * inv[..., None]).astype(np.float32)
+    codes = np.clip(np.rint(prod), -127, 127).astype(np.int8)
+    return codes, scale
+
+
+def dequantize_rows_int8(codes, scales):
+    """code * scale per element, float64."""
+    return np.asarray(codes, dtype=np.float64) * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+def reshape_and_cache_int8(key, value, key_codes, value_codes, key_scales, value_scales, slots):
+    """The cache write of an INT8 cache: each new row is quantised (quantize_rows_int8)
+    and its codes and scale are copied to the slot.  Caches [num_blocks, block_size,
+    Hkv, D] int8 and scales [num_blocks, block_size, Hkv] float32; returns new copies."""
+    kq, ks = quantize_rows_int8(key)
+    vq, vs = quantize_rows_int8(value)
+    kc, vc = np.array(key_codes, copy=True), np.array(value_codes, copy=True)
+    ksc, vsc = np.array(key_scales, copy=True), np.array(value_scales, copy=True)
+    bs = kc.shape[1]
+    for t, slot in enumerate(np.asarray(slots).tolist()):
+        if slot < 0:
+            continue
+        kc[slot // bs, slot % bs], ksc[slot // bs, slot % bs] = kq[t], ks[t]
+        vc[slot // bs, slot % bs], vsc[slot // bs, slot % bs] = vq[t], vs[t]
+    return kc, vc, ksc, vsc
+
+
+def paged_decode_int8(q, key_codes, value_codes, key_scales, value_scales, block_table,
+                      seq_lens, scale: float):
+    """paged_decode over an INT8 cache: the cached rows are dequantised, then attended."""
+    return paged_decode(q, dequantize_rows_int8(key_codes, key_scales),
+                        dequantize_rows_int8(value_codes, value_scales), block_table, seq_lens,
+                        scale)
 
 
 def mla_paged_decode(q_nope, q_rope, cache_nope, cache_rope, block_table, seq_lens,
