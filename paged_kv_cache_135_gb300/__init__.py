@@ -3,8 +3,9 @@
 Argument marshalling only: every step of the hot path runs in the CUDA
 kernels behind the C ABI declared in ``include/kvc.h``.  Tensors must be
 contiguous CUDA tensors; work is enqueued on torch's current CUDA stream.
-There is no CPU fallback: if ``_build/libkvc.so`` is missing, every call
-raises.
+The one host-side object, ``BlockManager`` (the library's block allocator,
+``kvc_bm_*``), works in host memory and returns host tensors.  There is no
+CPU fallback: if ``_build/libkvc.so`` is missing, every call raises.
 """
 
 from __future__ import annotations
