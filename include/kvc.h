@@ -396,6 +396,21 @@ kvc_status kvc_bm_free(kvc_block_manager* bm, int64_t seq_id);
 kvc_status kvc_bm_tables(const kvc_block_manager* bm, const int64_t* seq_ids, int n,
                          int32_t pad, int32_t* block_table, int32_t* seq_lens);
 
+/* One decode step of a serving loop in one call: for each of the n distinct
+ * sequences seq_ids[i], the effect of kvc_bm_append (slots[i], cow_src[i],
+ * cow_dst[i] receive its results; all three arrays are host int32 [n] and
+ * required), then, if block_table is not NULL, the effect of kvc_bm_tables
+ * on the same ids (block_table [n][max_blocks_per_seq], seq_lens [n] may be
+ * NULL; without block_table, seq_lens alone may still be filled).  The step
+ * happens for every sequence or for none: KVC_ERR_INVALID_ARG for an unknown
+ * or repeated id or a table that would overflow, KVC_ERR_OUT_OF_BLOCKS if the
+ * new blocks and copies need more free blocks than there are (counting that a
+ * shared block stops needing a copy once its other holders have moved away in
+ * the same step). */
+kvc_status kvc_bm_step(kvc_block_manager* bm, const int64_t* seq_ids, int n, int32_t pad,
+                       int32_t* slots, int32_t* cow_src, int32_t* cow_dst,
+                       int32_t* block_table, int32_t* seq_lens);
+
 #ifdef __cplusplus
 }
 #endif

@@ -54,6 +54,7 @@ _SIGS = {
     "kvc_bm_append": (_I, [_P, ctypes.c_int64, _P, _P, _P]),
     "kvc_bm_free": (_I, [_P, ctypes.c_int64]),
     "kvc_bm_tables": (_I, [_P, _P, _I, ctypes.c_int32, _P, _P]),
+    "kvc_bm_step": (_I, [_P, _P, _I, ctypes.c_int32, _P, _P, _P, _P, _P]),
 }
 
 
@@ -404,3 +405,47 @@ class BlockManager:
             self._h, ids.data_ptr() if n else None, n, pad, table.data_ptr() if n else None,
             lens.data_ptr() if n else None))
         return table, lens
+
+    def step_buffer(self, n: int, pin_memory: bool = False) -> "StepBuffer":
+        """Reusable host int32 outputs of step() for n sequences."""
+        return StepBuffer(n, self.max_blocks_per_seq, pin_memory)
+
+    def step(self, seq_ids, pad: int = 0, out: Optional["StepBuffer"] = None,
+             pin_memory: bool = False):
+        """One decode step for the given sequences in one native call: each gets room
+        for one more token.  Returns (slots, cow_src, cow_dst, block_table, seq_lens),
+        host int32 tensors: the views of `out` (a step_buffer(n), reusable between
+        steps; a new one, page-locked if pin_memory, when it is None).  All or nothing.
+        seq_ids may be a host int64 tensor, which is then used as it is."""
+        if isinstance(seq_ids, torch.Tensor):
+            if seq_ids.dtype != torch.int64 or seq_ids.is_cuda or not seq_ids.is_contiguous():
+                raise ValueError("seq_ids must be a contiguous host int64 tensor")
+            ids = seq_ids
+        else:
+            ids = torch.tensor(list(seq_ids), dtype=torch.int64)
+        n = ids.numel()
+        if out is None:
+            out = StepBuffer(n, self.max_blocks_per_seq, pin_memory)
+        elif out.n != n or out.max_blocks != self.max_blocks_per_seq:
+            raise ValueError("out was made for another number of sequences or table width")
+        if n:
+            p = out.ptrs
+            _check("kvc_bm_step", lib().kvc_bm_step(self._h, ids.data_ptr(), n, pad, p[0], p[1],
+                                                     p[2], p[3], p[4]))
+        return out.views
+
+
+class StepBuffer:
+    """Host int32 outputs of BlockManager.step for n sequences in one allocation (page-
+    locked if pin_memory, so the block table and lengths can be copied to the device
+    without blocking): `views` = (slots [n], cow_src [n], cow_dst [n], block_table
+    [n, max_blocks], seq_lens [n])."""
+
+    def __init__(self, n: int, max_blocks: int, pin_memory: bool = False):
+        self.n, self.max_blocks = n, max_blocks
+        self.data = torch.empty(n * (4 + max_blocks), dtype=torch.int32, pin_memory=pin_memory)
+        d, m = self.data, max_blocks
+        self.views = (d[:n], d[n:2 * n], d[2 * n:3 * n], d[3 * n:3 * n + n * m].view(n, m),
+                      d[3 * n + n * m:4 * n + n * m])
+        base = d.data_ptr()
+        self.ptrs = (base, base + 4 * n, base + 8 * n, base + 12 * n, base + 12 * n + 4 * n * m)

@@ -17,6 +17,7 @@
 // nothing.
 #include <stdint.h>
 
+#include <algorithm>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -27,11 +28,18 @@ struct kvc_block_manager {
   struct Seq {
     std::vector<int32_t> blocks;  // physical blocks in logical order
     int len = 0;                  // tokens with a slot
+    uint64_t mark = 0;            // the step that last listed it
   };
   int num_blocks = 0, block_size = 0, max_blocks = 0;
   std::vector<int32_t> free_list;
   std::vector<int> ref;
-  std::unordered_map<int64_t, Seq> seqs;
+  std::unordered_map<int64_t, Seq> seqs;  // node-based: a Seq never moves
+  // Scratch of kvc_bm_step, kept between calls so a step allocates nothing:
+  // the step's sequences, and per block the holders not yet moved away.
+  uint64_t epoch = 0;
+  std::vector<Seq*> step_seqs;
+  std::vector<int> left;
+  std::vector<uint64_t> left_mark;
 
   int32_t take() {
     const int32_t b = free_list.back();
@@ -44,6 +52,11 @@ struct kvc_block_manager {
   }
   int32_t slot(const Seq& s, int pos) const {
     return s.blocks[pos / block_size] * block_size + pos % block_size;
+  }
+  void table_row(const Seq& s, int32_t pad, int32_t* row) const {
+    const size_t nb = s.blocks.size();
+    std::copy(s.blocks.begin(), s.blocks.end(), row);
+    std::fill(row + nb, row + max_blocks, pad);
   }
 };
 
@@ -70,6 +83,8 @@ kvc_status kvc_bm_create(int num_blocks, int block_size, int max_blocks_per_seq,
     bm->free_list.resize(num_blocks);
     for (int i = 0; i < num_blocks; ++i) bm->free_list[i] = i;  // popped from the end
     bm->ref.assign(num_blocks, 0);
+    bm->left.assign(num_blocks, 0);
+    bm->left_mark.assign(num_blocks, 0);
   } catch (...) {
     delete bm;
     return KVC_ERR_INVALID_ARG;
@@ -176,10 +191,72 @@ kvc_status kvc_bm_tables(const kvc_block_manager* bm, const int64_t* seq_ids, in
     if (!bm->seqs.count(seq_ids[i])) return KVC_ERR_INVALID_ARG;
   for (int i = 0; i < n; ++i) {
     const kvc_block_manager::Seq& s = bm->seqs.find(seq_ids[i])->second;
-    int32_t* row = block_table + static_cast<long long>(i) * bm->max_blocks;
-    const int nb = static_cast<int>(s.blocks.size());
-    for (int j = 0; j < bm->max_blocks; ++j) row[j] = j < nb ? s.blocks[j] : pad;
+    bm->table_row(s, pad, block_table + static_cast<long long>(i) * bm->max_blocks);
     if (seq_lens) seq_lens[i] = s.len;
+  }
+  return KVC_OK;
+}
+
+kvc_status kvc_bm_step(kvc_block_manager* bm, const int64_t* seq_ids, int n, int32_t pad,
+                       int32_t* slots, int32_t* cow_src, int32_t* cow_dst, int32_t* block_table,
+                       int32_t* seq_lens) {
+  if (bm == nullptr || n < 0) return KVC_ERR_INVALID_ARG;
+  if (n == 0) return KVC_OK;
+  if (seq_ids == nullptr || slots == nullptr || cow_src == nullptr || cow_dst == nullptr)
+    return KVC_ERR_INVALID_ARG;
+  // Check first, so that the step either happens for every sequence or for
+  // none: ids known and distinct, room in every table, and enough free blocks
+  // for the new blocks and the copies.  A shared partly filled block costs a
+  // copy for each appending holder while another holder remains, so each such
+  // block's remaining holders are counted (scratch stamped with this step).
+  try {
+    if (static_cast<int>(bm->step_seqs.size()) < n) bm->step_seqs.resize(n);
+  } catch (...) {
+    return KVC_ERR_INVALID_ARG;  // host memory exhausted; nothing changed
+  }
+  const uint64_t ep = ++bm->epoch;
+  kvc_block_manager::Seq** seq = bm->step_seqs.data();
+  int need = 0;
+  for (int i = 0; i < n; ++i) {
+    const auto it = bm->seqs.find(seq_ids[i]);
+    if (it == bm->seqs.end() || it->second.mark == ep) return KVC_ERR_INVALID_ARG;
+    it->second.mark = ep;
+    seq[i] = &it->second;
+    const int p = seq[i]->len;
+    if (p % bm->block_size == 0) {
+      if (static_cast<int>(seq[i]->blocks.size()) >= bm->max_blocks) return KVC_ERR_INVALID_ARG;
+      ++need;
+    } else {
+      const int32_t blk = seq[i]->blocks.back();
+      if (bm->left_mark[blk] != ep) {
+        bm->left_mark[blk] = ep;
+        bm->left[blk] = bm->ref[blk];
+      }
+      if (bm->left[blk] > 1) {
+        ++need;
+        --bm->left[blk];
+      }
+    }
+  }
+  if (need > static_cast<int>(bm->free_list.size())) return KVC_ERR_OUT_OF_BLOCKS;
+  for (int i = 0; i < n; ++i) {
+    kvc_block_manager::Seq& sq = *seq[i];
+    const int p = sq.len;
+    int32_t src = -1, dst = -1;
+    if (p % bm->block_size == 0) {
+      sq.blocks.push_back(bm->take());  // capacity reserved when the sequence was made
+    } else if (bm->ref[sq.blocks.back()] > 1) {
+      src = sq.blocks.back();
+      dst = bm->take();
+      bm->release(src);
+      sq.blocks.back() = dst;
+    }
+    sq.len = p + 1;
+    slots[i] = bm->slot(sq, p);
+    cow_src[i] = src;
+    cow_dst[i] = dst;
+    if (block_table) bm->table_row(sq, pad, block_table + static_cast<long long>(i) * bm->max_blocks);
+    if (seq_lens) seq_lens[i] = sq.len;
   }
   return KVC_OK;
 }

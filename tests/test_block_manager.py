@@ -13,6 +13,7 @@ its block table equals its contiguous history, and so does its attention.
 
 import numpy as np
 import pytest
+import torch
 
 import paged_kv_cache_135_gb300 as kvc
 from oracle import kvc_oracle as O
@@ -247,3 +248,89 @@ def test_multi_step_lifecycle_double_track():
         lin = O.contiguous_decode(q, k_lin, v_lin, lens, 0.3)
         assert np.allclose(paged, lin, rtol=0, atol=1e-12)
     assert next_id > 5 and n_cow > 0 and n_freed > 0 and n_reused > 0, (n_cow, n_freed, n_reused)
+
+
+def _history(bm, ops):
+    for op in ops:
+        getattr(bm, op[0])(*op[1:])
+
+
+def test_step_equals_single_appends():
+    rng = np.random.default_rng(21)
+    for trial in range(20):
+        ops, ids = [], []
+        for sid in range(int(rng.integers(1, 6))):
+            ops.append(("add", sid, int(rng.integers(0, 12))))
+            ids.append(sid)
+        for child in range(10, 10 + int(rng.integers(0, 4))):
+            ops.append(("fork", ids[int(rng.integers(len(ids)))], child))
+            ids.append(child)
+        a, b = kvc.BlockManager(40, 4, 8), kvc.BlockManager(40, 4, 8)
+        _history(a, ops)
+        _history(b, ops)
+        step_ids = [i for i in ids if rng.random() < 0.8]
+        rng.shuffle(step_ids)
+        slots, cs, cd, table, lens = a.step(step_ids, pad=-1)
+        for i, sid in enumerate(step_ids):
+            assert b.append(sid) == (int(slots[i]), int(cs[i]), int(cd[i]))
+        t2, l2 = b.tables(step_ids, pad=-1)
+        assert np.array_equal(table.numpy(), t2.numpy()) and np.array_equal(lens.numpy(), l2.numpy())
+        assert [a.ref_count(k) for k in range(40)] == [b.ref_count(k) for k in range(40)]
+        assert a.num_free == b.num_free
+        check_invariants(a, ids)
+
+
+def test_step_is_all_or_nothing():
+    bm = kvc.BlockManager(6, 4, 3)
+    bm.add(0, 4)                                # position 4 opens a block
+    bm.add(1, 6)
+    bm.fork(1, 2)                               # a shared partly filled block
+    before = ([bm.ref_count(k) for k in range(6)], bm.num_free,
+              [table_of(bm, s) for s in (0, 1, 2)], [bm.seq_len(s) for s in (0, 1, 2)])
+
+    def unchanged():
+        return before == ([bm.ref_count(k) for k in range(6)], bm.num_free,
+                          [table_of(bm, s) for s in (0, 1, 2)], [bm.seq_len(s) for s in (0, 1, 2)])
+
+    for ids, status in (([0, 9], kvc.KVC_ERR_INVALID_ARG), ([1, 1], kvc.KVC_ERR_INVALID_ARG)):
+        with pytest.raises(kvc.KvcError) as e:
+            bm.step(ids)
+        assert e.value.status == status and unchanged()
+    # 3 free blocks; sequences 0, 1 and 2 need 1 + 1 (copy) + 0 (2 then holds it alone).
+    bm.add(3, 4)                                # leaves 2 free blocks
+    bm.step([0, 1, 2])
+    assert bm.num_free == 0 and [bm.seq_len(s) for s in (0, 1, 2)] == [5, 7, 7]
+    with pytest.raises(kvc.KvcError) as e:
+        bm.step([3])                            # position 4 of sequence 3 needs a block
+    assert e.value.status == kvc.KVC_ERR_OUT_OF_BLOCKS and bm.seq_len(3) == 4
+    check_invariants(bm, [0, 1, 2, 3])
+
+
+def test_step_copies_a_shared_block_once():
+    bm = kvc.BlockManager(16, 4, 4)
+    bm.add(0, 6)
+    bm.fork(0, 1)
+    bm.fork(0, 2)                               # block 14 held three times
+    slots, cs, cd, table, lens = bm.step([0, 1, 2], pad=-1)
+    assert cs.tolist() == [14, 14, -1]          # the last holder keeps the block
+    assert cd[0] >= 0 and cd[1] >= 0 and cd[0] != cd[1]
+    assert table[2, 1] == 14 and bm.ref_count(14) == 1 and lens.tolist() == [7, 7, 7]
+    check_invariants(bm, [0, 1, 2])
+
+
+def test_step_buffer_reuse():
+    a, b = kvc.BlockManager(64, 4, 16), kvc.BlockManager(64, 4, 16)
+    for bm in (a, b):
+        bm.add(0, 3)
+        bm.add(1, 9)
+        bm.fork(1, 2)
+    ids = torch.tensor([2, 0, 1], dtype=torch.int64)
+    buf = a.step_buffer(3)
+    for _ in range(10):
+        got = [t.clone() for t in a.step(ids, pad=-1, out=buf)]
+        want = b.step([2, 0, 1], pad=-1)
+        assert all(torch.equal(g, w) for g, w in zip(got, want))
+    with pytest.raises(ValueError):
+        a.step([0, 1], out=buf)                 # made for 3 sequences
+    with pytest.raises(ValueError):
+        a.step(torch.tensor([0, 1, 2], dtype=torch.int32))
