@@ -23,7 +23,7 @@ definitions on the source pages, with no blocking, fusion or reordering:
 * INT8 KV cache -- KVCache skill 4 (quantized KV: antiquant / dequant scales)
   and its INT8 KVCache Quantization note; ai6s.net article 3 (FP16 -> INT8).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   - q head h uses kv head h // (Hq / Hkv) (contiguous GQA groups);
   - causal attention includes the query's own position;
   - seq_lens counts cached tokens including the one written this step;
