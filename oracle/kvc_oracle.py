@@ -400,8 +400,10 @@ def dequantize_rows_int8(codes, scales):
 
 def reshape_and_cache_int8(key, value, key_codes, value_codes, key_scales, value_scales, slots):
     """The cache write of an INT8 cache: each new row is quantised (quantize_rows_int8)
-    and its codes and scale are copied to the slot.  Caches [num_blocks, block_size,
-    Hkv, D] int8 and scales [num_blocks, block_size, Hkv] float32; returns new copies."""
+    and its codes and scale are copied to the slot.  Codes [num_blocks, block_size, Hkv,
+    D] int8 (the layout of the 16-bit cache); scales [num_blocks, Hkv, block_size]
+    float32, head-major inside a block so that one head's scales of consecutive tokens
+    are contiguous.  Returns new copies."""
     kq, ks = quantize_rows_int8(key)
     vq, vs = quantize_rows_int8(value)
     kc, vc = np.array(key_codes, copy=True), np.array(value_codes, copy=True)
@@ -410,17 +412,19 @@ def reshape_and_cache_int8(key, value, key_codes, value_codes, key_scales, value
     for t, slot in enumerate(np.asarray(slots).tolist()):
         if slot < 0:
             continue
-        kc[slot // bs, slot % bs], ksc[slot // bs, slot % bs] = kq[t], ks[t]
-        vc[slot // bs, slot % bs], vsc[slot // bs, slot % bs] = vq[t], vs[t]
+        kc[slot // bs, slot % bs], ksc[slot // bs, :, slot % bs] = kq[t], ks[t]
+        vc[slot // bs, slot % bs], vsc[slot // bs, :, slot % bs] = vq[t], vs[t]
     return kc, vc, ksc, vsc
 
 
 def paged_decode_int8(q, key_codes, value_codes, key_scales, value_scales, block_table,
                       seq_lens, scale: float):
-    """paged_decode over an INT8 cache: the cached rows are dequantised, then attended."""
-    return paged_decode(q, dequantize_rows_int8(key_codes, key_scales),
-                        dequantize_rows_int8(value_codes, value_scales), block_table, seq_lens,
-                        scale)
+    """paged_decode over an INT8 cache (scales [num_blocks, Hkv, block_size]): the
+    cached rows are dequantised, then attended."""
+    ks = np.swapaxes(np.asarray(key_scales), 1, 2)
+    vs = np.swapaxes(np.asarray(value_scales), 1, 2)
+    return paged_decode(q, dequantize_rows_int8(key_codes, ks),
+                        dequantize_rows_int8(value_codes, vs), block_table, seq_lens, scale)
 
 
 def mla_paged_decode(q_nope, q_rope, cache_nope, cache_rope, block_table, seq_lens,

@@ -108,7 +108,7 @@ def test_int8_cache_write():
     val = rng.standard_normal((5, Hkv, D)).astype(np.float32)
     slots = np.array([3, 17, -1, 8, 22])
     kc = np.zeros((NB, bs, Hkv, D), np.int8)
-    ks = np.full((NB, bs, Hkv), -1.0, np.float32)
+    ks = np.full((NB, Hkv, bs), -1.0, np.float32)
     kc2, vc2, ks2, vs2 = O.reshape_and_cache_int8(key, val, kc, kc.copy(), ks, ks.copy(), slots)
     kq, kscale = O.quantize_rows_int8(key)
     vq, vscale = O.quantize_rows_int8(val)
@@ -119,18 +119,19 @@ def test_int8_cache_write():
         written.add(sl)
         assert np.array_equal(kc2[sl // bs, sl % bs], kq[t])
         assert np.array_equal(vc2[sl // bs, sl % bs], vq[t])
-        assert np.array_equal(ks2[sl // bs, sl % bs], kscale[t])
-        assert np.array_equal(vs2[sl // bs, sl % bs], vscale[t])
+        assert np.array_equal(ks2[sl // bs, :, sl % bs], kscale[t])
+        assert np.array_equal(vs2[sl // bs, :, sl % bs], vscale[t])
     for sl in range(NB * bs):
         if sl not in written:
-            assert (kc2[sl // bs, sl % bs] == 0).all() and (ks2[sl // bs, sl % bs] == -1).all()
+            assert (kc2[sl // bs, sl % bs] == 0).all() and (ks2[sl // bs, :, sl % bs] == -1).all()
 
 
 def test_int8_decode_is_close_to_fp64_and_a_dropped_scale_is_not(monkeypatch):
     c = decode_case(4, 3, [40, 7, 100], 8, 2, 64, 16, dtype="bf16")
     kf, vf = c.key_cache.double().numpy(), c.value_cache.double().numpy()
-    kq, ks = O.quantize_rows_int8(kf)
+    kq, ks = O.quantize_rows_int8(kf)           # scales [NB, bs, Hkv] ...
     vq, vs = O.quantize_rows_int8(vf)
+    ks, vs = np.swapaxes(ks, 1, 2), np.swapaxes(vs, 1, 2)   # ... stored [NB, Hkv, bs]
     q, bt, sl = c.q.double().numpy(), c.block_table.numpy(), c.seq_lens.numpy()
     ref = O.paged_decode(q, kf, vf, bt, sl, c.scale)
     got = O.paged_decode_int8(q, kq, vq, ks, vs, bt, sl, c.scale)
