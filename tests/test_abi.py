@@ -102,3 +102,23 @@ def test_workspace_query_rejects_bad_shapes(lib):
     # explicit CTA count: no device query needed
     # 10 CTAs: counters (padded to 256 B) + 2 shares x 4 rows x (128 + 2) floats each
     assert lib.kvc_paged_decode_workspace_size(8, 2, 128, 10) == 256 + 10 * 2 * 4 * 130 * 4
+
+
+def test_block_manager_calls_reject_a_null_handle(lib):
+    inv = 1  # KVC_ERR_INVALID_ARG
+    buf = (ctypes.c_int32 * 8)()
+    ids = (ctypes.c_int64 * 2)(0, 1)
+    p = ctypes.addressof(buf)
+    assert lib.kvc_bm_create(0, 16, 4, ctypes.byref(ctypes.c_void_p())) == inv
+    assert lib.kvc_bm_create(4, 16, 4, None) == inv
+    lib.kvc_bm_destroy(None)                      # no-op
+    assert lib.kvc_bm_num_free(None) == -1
+    assert lib.kvc_bm_ref_count(None, 0) == -1
+    assert lib.kvc_bm_seq_len(None, 0) == -1
+    assert lib.kvc_bm_add(None, 0, 4, None) == inv
+    assert lib.kvc_bm_fork(None, 0, 1) == inv
+    assert lib.kvc_bm_append(None, 0, p, None, None) == inv
+    assert lib.kvc_bm_free(None, 0) == inv
+    assert lib.kvc_bm_tables(None, ctypes.addressof(ids), 2, 0, p, None) == inv
+    assert lib.kvc_bm_step(None, ctypes.addressof(ids), 2, 0, p, p, p, None, None) == inv
+    assert lib.kvc_status_string(5) == b"KVC_ERR_OUT_OF_BLOCKS"
