@@ -103,7 +103,8 @@ def kernel_source_digest():
 def recorded_traffic(profile_md, digest):
     """DRAM bytes per launch from a committed ncu summary, if it matches the source."""
     try:
-        text = open(os.path.join(ROOT, "profiles", profile_md)).read()
+        with open(os.path.join(ROOT, "profiles", profile_md)) as f:
+            text = f.read()
     except OSError:
         return None
     m_d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)

@@ -7,6 +7,7 @@ any CUDA call, so they run without a GPU.
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -22,7 +23,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    with open(os.path.join(ROOT, "include", "kvc.h")) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(kvc_[a-z0-9_]+)\s*\(", text)))
 
@@ -39,7 +41,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_exported_symbols_are_c_linkage():
-    out = os.popen(f"nm -D --defined-only {kvc.LIB_PATH}").read()
+    out = subprocess.run(["nm", "-D", "--defined-only", kvc.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
     exported = set(re.findall(r" T (kvc_[a-z0-9_]+)$", out, flags=re.M))
     assert set(declared_functions()) <= exported
 
