@@ -137,6 +137,32 @@ kvc_status kvc_reshape_and_cache(const void* key, const void* value, void* key_c
                                  uint32_t* err_flag, kvc_stream_t stream);
 
 /*
+ * kvc_copy_blocks -- the copy-on-write copies of the host block manager.
+ * [NOTES] 5.2 (sequences that share a prefix share its blocks, counted by
+ * reference); a sequence about to write into a shared, partly filled block
+ * first gets a private copy of it (kvc_bm_append / kvc_bm_step report the
+ * pair: this library's reading, the notes are silent on it).
+ *
+ *   for each i < num_pairs with src_blocks[i] >= 0:
+ *     key_cache block dst_blocks[i]   <- key_cache block src_blocks[i]
+ *     value_cache block dst_blocks[i] <- value_cache block src_blocks[i]
+ *
+ * Whole blocks are copied bit for bit (rows past the shared prefix are
+ * rewritten before any read).  src_blocks, dst_blocks: device int32
+ * [num_pairs] -- the cow_src / cow_dst arrays of kvc_bm_step, -1 meaning "no
+ * copy".  block_bytes_k / block_bytes_v: bytes of one block of each cache
+ * (block_size * num_kv_heads * head_dim * element size), multiples of 16;
+ * value_cache may be NULL.  Any cache whose blocks are contiguous works (16-bit
+ * caches, INT8 codes, scale arrays).  A block id outside [0, num_blocks) skips
+ * the pair and sets KVC_FLAG_BLOCK_ID_RANGE.  The pairs of one call must not
+ * overlap (no block both a source and a destination).
+ */
+kvc_status kvc_copy_blocks(void* key_cache, void* value_cache, const int32_t* src_blocks,
+                           const int32_t* dst_blocks, int num_pairs, long long block_bytes_k,
+                           long long block_bytes_v, int num_blocks, uint32_t* err_flag,
+                           kvc_stream_t stream);
+
+/*
  * Bytes of workspace kvc_paged_decode needs for this head shape when it runs
  * with `num_ctas` persistent CTAs (0 = the automatic choice for the current
  * device: SM count x resident CTAs per SM).  Independent of batch and lengths.
@@ -180,9 +206,9 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
                             size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream);
 
 /*
- * kvc_paged_decode_append -- one decode step in one launch: rows a1 (slot
- * mapping), a2 (cache write of the new token) and a3/a4 (paged decode with
- * split-KV) fused.  Identical in effect to kvc_build_slot_mapping (start_pos =
+ * kvc_paged_decode_append -- one decode step in one launch: the slot mapping,
+ * the cache write of the new token and the paged decode with split-KV,
+ * fused.  Identical in effect to kvc_build_slot_mapping (start_pos =
  * seq_lens - 1) + kvc_reshape_and_cache + kvc_paged_decode for every sequence
  * with seq_lens[b] >= 1: the pages describe the cache write before the
  * attention that reads it ([SKILL] 3.6, [ATB] 4.2).  Not a separate operation
@@ -310,6 +336,10 @@ kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const vo
  * uses (the array keeps the previous call's contents), then runs the decode.
  * All calls on a device share the one array: calls that overlap on the GPU
  * (for example on two streams) race, so the caller must serialise them.
+ * Every argument is checked before the clear, so a rejected call enqueues
+ * nothing.  The looked-up address belongs to the device's primary context:
+ * after cudaDeviceReset on a device this entry point has run on, it must not
+ * be called there again in the same process.
  */
 #define KVC_NO_ALLOC_SCRATCH_BYTES (8u << 20)
 kvc_status kvc_paged_decode_no_alloc(const void* q, const void* key_cache,

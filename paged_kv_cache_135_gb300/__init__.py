@@ -34,6 +34,8 @@ _SIGS = {
     "kvc_version": (_I, []),
     "kvc_build_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "kvc_copy_blocks": (_I, [_P, _P, _P, _P, _I, ctypes.c_longlong, ctypes.c_longlong, _I, _P,
+                             _P]),
     "kvc_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
     "kvc_mla_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
     "kvc_mla_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
@@ -158,6 +160,28 @@ def reshape_and_cache(key: torch.Tensor, value: Optional[torch.Tensor], key_cach
         key.data_ptr(), _ptr(value), key_cache.data_ptr(), _ptr(value_cache),
         slot_mapping.data_ptr(), key.shape[0], H, dk, dv, bs, NB, _DT[key.dtype],
         _flag(err_flag), _stream()))
+
+
+def copy_blocks(key_cache: torch.Tensor, value_cache: Optional[torch.Tensor],
+                src_blocks: torch.Tensor, dst_blocks: torch.Tensor,
+                err_flag: Optional[torch.Tensor] = None) -> None:
+    """Copy-on-write: block src_blocks[i] -> block dst_blocks[i] in each cache (pairs with
+    src < 0 are skipped); src/dst are the cow_src / cow_dst of BlockManager.step, on the
+    device."""
+    _cuda("key_cache", key_cache)
+    _cuda("src_blocks", src_blocks, torch.int32)
+    _cuda("dst_blocks", dst_blocks, torch.int32)
+    nb = key_cache.shape[0]
+    bk = key_cache.numel() // nb * key_cache.element_size()
+    bv = 0
+    if value_cache is not None:
+        _cuda("value_cache", value_cache)
+        if value_cache.shape[0] != nb:
+            raise ValueError("key_cache and value_cache must have the same number of blocks")
+        bv = value_cache.numel() // nb * value_cache.element_size()
+    _check("kvc_copy_blocks", lib().kvc_copy_blocks(
+        key_cache.data_ptr(), _ptr(value_cache), src_blocks.data_ptr(), dst_blocks.data_ptr(),
+        src_blocks.numel(), bk, bv, nb, _flag(err_flag), _stream()))
 
 
 def decode_workspace_size(num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -71,6 +71,63 @@ bool encode_tmap_16bit(CUtensorMap* map, kvc_dtype dtype, int rank, const void* 
   return r == CUDA_SUCCESS;
 }
 
+DecodeArgs make_decode_args(const void* q, const void* key_cache, const void* value_cache,
+                            const int32_t* block_table, const int32_t* seq_lens, void* out,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                            kvc_dtype dtype, int num_ctas, void* workspace,
+                            size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream) {
+  DecodeArgs a;
+  a.q = q;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.num_ctas = num_ctas;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err_flag = err_flag;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return a;
+}
+
+kvc_status check_decode_args(const DecodeArgs& a, bool* empty) {
+  *empty = false;
+  if (a.dtype != KVC_F16 && a.dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (a.batch < 0 || a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.head_dim <= 0 ||
+      a.block_size <= 0 || a.max_blocks_per_seq <= 0 || a.num_blocks <= 0 || a.num_ctas < 0 ||
+      a.window < 0)
+    return KVC_ERR_INVALID_ARG;
+  if (a.num_q_heads % a.num_kv_heads) return KVC_ERR_INVALID_ARG;
+  if (!isfinite(a.scale)) return KVC_ERR_INVALID_ARG;
+  if (a.num_q_heads / a.num_kv_heads > 16) return KVC_ERR_UNSUPPORTED;
+  if (a.head_dim != 64 && a.head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (!is_pow2(a.block_size) || a.block_size < 8) return KVC_ERR_UNSUPPORTED;
+  if (a.batch > 1024) return KVC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(a.max_blocks_per_seq) * a.block_size > 0x7fffffffLL)
+    return KVC_ERR_UNSUPPORTED;
+  if (a.batch == 0) {
+    *empty = true;
+    return KVC_OK;
+  }
+  if (!a.q || !a.key_cache || !a.value_cache || !a.block_table || !a.seq_lens || !a.out)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned16(a.q) || !aligned16(a.out) || !aligned16(a.key_cache) ||
+      !aligned16(a.value_cache) || !aligned16(a.workspace))
+    return KVC_ERR_INVALID_ARG;
+  return KVC_OK;
+}
+
 }  // namespace kvc
 
 using kvc::aligned16;
@@ -133,6 +190,22 @@ kvc_status kvc_reshape_and_cache(const void* key, const void* value, void* key_c
                                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+kvc_status kvc_copy_blocks(void* key_cache, void* value_cache, const int32_t* src_blocks,
+                           const int32_t* dst_blocks, int num_pairs, long long block_bytes_k,
+                           long long block_bytes_v, int num_blocks, uint32_t* err_flag,
+                           kvc_stream_t stream) {
+  if (num_pairs < 0 || num_blocks <= 0 || block_bytes_k <= 0 || block_bytes_k % 16)
+    return KVC_ERR_INVALID_ARG;
+  if (value_cache && (block_bytes_v <= 0 || block_bytes_v % 16)) return KVC_ERR_INVALID_ARG;
+  if (num_pairs == 0) return KVC_OK;
+  if (!key_cache || !src_blocks || !dst_blocks) return KVC_ERR_INVALID_ARG;
+  if (!aligned16(key_cache) || (value_cache && !aligned16(value_cache)))
+    return KVC_ERR_INVALID_ARG;
+  return kvc::launch_copy_blocks(key_cache, value_cache, src_blocks, dst_blocks, num_pairs,
+                                 block_bytes_k, block_bytes_v, num_blocks, err_flag,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t kvc_paged_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
                                        int num_ctas) {
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
@@ -150,45 +223,13 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
                             int block_size, int max_blocks_per_seq, int num_blocks, float scale,
                             kvc_dtype dtype, int num_ctas, void* workspace,
                             size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream) {
-  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
-  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-      max_blocks_per_seq <= 0 || num_blocks <= 0 || num_ctas < 0)
-    return KVC_ERR_INVALID_ARG;
-  if (num_q_heads % num_kv_heads) return KVC_ERR_INVALID_ARG;
-  if (!isfinite(scale)) return KVC_ERR_INVALID_ARG;
-  if (num_q_heads / num_kv_heads > 16) return KVC_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return KVC_ERR_UNSUPPORTED;
-  if (!is_pow2(block_size) || block_size < 8) return KVC_ERR_UNSUPPORTED;
-  if (batch > 1024) return KVC_ERR_UNSUPPORTED;
-  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
-    return KVC_ERR_UNSUPPORTED;
-  if (batch == 0) return KVC_OK;
-  if (!q || !key_cache || !value_cache || !block_table || !seq_lens || !out)
-    return KVC_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache) ||
-      !aligned16(workspace))
-    return KVC_ERR_INVALID_ARG;
-  kvc::DecodeArgs a;
-  a.q = q;
-  a.key_cache = key_cache;
-  a.value_cache = value_cache;
-  a.block_table = block_table;
-  a.seq_lens = seq_lens;
-  a.out = out;
-  a.batch = batch;
-  a.num_q_heads = num_q_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.head_dim = head_dim;
-  a.block_size = block_size;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_blocks = num_blocks;
-  a.scale = scale;
-  a.dtype = dtype;
-  a.num_ctas = num_ctas;
-  a.workspace = workspace;
-  a.workspace_bytes = workspace_bytes;
-  a.err_flag = err_flag;
-  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  const kvc::DecodeArgs a = kvc::make_decode_args(
+      q, key_cache, value_cache, block_table, seq_lens, out, batch, num_q_heads, num_kv_heads,
+      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, num_ctas, workspace,
+      workspace_bytes, err_flag, stream);
+  bool empty = false;
+  const kvc_status st = kvc::check_decode_args(a, &empty);
+  if (st != KVC_OK || empty) return st;
   return kvc::launch_paged_decode(a);
 }
 
@@ -202,48 +243,16 @@ kvc_status kvc_paged_decode_append(const void* q, const void* new_key, const voi
                                    kvc_stream_t stream) {
   if (batch > 0 && (!new_key || !new_value || !aligned16(new_key) || !aligned16(new_value)))
     return KVC_ERR_INVALID_ARG;
-  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
-  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-      max_blocks_per_seq <= 0 || num_blocks <= 0 || num_ctas < 0)
-    return KVC_ERR_INVALID_ARG;
-  if (num_q_heads % num_kv_heads) return KVC_ERR_INVALID_ARG;
-  if (!isfinite(scale)) return KVC_ERR_INVALID_ARG;
-  if (num_q_heads / num_kv_heads > 16) return KVC_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return KVC_ERR_UNSUPPORTED;
-  if (!is_pow2(block_size) || block_size < 8) return KVC_ERR_UNSUPPORTED;
-  if (batch > 1024) return KVC_ERR_UNSUPPORTED;
-  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
-    return KVC_ERR_UNSUPPORTED;
-  if (batch == 0) return KVC_OK;
-  if (!q || !key_cache || !value_cache || !block_table || !seq_lens || !out)
-    return KVC_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache) ||
-      !aligned16(workspace))
-    return KVC_ERR_INVALID_ARG;
-  kvc::DecodeArgs a;
-  a.q = q;
-  a.key_cache = key_cache;
-  a.value_cache = value_cache;
-  a.block_table = block_table;
-  a.seq_lens = seq_lens;
-  a.out = out;
-  a.batch = batch;
-  a.num_q_heads = num_q_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.head_dim = head_dim;
-  a.block_size = block_size;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_blocks = num_blocks;
-  a.scale = scale;
-  a.dtype = dtype;
-  a.num_ctas = num_ctas;
-  a.workspace = workspace;
-  a.workspace_bytes = workspace_bytes;
-  a.err_flag = err_flag;
-  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  kvc::DecodeArgs a = kvc::make_decode_args(
+      q, key_cache, value_cache, block_table, seq_lens, out, batch, num_q_heads, num_kv_heads,
+      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, num_ctas, workspace,
+      workspace_bytes, err_flag, stream);
   a.new_key = new_key;
   a.new_value = new_value;
   a.slot_out = slot_mapping;
+  bool empty = false;
+  const kvc_status st = kvc::check_decode_args(a, &empty);
+  if (st != KVC_OK || empty) return st;
   return kvc::launch_paged_decode(a);
 }
 

@@ -137,8 +137,8 @@ kvc_status kvc_bm_fork(kvc_block_manager* bm, int64_t parent, int64_t child) {
   if (it == bm->seqs.end() || bm->seqs.count(child)) return KVC_ERR_INVALID_ARG;
   try {
     kvc_block_manager::Seq s;
-    s.blocks.reserve(bm->max_blocks);
-    s.blocks = it->second.blocks;
+    s.blocks.reserve(bm->max_blocks);  // assign() keeps this capacity; operator= need not
+    s.blocks.assign(it->second.blocks.begin(), it->second.blocks.end());
     s.len = it->second.len;
     const auto& placed = bm->seqs.emplace(child, std::move(s)).first->second;
     for (const int32_t b : placed.blocks) ++bm->ref[b];  // after the insert, which may throw
@@ -225,6 +225,15 @@ kvc_status kvc_bm_step(kvc_block_manager* bm, const int64_t* seq_ids, int n, int
     const int p = seq[i]->len;
     if (p % bm->block_size == 0) {
       if (static_cast<int>(seq[i]->blocks.size()) >= bm->max_blocks) return KVC_ERR_INVALID_ARG;
+      // The second pass must not reallocate (it could throw half-way): make
+      // sure of the capacity now, while nothing has changed yet.
+      if (seq[i]->blocks.capacity() < static_cast<size_t>(bm->max_blocks)) {
+        try {
+          seq[i]->blocks.reserve(bm->max_blocks);
+        } catch (...) {
+          return KVC_ERR_OUT_OF_BLOCKS;
+        }
+      }
       ++need;
     } else {
       const int32_t blk = seq[i]->blocks.back();

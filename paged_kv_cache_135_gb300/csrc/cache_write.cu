@@ -1,5 +1,4 @@
-// Slot-mapping construction and the paged cache write (rows a1 and a2 of the
-// hot path).
+// Slot-mapping construction and the paged cache write.
 //
 // Slot formula: "external-cannbot-model-model-infer-kvcache", 3.1 Mapping
 // Formula (logical block = pos / block_size, offset = pos % block_size,
@@ -87,7 +86,56 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ key,
   }
 }
 
+// Copy-on-write block copies: pair i copies block src[i] to block dst[i], as
+// 16-byte chunks (one thread per chunk, consecutive threads on consecutive
+// chunks, so reads and writes are coalesced).  K chunks of a pair come first,
+// then V chunks.  A pair with src < 0 is skipped; an id outside the pool is
+// skipped and flagged.
+__global__ void copy_blocks_kernel(uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                                   const int32_t* __restrict__ src,
+                                   const int32_t* __restrict__ dst, int num_pairs,
+                                   int64_t chunks_k, int64_t chunks_v, int num_blocks,
+                                   uint32_t* err_flag) {
+  const int64_t per_pair = chunks_k + chunks_v;
+  const int64_t total = static_cast<int64_t>(num_pairs) * per_pair;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int pair = static_cast<int>(i / per_pair);
+    const int64_t c = i - static_cast<int64_t>(pair) * per_pair;
+    const int32_t s = src[pair], d = dst[pair];
+    if (s < 0) continue;
+    if (s >= num_blocks || d < 0 || d >= num_blocks) {
+      if (c == 0) set_flag(err_flag, KVC_FLAG_BLOCK_ID_RANGE);
+      continue;
+    }
+    if (c < chunks_k) {
+      key_cache[d * chunks_k + c] = key_cache[s * chunks_k + c];
+    } else {
+      const int64_t cv = c - chunks_k;
+      value_cache[d * chunks_v + cv] = value_cache[s * chunks_v + cv];
+    }
+  }
+}
+
 }  // namespace
+
+kvc_status launch_copy_blocks(void* key_cache, void* value_cache, const int32_t* src,
+                              const int32_t* dst, int num_pairs, int64_t block_bytes_k,
+                              int64_t block_bytes_v, int num_blocks, uint32_t* err_flag,
+                              cudaStream_t stream) {
+  if (num_pairs == 0) return KVC_OK;
+  const int64_t chunks_k = block_bytes_k / 16;
+  const int64_t chunks_v = value_cache ? block_bytes_v / 16 : 0;
+  const int64_t total = static_cast<int64_t>(num_pairs) * (chunks_k + chunks_v);
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int cap = device_sm_count() * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  copy_blocks_kernel<<<grid, threads, 0, stream>>>(
+      static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache), src, dst, num_pairs,
+      chunks_k, chunks_v, num_blocks, err_flag);
+  return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
 
 kvc_status launch_slot_mapping(const int32_t* block_table, int max_blocks_per_seq,
                                const int32_t* cu_seqlens, const int32_t* start_pos, int num_seqs,

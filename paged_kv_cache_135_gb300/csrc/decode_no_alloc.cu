@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/kvc.h"
+#include "kvc_host.h"
 
 namespace {
 
@@ -29,7 +30,10 @@ std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
 // Device address of the scratch array on the current device, looked up once
-// per device (the first call on each device does this).
+// per device (the first call on each device does this).  The address stays
+// valid for the life of the device's primary context: after cudaDeviceReset
+// the module is loaded again and this cached address is stale, so the entry
+// point must not be used after a reset of a device it has run on.
 kvc_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_ERR_CUDA;
@@ -51,23 +55,22 @@ extern "C" kvc_status kvc_paged_decode_no_alloc(
     const int32_t* seq_lens, void* out, int batch, int num_q_heads, int num_kv_heads,
     int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
     kvc_dtype dtype, int num_ctas, uint32_t* err_flag, kvc_stream_t stream) {
-  void* scratch = nullptr;
-  const kvc_status st = scratch_address(&scratch);
-  if (st != KVC_OK) return st;
-  // Shapes the regular entry point rejects, or an empty batch: let it answer
-  // without touching the scratch.
-  const bool shape_ok = batch > 0 && num_q_heads > 0 && num_kv_heads > 0 && num_ctas >= 0 &&
-                        num_q_heads % num_kv_heads == 0 &&
-                        num_q_heads / num_kv_heads <= 16 && (head_dim == 64 || head_dim == 128);
-  if (!shape_ok)
-    return kvc_paged_decode(q, key_cache, value_cache, block_table, seq_lens, out, batch,
-                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                            num_blocks, scale, dtype, num_ctas, scratch, kScratchBytes, err_flag,
-                            stream);
+  // Every argument is checked before anything is enqueued, so a rejected call
+  // leaves nothing on the stream (not even the scratch clear below).
+  const kvc::DecodeArgs args = kvc::make_decode_args(
+      q, key_cache, value_cache, block_table, seq_lens, out, batch, num_q_heads, num_kv_heads,
+      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, num_ctas, nullptr, 0,
+      err_flag, stream);
+  bool empty = false;
+  const kvc_status checked = kvc::check_decode_args(args, &empty);
+  if (checked != KVC_OK || empty) return checked;
   const size_t need = kvc_paged_decode_workspace_size(num_q_heads, num_kv_heads, head_dim,
                                                       num_ctas);
   if (need == 0) return KVC_ERR_CUDA;
   if (need > kScratchBytes) return KVC_ERR_WORKSPACE;  // more CTAs or a wider group than fits
+  void* scratch = nullptr;
+  const kvc_status st = scratch_address(&scratch);
+  if (st != KVC_OK) return st;
   // The array keeps whatever the previous call left; the split-KV arrival
   // counters must start at zero, so clear the part this call uses.
   if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -40,6 +40,11 @@ kvc_status launch_reshape_and_cache(const void* key, const void* value, void* ke
                                     int head_dim_v, int block_size, int num_blocks,
                                     uint32_t* err_flag, cudaStream_t stream);
 
+kvc_status launch_copy_blocks(void* key_cache, void* value_cache, const int32_t* src,
+                              const int32_t* dst, int num_pairs, int64_t block_bytes_k,
+                              int64_t block_bytes_v, int num_blocks, uint32_t* err_flag,
+                              cudaStream_t stream);
+
 struct DecodeArgs {
   const void* q;
   const void* key_cache;
@@ -59,7 +64,20 @@ struct DecodeArgs {
   const void* new_key = nullptr;
   const void* new_value = nullptr;
   int32_t* slot_out = nullptr;
+  // Band decode: attend to the last `window` tokens only (0: all of them).
+  int window = 0;
 };
+
+// The arguments of kvc_paged_decode gathered into a DecodeArgs.
+DecodeArgs make_decode_args(const void* q, const void* key_cache, const void* value_cache,
+                            const int32_t* block_table, const int32_t* seq_lens, void* out,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                            kvc_dtype dtype, int num_ctas, void* workspace,
+                            size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream);
+// Host-side checks shared by the decode entry points (every check except the
+// workspace size); *empty is set for a batch of 0, which has nothing to do.
+kvc_status check_decode_args(const DecodeArgs& a, bool* empty);
 
 // Persistent CTAs the decode kernel would use for this shape (num_ctas <= 0
 // means "auto").  Returns 0 for an unsupported shape.

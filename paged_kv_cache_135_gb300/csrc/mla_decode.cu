@@ -1,4 +1,4 @@
-// MLA paged decode on the tcgen05 tensor cores (row a6 of the hot path).
+// MLA paged decode on the tcgen05 tensor cores.
 //
 // What it computes: "external-cannbot-model-model-infer-kvcache" Mode 3 --
 // the cache holds only the compressed latent cache_nope (kv_lora_rank = 512)

@@ -1,4 +1,4 @@
-// Paged decode attention with split-KV (rows a3 and a4 of the hot path).
+// Paged decode attention with split-KV and its in-kernel merge.
 //
 // What it computes: "external-cannbot-model-model-infer-kvcache" Mode 2 --
 // one query token per sequence attends to the sequence's cached K/V, read

@@ -1,6 +1,6 @@
 // Packed-varlen causal prefill over the paged cache on the tcgen05 tensor
-// cores (row a5 of the hot path, attention part; the call's cache write is
-// in cache_write.cu).
+// cores (the attention part of kvc_varlen_prefill_paged; the call's cache
+// write is in cache_write.cu).
 //
 // What it computes: the hotelren.com notes "Paged KV Cache + Packed
 // Sequence" 3.1-3.3 -- packed sequences delimited by cu_seqlens, each token

@@ -1,6 +1,6 @@
 // Packed-varlen causal prefill over the paged cache on the tcgen05 tensor
-// cores, two query heads of one GQA group per CTA (row a5 of the hot path,
-// attention part, used when the group size is even).
+// cores, two query heads of one GQA group per CTA (the attention part of
+// kvc_varlen_prefill_paged, used when the group size is even).
 //
 // What it computes: the hotelren.com notes "Paged KV Cache + Packed
 // Sequence" 3.1-3.3 -- packed sequences delimited by cu_seqlens, each token

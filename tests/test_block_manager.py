@@ -334,3 +334,24 @@ def test_step_buffer_reuse():
         a.step([0, 1], out=buf)                 # made for 3 sequences
     with pytest.raises(ValueError):
         a.step(torch.tensor([0, 1, 2], dtype=torch.int32))
+
+
+def test_forked_sequences_step_past_several_block_boundaries():
+    """A fork's block list is built once; stepping it through many new blocks must
+    keep every step all-or-nothing and the tables equal to single appends."""
+    a, b = kvc.BlockManager(200, 4, 24), kvc.BlockManager(200, 4, 24)
+    for bm in (a, b):
+        bm.add(0, 5)
+        bm.fork(0, 1)
+        bm.fork(1, 2)
+    ids = [0, 1, 2]
+    for _ in range(30):                         # 30 tokens = 7+ new blocks per sequence
+        slots, cs, cd, table, lens = a.step(ids, pad=-1)
+        for i, sid in enumerate(ids):
+            assert b.append(sid) == (int(slots[i]), int(cs[i]), int(cd[i]))
+        t2, l2 = b.tables(ids, pad=-1)
+        assert np.array_equal(table.numpy(), t2.numpy()) and np.array_equal(lens.numpy(), l2.numpy())
+    assert [a.seq_len(s) for s in ids] == [35, 35, 35]
+    check_invariants(a, ids)
+    # the first shared partial block was copied for two of the three holders only
+    assert a.ref_count(table_of(a, 0)[0]) == 3
