@@ -206,6 +206,89 @@ kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* va
                             size_t workspace_bytes, uint32_t* err_flag, kvc_stream_t stream);
 
 /*
+ * kvc_paged_decode_window -- kvc_paged_decode restricted to a band: each
+ * sequence attends to its last `window` cached tokens only.
+ * [SKILL] Appendix C, sparse_mode 4 (band attention, named for sliding-window
+ * models together with pre_tokens); ai6s.net KVCache article, section 3 item
+ * 4 (a sliding window keeps only the most recent N tokens).  Neither fixes the
+ * band's edges; this library's reading: the band ends at the query's own
+ * position and holds `window` positions.
+ *
+ *   lo = max(0, seq_lens[b] - window)
+ *   out[b][h][:] = sum_{lo <= j < seq_lens[b]} softmax_j(scale * q[b][h] . K_b[j][g]) V_b[j][g]
+ *
+ * window >= 1 (else KVC_ERR_INVALID_ARG); a window of at least seq_lens[b]
+ * gives kvc_paged_decode's result, bit for bit.  Every other argument, the
+ * workspace rules and the errors are those of kvc_paged_decode.  Blocks that
+ * lie wholly before the band are never read (their table entries are not
+ * looked up either).
+ */
+kvc_status kvc_paged_decode_window(const void* q, const void* key_cache, const void* value_cache,
+                                   const int32_t* block_table, const int32_t* seq_lens, void* out,
+                                   int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_blocks_per_seq, int num_blocks,
+                                   float scale, int window, kvc_dtype dtype, int num_ctas,
+                                   void* workspace, size_t workspace_bytes, uint32_t* err_flag,
+                                   kvc_stream_t stream);
+
+/*
+ * kvc_reshape_and_cache_int8 -- the cache write of an INT8 KV cache.
+ * [ATB] section 4.2 (new rows go to their cache position) with the rows
+ * quantised as [SKILL] 4 (quantized KV: codes plus antiquant / dequant
+ * scales) and the article's section 3 (FP16 -> INT8 halves the bytes per
+ * element) imply.  The pages fix no scheme; this library's reading: one
+ * symmetric fp32 scale per written row (token, kv head), so a decode write
+ * never re-quantises earlier tokens, decided in IEEE fp32:
+ *
+ *   amax = max_d |x[d]|;  inv = 127 / amax;  scale = amax / 127
+ *   code[d] = clamp(round_half_even(x[d] * inv), -127, 127)
+ *   (a row of zeros: scale 0, codes 0; both divisions and the product are
+ *    single fp32 operations rounded to nearest)
+ *   key_codes[slot / bs][slot % bs][h][:] = code;  key_scales[slot / bs][h][slot % bs] = scale
+ *   (the same for value)
+ *
+ * key, value: [num_tokens, num_kv_heads, head_dim] fp16/bf16; key_codes,
+ * value_codes: int8 [num_blocks, block_size, num_kv_heads, head_dim] (the
+ * 16-bit cache's layout); key_scales, value_scales: fp32 [num_blocks,
+ * num_kv_heads, block_size] (head-major inside a block, so one head's scales
+ * of consecutive tokens are contiguous).  slot_mapping as for
+ * kvc_reshape_and_cache (negative: skip; out of range: skip and
+ * KVC_FLAG_SLOT_RANGE).  head_dim 64 or 128.
+ */
+kvc_status kvc_reshape_and_cache_int8(const void* key, const void* value, int8_t* key_codes,
+                                      int8_t* value_codes, float* key_scales,
+                                      float* value_scales, const int32_t* slot_mapping,
+                                      int num_tokens, int num_kv_heads, int head_dim,
+                                      int block_size, int num_blocks, kvc_dtype dtype,
+                                      uint32_t* err_flag, kvc_stream_t stream);
+
+/*
+ * kvc_paged_decode_int8 -- kvc_paged_decode over an INT8 KV cache written by
+ * kvc_reshape_and_cache_int8: every cached row is code * scale.
+ * [SKILL] Mode 2 and 4 (FA over a quantized KV cache with its dequantisation
+ * scales); ai6s.net KVCache article section 3 (INT8 halves the bytes).
+ *
+ *   out[b][h][:] = sum_{j < seq_lens[b]} softmax_j(scale * q[b][h] . Kd_b[j][g]) Vd_b[j][g]
+ *   Kd_b[j][g][d] = key_codes[blk][off][g][d] * key_scales[blk][g][off]
+ *   (blk = block_table[b][j / block_size], off = j % block_size; V alike)
+ *
+ * q, out: fp16/bf16 [batch, num_q_heads, 128] (`dtype`); the kernel reads the
+ * codes and scales (about half the bytes of a 16-bit cache) and computes in
+ * fp32 as kvc_paged_decode does.  head_dim 128 only (KVC_ERR_UNSUPPORTED
+ * otherwise); every other argument, the workspace (same size query) and the
+ * errors are those of kvc_paged_decode.
+ */
+kvc_status kvc_paged_decode_int8(const void* q, const int8_t* key_codes,
+                                 const int8_t* value_codes, const float* key_scales,
+                                 const float* value_scales, const int32_t* block_table,
+                                 const int32_t* seq_lens, void* out, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int max_blocks_per_seq, int num_blocks, float scale,
+                                 kvc_dtype dtype, int num_ctas, void* workspace,
+                                 size_t workspace_bytes, uint32_t* err_flag,
+                                 kvc_stream_t stream);
+
+/*
  * kvc_paged_decode_append -- one decode step in one launch: the slot mapping,
  * the cache write of the new token and the paged decode with split-KV,
  * fused.  Identical in effect to kvc_build_slot_mapping (start_pos =
@@ -272,6 +355,31 @@ kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* 
                                     int num_kv_heads, int head_dim, int block_size,
                                     int max_blocks_per_seq, int num_blocks, float scale,
                                     kvc_dtype dtype, uint32_t* err_flag, kvc_stream_t stream);
+
+/*
+ * kvc_varlen_prefill_paged_window -- kvc_varlen_prefill_paged with band
+ * attention: each query sees only the last `window` positions up to its own.
+ * [SKILL] Appendix C, sparse_mode 4 (band, for sliding-window models with
+ * pre_tokens); ai6s.net KVCache article section 3 item 4 (keep the most recent
+ * N tokens).  The band's edges are this library's reading: it ends at the
+ * query's own position and holds `window` positions.
+ *
+ *   token i of sequence s at position p = context_lens[s] + i:
+ *   out[t][h] = sum_{max(0, p - window + 1) <= j <= p}
+ *                 softmax_j(scale * q[t][h] . K_s[j][g]) V_s[j][g]
+ *
+ * window >= 1 (else KVC_ERR_INVALID_ARG); window >= p + 1 for every query
+ * gives kvc_varlen_prefill_paged's result.  The cache write and every other
+ * argument and error are those of kvc_varlen_prefill_paged.  Key tiles that
+ * lie wholly before the band of a query tile are not read.
+ */
+kvc_status kvc_varlen_prefill_paged_window(
+    const void* q, const void* key, const void* value, const int32_t* cu_seqlens,
+    const int32_t* context_lens, const int32_t* slot_mapping, const int32_t* block_table,
+    void* key_cache, void* value_cache, void* out, int num_seqs, int num_tokens,
+    int max_seqlen_q, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int max_blocks_per_seq, int num_blocks, float scale, int window, kvc_dtype dtype,
+    uint32_t* err_flag, kvc_stream_t stream);
 
 /*
  * Bytes of workspace kvc_mla_paged_decode needs with `num_ctas` CTAs (0 = as

@@ -42,10 +42,18 @@ _SIGS = {
                                   _I, _P, _S, _P, _P]),
     "kvc_varlen_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _I, _I, _F, _I, _P, _P]),
+    "kvc_varlen_prefill_paged_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                             _I, _I, _I, _I, _I, _F, _I, _I, _P, _P]),
     "kvc_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                               _P, _S, _P, _P]),
     "kvc_paged_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                      _I, _F, _I, _I, _P, _S, _P, _P]),
+    "kvc_paged_decode_window": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                     _I, _I, _P, _S, _P, _P]),
+    "kvc_reshape_and_cache_int8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P,
+                                        _P]),
+    "kvc_paged_decode_int8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                   _F, _I, _I, _P, _S, _P, _P]),
     "kvc_bm_create": (_I, [_I, _I, _I, _P]),
     "kvc_bm_destroy": (None, [_P]),
     "kvc_bm_num_free": (_I, [_P]),
@@ -222,6 +230,88 @@ def paged_decode(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Te
     return out
 
 
+def _decode_ws(workspace, Hq, Hkv, D, num_ctas, device):
+    if workspace is None:
+        n = decode_workspace_size(Hq, Hkv, D, num_ctas)
+        workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+    _cuda("workspace", workspace)
+    return workspace
+
+
+def paged_decode_window(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                        block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                        window: int, out: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                        workspace: Optional[torch.Tensor] = None,
+                        err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """paged_decode over each sequence's last `window` cached tokens only (band attention)."""
+    _cuda("q", q)
+    _cuda("key_cache", key_cache, q.dtype)
+    _cuda("value_cache", value_cache, q.dtype)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("seq_lens", seq_lens, torch.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, q.dtype)
+    workspace = _decode_ws(workspace, Hq, Hkv, D, num_ctas, q.device)
+    _check("kvc_paged_decode_window", lib().kvc_paged_decode_window(
+        q.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(), block_table.data_ptr(),
+        seq_lens.data_ptr(), out.data_ptr(), B, Hq, Hkv, D, bs, block_table.shape[1], NB,
+        float(scale), int(window), _DT[q.dtype], num_ctas, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _flag(err_flag), _stream()))
+    return out
+
+
+def reshape_and_cache_int8(key: torch.Tensor, value: torch.Tensor, key_codes: torch.Tensor,
+                           value_codes: torch.Tensor, key_scales: torch.Tensor,
+                           value_scales: torch.Tensor, slot_mapping: torch.Tensor,
+                           err_flag: Optional[torch.Tensor] = None) -> None:
+    """Quantise key/value rows [T, Hkv, D] into an INT8 cache at slot_mapping[t]: codes int8
+    [NB, bs, Hkv, D], one fp32 scale per row in scales [NB, Hkv, bs]."""
+    _cuda("key", key)
+    _cuda("value", value, key.dtype)
+    _cuda("key_codes", key_codes, torch.int8)
+    _cuda("value_codes", value_codes, torch.int8)
+    _cuda("key_scales", key_scales, torch.float32)
+    _cuda("value_scales", value_scales, torch.float32)
+    _cuda("slot_mapping", slot_mapping, torch.int32)
+    NB, bs, H, D = key_codes.shape
+    _check("kvc_reshape_and_cache_int8", lib().kvc_reshape_and_cache_int8(
+        key.data_ptr(), value.data_ptr(), key_codes.data_ptr(), value_codes.data_ptr(),
+        key_scales.data_ptr(), value_scales.data_ptr(), slot_mapping.data_ptr(), key.shape[0], H,
+        D, bs, NB, _DT[key.dtype], _flag(err_flag), _stream()))
+
+
+def paged_decode_int8(q: torch.Tensor, key_codes: torch.Tensor, value_codes: torch.Tensor,
+                      key_scales: torch.Tensor, value_scales: torch.Tensor,
+                      block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                      out: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                      workspace: Optional[torch.Tensor] = None,
+                      err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """paged_decode over an INT8 cache (codes [NB, bs, Hkv, 128], scales [NB, Hkv, bs])."""
+    _cuda("q", q)
+    _cuda("key_codes", key_codes, torch.int8)
+    _cuda("value_codes", value_codes, torch.int8)
+    _cuda("key_scales", key_scales, torch.float32)
+    _cuda("value_scales", value_scales, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("seq_lens", seq_lens, torch.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = key_codes.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, q.dtype)
+    workspace = _decode_ws(workspace, Hq, Hkv, D, num_ctas, q.device)
+    _check("kvc_paged_decode_int8", lib().kvc_paged_decode_int8(
+        q.data_ptr(), key_codes.data_ptr(), value_codes.data_ptr(), key_scales.data_ptr(),
+        value_scales.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(), B,
+        Hq, Hkv, D, bs, block_table.shape[1], NB, float(scale), _DT[q.dtype], num_ctas,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _flag(err_flag),
+        _stream()))
+    return out
+
+
 def paged_decode_append(q: torch.Tensor, new_key: torch.Tensor, new_value: torch.Tensor,
                         key_cache: torch.Tensor, value_cache: torch.Tensor,
                         block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
@@ -295,6 +385,38 @@ def varlen_prefill_paged(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor
         _ptr(context_lens), slot_mapping.data_ptr(), block_table.data_ptr(),
         key_cache.data_ptr(), value_cache.data_ptr(), out.data_ptr(), cu_seqlens.numel() - 1, T,
         int(max_seqlen_q), Hq, Hkv, D, bs, block_table.shape[1], NB, float(scale),
+        _DT[q.dtype], _flag(err_flag), _stream()))
+    return out
+
+
+def varlen_prefill_paged_window(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                                cu_seqlens: torch.Tensor, slot_mapping: torch.Tensor,
+                                block_table: torch.Tensor, key_cache: torch.Tensor,
+                                value_cache: torch.Tensor, scale: float, max_seqlen_q: int,
+                                window: int, context_lens: Optional[torch.Tensor] = None,
+                                out: Optional[torch.Tensor] = None,
+                                err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """varlen_prefill_paged with band attention: a query at position p sees p - window + 1 .. p."""
+    _cuda("q", q)
+    _cuda("key", key, q.dtype)
+    _cuda("value", value, q.dtype)
+    _cuda("cu_seqlens", cu_seqlens, torch.int32)
+    _cuda("slot_mapping", slot_mapping, torch.int32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("key_cache", key_cache, q.dtype)
+    _cuda("value_cache", value_cache, q.dtype)
+    if context_lens is not None:
+        _cuda("context_lens", context_lens, torch.int32)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, _ = key_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, q.dtype)
+    _check("kvc_varlen_prefill_paged_window", lib().kvc_varlen_prefill_paged_window(
+        q.data_ptr(), key.data_ptr(), value.data_ptr(), cu_seqlens.data_ptr(),
+        _ptr(context_lens), slot_mapping.data_ptr(), block_table.data_ptr(),
+        key_cache.data_ptr(), value_cache.data_ptr(), out.data_ptr(), cu_seqlens.numel() - 1, T,
+        int(max_seqlen_q), Hq, Hkv, D, bs, block_table.shape[1], NB, float(scale), int(window),
         _DT[q.dtype], _flag(err_flag), _stream()))
     return out
 

@@ -51,6 +51,15 @@ EncodeTiledFn encode_fn() {
 bool encode_tmap_16bit(CUtensorMap* map, kvc_dtype dtype, int rank, const void* base,
                        const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                        bool swizzle128) {
+  return encode_tmap(map,
+                     dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     rank, base, dims, strides_bytes, box, swizzle128);
+}
+
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[5], s[4];
@@ -61,10 +70,8 @@ bool encode_tmap_16bit(CUtensorMap* map, kvc_dtype dtype, int rank, const void* 
     e[i] = 1;
     if (i + 1 < rank) s[i] = strides_bytes[i];
   }
-  const CUresult r = fn(map,
-                        dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
+  const CUresult r = fn(map, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s,
+                        b, e,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -212,9 +219,16 @@ size_t kvc_paged_decode_workspace_size(int num_q_heads, int num_kv_heads, int he
   const int group = num_q_heads / num_kv_heads;
   if (group > 16 || (head_dim != 64 && head_dim != 128)) return 0;
   // Enough for either dtype: the automatic CTA count may differ between them.
-  const int c16 = kvc::paged_decode_num_ctas(group, head_dim, KVC_F16, num_ctas);
-  const int cbf = kvc::paged_decode_num_ctas(group, head_dim, KVC_BF16, num_ctas);
-  return kvc::paged_decode_workspace_bytes(group, head_dim, c16 > cbf ? c16 : cbf);
+  // Enough for every variant (dtype, 16-bit or INT8 cache): the automatic
+  // CTA count may differ between them.
+  int ctas = 0;
+  for (const kvc_dtype dt : {KVC_F16, KVC_BF16})
+    for (const bool i8 : {false, true}) {
+      if (i8 && head_dim != 128) continue;
+      const int c = kvc::paged_decode_num_ctas(group, head_dim, dt, num_ctas, i8);
+      if (c > ctas) ctas = c;
+    }
+  return kvc::paged_decode_workspace_bytes(group, head_dim, ctas);
 }
 
 kvc_status kvc_paged_decode(const void* q, const void* key_cache, const void* value_cache,
@@ -256,14 +270,82 @@ kvc_status kvc_paged_decode_append(const void* q, const void* new_key, const voi
   return kvc::launch_paged_decode(a);
 }
 
-kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* value,
-                                    const int32_t* cu_seqlens, const int32_t* context_lens,
-                                    const int32_t* slot_mapping, const int32_t* block_table,
-                                    void* key_cache, void* value_cache, void* out, int num_seqs,
-                                    int num_tokens, int max_seqlen_q, int num_q_heads,
-                                    int num_kv_heads, int head_dim, int block_size,
-                                    int max_blocks_per_seq, int num_blocks, float scale,
-                                    kvc_dtype dtype, uint32_t* err_flag, kvc_stream_t stream) {
+kvc_status kvc_paged_decode_window(const void* q, const void* key_cache, const void* value_cache,
+                                   const int32_t* block_table, const int32_t* seq_lens, void* out,
+                                   int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_blocks_per_seq, int num_blocks,
+                                   float scale, int window, kvc_dtype dtype, int num_ctas,
+                                   void* workspace, size_t workspace_bytes, uint32_t* err_flag,
+                                   kvc_stream_t stream) {
+  if (window < 1) return KVC_ERR_INVALID_ARG;
+  kvc::DecodeArgs a = kvc::make_decode_args(
+      q, key_cache, value_cache, block_table, seq_lens, out, batch, num_q_heads, num_kv_heads,
+      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, num_ctas, workspace,
+      workspace_bytes, err_flag, stream);
+  a.window = window;
+  bool empty = false;
+  const kvc_status st = kvc::check_decode_args(a, &empty);
+  if (st != KVC_OK || empty) return st;
+  return kvc::launch_paged_decode(a);
+}
+
+kvc_status kvc_reshape_and_cache_int8(const void* key, const void* value, int8_t* key_codes,
+                                      int8_t* value_codes, float* key_scales,
+                                      float* value_scales, const int32_t* slot_mapping,
+                                      int num_tokens, int num_kv_heads, int head_dim,
+                                      int block_size, int num_blocks, kvc_dtype dtype,
+                                      uint32_t* err_flag, kvc_stream_t stream) {
+  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return KVC_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return KVC_OK;
+  if (!key || !value || !key_codes || !value_codes || !key_scales || !value_scales ||
+      !slot_mapping)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_codes) || !aligned16(value_codes) ||
+      !aligned16(key_scales) || !aligned16(value_scales))
+    return KVC_ERR_INVALID_ARG;
+  return kvc::launch_reshape_and_cache_int8(key, value, key_codes, value_codes, key_scales,
+                                            value_scales, slot_mapping, num_tokens, num_kv_heads,
+                                            head_dim, block_size, num_blocks, dtype, err_flag,
+                                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_paged_decode_int8(const void* q, const int8_t* key_codes,
+                                 const int8_t* value_codes, const float* key_scales,
+                                 const float* value_scales, const int32_t* block_table,
+                                 const int32_t* seq_lens, void* out, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int max_blocks_per_seq, int num_blocks, float scale,
+                                 kvc_dtype dtype, int num_ctas, void* workspace,
+                                 size_t workspace_bytes, uint32_t* err_flag,
+                                 kvc_stream_t stream) {
+  kvc::DecodeArgs a = kvc::make_decode_args(
+      q, key_codes, value_codes, block_table, seq_lens, out, batch, num_q_heads, num_kv_heads,
+      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, num_ctas, workspace,
+      workspace_bytes, err_flag, stream);
+  bool empty = false;
+  const kvc_status st = kvc::check_decode_args(a, &empty);
+  if (st != KVC_OK || empty) return st;
+  if (head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (!key_scales || !value_scales || !aligned16(key_scales) || !aligned16(value_scales))
+    return KVC_ERR_INVALID_ARG;
+  a.key_scales = key_scales;
+  a.value_scales = value_scales;
+  return kvc::launch_paged_decode(a);
+}
+
+namespace {
+kvc_status varlen_prefill(const void* q, const void* key, const void* value,
+                          const int32_t* cu_seqlens, const int32_t* context_lens,
+                          const int32_t* slot_mapping, const int32_t* block_table,
+                          void* key_cache, void* value_cache, void* out, int num_seqs,
+                          int num_tokens, int max_seqlen_q, int num_q_heads, int num_kv_heads,
+                          int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                          float scale, int window, kvc_dtype dtype, uint32_t* err_flag,
+                          kvc_stream_t stream) {
   if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_tokens < 0 || max_seqlen_q < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
@@ -307,7 +389,37 @@ kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* 
   a.dtype = dtype;
   a.err_flag = err_flag;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.window = window;
   return kvc::launch_varlen_prefill(a);
+}
+}  // namespace
+
+kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* value,
+                                    const int32_t* cu_seqlens, const int32_t* context_lens,
+                                    const int32_t* slot_mapping, const int32_t* block_table,
+                                    void* key_cache, void* value_cache, void* out, int num_seqs,
+                                    int num_tokens, int max_seqlen_q, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int num_blocks, float scale,
+                                    kvc_dtype dtype, uint32_t* err_flag, kvc_stream_t stream) {
+  return varlen_prefill(q, key, value, cu_seqlens, context_lens, slot_mapping, block_table,
+                        key_cache, value_cache, out, num_seqs, num_tokens, max_seqlen_q,
+                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                        num_blocks, scale, 0, dtype, err_flag, stream);
+}
+
+kvc_status kvc_varlen_prefill_paged_window(
+    const void* q, const void* key, const void* value, const int32_t* cu_seqlens,
+    const int32_t* context_lens, const int32_t* slot_mapping, const int32_t* block_table,
+    void* key_cache, void* value_cache, void* out, int num_seqs, int num_tokens,
+    int max_seqlen_q, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int max_blocks_per_seq, int num_blocks, float scale, int window, kvc_dtype dtype,
+    uint32_t* err_flag, kvc_stream_t stream) {
+  if (window < 1) return KVC_ERR_INVALID_ARG;
+  return varlen_prefill(q, key, value, cu_seqlens, context_lens, slot_mapping, block_table,
+                        key_cache, value_cache, out, num_seqs, num_tokens, max_seqlen_q,
+                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                        num_blocks, scale, window, dtype, err_flag, stream);
 }
 
 size_t kvc_mla_paged_decode_workspace_size(int num_heads, int d_nope, int d_rope, int num_ctas) {

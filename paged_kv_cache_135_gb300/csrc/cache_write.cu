@@ -8,7 +8,18 @@
 // -> logical block -> physical block).
 // Cache write: ai6s.net KVCache article 4.2 -- each new row is copied,
 // unchanged, to its cache position.
+// INT8 cache write: the same placement, with each row quantised as the
+// KVCache skill's quantized-KV parameters imply (codes plus dequantisation
+// scales; the article's FP16 -> INT8 halving of the bytes).  The pages fix no
+// scheme; this library stores one symmetric fp32 scale per written row
+// (token, kv head), its codes decided in IEEE fp32: amax = max|x|, inv = 127 /
+// amax, scale = amax / 127 (round-to-nearest divisions), code = x * inv
+// (round-to-nearest product) rounded half to even and clamped to +-127; a
+// zero row has scale 0 and codes 0.  Codes keep the 16-bit cache's layout
+// [num_blocks, block_size, Hkv, D]; scales are [num_blocks, Hkv, block_size].
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "kvc_device.cuh"
 #include "kvc_host.h"
@@ -117,7 +128,107 @@ __global__ void copy_blocks_kernel(uint4* __restrict__ key_cache, uint4* __restr
   }
 }
 
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+
+// One warp per (token, kv head, K or V) row of D elements: lane l holds D/32
+// consecutive elements, amax is a warp max, and the lane writes its codes.
+template <typename T, int D>
+__global__ void reshape_and_cache_int8_kernel(const T* __restrict__ key,
+                                              const T* __restrict__ value,
+                                              int8_t* __restrict__ key_codes,
+                                              int8_t* __restrict__ value_codes,
+                                              float* __restrict__ key_scales,
+                                              float* __restrict__ value_scales,
+                                              const int32_t* __restrict__ slot_mapping,
+                                              int num_tokens, int num_kv_heads, int block_size,
+                                              int64_t num_slots, uint32_t* err_flag) {
+  constexpr int E = D / 32;  // elements per lane: 2 (D 64) or 4 (D 128)
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads * 2;
+  for (int64_t r = w0; r < rows; r += nw) {
+    const int is_v = static_cast<int>(r & 1);
+    const int64_t th = r >> 1;  // token * Hkv + head
+    const int t = static_cast<int>(th / num_kv_heads);
+    const int h = static_cast<int>(th - static_cast<int64_t>(t) * num_kv_heads);
+    const int32_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (lane == 0 && is_v == 0 && h == 0) set_flag(err_flag, KVC_FLAG_SLOT_RANGE);
+      continue;
+    }
+    const T* src = (is_v ? value : key) + th * D + lane * E;
+    float x[E];
+    if constexpr (E == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(src);
+      const T* pv = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = to_f32(pv[e]);
+    } else {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+      const T* pv = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) x[e] = to_f32(pv[e]);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
+    const float scale = __fdiv_rn(amax, 127.f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      int c = __float2int_rn(__fmul_rn(x[e], inv));
+      c = c > 127 ? 127 : (c < -127 ? -127 : c);
+      packed |= (static_cast<uint32_t>(c) & 0xffu) << (8 * e);
+    }
+    const int64_t blk = slot / block_size, in_blk = slot - blk * block_size;
+    int8_t* dst = (is_v ? value_codes : key_codes) +
+                  (static_cast<int64_t>(slot) * num_kv_heads + h) * D + lane * E;
+    if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = packed;
+    else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+    if (lane == 0)
+      (is_v ? value_scales : key_scales)[(blk * num_kv_heads + h) * block_size + in_blk] = scale;
+  }
+}
+
 }  // namespace
+
+kvc_status launch_reshape_and_cache_int8(const void* key, const void* value, void* key_codes,
+                                         void* value_codes, float* key_scales,
+                                         float* value_scales, const int32_t* slot_mapping,
+                                         int num_tokens, int num_kv_heads, int head_dim,
+                                         int block_size, int num_blocks, kvc_dtype dtype,
+                                         uint32_t* err_flag, cudaStream_t stream) {
+  if (num_tokens == 0) return KVC_OK;
+  const int64_t rows = static_cast<int64_t>(num_tokens) * num_kv_heads * 2;
+  const int threads = 256;  // 8 rows per CTA pass
+  const int64_t want = (rows * 32 + threads - 1) / threads;
+  const int cap = device_sm_count() * 16;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  const int64_t ns = static_cast<int64_t>(num_blocks) * block_size;
+  auto go = [&](auto tag, auto dim) {
+    using T = decltype(tag);
+    constexpr int D = decltype(dim)::value;
+    reshape_and_cache_int8_kernel<T, D><<<grid, threads, 0, stream>>>(
+        static_cast<const T*>(key), static_cast<const T*>(value),
+        static_cast<int8_t*>(key_codes), static_cast<int8_t*>(value_codes), key_scales,
+        value_scales, slot_mapping, num_tokens, num_kv_heads, block_size, ns, err_flag);
+  };
+  using D64 = std::integral_constant<int, 64>;
+  using D128 = std::integral_constant<int, 128>;
+  if (dtype == KVC_BF16) {
+    if (head_dim == 128) go(__nv_bfloat16(), D128()); else go(__nv_bfloat16(), D64());
+  } else {
+    if (head_dim == 128) go(__half(), D128()); else go(__half(), D64());
+  }
+  return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
 
 kvc_status launch_copy_blocks(void* key_cache, void* value_cache, const int32_t* src,
                               const int32_t* dst, int num_pairs, int64_t block_bytes_k,

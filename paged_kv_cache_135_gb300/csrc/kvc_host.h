@@ -28,6 +28,10 @@ int device_sm_count();
 bool encode_tmap_16bit(CUtensorMap* map, kvc_dtype dtype, int rank, const void* base,
                        const uint64_t* dims, const uint64_t* strides_bytes,
                        const uint32_t* box, bool swizzle128);
+// The same for any element type.
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 bool swizzle128);
 
 kvc_status launch_slot_mapping(const int32_t* block_table, int max_blocks_per_seq,
                                const int32_t* cu_seqlens, const int32_t* start_pos, int num_seqs,
@@ -44,6 +48,13 @@ kvc_status launch_copy_blocks(void* key_cache, void* value_cache, const int32_t*
                               const int32_t* dst, int num_pairs, int64_t block_bytes_k,
                               int64_t block_bytes_v, int num_blocks, uint32_t* err_flag,
                               cudaStream_t stream);
+
+kvc_status launch_reshape_and_cache_int8(const void* key, const void* value, void* key_codes,
+                                         void* value_codes, float* key_scales,
+                                         float* value_scales, const int32_t* slot_mapping,
+                                         int num_tokens, int num_kv_heads, int head_dim,
+                                         int block_size, int num_blocks, kvc_dtype dtype,
+                                         uint32_t* err_flag, cudaStream_t stream);
 
 struct DecodeArgs {
   const void* q;
@@ -66,6 +77,10 @@ struct DecodeArgs {
   int32_t* slot_out = nullptr;
   // Band decode: attend to the last `window` tokens only (0: all of them).
   int window = 0;
+  // INT8 cache (null for a 16-bit cache): key_cache / value_cache hold int8
+  // codes, these the fp32 scales [num_blocks, Hkv, block_size].
+  const float* key_scales = nullptr;
+  const float* value_scales = nullptr;
 };
 
 // The arguments of kvc_paged_decode gathered into a DecodeArgs.
@@ -81,7 +96,8 @@ kvc_status check_decode_args(const DecodeArgs& a, bool* empty);
 
 // Persistent CTAs the decode kernel would use for this shape (num_ctas <= 0
 // means "auto").  Returns 0 for an unsupported shape.
-int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas);
+int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas,
+                          bool int8 = false);
 size_t paged_decode_workspace_bytes(int group, int head_dim, int ctas);
 kvc_status launch_paged_decode(const DecodeArgs& a);
 
@@ -102,6 +118,8 @@ struct PrefillArgs {
   kvc_dtype dtype;
   uint32_t* err_flag;
   cudaStream_t stream;
+  // Band: a query at position p sees p - window + 1 .. p only (0: 0 .. p).
+  int window = 0;
 };
 
 // Cache write of the chunk's K/V rows, then the causal attention kernel.

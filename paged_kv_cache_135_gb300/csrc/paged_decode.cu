@@ -54,6 +54,9 @@ constexpr int kStages = 3;
 constexpr int kMaxBatch = 1024;
 constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a K or V tile
 constexpr int kMaxPieces = 62;           // split shares merged from a shared-memory list
+// INT8 cache: a tile's per-token scales arrive as one TMA box per physical
+// block (min(block_size, 64) floats); each box gets its own 128-byte slot.
+constexpr int kScaleBytes = (kTile / 8) * 128;
 
 struct DecodeParams {
   const void* q;
@@ -74,7 +77,8 @@ struct DecodeParams {
   void* v_cache;
   int32_t* slot_out;
   int batch, num_q_heads, num_kv_heads, group, head_dim;
-  int block_size, log2_bs, max_blocks, num_blocks, box_tokens;
+  int block_size, log2_bs, max_blocks, num_blocks, box_tokens, log2_box;
+  int window;  // band of the last `window` cached tokens (0: the whole sequence)
   float scale_log2;
 };
 
@@ -83,13 +87,19 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 // Dynamic shared memory of the decode kernel.  A stage holds the K tile, the
 // V tile and the query rows of the tile's (b, g) (all 128-byte swizzled, each
 // 1024-byte aligned as the TMA swizzle requires); every other region starts
-// on a 16-byte boundary.
-template <int D>
+// on a 16-byte boundary.  Over an INT8 cache (kI8) the K and V tiles hold the
+// int8 codes (one 128-byte row per token), the stage also holds the tile's
+// per-token K and V scales, and each consumer warp owns a staging tile for
+// its 16 value rows converted to 16 bits.
+template <int D, bool kI8>
 struct Layout {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kKBytes = kHalves * kHalfBytes;
+  static constexpr int kHalves = D / 64;  // 64-element halves of a 16-bit row
+  static constexpr int kKBytes = kI8 ? kTile * D : kHalves * kHalfBytes;  // one K or V tile
   int q_half;   // bytes of one 64-wide half of the G query rows (1024-aligned)
-  int stage;    // K tile, V tile, query rows
+  int scales;   // INT8: K scales then V scales of the stage, kTile floats each
+  int qoff;     // query rows of the stage (1024-aligned)
+  int vstg;     // INT8: per consumer warp, its 16 value rows as 16-bit values
+  int stage;    // K tile, V tile, (scales), query rows
   int bar;      // full[kStages], empty[kStages]
   int flags;    // abort, last, npieces
   int pieces;   // int[kMaxPieces]
@@ -99,14 +109,18 @@ struct Layout {
   int total;    // bytes to request (with 1024 bytes of alignment slack)
   __host__ __device__ Layout(int batch, int group) {
     q_half = align_up(group * 128, 1024);
-    stage = 2 * kKBytes + kHalves * q_half;
+    scales = 2 * kKBytes;
+    qoff = kI8 ? align_up(scales + 2 * kScaleBytes, 1024) : 2 * kKBytes;
+    stage = qoff + kHalves * q_half;
     bar = kStages * stage;
     flags = bar + 2 * kStages * 8;
     pieces = align_up(flags + 12, 16);
     lens = align_up(pieces + kMaxPieces * 4, 16);
     cum = align_up(lens + batch * 4, 16);
     cmb = align_up(cum + (batch + 1) * 4, 16);
-    total = 1024 + cmb + kConsumerWarps * group * (D + 2) * 4;
+    vstg = align_up(cmb + kConsumerWarps * group * (D + 2) * 4, 1024);
+    total = 1024 + (kI8 ? vstg + kConsumerWarps * 16 * D * 2
+                        : cmb + kConsumerWarps * group * (D + 2) * 4);
   }
 };
 
@@ -159,11 +173,21 @@ struct Cursor {
   }
 };
 
-__device__ __forceinline__ uint32_t keep_rows(uint32_t x, int k, int valid) {
-  const uint32_t lo = k < valid ? 0x0000FFFFu : 0u;
-  const uint32_t hi = k + 1 < valid ? 0xFFFF0000u : 0u;
+// Rows k and k + 1 of a value fragment (low and high 16 bits) kept if they lie
+// in [vlo, valid), zeroed otherwise.
+__device__ __forceinline__ uint32_t keep_rows(uint32_t x, int k, int vlo, int valid) {
+  const uint32_t lo = k >= vlo && k < valid ? 0x0000FFFFu : 0u;
+  const uint32_t hi = k + 1 >= vlo && k + 1 < valid ? 0xFFFF0000u : 0u;
   return x & (lo | hi);
 }
+
+// Band attention (sliding window): a sequence of L cached tokens attends to
+// positions band_lo .. L-1 only, the last `window` of them (0: all).  Its
+// tiles start at the 64-token tile holding band_lo.
+__device__ __forceinline__ int band_lo(int L, int window) {
+  return window > 0 && L > window ? L - window : 0;
+}
+__device__ __forceinline__ int first_tile(int L, int window) { return band_lo(L, window) / kTile; }
 
 // out[0..3] = v * inv, rounded to T (one 8-byte store).
 template <typename T>
@@ -178,7 +202,7 @@ __device__ __forceinline__ void store4(T* dst, float4 v, float inv) {
 // One warp's 16 tokens of a stage: S = Q K^T, online softmax, O += P V.
 template <typename T, int D>
 __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int warp, int lane,
-                                          int valid, float scale_log2, uint32_t qbase,
+                                          int vlo, int valid, float scale_log2, uint32_t qbase,
                                           int q_half, int group, float (&o)[D / 8][4],
                                           float (&m)[2], float (&l)[2]) {
   const int mi = lane >> 3, rr = lane & 7;
@@ -208,7 +232,7 @@ __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int wa
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int k = nt * 8 + c0 + (e & 1);
-      s[nt][e] = k < valid ? s[nt][e] * scale_log2 : -INFINITY;
+      s[nt][e] = k >= vlo && k < valid ? s[nt][e] * scale_log2 : -INFINITY;
     }
   float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
   float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
@@ -245,15 +269,177 @@ __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int wa
     const int dcol = dp * 16 + (mi >> 1) * 8;
     uint32_t b0, b1, b2, b3;
     ldsm_x4_t(vbase + (dcol >> 6) * kHalfBytes + swz128(tok, (dcol & 63) >> 3), b0, b1, b2, b3);
-    if (valid < 16) {
-      b0 = keep_rows(b0, c0, valid);
-      b1 = keep_rows(b1, 8 + c0, valid);
-      b2 = keep_rows(b2, c0, valid);
-      b3 = keep_rows(b3, 8 + c0, valid);
+    if (valid < 16 || vlo > 0) {
+      b0 = keep_rows(b0, c0, vlo, valid);
+      b1 = keep_rows(b1, 8 + c0, vlo, valid);
+      b2 = keep_rows(b2, c0, vlo, valid);
+      b3 = keep_rows(b3, 8 + c0, vlo, valid);
     }
     MmaOp<T>::run(o[2 * dp], pa, b0, b1);
     MmaOp<T>::run(o[2 * dp + 1], pa, b2, b3);
   }
+}
+
+// ---- INT8 cache: codes to 16-bit values, scales, and one warp's 16 tokens.
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
+                                       uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z),
+               "r"(w)
+               : "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+
+// Two int8 codes (the low 16 bits, element 0 first) as a pair of T, exactly:
+// a code c is an integer with |c| <= 128, so it is representable in both
+// 16-bit types.  The byte, biased to c + 128, becomes the low mantissa bits of
+// the fp32 2^23 + c + 128, from which 2^23 + 128 is subtracted exactly.
+template <typename T>
+__device__ __forceinline__ uint32_t i8x2_to_16(uint32_t two) {
+  const uint32_t x = two ^ 0x8080u;
+  const float f0 = __uint_as_float(0x4B000000u | (x & 0xffu)) - 8388736.f;
+  const float f1 = __uint_as_float(0x4B000000u | ((x >> 8) & 0xffu)) - 8388736.f;
+  float ra, rb;
+  return Pack<T>::run(f0, f1, ra, rb);
+}
+
+// Address of token t's scale in a stage's scale region (one 128-byte slot per
+// TMA box of 2^log2_box tokens).
+__device__ __forceinline__ uint32_t scale_addr(uint32_t base, int t, int log2_box) {
+  return base + ((t >> log2_box) << 7) + ((t & ((1 << log2_box) - 1)) << 2);
+}
+
+// One warp's 16 tokens of a stage over an INT8 cache.  A cached row is
+// code * scale, so q . k = scale_k * (q . codes_k) and sum_j p_j v_j =
+// sum_j (p_j * scale_v_j) codes_v_j: S = Q K^T runs on the exact integer codes
+// (converted to T in registers, straight from the 128-byte swizzled code
+// tile), each score column is multiplied by its key scale, and each weight by
+// its value scale before it is rounded to T for P V; l sums the plain p.  The
+// warp's 16 value rows are first converted into `vst`, in the layout of a
+// 16-bit tile, so P V reads them with ldmatrix.trans as the 16-bit path does.
+template <typename T, int D>
+__device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
+                                             uint32_t vscale, int log2_box, int warp, int lane,
+                                             int vlo, int valid, float scale_log2,
+                                             uint32_t qbase, int q_half, int group, uint32_t vst,
+                                             float (&o)[D / 8][4], float (&m)[2],
+                                             float (&l)[2]) {
+  static_assert(D == 128, "one 128-byte code row per token");
+  const int mi = lane >> 3, rr = lane & 7;
+  {  // value codes -> T: lane converts 64 codes of row lane / 2
+    const int row = lane >> 1, tok = warp * 16 + row;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = (lane & 1) * 4 + i;  // 16 dims
+      const uint4 u = lds_v4(vbase + swz128(tok, c));
+      const uint32_t w0 = i8x2_to_16<T>(u.x & 0xffffu), w1 = i8x2_to_16<T>(u.x >> 16);
+      const uint32_t w2 = i8x2_to_16<T>(u.y & 0xffffu), w3 = i8x2_to_16<T>(u.y >> 16);
+      const uint32_t w4 = i8x2_to_16<T>(u.z & 0xffffu), w5 = i8x2_to_16<T>(u.z >> 16);
+      const uint32_t w6 = i8x2_to_16<T>(u.w & 0xffffu), w7 = i8x2_to_16<T>(u.w >> 16);
+      const uint32_t half = vst + (c >> 2) * (16 * 128);
+      sts_v4(half + swz128(row, (c & 3) * 2), w0, w1, w2, w3);
+      sts_v4(half + swz128(row, (c & 3) * 2 + 1), w4, w5, w6, w7);
+    }
+    __syncwarp();
+  }
+  float s[2][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[i][e] = 0.f;
+  {
+    const int qr = (mi & 1) * 8 + rr < group ? (mi & 1) * 8 + rr : 0;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(qbase + (kk >> 2) * q_half + swz128(qr, (kk & 3) * 2 + (mi >> 1)), a[0], a[1],
+              a[2], a[3]);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        // B fragment: dims kk*16 + 2*(lane%4) + {0,1} and + 8 of token lane/4
+        // (one int8 chunk of the swizzled code row = 16 dims).
+        const int tk = warp * 16 + nt * 8 + (lane >> 2);
+        const uint32_t at = kbase + swz128(tk, kk) + 2 * (lane & 3);
+        MmaOp<T>::run(s[nt], a, i8x2_to_16<T>(lds_u16(at)), i8x2_to_16<T>(lds_u16(at + 8)));
+      }
+    }
+  }
+  const int c0 = 2 * (lane & 3);
+  float vsc[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int k = nt * 8 + c0 + e;
+      const int t = warp * 16 + k;
+      const bool in = k >= vlo && k < valid;
+      // Stale stage contents outside [vlo, valid) never enter arithmetic.
+      const float ks = in ? lds_f32(scale_addr(kscale, t, log2_box)) : 0.f;
+      vsc[nt][e] = in ? lds_f32(scale_addr(vscale, t, log2_box)) : 0.f;
+      s[nt][e] = in ? s[nt][e] * (scale_log2 * ks) : -INFINITY;
+      s[nt][e + 2] = in ? s[nt][e + 2] * (scale_log2 * ks) : -INFINITY;
+    }
+  float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+  float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const float corr0 = fast_exp2(m[0] - mn0), corr1 = fast_exp2(m[1] - mn1);
+  m[0] = mn0;
+  m[1] = mn1;
+  float p[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    p[nt][0] = fast_exp2(s[nt][0] - mn0);
+    p[nt][1] = fast_exp2(s[nt][1] - mn0);
+    p[nt][2] = fast_exp2(s[nt][2] - mn1);
+    p[nt][3] = fast_exp2(s[nt][3] - mn1);
+  }
+  l[0] = l[0] * corr0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+  l[1] = l[1] * corr1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+  uint32_t pa[4];
+  float ra, rb;
+  pa[0] = Pack<T>::run(p[0][0] * vsc[0][0], p[0][1] * vsc[0][1], ra, rb);
+  pa[1] = Pack<T>::run(p[0][2] * vsc[0][0], p[0][3] * vsc[0][1], ra, rb);
+  pa[2] = Pack<T>::run(p[1][0] * vsc[1][0], p[1][1] * vsc[1][1], ra, rb);
+  pa[3] = Pack<T>::run(p[1][2] * vsc[1][0], p[1][3] * vsc[1][1], ra, rb);
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    o[n][0] *= corr0;
+    o[n][1] *= corr0;
+    o[n][2] *= corr1;
+    o[n][3] *= corr1;
+  }
+  const int tok = (mi & 1) * 8 + rr;  // row of the warp's staging tile
+#pragma unroll
+  for (int dp = 0; dp < D / 16; ++dp) {
+    const int dcol = dp * 16 + (mi >> 1) * 8;
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(vst + (dcol >> 6) * (16 * 128) + swz128(tok, (dcol & 63) >> 3), b0, b1, b2, b3);
+    // Codes are finite, and the weights outside [vlo, valid) are exact zeros,
+    // so no value row needs masking here.
+    MmaOp<T>::run(o[2 * dp], pa, b0, b1);
+    MmaOp<T>::run(o[2 * dp + 1], pa, b2, b3);
+  }
+  __syncwarp();  // the staging tile is rewritten by the warp's next tile
 }
 
 // The end of one segment share (cold path, kept out of line to spare the
@@ -369,15 +555,18 @@ __device__ __noinline__ void finish_share(const DecodeParams& p, const float* cm
   if (ctid == 0) p.ws_cnt[cfirst * 2 + slot0] = 0;
 }
 
-template <typename T, int D>
+// tm_ks / tm_vs: the INT8 cache's K and V scales (unused for a 16-bit cache).
+template <typename T, int D, bool kI8>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_ks,
+                        const __grid_constant__ CUtensorMap tm_vs,
                         const __grid_constant__ DecodeParams p) {
-  constexpr int kHalves = Layout<D>::kHalves;
-  constexpr int kKBytes = Layout<D>::kKBytes;
-  const Layout<D> L(p.batch, p.group);
+  constexpr int kHalves = Layout<D, kI8>::kHalves;
+  constexpr int kKBytes = Layout<D, kI8>::kKBytes;
+  const Layout<D, kI8> L(p.batch, p.group);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -407,6 +596,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_q);
+    if constexpr (kI8) {
+      prefetch_tmap(&tm_ks);
+      prefetch_tmap(&tm_vs);
+    }
   }
   // Plan: clamped lengths and the prefix sum of 64-token tiles per sequence.
   for (int i = tid; i < B; i += kThreads) lens[i] = clamp_len(p.seq_lens[i], cap, p.err_flag);
@@ -415,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int carry = 0;
     for (int base = 0; base < B; base += 32) {
       const int i = base + lane;
-      const int n = i < B ? (lens[i] + kTile - 1) / kTile : 0;
+      const int n = i < B ? (lens[i] + kTile - 1) / kTile - first_tile(lens[i], p.window) : 0;
       int x = n;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -451,6 +644,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     Cursor cur;
     cur.locate(t_begin, cum, B, hkv);
     const int nsub = kTile / p.box_tokens;
+    // Bytes of one box: a 64-element half of box_tokens 16-bit rows, or
+    // box_tokens whole 128-byte code rows.
     const uint32_t box_bytes = static_cast<uint32_t>(p.box_tokens) * 128u;
     const uint32_t q_bytes = static_cast<uint32_t>(G) * 128u * kHalves;
     int it = 0;
@@ -460,12 +655,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       // Look up this tile's physical blocks first: the table load's latency
       // overlaps the wait for a free stage.
       const int Lb = lens[cur.b];
-      const int tok = cur.j * kTile + lane * p.box_tokens;
+      const int tok = (first_tile(Lb, p.window) + cur.j) * kTile + lane * p.box_tokens;
+      // A box wholly below the band is not fetched (its rows are masked).
+      const bool wanted = lane < nsub && tok < Lb && tok + p.box_tokens > band_lo(Lb, p.window);
       int pb = -1;
-      if (lane < nsub && tok < Lb)
+      if (wanted)
         pb = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks +
                                   (tok >> p.log2_bs)]);
-      if (p.new_k != nullptr && cur.j == cur.n - 1) {
+      if (!kI8 && p.new_k != nullptr && cur.j == cur.n - 1) {
         // The last tile of segment (b, g) holds the new token: write its K/V
         // rows for head g (16 bytes per lane), make the writes visible to the
         // TMA unit, then load the tile as usual.  No other CTA reads them.
@@ -502,28 +699,39 @@ __global__ void __launch_bounds__(kThreads, 2)
         *abort_flag = 1;
       } else {
         bool valid = false;
-        if (lane < nsub && tok < Lb) {
+        if (wanted) {
           if (pb < 0 || pb >= p.num_blocks) set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
           else valid = true;
         }
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
         uint8_t* st = smem + stage * L.stage;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], nvalid * box_bytes * kHalves * 2 + q_bytes);
+          const uint32_t per_box =
+              kI8 ? box_bytes * 2 + static_cast<uint32_t>(p.box_tokens) * 8u
+                  : box_bytes * kHalves * 2;
+          mbar_arrive_expect_tx(&full[stage], nvalid * per_box + q_bytes);
 #pragma unroll
           for (int h = 0; h < kHalves; ++h)
-            tma_load_3d(st + 2 * kKBytes + h * L.q_half, &tm_q, &full[stage], h * 64, cur.g * G,
+            tma_load_3d(st + L.qoff + h * L.q_half, &tm_q, &full[stage], h * 64, cur.g * G,
                         cur.b);
         }
         __syncwarp();
         if (valid) {
           uint8_t* kdst = st + lane * box_bytes;
           const int in_blk = tok & (p.block_size - 1);
+          if constexpr (kI8) {
+            tma_load_4d(kdst, &tm_k, &full[stage], 0, cur.g, in_blk, pb);
+            tma_load_4d(kdst + kKBytes, &tm_v, &full[stage], 0, cur.g, in_blk, pb);
+            uint8_t* sdst = st + L.scales + lane * 128;
+            tma_load_3d(sdst, &tm_ks, &full[stage], in_blk, cur.g, pb);
+            tma_load_3d(sdst + kScaleBytes, &tm_vs, &full[stage], in_blk, cur.g, pb);
+          } else {
 #pragma unroll
-          for (int h = 0; h < kHalves; ++h) {
-            tma_load_4d(kdst + h * kHalfBytes, &tm_k, &full[stage], h * 64, cur.g, in_blk, pb);
-            tma_load_4d(kdst + kKBytes + h * kHalfBytes, &tm_v, &full[stage], h * 64, cur.g,
-                        in_blk, pb);
+            for (int h = 0; h < kHalves; ++h) {
+              tma_load_4d(kdst + h * kHalfBytes, &tm_k, &full[stage], h * 64, cur.g, in_blk, pb);
+              tma_load_4d(kdst + kKBytes + h * kHalfBytes, &tm_v, &full[stage], h * 64, cur.g,
+                          in_blk, pb);
+            }
           }
         }
       }
@@ -562,11 +770,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t phase = (it / kStages) & 1;
     bool ok = !*abort_flag && mbar_wait_bounded(&full[stage], phase, p.err_flag);
     if (!ok) *abort_flag = 1;
-    const int valid = min(16, lens[cur.b] - cur.j * kTile - warp * 16);
-    if (ok && valid > 0) {
+    const int Lc = lens[cur.b];
+    const int row0 = (first_tile(Lc, p.window) + cur.j) * kTile + warp * 16;
+    const int valid = min(16, Lc - row0);                     // rows [vlo, valid) of the
+    const int vlo = max(0, band_lo(Lc, p.window) - row0);     // warp's 16 are attended
+    if (ok && valid > vlo) {
       const uint32_t kb = sbase + stage * L.stage;
-      attend_16<T, D>(kb, kb + kKBytes, warp, lane, valid, p.scale_log2, kb + 2 * kKBytes,
-                      L.q_half, G, o, m, l);
+      if constexpr (kI8)
+        attend_16_i8<T, D>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
+                           p.log2_box, warp, lane, vlo, valid, p.scale_log2, kb + L.qoff,
+                           L.q_half, G, sbase + L.vstg + warp * 16 * D * 2, o, m, l);
+      else
+        attend_16<T, D>(kb, kb + kKBytes, warp, lane, vlo, valid, p.scale_log2, kb + L.qoff,
+                        L.q_half, G, o, m, l);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -612,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kI8>
 struct DecodeKernel {
   // Resident CTAs per SM for a launch with `smem` bytes of dynamic shared
   // memory (cached per device and size; also sets the kernel's smem limit).
@@ -624,35 +840,66 @@ struct DecodeKernel {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find({dev, smem});
     if (it != cache.end()) return it->second;
-    cudaFuncSetAttribute(paged_decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Layout<D>(kMaxBatch, 16).total);
+    cudaFuncSetAttribute(paged_decode_kernel<T, D, kI8>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Layout<D, kI8>(kMaxBatch, 16).total);
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<T, D>, kThreads,
-                                                      smem) != cudaSuccess || occ < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<T, D, kI8>,
+                                                      kThreads, smem) != cudaSuccess ||
+        occ < 1)
       occ = 1;
     cache[{dev, smem}] = occ;
     return occ;
   }
 };
 
-template <typename T, int D>
+template <typename T, int D, bool kI8>
 kvc_status run_decode(const DecodeArgs& a) {
   const int G = a.num_q_heads / a.num_kv_heads;
-  const size_t smem = Layout<D>(a.batch, G).total;
-  const int occ = DecodeKernel<T, D>::occupancy(smem);  // also sets the smem limit
+  const size_t smem = Layout<D, kI8>(a.batch, G).total;
+  const int occ = DecodeKernel<T, D, kI8>::occupancy(smem);  // also sets the smem limit
   const int P = a.num_ctas > 0 ? a.num_ctas : device_sm_count() * occ;
   if (a.workspace_bytes < paged_decode_workspace_bytes(G, D, P) || a.workspace == nullptr)
     return KVC_ERR_WORKSPACE;
 
-  CUtensorMap tk, tv;
   const int box_tokens = a.block_size < kTile ? a.block_size : kTile;
+  const uint64_t elt = kI8 ? 1 : 2;
   const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_kv_heads),
                             static_cast<uint64_t>(a.block_size),
                             static_cast<uint64_t>(a.num_blocks)};
-  const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2,
-                               static_cast<uint64_t>(a.num_kv_heads) * D * 2,
-                               static_cast<uint64_t>(a.block_size) * a.num_kv_heads * D * 2};
-  const uint32_t box[4] = {64, 1, static_cast<uint32_t>(box_tokens), 1};
+  const uint64_t strides[3] = {static_cast<uint64_t>(D) * elt,
+                               static_cast<uint64_t>(a.num_kv_heads) * D * elt,
+                               static_cast<uint64_t>(a.block_size) * a.num_kv_heads * D * elt};
+  // 16-bit cache: boxes of one 64-element (128-byte) half of box_tokens rows;
+  // INT8 cache: boxes of box_tokens whole 128-byte code rows.
+  const uint32_t box[4] = {kI8 ? static_cast<uint32_t>(D) : 64u, 1,
+                           static_cast<uint32_t>(box_tokens), 1};
+  const CUtensorMapDataType cache_type =
+      kI8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+          : (a.dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  CUtensorMap tk, tv, tks, tvs;
+  if (!encode_tmap(&tk, cache_type, 4, a.key_cache, dims, strides, box, true) ||
+      !encode_tmap(&tv, cache_type, 4, a.value_cache, dims, strides, box, true))
+    return KVC_ERR_CUDA;
+  if constexpr (kI8) {
+    // Scales [num_blocks, Hkv, block_size] fp32: a box = one head's scales of
+    // the box_tokens tokens of one block.
+    const uint64_t sdims[3] = {static_cast<uint64_t>(a.block_size),
+                               static_cast<uint64_t>(a.num_kv_heads),
+                               static_cast<uint64_t>(a.num_blocks)};
+    const uint64_t sstrides[2] = {static_cast<uint64_t>(a.block_size) * 4,
+                                  static_cast<uint64_t>(a.num_kv_heads) * a.block_size * 4};
+    const uint32_t sbox[3] = {static_cast<uint32_t>(box_tokens), 1, 1};
+    if (!encode_tmap(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.key_scales, sdims, sstrides,
+                     sbox, false) ||
+        !encode_tmap(&tvs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.value_scales, sdims, sstrides,
+                     sbox, false))
+      return KVC_ERR_CUDA;
+  } else {
+    tks = tk;  // not read
+    tvs = tv;
+  }
   // Query [B, Hq, D]: one box = the G rows of a query group, 64 elements wide.
   CUtensorMap tq;
   const uint64_t qdims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_q_heads),
@@ -660,10 +907,7 @@ kvc_status run_decode(const DecodeArgs& a) {
   const uint64_t qstrides[2] = {static_cast<uint64_t>(D) * 2,
                                 static_cast<uint64_t>(a.num_q_heads) * D * 2};
   const uint32_t qbox[3] = {64, static_cast<uint32_t>(G), 1};
-  if (!encode_tmap_16bit(&tk, a.dtype, 4, a.key_cache, dims, strides, box, true) ||
-      !encode_tmap_16bit(&tv, a.dtype, 4, a.value_cache, dims, strides, box, true) ||
-      !encode_tmap_16bit(&tq, a.dtype, 3, a.q, qdims, qstrides, qbox, true))
-    return KVC_ERR_CUDA;
+  if (!encode_tmap_16bit(&tq, a.dtype, 3, a.q, qdims, qstrides, qbox, true)) return KVC_ERR_CUDA;
 
   DecodeParams p;
   p.q = a.q;
@@ -689,10 +933,30 @@ kvc_status run_decode(const DecodeArgs& a) {
   p.max_blocks = a.max_blocks_per_seq;
   p.num_blocks = a.num_blocks;
   p.box_tokens = box_tokens;
+  p.log2_box = ilog2(box_tokens);
+  p.window = a.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
 
-  paged_decode_kernel<T, D><<<P, kThreads, smem, a.stream>>>(tk, tv, tq, p);
+  paged_decode_kernel<T, D, kI8><<<P, kThreads, smem, a.stream>>>(tk, tv, tq, tks, tvs, p);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+template <bool kI8>
+int num_ctas_for(int group, int head_dim, kvc_dtype dtype) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  // The smallest batch needs the least shared memory, hence the most CTAs.
+  if (head_dim == 64 && !kI8) {
+    const size_t smem = Layout<64, false>(1, group).total;
+    return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 64, false>::occupancy(smem)
+                                    : DecodeKernel<__half, 64, false>::occupancy(smem));
+  }
+  if (head_dim == 128) {
+    const size_t smem = Layout<128, kI8>(1, group).total;
+    return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 128, kI8>::occupancy(smem)
+                                    : DecodeKernel<__half, 128, kI8>::occupancy(smem));
+  }
+  return 0;
 }
 
 }  // namespace
@@ -701,29 +965,24 @@ size_t paged_decode_workspace_bytes(int group, int head_dim, int ctas) {
   return counter_bytes(ctas) + static_cast<size_t>(ctas) * 2 * group * (head_dim + 2) * sizeof(float);
 }
 
-int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas) {
+int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas, bool int8) {
   if (num_ctas > 0) return num_ctas;
-  const int sms = device_sm_count();
-  if (sms <= 0) return 0;
-  // The smallest batch needs the least shared memory, hence the most CTAs.
-  if (head_dim == 64) {
-    const size_t smem = Layout<64>(1, group).total;
-    return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 64>::occupancy(smem)
-                                    : DecodeKernel<__half, 64>::occupancy(smem));
-  }
-  if (head_dim == 128) {
-    const size_t smem = Layout<128>(1, group).total;
-    return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 128>::occupancy(smem)
-                                    : DecodeKernel<__half, 128>::occupancy(smem));
-  }
-  return 0;
+  return int8 ? num_ctas_for<true>(group, head_dim, dtype)
+              : num_ctas_for<false>(group, head_dim, dtype);
 }
 
 kvc_status launch_paged_decode(const DecodeArgs& a) {
+  if (a.key_scales != nullptr) {  // INT8 cache (head_dim 128, plain decode)
+    if (a.head_dim != 128 || a.new_key != nullptr) return KVC_ERR_UNSUPPORTED;
+    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 128, true>(a)
+                               : run_decode<__half, 128, true>(a);
+  }
   if (a.head_dim == 64)
-    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 64>(a) : run_decode<__half, 64>(a);
+    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 64, false>(a)
+                               : run_decode<__half, 64, false>(a);
   if (a.head_dim == 128)
-    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 128>(a) : run_decode<__half, 128>(a);
+    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 128, false>(a)
+                               : run_decode<__half, 128, false>(a);
   return KVC_ERR_UNSUPPORTED;
 }
 

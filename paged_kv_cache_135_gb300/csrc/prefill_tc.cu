@@ -55,8 +55,14 @@ struct TcPrefillParams {
   uint32_t* err_flag;
   int num_seqs, num_q_heads, group;
   int block_size, log2_bs, max_blocks, num_blocks, box_tokens;
+  int window;  // band: a query at position p sees p - window + 1 .. p (0: all of 0 .. p)
   float scale_log2;
 };
+
+// First key position of the band of a query at position `pos` (0 without a band).
+__device__ __forceinline__ int band_start(int pos, int window) {
+  return window > 0 && pos >= window ? pos - window + 1 : 0;
+}
 
 template <int D>
 struct TcLayout {
@@ -129,7 +135,8 @@ __device__ __forceinline__ void tc_producer(const TcPrefillParams& p, const CUte
                                             const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                             uint8_t* smem, uint64_t* bars,
                                             volatile int* abort_flag, int s, int h, int g,
-                                            int tok0, int kv_len, int n_tiles, int lane) {
+                                            int tok0, int kv_len, int j0, int n_tiles, int band0,
+                                            int lane) {
   using L = TcLayout<D>;
   if (lane == 0) {
     mbar_arrive_expect_tx(&bars[kQFull], L::kHalves * kChunk);
@@ -141,12 +148,15 @@ __device__ __forceinline__ void tc_producer(const TcPrefillParams& p, const CUte
   const uint32_t box_bytes = static_cast<uint32_t>(p.box_tokens) * 128u;
   for (int j = 0; j < n_tiles; ++j) {
     const int stage = j & 1;
-    const int tok = j * kBN + lane * p.box_tokens;
+    const int tok = (j0 + j) * kBN + lane * p.box_tokens;
+    // A box wholly before the band of the tile's first query row is not
+    // fetched (its rows are masked for every row and zeroed in V).
+    const bool wanted = lane < nsub && tok < kv_len && tok + p.box_tokens > band0;
     int pb = -1;
-    if (lane < nsub && tok < kv_len)
+    if (wanted)
       pb = __ldg(&p.block_table[static_cast<long long>(s) * p.max_blocks + (tok >> p.log2_bs)]);
     bool valid = false;
-    if (lane < nsub && tok < kv_len) {
+    if (wanted) {
       if (pb < 0 || pb >= p.num_blocks) set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
       else valid = true;
     }
@@ -240,8 +250,8 @@ namespace {
 template <typename T, int D>
 __device__ __forceinline__ void tc_softmax(const TcPrefillParams& p, uint8_t* smem, uint64_t* bars,
                                            volatile int* abort_flag, uint32_t tmem, int t,
-                                           int n_tiles, int q0, int ctx, int kv_len, int q_rows,
-                                           int tok0, int h) {
+                                           int j0, int n_tiles, int q0, int ctx, int kv_len,
+                                           int q_rows, int tok0, int h) {
   using L = TcLayout<D>;
   const int warp = t >> 5, lane = t & 31;
   const int quad = warp & 3, half = warp >> 2;
@@ -262,16 +272,18 @@ __device__ __forceinline__ void tc_softmax(const TcPrefillParams& p, uint8_t* sm
     tc_fence_before();
     mbar_arrive(&bars[kSFree0 + stage]);
 
-    // causal + length mask (only tiles reaching past this row need it)
-    const int kv0 = j * kBN + half * 64;
-    const bool need_mask = kv0 + 63 > pos || kv0 + 64 > kv_len;
+    // band + causal + length mask (only tiles reaching past this row, or
+    // starting before its band, need it)
+    const int kv0 = (j0 + j) * kBN + half * 64;
+    const int lo = band_start(pos, p.window);
+    const bool need_mask = kv0 + 63 > pos || kv0 + 64 > kv_len || kv0 < lo;
     float mx8[8];
 #pragma unroll
     for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
 #pragma unroll
     for (int k = 0; k < 64; ++k) {
       float v = s[k] * p.scale_log2;
-      if (need_mask && (kv0 + k > pos || kv0 + k >= kv_len)) v = -INFINITY;
+      if (need_mask && (kv0 + k > pos || kv0 + k >= kv_len || kv0 + k < lo)) v = -INFINITY;
       s[k] = v;
       mx8[k & 7] = fmaxf(mx8[k & 7], v);
     }
@@ -291,11 +303,14 @@ __device__ __forceinline__ void tc_softmax(const TcPrefillParams& p, uint8_t* sm
       m_used = mx;
       rescale = true;
     }
+    // A row that has seen no visible key yet (possible inside a band) keeps
+    // m_used = -inf and all its scores at -inf: its p are 0, not NaN.
+    const float mu = m_used == -INFINITY ? 0.f : m_used;
     uint32_t pk[32];
     float ps[4] = {0.f, 0.f, 0.f, 0.f}, ra, rb;
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-      pk[k] = Pack<T>::run(fast_exp2(s[2 * k] - m_used), fast_exp2(s[2 * k + 1] - m_used), ra, rb);
+      pk[k] = Pack<T>::run(fast_exp2(s[2 * k] - mu), fast_exp2(s[2 * k + 1] - mu), ra, rb);
       ps[k & 3] += ra + rb;
     }
     l = l * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
@@ -323,15 +338,19 @@ __device__ __forceinline__ void tc_softmax(const TcPrefillParams& p, uint8_t* sm
     for (int ch = 0; ch < 8; ++ch)
       *reinterpret_cast<uint4*>(pc + swz128(row, ch)) =
           make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-    // Value rows past the cached tokens are zeroed so stale cache contents
-    // cannot reach P V.
-    const int valid = kv_len - j * kBN;
-    if (valid < kBN) {
+    // Value rows past the cached tokens, and rows before the band of the
+    // tile's first query row (seen by no row), are zeroed so stale cache
+    // contents cannot reach P V.
+    const int valid = kv_len - (j0 + j) * kBN;
+    const int zlo = band_start(ctx + q0, p.window) - (j0 + j) * kBN;
+    if (valid < kBN || zlo > 0) {
       wait_tc(&bars[kVFull0 + stage], (j >> 1) & 1, abort_flag, p.err_flag);
       uint8_t* vst = smem + L::kV + stage * L::kStageBytes;
-      const int n16 = (kBN - valid) * L::kHalves * 8;
+      const int top = valid < kBN ? kBN - valid : 0, bottom = zlo > 0 ? min(zlo, kBN) : 0;
+      const int n16 = (top + bottom) * L::kHalves * 8;
       for (int e = t; e < n16; e += kSmxThreads) {
-        const int r = valid + e / (L::kHalves * 8), c = (e / 8) % L::kHalves, q = e % 8;
+        const int i = e / (L::kHalves * 8), c = (e / 8) % L::kHalves, q = e % 8;
+        const int r = i < bottom ? i : valid + (i - bottom);
         *reinterpret_cast<uint4*>(vst + c * kChunk + r * 128 + q * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
@@ -428,7 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) set_flag(p.err_flag, KVC_FLAG_LEN_RANGE);
     return;
   }
-  const int n_tiles = (ctx + q0 + q_rows - 1) / kBN + 1;
+  // Key tiles j0 .. j0 + n_tiles - 1: from the tile holding the band start of
+  // the first query row to the tile holding the last row.
+  const int band0 = band_start(ctx + q0, p.window);
+  const int j0 = band0 / kBN;
+  const int n_tiles = (ctx + q0 + q_rows - 1) / kBN + 1 - j0;
   const int tok0 = p.cu_seqlens[s] + q0;
 
   uint32_t leader = 0;  // the MMA warp's issuing lane
@@ -442,8 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tslot;
 
   if (warp < kProducerWarp) {
-    tc_softmax<T, D>(p, smem, bars, abort_flag, tmem, tid, n_tiles, q0, ctx, kv_len, q_rows, tok0,
-                     h);
+    tc_softmax<T, D>(p, smem, bars, abort_flag, tmem, tid, j0, n_tiles, q0, ctx, kv_len, q_rows,
+                     tok0, h);
   } else if (warp == kProducerWarp) {
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -451,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_v);
     }
     tc_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, s, h, h / p.group, tok0, kv_len,
-                   n_tiles, lane);
+                   j0, n_tiles, band0, lane);
   } else {
     tc_mma<D, kBf16>(p, smem, bars, abort_flag, tmem, n_tiles, leader);
   }
@@ -509,6 +532,7 @@ kvc_status run_prefill_tc(const PrefillArgs& a) {
   p.max_blocks = a.max_blocks_per_seq;
   p.num_blocks = a.num_blocks;
   p.box_tokens = box_tokens;
+  p.window = a.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   // Upper bound of query tiles: sum ceil(L_s / BM) <= T / BM + S.
   const long long grid = (static_cast<long long>(a.num_tokens) / kBM + a.num_seqs) * a.num_q_heads;

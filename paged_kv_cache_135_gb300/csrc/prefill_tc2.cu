@@ -74,8 +74,14 @@ struct Tc2Params {
   uint32_t* err_flag;
   int num_seqs, num_q_heads, group;
   int block_size, log2_bs, max_blocks, num_blocks, box_tokens;
+  int window;  // band: a query at position p sees p - window + 1 .. p (0: all of 0 .. p)
   float scale_log2;
 };
+
+// First key position of the band of a query at position `pos` (0 without a band).
+__device__ __forceinline__ int band_start(int pos, int window) {
+  return window > 0 && pos >= window ? pos - window + 1 : 0;
+}
 
 template <int D>
 struct Tc2Layout {
@@ -151,8 +157,8 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint8_t* smem, uint64_t* bars,
                                              volatile int* abort_flag, int s, int h0, int g,
-                                             int tok0, int kv_len, int n_tiles, int gj0, int kit,
-                                             int lane) {
+                                             int tok0, int kv_len, int j0, int n_tiles,
+                                             int band0, int gj0, int kit, int lane) {
   using L = Tc2Layout<D>;
   // This item's query tiles replace the previous item's once its last S is
   // done (q_empty).
@@ -171,12 +177,15 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
   for (int j = 0; j < n_tiles; ++j) {
     const int gj = gj0 + j;  // the CTA's running tile count sets stage and phase
     const int stage = gj & 1;
-    const int tok = j * kBN + lane * p.box_tokens;
+    const int tok = (j0 + j) * kBN + lane * p.box_tokens;
+    // A box wholly before the band of the tile's first query row is not
+    // fetched (its rows are masked for every row and zeroed in V).
+    const bool wanted = lane < nsub && tok < kv_len && tok + p.box_tokens > band0;
     int pb = -1;
-    if (lane < nsub && tok < kv_len)
+    if (wanted)
       pb = __ldg(&p.block_table[static_cast<long long>(s) * p.max_blocks + (tok >> p.log2_bs)]);
     bool valid = false;
-    if (lane < nsub && tok < kv_len) {
+    if (wanted) {
       if (pb < 0 || pb >= p.num_blocks) set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
       else valid = true;
     }
@@ -309,8 +318,9 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
 template <typename T, int D>
 __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
                                             volatile int* abort_flag, uint32_t tmem, int x,
-                                            int row, int n_tiles, int q0, int ctx, int kv_len,
-                                            int q_rows, int tok0, int h, int gj0, int kit) {
+                                            int row, int j0, int n_tiles, int q0, int ctx,
+                                            int kv_len, int q_rows, int tok0, int h, int gj0,
+                                            int kit) {
   using L = Tc2Layout<D>;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(row & ~31) << 16);
   const int pos = ctx + q0 + row;
@@ -324,11 +334,13 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     // tensor memory and are read in halves of 64 columns to keep register
     // pressure down: half 1 first (for its max only), then half 0, which is
     // kept in registers for its exponentials, so the first half of P is
-    // released after two rounds of loads, not three.  Causal + length mask:
-    // token k of the tile is visible iff k < lim; only tiles that reach past
-    // this row take the masked path.
-    const int kv0 = j * kBN;
+    // released after two rounds of loads, not three.  Band + causal + length
+    // mask: token k of the tile is visible iff lo <= k < lim; only tiles that
+    // reach past this row, or start before its band, take the masked path.
+    const int kv0 = (j0 + j) * kBN;
     const int lim = min(pos + 1, kv_len) - kv0;
+    const int lo = band_start(pos, p.window) - kv0;
+    const bool masked = lim < kBN || lo > 0;
     float mx8[8];
 #pragma unroll
     for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
@@ -339,9 +351,12 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
       for (int c = 0; c < kBN / 32; ++c)
         tmem_ld16(lane_base + tmem_s(x) + hf * (kBN / 2) + c * 16, s + c * 16);
       tmem_wait_ld();
-      if (lim < kBN) {
+      if (masked) {
 #pragma unroll
-        for (int k = 0; k < kBN / 2; ++k) s[k] = hf * (kBN / 2) + k < lim ? s[k] : -INFINITY;
+        for (int k = 0; k < kBN / 2; ++k) {
+          const int kk = hf * (kBN / 2) + k;
+          s[k] = kk >= lo && kk < lim ? s[k] : -INFINITY;
+        }
       }
 #pragma unroll
       for (int k = 0; k < kBN / 2; k += 2) mx8[(k / 2) & 7] = fmax3(mx8[(k / 2) & 7], s[k], s[k + 1]);
@@ -377,20 +392,25 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) tmem_ld16(lane_base + tmem_s(x) + c * 16, s + c * 16);
       tmem_wait_ld();
-      if (lim < kBN) {
+      if (masked) {
 #pragma unroll
-        for (int k = 0; k < kBN / 2; ++k) s[k] = k < lim ? s[k] : -INFINITY;
+        for (int k = 0; k < kBN / 2; ++k) s[k] = k >= lo && k < lim ? s[k] : -INFINITY;
       }
     }
-    // Value rows past the cached tokens are zeroed (by both heads, before
-    // either head's P V of the tile) so stale contents cannot reach P V.
-    const int valid = kv_len - j * kBN;
-    if (valid < kBN) {
+    // Value rows past the cached tokens, and rows before the band of the
+    // item's first query row (seen by no row of the item), are zeroed (by
+    // both heads, before either head's P V of the tile) so stale contents
+    // cannot reach P V.
+    const int valid = kv_len - kv0;
+    const int zlo = band_start(ctx + q0, p.window) - kv0;
+    if (valid < kBN || zlo > 0) {
       wait_t2(&bars[kVFull0 + (gj & 1)], (gj >> 1) & 1, abort_flag, p.err_flag);
       uint8_t* vst = smem + L::kV + (gj & 1) * L::kStageBytes;
-      const int n16 = (kBN - valid) * L::kHalves * 8;
+      const int top = valid < kBN ? kBN - valid : 0, bottom = zlo > 0 ? min(zlo, kBN) : 0;
+      const int n16 = (top + bottom) * L::kHalves * 8;
       for (int e = row; e < n16; e += kHeadThreads) {
-        const int r = valid + e / (L::kHalves * 8), c = (e / 8) % L::kHalves, q = e % 8;
+        const int i = e / (L::kHalves * 8), c = (e / 8) % L::kHalves, q = e % 8;
+        const int r = i < bottom ? i : valid + (i - bottom);
         *reinterpret_cast<uint4*>(vst + c * kChunk + r * 128 + q * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
@@ -414,9 +434,12 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
         for (int c = 0; c < kBN / 32; ++c)
           tmem_ld16(lane_base + tmem_s(x) + (kBN / 2) + c * 16, s + c * 16);
         tmem_wait_ld();
-        if (lim < kBN) {
+        if (masked) {
 #pragma unroll
-          for (int k = 0; k < kBN / 2; ++k) s[k] = (kBN / 2) + k < lim ? s[k] : -INFINITY;
+          for (int k = 0; k < kBN / 2; ++k) {
+            const int kk = (kBN / 2) + k;
+            s[k] = kk >= lo && kk < lim ? s[k] : -INFINITY;
+          }
         }
       }
       uint32_t pk[kBN / 4];
@@ -482,9 +505,16 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
 // One work item: (sequence, 128-query tile, pair of query heads); every
 // lane of the calling warp gets the same result.
 struct Tc2Item {
-  int s, h0, q0, q_rows, ctx, kv_len, n_tiles, tok0;
+  int s, h0, q0, q_rows, ctx, kv_len, j0, n_tiles, tok0;
   bool ok;  // kv_len fits the block table
 };
+
+// Key tiles j0 .. j0 + n_tiles - 1 of a query tile: from the tile holding
+// the band start of its first row to the tile holding its last row.
+__device__ __forceinline__ void tc2_tiles(const Tc2Params& p, Tc2Item& it) {
+  it.j0 = band_start(it.ctx + it.q0, p.window) / kBN;
+  it.n_tiles = (it.ctx + it.q0 + it.q_rows - 1) / kBN + 1 - it.j0;
+}
 __device__ __forceinline__ bool tc2_item(const Tc2Params& p, int w, int lane, Tc2Item& it) {
   const int pairs = p.num_q_heads / 2;
   int s = 0, tile = 0, ctx = 0, len = 0;
@@ -496,7 +526,7 @@ __device__ __forceinline__ bool tc2_item(const Tc2Params& p, int w, int lane, Tc
   it.ctx = ctx;
   it.kv_len = ctx + len;
   it.ok = it.kv_len <= p.max_blocks * p.block_size;
-  it.n_tiles = (ctx + it.q0 + it.q_rows - 1) / kBN + 1;
+  tc2_tiles(p, it);
   it.tok0 = p.cu_seqlens[s] + it.q0;
   return true;
 }
@@ -512,7 +542,7 @@ __device__ __forceinline__ void tc2_item_at(const Tc2Params& p, int s, int t, in
   it.ctx = p.context_lens ? p.context_lens[s] : 0;
   it.kv_len = it.ctx + len;
   it.ok = it.kv_len <= p.max_blocks * p.block_size;
-  it.n_tiles = (it.ctx + it.q0 + it.q_rows - 1) / kBN + 1;
+  tc2_tiles(p, it);
   it.tok0 = p.cu_seqlens[s] + it.q0;
 }
 
@@ -553,7 +583,8 @@ __device__ int tc2_build_schedule(const Tc2Params& p, uint8_t* smem, int tid, in
   for (int i = tid; i < kMaxN; i += kThreads) hist[i] = 0;
   if (tid == 0) {
     misc[0] = 0;
-    misc[1] = pairs > 255 ? 1 : 0;
+    // The closed forms below assume causal weights; a band walks unsorted.
+    misc[1] = pairs > 255 || p.window > 0 ? 1 : 0;
   }
   __syncthreads();
   for (int s = tid; s < p.num_seqs; s += kThreads) {
@@ -696,8 +727,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       Tc2Item it;
       if (!next_item(k, it)) break;
       if (!it.ok) continue;
-      tc2_softmax<T, D>(p, smem, bars, abort_flag, tmem, x, tid % kHeadThreads, it.n_tiles, it.q0,
-                        it.ctx, it.kv_len, it.q_rows, it.tok0, it.h0 + x, gj0, ni);
+      tc2_softmax<T, D>(p, smem, bars, abort_flag, tmem, x, tid % kHeadThreads, it.j0,
+                        it.n_tiles, it.q0, it.ctx, it.kv_len, it.q_rows, it.tok0, it.h0 + x,
+                        gj0, ni);
       gj0 += it.n_tiles;
       ++ni;
       if (*abort_flag) break;
@@ -716,7 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       tc2_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, it.s, it.h0,
-                      it.h0 / p.group, it.tok0, it.kv_len, it.n_tiles, gj0, ni, lane);
+                      it.h0 / p.group, it.tok0, it.kv_len, it.j0, it.n_tiles,
+                      band_start(it.ctx + it.q0, p.window), gj0, ni, lane);
       gj0 += it.n_tiles;
       ++ni;
       if (*abort_flag) break;
@@ -790,6 +823,7 @@ kvc_status run_prefill_tc2(const PrefillArgs& a) {
   p.max_blocks = a.max_blocks_per_seq;
   p.num_blocks = a.num_blocks;
   p.box_tokens = box_tokens;
+  p.window = a.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   // Work items: (query tile, head pair); query tiles <= T / BM + S.  One
   // persistent CTA per SM, or fewer when there are fewer items.
