@@ -22,6 +22,9 @@ definitions on the source pages, with no blocking, fusion or reordering:
   and ai6s.net article 3 (4) (keep the most recent N tokens).
 * INT8 KV cache -- KVCache skill 4 (quantized KV: antiquant / dequant scales)
   and its INT8 KVCache Quantization note; ai6s.net article 3 (FP16 -> INT8).
+* Fused RMSNorm + RoPE + cache write -- KVCache skill Mode 2 step 3 and
+  Appendix D (the fused write operator, driven by slot_mapping), Mode 3 (the
+  latent cache split into cache_nope and cache_rope).
 
 Readings where the pages are silent:
   - q head h uses kv head h // (Hq / Hkv) (contiguous GQA groups);
@@ -31,7 +34,10 @@ Readings where the pages are silent:
   - a negative slot in slot_mapping means "do not write";
   - a band of `window` positions ends at the query's own position;
   - an INT8 cache row carries one fp32 scale per (token, kv head), its codes
-    decided in fp32 (quantize_rows_int8).
+    decided in fp32 (quantize_rows_int8);
+  - the fused write normalises the first d_norm channels of a row (RMS with a
+    weight gamma and eps) and rotates the last d_rope channels by RoPE in its
+    original pairwise form, theta_i = base^(-2i/d_rope).
 
 All floating-point work is float64.  Inputs given as fp16/bf16 values must be
 converted to float64 by the caller (the conversion is exact).
@@ -425,6 +431,73 @@ def paged_decode_int8(q, key_codes, value_codes, key_scales, value_scales, block
     vs = np.swapaxes(np.asarray(value_scales), 1, 2)
     return paged_decode(q, dequantize_rows_int8(key_codes, ks),
                         dequantize_rows_int8(value_codes, vs), block_table, seq_lens, scale)
+
+
+# ---------------------------------------------------------------------------
+# Fused RMSNorm + RoPE + cache write (KVCache skill Mode 2 step 3, the fused
+# write operator named beside scatter_update_, and Appendix D: "Fused
+# RMSNorm+RoPE+Cache write", driven by slot_mapping; Mode 3: the latent cache
+# is stored as a non-positional part, cache_nope, and a positional part,
+# cache_rope; 3.5: kv_len drives the RoPE positions; hotelren.com notes 3.1:
+# packed position ids restart at 0 for every sequence)
+# ---------------------------------------------------------------------------
+
+
+def rms_norm(x, gamma, eps: float):
+    """x / sqrt(mean(x^2) + eps) * gamma over the last axis, float64.
+
+    The pages name the normalisation but not its form; this is the usual
+    root-mean-square normalisation with a learned per-channel weight gamma.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(gamma, dtype=np.float64)
+
+
+def rope_angles(pos: int, rope_dim: int, base: float):
+    """Rotation angles pos * theta_i, theta_i = base^(-2i / rope_dim), i < rope_dim / 2.
+
+    The pages name RoPE but fix no convention; this is the rotary embedding
+    in its original form (frequencies base^(-2i/d)).
+    """
+    i = np.arange(rope_dim // 2, dtype=np.float64)
+    return float(pos) * np.power(float(base), -2.0 * i / rope_dim)
+
+
+def rope_rotate(x, pos: int, base: float):
+    """Rotate each consecutive pair (x[2i], x[2i+1]) of the last axis by pos * theta_i:
+    (a, b) -> (a cos - b sin, a sin + b cos), float64."""
+    x = np.asarray(x, dtype=np.float64)
+    ang = rope_angles(pos, x.shape[-1], base)
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+def rmsnorm_rope_cache(kv, gamma, eps: float, base: float, positions, slots, cache_norm,
+                       cache_rope):
+    """The fused cache write: row kv[t, h] = [norm part (d_norm) | rope part (d_rope)];
+    the norm part is RMS-normalised with gamma, the rope part rotated at positions[t],
+    and the two written to cache_norm / cache_rope at slots[t] (negative: skipped).
+
+    kv [T, H, d_norm + d_rope]; caches [num_blocks, block_size, H, d_*].  For MLA the
+    row is the latent [compressed kv (512) | key rope part (64)], H = 1, and the
+    caches are cache_nope / cache_rope.  Returns float64 copies of both caches.
+    """
+    kv = np.asarray(kv, dtype=np.float64)
+    dn = np.asarray(cache_norm).shape[-1]
+    cn = np.array(cache_norm, dtype=np.float64, copy=True)
+    cr = np.array(cache_rope, dtype=np.float64, copy=True)
+    bs = cn.shape[1]
+    for t, slot in enumerate(np.asarray(slots).tolist()):
+        if slot < 0:
+            continue
+        cn[slot // bs, slot % bs] = rms_norm(kv[t, :, :dn], gamma, eps)
+        cr[slot // bs, slot % bs] = rope_rotate(kv[t, :, dn:], int(positions[t]), base)
+    return cn, cr
 
 
 def mla_paged_decode(q_nope, q_rope, cache_nope, cache_rope, block_table, seq_lens,
