@@ -163,6 +163,49 @@ kvc_status kvc_copy_blocks(void* key_cache, void* value_cache, const int32_t* sr
                            kvc_stream_t stream);
 
 /*
+ * kvc_rope_cos_sin_table -- the angle table kvc_rmsnorm_rope_cache reads.
+ *   cos_sin[p][i] = cos(p * theta_i), cos_sin[p][rope_dim/2 + i] = sin(p * theta_i),
+ *   theta_i = base^(-2i / rope_dim), 0 <= p < max_position, 0 <= i < rope_dim / 2.
+ * Computed in fp64 on the device and stored as fp32.  cos_sin: device float
+ * [max_position, rope_dim], caller-owned; rope_dim even, base > 0.  Built once.
+ */
+kvc_status kvc_rope_cos_sin_table(float* cos_sin, int max_position, int rope_dim, float base,
+                                  kvc_stream_t stream);
+
+/*
+ * kvc_rmsnorm_rope_cache -- fused RMSNorm + RoPE + paged cache write.
+ * [SKILL] Mode 2 step 3 and Appendix D (a fused write operator, "RMSNorm +
+ * RoPE + Cache write", driven by slot_mapping, beside the plain write), Mode 3
+ * (the MLA latent stored as a non-positional cache_nope and a positional
+ * cache_rope), 3.5 (kv_len drives the RoPE positions); [NOTES] 3.1 (packed
+ * position ids restart at 0 per sequence).  The pages fix neither the norm's
+ * form nor the RoPE convention; this library's reading:
+ *
+ *   row = kv[t][h] = [x (d_norm) | y (d_rope)],  p = positions[t]
+ *   cache_norm[slot / bs][slot % bs][h] = x / sqrt(mean(x^2) + eps) * gamma
+ *   cache_rope[slot / bs][slot % bs][h][2i, 2i+1] = rotation of (y[2i], y[2i+1])
+ *       by the angle p * theta_i, read from cos_sin (kvc_rope_cos_sin_table)
+ *
+ * kv: [num_tokens, num_heads, d_norm + d_rope] (for MLA: the latent row
+ * [compressed kv 512 | key rope 64], num_heads 1); gamma: [d_norm] of the
+ * same dtype; cos_sin: fp32 [max_position, d_rope]; positions: int32
+ * [num_tokens] (decode: seq_lens - 1; packed prefill: context + offset in the
+ * sequence); slot_mapping: int32 [num_tokens]; cache_norm: [num_blocks,
+ * block_size, num_heads, d_norm]; cache_rope: [num_blocks, block_size,
+ * num_heads, d_rope].  fp32 arithmetic, one rounding per stored element.
+ * d_norm and d_rope multiples of 8.  slot < 0 skips the token; a slot beyond
+ * the pool (KVC_FLAG_SLOT_RANGE) or a position outside [0, max_position)
+ * (KVC_FLAG_LEN_RANGE) skips it and sets the flag.
+ */
+kvc_status kvc_rmsnorm_rope_cache(const void* kv, const void* gamma, float eps,
+                                  const float* cos_sin, int max_position,
+                                  const int32_t* positions, const int32_t* slot_mapping,
+                                  void* cache_norm, void* cache_rope, int num_tokens,
+                                  int num_heads, int d_norm, int d_rope, int block_size,
+                                  int num_blocks, kvc_dtype dtype, uint32_t* err_flag,
+                                  kvc_stream_t stream);
+
+/*
  * Bytes of workspace kvc_paged_decode needs for this head shape when it runs
  * with `num_ctas` persistent CTAs (0 = the automatic choice for the current
  * device: SM count x resident CTAs per SM).  Independent of batch and lengths.

@@ -36,6 +36,9 @@ _SIGS = {
     "kvc_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "kvc_copy_blocks": (_I, [_P, _P, _P, _P, _I, ctypes.c_longlong, ctypes.c_longlong, _I, _P,
                              _P]),
+    "kvc_rope_cos_sin_table": (_I, [_P, _I, _I, _F, _P]),
+    "kvc_rmsnorm_rope_cache": (_I, [_P, _P, _F, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                    _I, _P, _P]),
     "kvc_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
     "kvc_mla_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
     "kvc_mla_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
@@ -190,6 +193,43 @@ def copy_blocks(key_cache: torch.Tensor, value_cache: Optional[torch.Tensor],
     _check("kvc_copy_blocks", lib().kvc_copy_blocks(
         key_cache.data_ptr(), _ptr(value_cache), src_blocks.data_ptr(), dst_blocks.data_ptr(),
         src_blocks.numel(), bk, bv, nb, _flag(err_flag), _stream()))
+
+
+def rope_cos_sin_table(max_position: int, rope_dim: int, base: float = 10000.0,
+                       device="cuda", out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """fp32 [max_position, rope_dim]: cos(p * theta_i) then sin(p * theta_i), theta_i =
+    base^(-2i/rope_dim); built on the device by the library."""
+    if out is None:
+        out = torch.empty(max_position, rope_dim, dtype=torch.float32, device=device)
+    _cuda("out", out, torch.float32)
+    _check("kvc_rope_cos_sin_table", lib().kvc_rope_cos_sin_table(
+        out.data_ptr(), max_position, rope_dim, float(base), _stream()))
+    return out
+
+
+def rmsnorm_rope_cache(kv: torch.Tensor, gamma: torch.Tensor, eps: float, cos_sin: torch.Tensor,
+                       positions: torch.Tensor, slot_mapping: torch.Tensor,
+                       cache_norm: torch.Tensor, cache_rope: torch.Tensor,
+                       err_flag: Optional[torch.Tensor] = None) -> None:
+    """Fused write of rows kv [T, H, d_norm + d_rope]: RMSNorm (gamma, eps) of the first
+    d_norm channels into cache_norm [NB, bs, H, d_norm], RoPE at positions[t] of the last
+    d_rope channels into cache_rope [NB, bs, H, d_rope], at slot_mapping[t]."""
+    _cuda("kv", kv)
+    _cuda("gamma", gamma, kv.dtype)
+    _cuda("cos_sin", cos_sin, torch.float32)
+    _cuda("positions", positions, torch.int32)
+    _cuda("slot_mapping", slot_mapping, torch.int32)
+    _cuda("cache_norm", cache_norm, kv.dtype)
+    _cuda("cache_rope", cache_rope, kv.dtype)
+    T, H, _ = kv.shape
+    NB, bs, _, dn = cache_norm.shape
+    dr = cache_rope.shape[-1]
+    if kv.shape[-1] != dn + dr or gamma.numel() != dn or cos_sin.shape[1] != dr:
+        raise ValueError("kv width must be d_norm + d_rope, gamma [d_norm], cos_sin [*, d_rope]")
+    _check("kvc_rmsnorm_rope_cache", lib().kvc_rmsnorm_rope_cache(
+        kv.data_ptr(), gamma.data_ptr(), float(eps), cos_sin.data_ptr(), cos_sin.shape[0],
+        positions.data_ptr(), slot_mapping.data_ptr(), cache_norm.data_ptr(),
+        cache_rope.data_ptr(), T, H, dn, dr, bs, NB, _DT[kv.dtype], _flag(err_flag), _stream()))
 
 
 def decode_workspace_size(num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -213,6 +213,39 @@ kvc_status kvc_copy_blocks(void* key_cache, void* value_cache, const int32_t* sr
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
+kvc_status kvc_rope_cos_sin_table(float* cos_sin, int max_position, int rope_dim, float base,
+                                  kvc_stream_t stream) {
+  if (max_position <= 0 || rope_dim <= 0 || rope_dim % 2 || !(base > 0.f) || !isfinite(base))
+    return KVC_ERR_INVALID_ARG;
+  if (!cos_sin) return KVC_ERR_INVALID_ARG;
+  return kvc::launch_rope_table(cos_sin, max_position, rope_dim, base,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_rmsnorm_rope_cache(const void* kv, const void* gamma, float eps,
+                                  const float* cos_sin, int max_position,
+                                  const int32_t* positions, const int32_t* slot_mapping,
+                                  void* cache_norm, void* cache_rope, int num_tokens,
+                                  int num_heads, int d_norm, int d_rope, int block_size,
+                                  int num_blocks, kvc_dtype dtype, uint32_t* err_flag,
+                                  kvc_stream_t stream) {
+  if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_heads <= 0 || d_norm <= 0 || d_rope <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_position <= 0 || !(eps >= 0.f) || !isfinite(eps))
+    return KVC_ERR_INVALID_ARG;
+  if (d_norm % 8 || d_rope % 8) return KVC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return KVC_OK;
+  if (!kv || !gamma || !cos_sin || !positions || !slot_mapping || !cache_norm || !cache_rope)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned16(kv) || !aligned16(gamma) || !aligned16(cache_norm) || !aligned16(cache_rope))
+    return KVC_ERR_INVALID_ARG;
+  return kvc::launch_rmsnorm_rope_cache(kv, gamma, eps, cos_sin, max_position, positions,
+                                        slot_mapping, cache_norm, cache_rope, num_tokens,
+                                        num_heads, d_norm, d_rope, block_size, num_blocks, dtype,
+                                        err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t kvc_paged_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
                                        int num_ctas) {
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;

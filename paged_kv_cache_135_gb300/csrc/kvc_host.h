@@ -56,6 +56,16 @@ kvc_status launch_reshape_and_cache_int8(const void* key, const void* value, voi
                                          int block_size, int num_blocks, kvc_dtype dtype,
                                          uint32_t* err_flag, cudaStream_t stream);
 
+kvc_status launch_rope_table(float* cos_sin, int max_position, int rope_dim, float base,
+                             cudaStream_t stream);
+kvc_status launch_rmsnorm_rope_cache(const void* kv, const void* gamma, float eps,
+                                     const float* cos_sin, int max_position,
+                                     const int32_t* positions, const int32_t* slot_mapping,
+                                     void* cache_norm, void* cache_rope, int num_tokens,
+                                     int num_heads, int d_norm, int d_rope, int block_size,
+                                     int num_blocks, kvc_dtype dtype, uint32_t* err_flag,
+                                     cudaStream_t stream);
+
 struct DecodeArgs {
   const void* q;
   const void* key_cache;
