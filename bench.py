@@ -22,7 +22,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -45,7 +44,11 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
 def peaks():
+    """(HBM GB/s, kind): the measured copy bandwidth, else the fallback figure."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
@@ -53,6 +56,17 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """(dense bf16 TFLOP/s burst, kind) for a kernel timed on its own."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def decode_bytes(seq_lens, Hq, Hkv, D, bs, elt=2):
@@ -100,18 +114,20 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(profile_md, digest):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the source."""
+TRAFFIC_RECORD = "traffic.json"
+
+
+def recorded_traffic(key, digest):
+    """DRAM bytes per launch recorded by ncu (profiles/traffic.json, entry `key`), if the
+    record was taken on this kernel source (same digest); else None."""
     try:
-        with open(os.path.join(ROOT, "profiles", profile_md)) as f:
-            text = f.read()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", TRAFFIC_RECORD)) as f:
+            rec = json.load(f).get(key)
+    except (OSError, ValueError):
         return None
-    m_d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
-    m_t = re.search(r"traffic_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
-    if not m_d or not m_t or m_d.group(1) != digest:
+    if not rec or rec.get("kernel_source_digest") != digest:
         return None
-    return float(m_t.group(1))
+    return float(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -255,6 +271,69 @@ def cpu_oracle_rate(case, budget_s=10.0):
     return done_bytes / t_total / 1e9, n_seq, B, t_total
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def cpu_oracle_rate_all_cores(case, budget_s=10.0):
+    """The oracle on every host core: one spawned worker process per core (single-threaded
+    BLAS each) evaluating whole sequences, inputs memory-mapped; passes over the workload's
+    sequences until about budget_s of wall time.  Returns (GB/s, evaluations, workers, s)."""
+    from oracle.pool import OraclePool
+    m = case.meta
+    bs, B = case.block_size, case.q.shape[0]
+    kb, vb, lens = [], [], []
+    for b in range(B):
+        L = int(case.seq_lens[b])
+        nblk = max(1, -(-L // bs))
+        ids = case.block_table[b, :nblk].long()
+        kb.append(case.key_cache[ids.to(case.key_cache.device)].view(torch.int16).cpu().numpy())
+        vb.append(case.value_cache[ids.to(case.value_cache.device)].view(torch.int16).cpu().numpy())
+        lens.append(L)
+    workers = os.cpu_count() or 1
+    pool = OraclePool(kb, vb, case.q.view(torch.int16).cpu().numpy(), lens, case.dtype, workers)
+    try:
+        pool.run(range(min(B, workers)), case.scale)          # workers up, pages mapped
+        per = [decode_bytes([L], m["num_q_heads"], m["num_kv_heads"], m["head_dim"], bs)
+               for L in lens]
+        done, t, passes = 0, 0.0, 0
+        while t < budget_s and passes < 1000:
+            t += pool.run(range(B), case.scale)
+            done += sum(per)
+            passes += 1
+    finally:
+        pool.close()
+    return done / t / 1e9, passes * B, workers, t
+
+
+def cpu_baseline(case):
+    """The oracle timed on this host: all cores (the reported value) and one core."""
+    gbs1, n1, B, t1 = cpu_oracle_rate(case)
+    gbs, n, workers, t = cpu_oracle_rate_all_cores(case)
+    return {"value": gbs, "unit": "GB/s", "cores": workers, "kind": "oracle",
+            "sample": f"{n} sequence evaluations ({n // B} passes over the {B} sequences) "
+                      f"spread over {workers} spawned single-threaded worker processes, fp64 "
+                      f"NumPy oracle, {t:.1f} s wall",
+            "single_core": {"value": gbs1, "unit": "GB/s", "cores": 1,
+                            "sample": f"{n1} sequence evaluations, {t1:.1f} s"},
+            "cpu_count": os.cpu_count(), "cpu_model": cpu_model(), "blas_threads_per_worker": 1}
+
+
 def run_reference(args):
     ws, rank, _ = dist_info()
     if rank != 0:
@@ -331,8 +410,20 @@ def prefill_flops(lens, ctx, Hq, D):
     return 4 * Hq * D * pairs
 
 
-def run_mixed(args, kvc, dev, rank):
-    """Mixed packed batch: 16 packed prefills, then a 128-sequence decode step."""
+def _roofline(name, ms, work, unit, peak, peak_kind, clocks, **extra):
+    """A secondary figure: the kernel's mean time per launch and its roofline fraction."""
+    achieved = work / (ms * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+    d = {"kernel": name, "avg_launch_ms": ms, "achieved": achieved, "unit": unit,
+         "peak": peak, "peak_kind": peak_kind, "frac": achieved / peak,
+         ("algorithmic_bytes" if unit == "GB/s" else "algorithmic_flops"): work,
+         "clocks": clocks}
+    d.update(extra)
+    return d
+
+
+def measure_mixed(kvc, dev, rank, steps, warmup):
+    """Mixed packed batch (one stream): packed slot mapping + prefill, then the 128-sequence
+    decode step.  Returns (prefill figure, decode figure, ms per whole step)."""
     pre, dec = make_config("mixed_packed", seed=rank, value_device=str(dev))
     m = pre.meta
     Hq, Hkv, D, bs = m["num_q_heads"], m["num_kv_heads"], m["head_dim"], pre.block_size
@@ -352,38 +443,33 @@ def run_mixed(args, kvc, dev, rank):
                                  P["block_table"], kc, vc, pre.scale, pre.max_seqlen_q,
                                  context_lens=P["context_lens"], out=pout)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         prefill()
-        step.write()
-        step.decode()
+        step.step()
     torch.cuda.synchronize()
-    graphs = [("prefill", capture(prefill)), ("decode_write", capture(step.write)),
-              ("decode", capture(step.decode))]
-    for _ in range(args.warmup):
+    graphs = [("prefill", capture(prefill)), ("decode", capture(step.step))]
+    for _ in range(warmup):
         for _, g in graphs:
             g.replay()
-    steps = max(3, args.steps // 4)
     with ClockSampler(dev.index or 0) as clk:
         total_ms, per = time_graphs(graphs, steps)
     lens = pre.meta["lens"]
     flops = prefill_flops(lens, [0] * len(lens), Hq, D)
     d_lens = dec.seq_lens.tolist()
-    d_bytes = decode_bytes(d_lens, Hq, Hkv, D, bs)
-    peak, kind = peaks()
-    ms_step = total_ms / steps
-    print(json.dumps({
-        "workload": CONFIGS["mixed_packed"]["about"], "steps": steps,
-        "ms_per_step": ms_step,
-        "prefill": {"ms": per["prefill"], "tokens": T, "attention_tflops": flops / per["prefill"]
-                    / 1e9, "tokens_per_s": T / (per["prefill"] * 1e-3)},
-        "decode": {"ms": per["decode"], "write_ms": per["decode_write"],
-                   "achieved_gbs": d_bytes / (per["decode"] * 1e-3) / 1e9,
-                   "frac_of_" + kind: d_bytes / (per["decode"] * 1e-3) / 1e9 / peak},
-        "clocks": clk.summary(),
-    }), flush=True)
+    d_bytes = decode_bytes(d_lens, Hq, Hkv, D, bs) + write_bytes(len(d_lens), Hkv, D)
+    tp, tkind = tensor_peak()
+    hp, hkind = peaks()
+    clocks = clk.summary()
+    pf = _roofline("prefill_tc2_kernel (kvc_varlen_prefill_paged: packed slot mapping, cache "
+                   "write, causal attention)", per["prefill"], flops, "TFLOP/s", tp, tkind, clocks,
+                   tokens=T, bound="tensor")
+    dc = _roofline("paged_decode_kernel (kvc_paged_decode_append, 128 sequences on the shared "
+                   "pool)", per["decode"], d_bytes, "GB/s", hp, hkind, clocks, bound="hbm")
+    del P, kc, vc, pre, dec, step, graphs
+    return pf, dc, total_ms / steps
 
 
-def run_mla(args, kvc, dev, rank):
+def measure_mla(kvc, dev, rank, steps, warmup):
     """MLA decode step: latent write of the new token, then MLA decode."""
     c = make_config("mla_decode", seed=rank, value_device=str(dev))
     d = {k: getattr(c, k).to(dev) for k in ("q_nope", "q_rope", "cache_nope", "cache_rope",
@@ -404,30 +490,175 @@ def run_mla(args, kvc, dev, rank):
         kvc.mla_paged_decode(d["q_nope"], d["q_rope"], d["cache_nope"], d["cache_rope"],
                              d["block_table"], d["seq_lens"], c.scale, out=out, workspace=ws)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         write()
         decode()
     torch.cuda.synchronize()
     graphs = [("write", capture(write)), ("decode", capture(decode))]
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         for _, g in graphs:
             g.replay()
     with ClockSampler(dev.index or 0) as clk:
-        total_ms, per = time_graphs(graphs, args.steps)
+        total_ms, per = time_graphs(graphs, steps)
     lens = c.seq_lens.tolist()
     toks = sum(lens)
-    by = toks * 576 * 2 + B * 128 * (576 + 512) * 2 + 4 * sum(-(-x // c.block_size) for x in lens) + 4 * B
+    by = toks * 576 * 2 + B * 128 * (576 + 512) * 2 + \
+        4 * sum(-(-x // c.block_size) for x in lens) + 4 * B
     flops = toks * 128 * (2 * 576 + 2 * 512)
-    peak, kind = peaks()
-    ms = per["decode"]
-    print(json.dumps({
-        "workload": CONFIGS["mla_decode"]["about"], "steps": args.steps,
-        "ms_per_step": total_ms / args.steps, "decode_ms": ms, "write_ms": per["write"],
-        "algorithmic_bytes": by, "achieved_gbs": by / (ms * 1e-3) / 1e9,
-        "frac_of_" + kind + "_hbm": by / (ms * 1e-3) / 1e9 / peak,
-        "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": B / (total_ms / args.steps * 1e-3),
-        "clocks": clk.summary(),
-    }), flush=True)
+    hp, hkind = peaks()
+    tp, tkind = tensor_peak()
+    fig = _roofline("mla_decode_kernel + mla_merge_kernel (kvc_mla_paged_decode)", per["decode"],
+                    by, "GB/s", hp, hkind, clk.summary(), bound="hbm",
+                    tflops=flops / (per["decode"] * 1e-3) / 1e12, tensor_peak=tp,
+                    tensor_frac=flops / (per["decode"] * 1e-3) / 1e12 / tp,
+                    write_ms=per["write"], ms_per_step=total_ms / steps,
+                    tokens_per_s=B / (total_ms / steps * 1e-3))
+    del d, out, ws, c, graphs
+    return fig
+
+
+def measure_decode(kvc, dev, rank, name, steps, warmup):
+    """A decode workload's one-launch step (kvc_paged_decode_append), graph-replayed."""
+    case = make_config(name, seed=rank, value_device=str(dev))
+    m = case.meta
+    step = DecodeStep(kvc, case, dev)
+    for _ in range(warmup):
+        step.step()
+    torch.cuda.synchronize()
+    graphs = [("step", capture(step.step))]
+    for _ in range(warmup):
+        graphs[0][1].replay()
+    with ClockSampler(dev.index or 0) as clk:
+        _, per = time_graphs(graphs, steps)
+    lens = case.seq_lens.tolist()
+    by = decode_bytes(lens, m["num_q_heads"], m["num_kv_heads"], m["head_dim"],
+                      case.block_size) + write_bytes(len(lens), m["num_kv_heads"], m["head_dim"])
+    hp, hkind = peaks()
+    fig = _roofline("paged_decode_kernel (kvc_paged_decode_append)", per["step"], by, "GB/s", hp,
+                    hkind, clk.summary(), bound="hbm", workload=CONFIGS[name]["about"])
+    del step, case, graphs
+    return fig
+
+
+def int8_decode_bytes(seq_lens, Hq, Hkv, D, bs):
+    """Algorithmic bytes of one INT8-cache decode: codes and fp32 scales of the K/V rows
+    attended, Q and O (16-bit), table entries, lengths."""
+    toks = int(sum(int(x) for x in seq_lens))
+    blocks = sum(-(-int(x) // bs) for x in seq_lens)
+    B = len(seq_lens)
+    return toks * Hkv * (D + 4) * 2 + 2 * B * Hq * D * 2 + 4 * blocks + 4 * B
+
+
+def measure_int8(kvc, dev, rank, steps, warmup):
+    """The GQA 8B-shape decode over an INT8 cache (codes + one fp32 scale per row)."""
+    case = make_config(WORKLOAD, seed=rank, value_device=str(dev))
+    m = case.meta
+    Hq, Hkv, D, bs = m["num_q_heads"], m["num_kv_heads"], m["head_dim"], case.block_size
+    NB = case.key_cache.shape[0]
+    codes = [torch.empty(NB, bs, Hkv, D, dtype=torch.int8, device=dev) for _ in range(2)]
+    scales = [torch.empty(NB, Hkv, bs, dtype=torch.float32, device=dev) for _ in range(2)]
+    # quantise the whole pool once with the library's own write (every slot in order)
+    allslots = torch.arange(NB * bs, dtype=torch.int32, device=dev)
+    kvc.reshape_and_cache_int8(case.key_cache.view(NB * bs, Hkv, D),
+                               case.value_cache.view(NB * bs, Hkv, D), codes[0], codes[1],
+                               scales[0], scales[1], allslots)
+    del case.key_cache, case.value_cache
+    q, bt, sl = case.q.to(dev), case.block_table.to(dev), case.seq_lens.to(dev)
+    out = torch.empty_like(q)
+    ws = torch.zeros(max(kvc.decode_workspace_size(Hq, Hkv, D), 16), dtype=torch.uint8,
+                     device=dev)
+
+    def decode():
+        kvc.paged_decode_int8(q, codes[0], codes[1], scales[0], scales[1], bt, sl, case.scale,
+                              out=out, workspace=ws)
+
+    for _ in range(warmup):
+        decode()
+    torch.cuda.synchronize()
+    graphs = [("decode", capture(decode))]
+    for _ in range(warmup):
+        graphs[0][1].replay()
+    with ClockSampler(dev.index or 0) as clk:
+        _, per = time_graphs(graphs, steps)
+    lens = case.seq_lens.tolist()
+    by = int8_decode_bytes(lens, Hq, Hkv, D, bs)
+    hp, hkind = peaks()
+    fig = _roofline("paged_decode_kernel, INT8 cache (kvc_paged_decode_int8)", per["decode"], by,
+                    "GB/s", hp, hkind, clk.summary(), bound="hbm",
+                    bytes_vs_16bit=by / decode_bytes(lens, Hq, Hkv, D, bs))
+    del codes, scales, q, bt, sl, out, ws, graphs
+    return fig
+
+
+def measure_serving_loop(kvc, dev, rank, steps):
+    """A decode loop driven by the host block manager on the GQA 8B-shape workload, timed
+    end to end on the host clock: per step BlockManager.step (slots, copy pairs, table,
+    lengths for 64 sequences), their copy to the device, kvc_paged_decode_append, and a
+    synchronisation."""
+    case = make_config(WORKLOAD, seed=rank, value_device=str(dev))
+    m = case.meta
+    bs, NB = case.block_size, case.key_cache.shape[0]
+    lens = case.seq_lens.tolist()
+    maxb = case.block_table.shape[1] + 1 + (steps + 3) // bs   # room for the steps' tokens
+    bm = kvc.BlockManager(NB, bs, maxb)
+    for b, L in enumerate(lens):          # prompts already cached: L - 1 tokens
+        bm.add(b, L - 1)
+    ids = torch.arange(len(lens), dtype=torch.int64)
+    buf = bm.step_buffer(len(lens), pin_memory=True)
+    step = DecodeStep(kvc, case, dev)
+    dtab = torch.empty(len(lens), maxb, dtype=torch.int32, device=dev)
+    dlen = torch.empty(len(lens), dtype=torch.int32, device=dev)
+    step.bt, step.sl = dtab, dlen
+
+    def one():
+        _, cs, cd, table, ln = bm.step(ids, out=buf)
+        dtab.copy_(table, non_blocking=True)
+        dlen.copy_(ln, non_blocking=True)
+        step.step()
+        torch.cuda.synchronize()
+
+    for _ in range(3):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    wall = (time.perf_counter() - t0) / steps
+    by = decode_bytes([L + 3 + steps for L in lens], m["num_q_heads"], m["num_kv_heads"],
+                      m["head_dim"], bs)
+    res = {"ms_per_step": wall * 1e3, "tokens_per_s": len(lens) / wall,
+           "approx_gbs": by / wall / 1e9, "steps": steps,
+           "step": "BlockManager.step (host) + H2D of block table and lengths + "
+                   "kvc_paged_decode_append + synchronize, host clock"}
+    del step, case, bm
+    return res
+
+
+def run_mixed(args, kvc, dev, rank):
+    pf, dc, ms = measure_mixed(kvc, dev, rank, max(3, args.steps // 4), args.warmup)
+    print(json.dumps({"workload": CONFIGS["mixed_packed"]["about"], "ms_per_step": ms,
+                      "prefill": pf, "decode": dc}), flush=True)
+
+
+def run_mla(args, kvc, dev, rank):
+    print(json.dumps(dict(workload=CONFIGS["mla_decode"]["about"],
+                          **measure_mla(kvc, dev, rank, args.steps, args.warmup))), flush=True)
+
+
+def secondary(kvc, dev, rank, steps, warmup):
+    """Builder-timed figures of the other kernels, each against its own roofline."""
+    out = {}
+    out["mla_decode"] = measure_mla(kvc, dev, rank, steps, warmup)
+    torch.cuda.empty_cache()
+    out["mixed_prefill"], out["mixed_decode"], _ = measure_mixed(kvc, dev, rank, steps, warmup)
+    torch.cuda.empty_cache()
+    out["llama7b_mha_decode"] = measure_decode(kvc, dev, rank, "llama7b_mha_decode", steps,
+                                               warmup)
+    torch.cuda.empty_cache()
+    out["gqa8b_decode_int8"] = measure_int8(kvc, dev, rank, steps, warmup)
+    torch.cuda.empty_cache()
+    out["serving_loop"] = measure_serving_loop(kvc, dev, rank, steps)
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -437,6 +668,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the builder-timed figures of the other kernels")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--profile", action="store_true",
                     help="short run for ncu: no CPU baseline, few e2e steps")
@@ -449,6 +682,7 @@ def main():
         return run_reference(args)
     if args.profile:
         args.no_cpu_baseline = True
+        args.no_secondary = True
         args.e2e_steps = 1
 
     ws, rank, local = dist_info()
@@ -573,7 +807,7 @@ def main():
     dec_avg_ms = statistics.mean(dec_ms)
     achieved = step_bytes / (dec_avg_ms * 1e-3) / 1e9
     digest = kernel_source_digest()
-    traffic = (recorded_traffic("paged_decode_gqa8b.md", digest)
+    traffic = (recorded_traffic("paged_decode_kernel/" + WORKLOAD, digest)
                if args.workload == WORKLOAD else None)
 
     if rank == 0:
@@ -609,12 +843,12 @@ def main():
             "gpu_launches": DecodeStep.LAUNCHES * args.steps,
             "clocks": clk.summary(),
         }
+        if not args.no_secondary:
+            del step, g_dec, d_pack, h_pack, h_out
+            torch.cuda.empty_cache()
+            res["secondary"] = secondary(kvc, dev, rank, min(args.steps, 100), args.warmup)
         if not args.no_cpu_baseline:
-            gbs, n_seq, Btot, t = cpu_oracle_rate(case)
-            res["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                   "sample": f"{n_seq} sequence evaluations ({n_seq / Btot:.1f} "
-                                             f"passes over the {Btot} sequences), fp64 NumPy "
-                                             f"oracle, {t:.1f} s"}
+            res["cpu_baseline"] = cpu_baseline(case)
         print(json.dumps(res), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()

@@ -49,10 +49,26 @@ def test_steps_per_graph_divides_the_timed_steps():
 
 
 def test_recorded_traffic_needs_the_matching_source_digest(tmp_path, monkeypatch):
+    import json
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "p.md").write_text(
-        "kernel_source_digest: 0123456789abcdef\ntraffic_bytes_per_launch_full_size: 598906624\n")
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({
+        "k/w": {"kernel_source_digest": "0123456789abcdef", "dram_bytes_per_launch": 598906624}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.recorded_traffic("p.md", "0123456789abcdef") == 598906624.0
-    assert bench.recorded_traffic("p.md", "fedcba9876543210") is None
-    assert bench.recorded_traffic("missing.md", "0123456789abcdef") is None
+    assert bench.recorded_traffic("k/w", "0123456789abcdef") == 598906624.0
+    assert bench.recorded_traffic("k/w", "fedcba9876543210") is None
+    assert bench.recorded_traffic("other", "0123456789abcdef") is None
+
+
+def test_all_core_oracle_baseline_runs_on_spawned_workers():
+    """The CPU baseline's pool: spawned workers, memory-mapped inputs, whole passes."""
+    from synth import make_config
+    case = make_config("tiny_decode", seed=0)
+    gbs, n, workers, t = bench.cpu_oracle_rate_all_cores(case, budget_s=0.2)
+    assert gbs > 0 and workers >= 1 and n % case.q.shape[0] == 0 and t > 0
+
+
+def test_int8_decode_bytes_counts_codes_scales_and_rows():
+    lens, Hq, Hkv, D, bs = [37, 5, 0], 4, 2, 128, 16
+    want = sum(L * Hkv * (D + 4) * 2 for L in lens) + 3 * 2 * Hq * D * 2 + \
+        4 * sum(math.ceil(L / bs) for L in lens) + 4 * 3
+    assert bench.int8_decode_bytes(lens, Hq, Hkv, D, bs) == want
