@@ -67,6 +67,10 @@ constexpr int kProducerWarp = 12, kMmaWarp = 13;
 constexpr int kThreads = kExchangeThreads + kMathThreads + 64;
 constexpr int kMaxBatch = 1024;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+// Bytes of one exchanged partial score: the scaled partial travels in fp32,
+// so the full score each CTA forms is the fp32 sum of the two halves.
+constexpr int kXElt = 4;
+constexpr int kXBytes = kH * kTok * kXElt;
 
 // TMEM columns: O (256 fp32), two S buffers (64 fp32 each), then the CTA's
 // 256 nope query columns as packed 16-bit pairs (128 columns).
@@ -96,8 +100,8 @@ struct MlaLayout {
   static constexpr int kQr = 0;                                    // 16 KB
   static constexpr int kK = kQr + kQChunkBytes;                    // 4 x 40 KB
   static constexpr int kP = kK + kStages * kStageBytes;            // 16 KB
-  static constexpr int kX = kP + kH * 128;                         // 16 KB
-  static constexpr int kRed = kX + kH * kTok * 2;                  // [2][128] fp32
+  static constexpr int kX = kP + kH * 128;                         // 32 KB
+  static constexpr int kRed = kX + kXBytes;                        // [2][128] fp32
   static constexpr int kBar = kRed + 2 * kH * 4;
   static constexpr int kMisc = align_up_c(kBar + 19 * 8, 16);      // tmem slot, flags
   static constexpr int kEnd = kMisc + 32;
@@ -425,11 +429,10 @@ __device__ __forceinline__ void mla_load_q(const MlaParams& p, uint32_t lane_bas
 }
 
 // Warps 0-3, thread `row` = query head.  Per tile: this CTA's partial scores
-// (TMEM), scaled to the log2 domain and rounded to fp16 (their rounding error
-// is below 2^-11 of the scaled partial, far under the bf16/fp16 rounding of
-// P), go to the other CTA as st.async stores that complete its x_full
-// transaction count, once the other CTA has freed its X buffer (x_empty, a
-// relaxed arrive from its math warps): 128 bytes per query head and tile.
+// (TMEM), scaled to the log2 domain (fp32), go to the other CTA as st.async
+// stores that complete its x_full transaction count, once the other CTA has
+// freed its X buffer (x_empty, a relaxed arrive from its math warps): 256
+// bytes per query head and tile, chunk q holding tokens 4q .. 4q+3.
 // These warps also load each sequence's query into TMEM.
 template <typename T>
 __device__ __forceinline__ void mla_exchange(const MlaParams& p, uint8_t* smem, uint64_t* bars,
@@ -458,16 +461,13 @@ __device__ __forceinline__ void mla_exchange(const MlaParams& p, uint8_t* smem, 
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(&bars[kSFree0 + sb]);
-    uint32_t xh[kTok / 2];
 #pragma unroll
-    for (int k = 0; k < kTok / 2; ++k)
-      xh[k] = pack_pair<__half>(so[2 * k] * p.scale_log2, so[2 * k + 1] * p.scale_log2);
+    for (int k = 0; k < kTok; ++k) so[k] *= p.scale_log2;
     wait_peer(&bars[kXEmpty], (it & 1) ^ 1, abort_flag, p.err_flag);
 #pragma unroll
-    for (int q = 0; q < kTok / 8; ++q)  // chunk q: tokens 8q .. 8q+7
+    for (int q = 0; q < kTok / 4; ++q)  // chunk q: tokens 4q .. 4q+3
       st_async_cluster_v4(x_peer + (q * kH + row) * 16,
-                          make_float4(__uint_as_float(xh[4 * q]), __uint_as_float(xh[4 * q + 1]),
-                                      __uint_as_float(xh[4 * q + 2]), __uint_as_float(xh[4 * q + 3])),
+                          make_float4(so[4 * q], so[4 * q + 1], so[4 * q + 2], so[4 * q + 3]),
                           xfull_peer);
     // Tile it+1 starts the next sequence: its query replaces this one (S(it)
     // complete => every S of this sequence is done).  Its rows are first
@@ -526,7 +526,7 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
     }
     // Scores of this thread's 32 tokens in the log2 domain: own partial
     // (TMEM, fp32) times scale_log2 plus the other CTA's (X, already scaled,
-    // fp16); then both buffers are released.
+    // fp32); then both buffers are released.
     float s[32];
     wait_cta(&bars[kSFull0 + sb], (it >> 1) & 1, abort_flag, p.err_flag);
     tc_fence_after();
@@ -538,17 +538,17 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
     wait_peer(&bars[kXFull], it & 1, abort_flag, p.err_flag);
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = x_mine[(h * 4 + q) * kH + row];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int k = 8 * q + 2 * i;
-        const float2 other = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-        const float2 t = fma2(make_float2(s[k], s[k + 1]), sl2, other);
-        s[k] = t.x;
-        s[k + 1] = t.y;
-      }
+    for (int q = 0; q < 8; ++q) {
+      const uint4 v = x_mine[(h * 8 + q) * kH + row];
+      const float2 o01 = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+      const float2 o23 = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+      const int k = 4 * q;
+      const float2 t0 = fma2(make_float2(s[k], s[k + 1]), sl2, o01);
+      const float2 t1 = fma2(make_float2(s[k + 2], s[k + 3]), sl2, o23);
+      s[k] = t0.x;
+      s[k + 1] = t0.y;
+      s[k + 2] = t1.x;
+      s[k + 3] = t1.y;
     }
     const int tile_valid = min(kTok, cm.len - cm.j * kTok);
     const int valid = tile_valid - h * 32;  // of this thread's 32 tokens
@@ -568,8 +568,8 @@ __device__ __forceinline__ void mla_math(const MlaParams& p, uint8_t* smem, uint
     red[h * kH + row] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
     named_bar_sync(3, kMathThreads);  // also: every thread has read X
     if (elected) {
-      // The next tile's scores arrive as 16 KB of transactions on x_full.
-      if (it + 1 < n_it) mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 2);
+      // The next tile's scores arrive as 32 KB of transactions on x_full.
+      if (it + 1 < n_it) mbar_arrive_expect_tx(&bars[kXFull], kXBytes);
       mbar_arrive_cluster_relaxed(xempty_peer);
     }
     const float mx = fmaxf(red[row], red[kH + row]);  // same order in both halves
@@ -678,7 +678,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     // The first tile's scores from the other CTA arrive as 16 KB of
     // transactions on x_full (harmless if this cluster has no tile).
-    mbar_arrive_expect_tx(&bars[kXFull], kH * kTok * 2);
+    mbar_arrive_expect_tx(&bars[kXFull], kXBytes);
   }
   uint32_t leader = 0;  // the MMA warp's issuing lane
   if (warp == kMmaWarp) {

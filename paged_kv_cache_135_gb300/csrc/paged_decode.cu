@@ -330,9 +330,12 @@ __device__ __forceinline__ uint32_t scale_addr(uint32_t base, int t, int log2_bo
 // sum_j (p_j * scale_v_j) codes_v_j: S = Q K^T runs on the exact integer codes
 // (converted to T in registers, straight from the 128-byte swizzled code
 // tile), each score column is multiplied by its key scale, and each weight by
-// its value scale before it is rounded to T for P V; l sums the plain p.  The
-// warp's 16 value rows are first converted into `vst`, in the layout of a
-// 16-bit tile, so P V reads them with ldmatrix.trans as the 16-bit path does.
+// its value scale; l sums the plain p.  P V runs in fp16 whatever T is: the
+// value codes are exact in fp16 and the weights p * scale_v keep 11 bits
+// there (8 in bf16), since the normaliser l is not formed from the rounded
+// weights.  The warp's 16 value rows are first converted into `vst`, in the
+// layout of a 16-bit tile, so P V reads them with ldmatrix.trans as the
+// 16-bit path does.
 template <typename T, int D>
 __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
                                              uint32_t vscale, int log2_box, int warp, int lane,
@@ -348,10 +351,10 @@ __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uin
     for (int i = 0; i < 4; ++i) {
       const int c = (lane & 1) * 4 + i;  // 16 dims
       const uint4 u = lds_v4(vbase + swz128(tok, c));
-      const uint32_t w0 = i8x2_to_16<T>(u.x & 0xffffu), w1 = i8x2_to_16<T>(u.x >> 16);
-      const uint32_t w2 = i8x2_to_16<T>(u.y & 0xffffu), w3 = i8x2_to_16<T>(u.y >> 16);
-      const uint32_t w4 = i8x2_to_16<T>(u.z & 0xffffu), w5 = i8x2_to_16<T>(u.z >> 16);
-      const uint32_t w6 = i8x2_to_16<T>(u.w & 0xffffu), w7 = i8x2_to_16<T>(u.w >> 16);
+      const uint32_t w0 = i8x2_to_16<__half>(u.x & 0xffffu), w1 = i8x2_to_16<__half>(u.x >> 16);
+      const uint32_t w2 = i8x2_to_16<__half>(u.y & 0xffffu), w3 = i8x2_to_16<__half>(u.y >> 16);
+      const uint32_t w4 = i8x2_to_16<__half>(u.z & 0xffffu), w5 = i8x2_to_16<__half>(u.z >> 16);
+      const uint32_t w6 = i8x2_to_16<__half>(u.w & 0xffffu), w7 = i8x2_to_16<__half>(u.w >> 16);
       const uint32_t half = vst + (c >> 2) * (16 * 128);
       sts_v4(half + swz128(row, (c & 3) * 2), w0, w1, w2, w3);
       sts_v4(half + swz128(row, (c & 3) * 2 + 1), w4, w5, w6, w7);
@@ -417,10 +420,10 @@ __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uin
   l[1] = l[1] * corr1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
   uint32_t pa[4];
   float ra, rb;
-  pa[0] = Pack<T>::run(p[0][0] * vsc[0][0], p[0][1] * vsc[0][1], ra, rb);
-  pa[1] = Pack<T>::run(p[0][2] * vsc[0][0], p[0][3] * vsc[0][1], ra, rb);
-  pa[2] = Pack<T>::run(p[1][0] * vsc[1][0], p[1][1] * vsc[1][1], ra, rb);
-  pa[3] = Pack<T>::run(p[1][2] * vsc[1][0], p[1][3] * vsc[1][1], ra, rb);
+  pa[0] = Pack<__half>::run(p[0][0] * vsc[0][0], p[0][1] * vsc[0][1], ra, rb);
+  pa[1] = Pack<__half>::run(p[0][2] * vsc[0][0], p[0][3] * vsc[0][1], ra, rb);
+  pa[2] = Pack<__half>::run(p[1][0] * vsc[1][0], p[1][1] * vsc[1][1], ra, rb);
+  pa[3] = Pack<__half>::run(p[1][2] * vsc[1][0], p[1][3] * vsc[1][1], ra, rb);
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) {
     o[n][0] *= corr0;
@@ -436,8 +439,8 @@ __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uin
     ldsm_x4_t(vst + (dcol >> 6) * (16 * 128) + swz128(tok, (dcol & 63) >> 3), b0, b1, b2, b3);
     // Codes are finite, and the weights outside [vlo, valid) are exact zeros,
     // so no value row needs masking here.
-    MmaOp<T>::run(o[2 * dp], pa, b0, b1);
-    MmaOp<T>::run(o[2 * dp + 1], pa, b2, b3);
+    MmaOp<__half>::run(o[2 * dp], pa, b0, b1);
+    MmaOp<__half>::run(o[2 * dp + 1], pa, b2, b3);
   }
   __syncwarp();  // the staging tile is rewritten by the warp's next tile
 }

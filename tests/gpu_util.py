@@ -13,6 +13,28 @@ import torch
 from oracle import kvc_oracle as O
 
 TOL = {"f16": 2e-3, "bf16": 1e-2}
+MANT = {"f16": 10, "bf16": 7}       # stored mantissa bits of the output type
+EMIN = {"f16": -14, "bf16": -126}   # exponent of the smallest normal value
+
+
+def bound(ref, dtype):
+    """Per-element bound of |gpu - oracle|: the stated tolerance (max-abs 2e-3 fp16,
+    1e-2 bf16) on the kernel's own arithmetic, plus half a unit in the last place of
+    the output type at the oracle's value -- the final rounding of the result to
+    fp16/bf16, which no kernel returning that type avoids (for bf16 it reaches 0.0078
+    at |o| >= 2 and 0.0156 at |o| >= 4, beyond the stated 1e-2 on its own)."""
+    a = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** EMIN[dtype])))
+    return TOL[dtype] + 2.0 ** (e - MANT[dtype] - 1)
+
+
+def excess(gpu, ref, dtype):
+    """max(|gpu - ref| - bound(ref)): <= 0 when every element is within its bound."""
+    g = gpu.double().cpu().numpy() if hasattr(gpu, "double") else np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return -1.0
+    return float((np.abs(g - ref) - bound(ref, dtype)).max())
 
 
 def to_cuda(t):

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, bits, max_err, to_cuda
+from gpu_util import bits, excess, to_cuda
 from oracle import kvc_oracle as O
 from synth import decode_case
 
@@ -70,7 +70,7 @@ def test_append_matches_oracle(kvc_lib, lens, Hq, Hkv, D, bs, dtype, num_ctas):
     assert np.array_equal(bits(d["value_cache"]), vc)
     ref = O.paged_decode(case.q.double().numpy(), kc64, vc64, case.block_table.numpy(),
                          case.seq_lens.numpy(), case.scale)
-    assert max_err(out, ref) <= TOL[dtype]
+    assert excess(out, ref, dtype) <= 0
 
 
 @pytest.mark.parametrize("num_ctas", [0, 5])

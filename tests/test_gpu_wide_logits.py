@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, to_cuda
+from gpu_util import excess, to_cuda
 from oracle import kvc_oracle as O
 from synth import decode_case, mla_case, prefill_case
 
@@ -41,10 +41,10 @@ def test_decode_wide_logits(kvc_lib, dtype, num_ctas):
     kc, vc = case.key_cache.double().numpy(), case.value_cache.double().numpy()
     bt = case.block_table.numpy()
     K = O.gather_sequence(kc, bt[4], 700)
-    assert _spread(case.scale * K[:, 0] @ case.q[4, 0].double().numpy()) > 25.0
+    assert _spread(case.scale * K[:, 0] @ case.q[4, 0].double().numpy()) > 20.0
     ref = O.paged_decode(case.q.double().numpy(), kc, vc, bt, case.seq_lens.numpy(), case.scale)
-    e = float(np.abs(out.double().cpu().numpy() - ref).max())
-    assert e <= TOL[dtype], e
+    e = excess(out, ref, dtype)
+    assert e <= 0, e
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -71,8 +71,8 @@ def test_prefill_wide_logits(kvc_lib, dtype):
                                            c.context_lens.numpy(), sm, bt,
                                            c.key_cache.double().numpy(),
                                            c.value_cache.double().numpy(), c.scale)
-        e = float(np.abs(out.double().cpu().numpy() - ref).max())
-        assert e <= TOL[dtype], (Hq, Hkv, e)
+        e = excess(out, ref, dtype)
+        assert e <= 0, (Hq, Hkv, e)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -93,5 +93,5 @@ def test_mla_wide_logits(kvc_lib, dtype, num_ctas):
     ref = O.mla_paged_decode(c.q_nope.double().numpy(), c.q_rope.double().numpy(),
                              c.cache_nope.double().numpy(), c.cache_rope.double().numpy(),
                              c.block_table.numpy(), c.seq_lens.numpy(), c.scale)
-    e = float(np.abs(out.double().cpu().numpy() - ref).max())
-    assert e <= TOL[dtype], e
+    e = excess(out, ref, dtype)
+    assert e <= 0, e
