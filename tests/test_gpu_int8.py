@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import excess, max_err, to_cuda
+from gpu_util import excess, to_cuda
 from oracle import kvc_oracle as O
 from synth import decode_case
 
@@ -122,12 +122,14 @@ def test_int8_step_write_then_decode(kvc_lib):
     ref = O.paged_decode_int8(case.q.double().numpy(), rk, rv, rks, rvs, case.block_table.numpy(),
                               case.seq_lens.numpy(), case.scale)
     assert excess(out, ref, "bf16") <= 0
-    # and the quantised cache stays close to the 16-bit attention it stands for
+    # and the quantised cache stays close to the 16-bit attention it stands for: the
+    # quantisation error (the oracle's pin bounds it by 2e-2 on such rows) plus the
+    # bf16 rounding of the output
     exact = O.paged_decode(case.q.double().numpy(), *O.reshape_and_cache(
         case.new_key.double().numpy(), case.new_value.double().numpy(),
         case.key_cache.double().numpy(), case.value_cache.double().numpy(), sm),
         case.block_table.numpy(), case.seq_lens.numpy(), case.scale)
-    assert max_err(out, exact) <= 2e-2
+    assert excess(out, exact, "bf16") <= 1e-2
 
 
 def test_int8_rejects_other_head_dims(kvc_lib):
