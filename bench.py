@@ -644,6 +644,17 @@ def run_mla(args, kvc, dev, rank):
                           **measure_mla(kvc, dev, rank, args.steps, args.warmup))), flush=True)
 
 
+MEASURES = {
+    "mla_decode": measure_mla,
+    "mixed": lambda kvc, dev, rank, steps, warmup: measure_mixed(kvc, dev, rank, steps, warmup),
+    "llama7b_mha_decode": lambda kvc, dev, rank, steps, warmup: measure_decode(
+        kvc, dev, rank, "llama7b_mha_decode", steps, warmup),
+    "gqa8b_decode_int8": measure_int8,
+    "serving_loop": lambda kvc, dev, rank, steps, warmup: measure_serving_loop(kvc, dev, rank,
+                                                                               steps),
+}
+
+
 def secondary(kvc, dev, rank, steps, warmup):
     """Builder-timed figures of the other kernels, each against its own roofline."""
     out = {}
@@ -675,6 +686,8 @@ def main():
                     help="short run for ncu: no CPU baseline, few e2e steps")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(CONFIGS),
                     help="the timed workload (default: the headline GQA 8B-shape decode)")
+    ap.add_argument("--measure", choices=sorted(MEASURES),
+                    help="print one of the secondary figures alone (a short run for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -696,6 +709,10 @@ def main():
     kvc.build()
     kvc.lib()
 
+    if args.measure:
+        print(json.dumps({args.measure: MEASURES[args.measure](kvc, dev, rank, args.steps,
+                                                              args.warmup)}), flush=True)
+        return
     if CONFIGS[args.workload]["kind"] == "mixed":
         return run_mixed(args, kvc, dev, rank)
     if CONFIGS[args.workload]["kind"] == "mla":

@@ -50,7 +50,10 @@ namespace {
 constexpr int kTile = 64;            // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;    // 16 tokens each
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 3;
+// Pipeline depth: 3 stages of ~33 KB (16-bit cache) or 4 of ~17 KB (INT8,
+// whose stages also hold scales; 4 keeps two CTAs per SM).
+template <bool kI8>
+constexpr int stages_of() { return kI8 ? 4 : 3; }
 constexpr int kMaxBatch = 1024;
 constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a K or V tile
 constexpr int kMaxPieces = 62;           // split shares merged from a shared-memory list
@@ -99,7 +102,9 @@ struct Layout {
   int scales;   // INT8: K scales then V scales of the stage, kTile floats each
   int qoff;     // query rows of the stage (1024-aligned)
   int vstg;     // INT8: per consumer warp, its 16 value rows as 16-bit values
+  int qfrag;    // INT8: the segment's fp16 query fragments, [D/16][32 lanes][4 words]
   int stage;    // K tile, V tile, (scales), query rows
+  static constexpr int kStages = stages_of<kI8>();
   int bar;      // full[kStages], empty[kStages]
   int flags;    // abort, last, npieces
   int pieces;   // int[kMaxPieces]
@@ -119,7 +124,8 @@ struct Layout {
     cum = align_up(lens + batch * 4, 16);
     cmb = align_up(cum + (batch + 1) * 4, 16);
     vstg = align_up(cmb + kConsumerWarps * group * (D + 2) * 4, 1024);
-    total = 1024 + (kI8 ? vstg + kConsumerWarps * 16 * D * 2
+    qfrag = vstg + kConsumerWarps * 16 * D * 2;
+    total = 1024 + (kI8 ? qfrag + (D / 16) * 32 * 16
                         : cmb + kConsumerWarps * group * (D + 2) * 4);
   }
 };
@@ -241,6 +247,7 @@ __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int wa
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
   const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const bool grew = mn0 != m[0] || mn1 != m[1];
   const float corr0 = fast_exp2(m[0] - mn0), corr1 = fast_exp2(m[1] - mn1);
   m[0] = mn0;
   m[1] = mn1;
@@ -256,12 +263,14 @@ __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int wa
   rs1 += ra + rb;
   l[0] = l[0] * corr0 + rs0;
   l[1] = l[1] * corr1 + rs1;
+  if (__any_sync(0xffffffffu, grew)) {  // O keeps its scale while no row max grows
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) {
-    o[n][0] *= corr0;
-    o[n][1] *= corr0;
-    o[n][2] *= corr1;
-    o[n][3] *= corr1;
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] *= corr0;
+      o[n][1] *= corr0;
+      o[n][2] *= corr1;
+      o[n][3] *= corr1;
+    }
   }
   const int tok = warp * 16 + (mi & 1) * 8 + rr;
 #pragma unroll
@@ -282,11 +291,6 @@ __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int wa
 
 // ---- INT8 cache: codes to 16-bit values, scales, and one warp's 16 tokens.
 
-__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
 __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -306,17 +310,32 @@ __device__ __forceinline__ float lds_f32(uint32_t a) {
   return v;
 }
 
-// Two int8 codes (the low 16 bits, element 0 first) as a pair of T, exactly:
-// a code c is an integer with |c| <= 128, so it is representable in both
-// 16-bit types.  The byte, biased to c + 128, becomes the low mantissa bits of
-// the fp32 2^23 + c + 128, from which 2^23 + 128 is subtracted exactly.
+// Four int8 codes (one 32-bit word, byte k = element k) as two fp16 pairs,
+// exactly: each code c (|c| <= 127) is biased to the byte c + 128, placed as
+// the low mantissa byte of the fp16 1024 + (c + 128), and 1152 is subtracted
+// (both steps exact).  lo = elements 0, 1; hi = elements 2, 3.
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140u);
+  const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342u);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 ra = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 rb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&ra);
+  hi = *reinterpret_cast<const uint32_t*>(&rb);
+}
+
+// A pair of 16-bit query values as an fp16 pair: unchanged for fp16; for bf16
+// exact whenever the values lie in fp16's normal range (|q| in [2^-14, 65504]),
+// since a bf16 significand (8 bits) fits fp16's (11 bits).
 template <typename T>
-__device__ __forceinline__ uint32_t i8x2_to_16(uint32_t two) {
-  const uint32_t x = two ^ 0x8080u;
-  const float f0 = __uint_as_float(0x4B000000u | (x & 0xffu)) - 8388736.f;
-  const float f1 = __uint_as_float(0x4B000000u | ((x >> 8) & 0xffu)) - 8388736.f;
-  float ra, rb;
-  return Pack<T>::run(f0, f1, ra, rb);
+__device__ __forceinline__ uint32_t q_pair_f16(uint32_t w);
+template <>
+__device__ __forceinline__ uint32_t q_pair_f16<__half>(uint32_t w) { return w; }
+template <>
+__device__ __forceinline__ uint32_t q_pair_f16<__nv_bfloat16>(uint32_t w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Address of token t's scale in a stage's scale region (one 128-byte slot per
@@ -325,76 +344,122 @@ __device__ __forceinline__ uint32_t scale_addr(uint32_t base, int t, int log2_bo
   return base + ((t >> log2_box) << 7) + ((t & ((1 << log2_box) - 1)) << 2);
 }
 
+// The query fragments of S = Q K^T over an INT8 cache, in fp16 and with the
+// 16 dims of every k-step permuted: lane (g = lane/4, c = lane%4) holds dims
+// 16kk + 4c .. 4c+3 of query rows g and g + 8, so that its key operand is the
+// 4 contiguous codes at the same dims (one 32-bit load).  The dot product does
+// not depend on the order of its terms.  Rows >= G are padding and read row
+// 0.  They are the same for every consumer warp and every tile of a (b, g)
+// segment: at the segment's first tile each warp builds two k-steps of them
+// (from the stage's query rows) into shared memory, [kk][lane] as 16 bytes.
+template <typename T, int D>
+__device__ __forceinline__ void build_q_i8(uint32_t qbase, int q_half, int group, int warp,
+                                           int lane, uint32_t qfrag) {
+  const int g = lane >> 2, c = lane & 3;
+  const int r0 = g < group ? g : 0, r1 = g + 8 < group ? g + 8 : 0;
+#pragma unroll
+  for (int i = 0; i < D / 16 / kConsumerWarps; ++i) {
+    const int kk = warp * (D / 16 / kConsumerWarps) + i;
+    const uint32_t off = (kk >> 2) * q_half;
+    const int chunk = (kk & 3) * 2 + (c >> 1), byte = (c & 1) * 8;
+    uint32_t w0, w1, w2, w3;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(w0), "=r"(w1) : "r"(qbase + off + swz128(r0, chunk) + byte));
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(w2), "=r"(w3) : "r"(qbase + off + swz128(r1, chunk) + byte));
+    // a0: row g dims 4c, 4c+1; a1: row g+8 same; a2: row g dims 4c+2, 4c+3; a3: row g+8 same
+    sts_v4(qfrag + (kk * 32 + lane) * 16, q_pair_f16<T>(w0), q_pair_f16<T>(w2), q_pair_f16<T>(w1),
+           q_pair_f16<T>(w3));
+  }
+}
+
 // One warp's 16 tokens of a stage over an INT8 cache.  A cached row is
 // code * scale, so q . k = scale_k * (q . codes_k) and sum_j p_j v_j =
-// sum_j (p_j * scale_v_j) codes_v_j: S = Q K^T runs on the exact integer codes
-// (converted to T in registers, straight from the 128-byte swizzled code
-// tile), each score column is multiplied by its key scale, and each weight by
-// its value scale; l sums the plain p.  P V runs in fp16 whatever T is: the
-// value codes are exact in fp16 and the weights p * scale_v keep 11 bits
-// there (8 in bf16), since the normaliser l is not formed from the rounded
-// weights.  The warp's 16 value rows are first converted into `vst`, in the
-// layout of a 16-bit tile, so P V reads them with ldmatrix.trans as the
-// 16-bit path does.
-template <typename T, int D>
+// sum_j (p_j * scale_v_j) codes_v_j.  Both products run on the tensor cores
+// in fp16 with fp32 accumulation: the codes are exact in fp16, the queries
+// are (qa, see load_q_i8), and the weights p * scale_v keep 11 bits (l sums
+// the plain p, so the weights are not renormalised after rounding).  Each
+// score column is multiplied by its key scale.  The warp's 16 value rows are
+// first converted into `vst`, in the layout of a 16-bit tile, so P V reads
+// them with ldmatrix.trans as the 16-bit path does.
+template <int D>
 __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
                                              uint32_t vscale, int log2_box, int warp, int lane,
                                              int vlo, int valid, float scale_log2,
-                                             uint32_t qbase, int q_half, int group, uint32_t vst,
+                                             uint32_t qfrag, uint32_t vst,
                                              float (&o)[D / 8][4], float (&m)[2],
                                              float (&l)[2]) {
   static_assert(D == 128, "one 128-byte code row per token");
   const int mi = lane >> 3, rr = lane & 7;
-  {  // value codes -> T: lane converts 64 codes of row lane / 2
+  const int c0 = 2 * (lane & 3);
+  // Shared-memory loads are issued in groups ahead of their use (the asm
+  // statements keep program order), so their latencies overlap.
+  float ksr[2][2], vsr[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = warp * 16 + nt * 8 + c0 + e;
+      ksr[nt][e] = lds_f32(scale_addr(kscale, t, log2_box));
+      vsr[nt][e] = lds_f32(scale_addr(vscale, t, log2_box));
+    }
+  {  // value codes -> fp16: lane converts 64 codes of row lane / 2
     const int row = lane >> 1, tok = warp * 16 + row;
+    uint4 u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = lds_v4(vbase + swz128(tok, (lane & 1) * 4 + i));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int c = (lane & 1) * 4 + i;  // 16 dims
-      const uint4 u = lds_v4(vbase + swz128(tok, c));
-      const uint32_t w0 = i8x2_to_16<__half>(u.x & 0xffffu), w1 = i8x2_to_16<__half>(u.x >> 16);
-      const uint32_t w2 = i8x2_to_16<__half>(u.y & 0xffffu), w3 = i8x2_to_16<__half>(u.y >> 16);
-      const uint32_t w4 = i8x2_to_16<__half>(u.z & 0xffffu), w5 = i8x2_to_16<__half>(u.z >> 16);
-      const uint32_t w6 = i8x2_to_16<__half>(u.w & 0xffffu), w7 = i8x2_to_16<__half>(u.w >> 16);
+      uint32_t w[8];
+      i8x4_to_f16(u[i].x, w[0], w[1]);
+      i8x4_to_f16(u[i].y, w[2], w[3]);
+      i8x4_to_f16(u[i].z, w[4], w[5]);
+      i8x4_to_f16(u[i].w, w[6], w[7]);
       const uint32_t half = vst + (c >> 2) * (16 * 128);
-      sts_v4(half + swz128(row, (c & 3) * 2), w0, w1, w2, w3);
-      sts_v4(half + swz128(row, (c & 3) * 2 + 1), w4, w5, w6, w7);
+      sts_v4(half + swz128(row, (c & 3) * 2), w[0], w[1], w[2], w[3]);
+      sts_v4(half + swz128(row, (c & 3) * 2 + 1), w[4], w[5], w[6], w[7]);
     }
     __syncwarp();
   }
+  // Key operands: token lane/4 of each octet, codes at dims 16kk + 4c .. 4c+3.
+  uint32_t kw[D / 16][2];
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int tk = warp * 16 + nt * 8 + (lane >> 2);
+      asm volatile("ld.shared.u32 %0, [%1];"
+                   : "=r"(kw[kk][nt])
+                   : "r"(kbase + swz128(tk, kk) + 4 * (lane & 3)));
+    }
   float s[2][4];
 #pragma unroll
   for (int i = 0; i < 2; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) s[i][e] = 0.f;
-  {
-    const int qr = (mi & 1) * 8 + rr < group ? (mi & 1) * 8 + rr : 0;
+  uint4 qn = lds_v4(qfrag + lane * 16);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t a[4];
-      ldsm_x4(qbase + (kk >> 2) * q_half + swz128(qr, (kk & 3) * 2 + (mi >> 1)), a[0], a[1],
-              a[2], a[3]);
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t qa[4] = {qn.x, qn.y, qn.z, qn.w};
+    if (kk + 1 < D / 16) qn = lds_v4(qfrag + ((kk + 1) * 32 + lane) * 16);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        // B fragment: dims kk*16 + 2*(lane%4) + {0,1} and + 8 of token lane/4
-        // (one int8 chunk of the swizzled code row = 16 dims).
-        const int tk = warp * 16 + nt * 8 + (lane >> 2);
-        const uint32_t at = kbase + swz128(tk, kk) + 2 * (lane & 3);
-        MmaOp<T>::run(s[nt], a, i8x2_to_16<T>(lds_u16(at)), i8x2_to_16<T>(lds_u16(at + 8)));
-      }
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t b0, b1;
+      i8x4_to_f16(kw[kk][nt], b0, b1);
+      MmaOp<__half>::run(s[nt], qa, b0, b1);
     }
   }
-  const int c0 = 2 * (lane & 3);
   float vsc[2][2];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int k = nt * 8 + c0 + e;
-      const int t = warp * 16 + k;
       const bool in = k >= vlo && k < valid;
       // Stale stage contents outside [vlo, valid) never enter arithmetic.
-      const float ks = in ? lds_f32(scale_addr(kscale, t, log2_box)) : 0.f;
-      vsc[nt][e] = in ? lds_f32(scale_addr(vscale, t, log2_box)) : 0.f;
+      const float ks = in ? ksr[nt][e] : 0.f;
+      vsc[nt][e] = in ? vsr[nt][e] : 0.f;
       s[nt][e] = in ? s[nt][e] * (scale_log2 * ks) : -INFINITY;
       s[nt][e + 2] = in ? s[nt][e + 2] * (scale_log2 * ks) : -INFINITY;
     }
@@ -405,6 +470,7 @@ __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uin
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
   const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const bool grew = mn0 != m[0] || mn1 != m[1];
   const float corr0 = fast_exp2(m[0] - mn0), corr1 = fast_exp2(m[1] - mn1);
   m[0] = mn0;
   m[1] = mn1;
@@ -424,23 +490,29 @@ __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uin
   pa[1] = Pack<__half>::run(p[0][2] * vsc[0][0], p[0][3] * vsc[0][1], ra, rb);
   pa[2] = Pack<__half>::run(p[1][0] * vsc[1][0], p[1][1] * vsc[1][1], ra, rb);
   pa[3] = Pack<__half>::run(p[1][2] * vsc[1][0], p[1][3] * vsc[1][1], ra, rb);
+  if (__any_sync(0xffffffffu, grew)) {  // O keeps its scale while no row max grows
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) {
-    o[n][0] *= corr0;
-    o[n][1] *= corr0;
-    o[n][2] *= corr1;
-    o[n][3] *= corr1;
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] *= corr0;
+      o[n][1] *= corr0;
+      o[n][2] *= corr1;
+      o[n][3] *= corr1;
+    }
   }
   const int tok = (mi & 1) * 8 + rr;  // row of the warp's staging tile
+  uint32_t vb[D / 16][4];
 #pragma unroll
   for (int dp = 0; dp < D / 16; ++dp) {
     const int dcol = dp * 16 + (mi >> 1) * 8;
-    uint32_t b0, b1, b2, b3;
-    ldsm_x4_t(vst + (dcol >> 6) * (16 * 128) + swz128(tok, (dcol & 63) >> 3), b0, b1, b2, b3);
-    // Codes are finite, and the weights outside [vlo, valid) are exact zeros,
-    // so no value row needs masking here.
-    MmaOp<__half>::run(o[2 * dp], pa, b0, b1);
-    MmaOp<__half>::run(o[2 * dp + 1], pa, b2, b3);
+    ldsm_x4_t(vst + (dcol >> 6) * (16 * 128) + swz128(tok, (dcol & 63) >> 3), vb[dp][0],
+              vb[dp][1], vb[dp][2], vb[dp][3]);
+  }
+  // Codes are finite, and the weights outside [vlo, valid) are exact zeros,
+  // so no value row needs masking here.
+#pragma unroll
+  for (int dp = 0; dp < D / 16; ++dp) {
+    MmaOp<__half>::run(o[2 * dp], pa, vb[dp][0], vb[dp][1]);
+    MmaOp<__half>::run(o[2 * dp + 1], pa, vb[dp][2], vb[dp][3]);
   }
   __syncwarp();  // the staging tile is rewritten by the warp's next tile
 }
@@ -569,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const __grid_constant__ DecodeParams p) {
   constexpr int kHalves = Layout<D, kI8>::kHalves;
   constexpr int kKBytes = Layout<D, kI8>::kKBytes;
+  constexpr int kStages = Layout<D, kI8>::kStages;
   const Layout<D, kI8> L(p.batch, p.group);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -764,6 +837,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     l[0] = l[1] = 0.f;
   };
   reset();
+  bool need_q = true;  // INT8: the segment's query fragments are still to be built
   int seg_first_j = cur.j;
   int slot = 0;  // 0 for the first segment this CTA touches, 1 afterwards
   const uint32_t sbase = smem_u32(smem);
@@ -773,6 +847,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t phase = (it / kStages) & 1;
     bool ok = !*abort_flag && mbar_wait_bounded(&full[stage], phase, p.err_flag);
     if (!ok) *abort_flag = 1;
+    if constexpr (kI8) {
+      // Every consumer warp reaches this point at the same tile (need_q is
+      // set at the same segment boundaries for all of them), whether or not
+      // its tokens are attended, so the barrier always completes; after a
+      // failed wait the stage's query rows are stale but still in bounds.
+      if (need_q) {
+        build_q_i8<T, D>(sbase + stage * L.stage + L.qoff, L.q_half, G, warp, lane,
+                         sbase + L.qfrag);
+        named_bar_sync(2, kConsumerWarps * 32);
+        need_q = false;
+      }
+    }
     const int Lc = lens[cur.b];
     const int row0 = (first_tile(Lc, p.window) + cur.j) * kTile + warp * 16;
     const int valid = min(16, Lc - row0);                     // rows [vlo, valid) of the
@@ -780,9 +866,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (ok && valid > vlo) {
       const uint32_t kb = sbase + stage * L.stage;
       if constexpr (kI8)
-        attend_16_i8<T, D>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
-                           p.log2_box, warp, lane, vlo, valid, p.scale_log2, kb + L.qoff,
-                           L.q_half, G, sbase + L.vstg + warp * 16 * D * 2, o, m, l);
+        attend_16_i8<D>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
+                        p.log2_box, warp, lane, vlo, valid, p.scale_log2, sbase + L.qfrag,
+                        sbase + L.vstg + warp * 16 * D * 2, o, m, l);
       else
         attend_16<T, D>(kb, kb + kKBytes, warp, lane, vlo, valid, p.scale_log2, kb + L.qoff,
                         L.q_half, G, o, m, l);
@@ -824,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       slot = 1;
       cur.advance(cum, B, hkv);
       reset();
+      need_q = true;
       seg_first_j = cur.j;
     } else {
       cur.advance(cum, B, hkv);

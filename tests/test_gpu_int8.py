@@ -122,14 +122,16 @@ def test_int8_step_write_then_decode(kvc_lib):
     ref = O.paged_decode_int8(case.q.double().numpy(), rk, rv, rks, rvs, case.block_table.numpy(),
                               case.seq_lens.numpy(), case.scale)
     assert excess(out, ref, "bf16") <= 0
-    # and the quantised cache stays close to the 16-bit attention it stands for: the
-    # quantisation error (the oracle's pin bounds it by 2e-2 on such rows) plus the
-    # bf16 rounding of the output
+    # and the quantised cache stays near the 16-bit attention it stands for.  A stored
+    # element is within half a code step of the row it encodes (amax / 254, about 0.014
+    # for these N(0, 1) rows); short sequences (5 and 17 tokens here) do not average
+    # that out, and the bf16 rounding of the output comes on top.
     exact = O.paged_decode(case.q.double().numpy(), *O.reshape_and_cache(
         case.new_key.double().numpy(), case.new_value.double().numpy(),
         case.key_cache.double().numpy(), case.value_cache.double().numpy(), sm),
         case.block_table.numpy(), case.seq_lens.numpy(), case.scale)
-    assert excess(out, exact, "bf16") <= 1e-2
+    half_step = float(np.max(vs)) / 2
+    assert excess(out, exact, "bf16") <= 2 * half_step
 
 
 def test_int8_rejects_other_head_dims(kvc_lib):
