@@ -82,6 +82,13 @@ struct Tc2Params {
 __device__ __forceinline__ int band_start(int pos, int window) {
   return window > 0 && pos >= window ? pos - window + 1 : 0;
 }
+// The band of a kernel instance: the kernel is compiled separately for band
+// and causal attention, so the causal instance carries none of the band's
+// arithmetic (its window is the constant 0).
+template <bool kBand>
+__device__ __forceinline__ int window_of(const Tc2Params& p) {
+  return kBand ? p.window : 0;
+}
 
 template <int D>
 struct Tc2Layout {
@@ -315,7 +322,7 @@ __device__ __forceinline__ void tc2_mma(const Tc2Params& p, uint8_t* smem, uint6
 
 // Softmax warpgroup of head x (threads x*128 .. +127): thread owns query row
 // `row`, all 128 columns of each tile.
-template <typename T, int D>
+template <typename T, int D, bool kBand>
 __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, uint64_t* bars,
                                             volatile int* abort_flag, uint32_t tmem, int x,
                                             int row, int j0, int n_tiles, int q0, int ctx,
@@ -339,7 +346,7 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     // reach past this row, or start before its band, take the masked path.
     const int kv0 = (j0 + j) * kBN;
     const int lim = min(pos + 1, kv_len) - kv0;
-    const int lo = band_start(pos, p.window) - kv0;
+    const int lo = kBand ? band_start(pos, p.window) - kv0 : 0;
     const bool masked = lim < kBN || lo > 0;
     float mx8[8];
 #pragma unroll
@@ -402,7 +409,7 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     // both heads, before either head's P V of the tile) so stale contents
     // cannot reach P V.
     const int valid = kv_len - kv0;
-    const int zlo = band_start(ctx + q0, p.window) - kv0;
+    const int zlo = kBand ? band_start(ctx + q0, p.window) - kv0 : 0;
     if (valid < kBN || zlo > 0) {
       wait_t2(&bars[kVFull0 + (gj & 1)], (gj >> 1) & 1, abort_flag, p.err_flag);
       uint8_t* vst = smem + L::kV + (gj & 1) * L::kStageBytes;
@@ -511,10 +518,12 @@ struct Tc2Item {
 
 // Key tiles j0 .. j0 + n_tiles - 1 of a query tile: from the tile holding
 // the band start of its first row to the tile holding its last row.
+template <bool kBand>
 __device__ __forceinline__ void tc2_tiles(const Tc2Params& p, Tc2Item& it) {
-  it.j0 = band_start(it.ctx + it.q0, p.window) / kBN;
+  it.j0 = band_start(it.ctx + it.q0, window_of<kBand>(p)) / kBN;
   it.n_tiles = (it.ctx + it.q0 + it.q_rows - 1) / kBN + 1 - it.j0;
 }
+template <bool kBand>
 __device__ __forceinline__ bool tc2_item(const Tc2Params& p, int w, int lane, Tc2Item& it) {
   const int pairs = p.num_q_heads / 2;
   int s = 0, tile = 0, ctx = 0, len = 0;
@@ -526,12 +535,13 @@ __device__ __forceinline__ bool tc2_item(const Tc2Params& p, int w, int lane, Tc
   it.ctx = ctx;
   it.kv_len = ctx + len;
   it.ok = it.kv_len <= p.max_blocks * p.block_size;
-  tc2_tiles(p, it);
+  tc2_tiles<kBand>(p, it);
   it.tok0 = p.cu_seqlens[s] + it.q0;
   return true;
 }
 
 // The work item of query tile t of sequence s, head pair `pair`.
+template <bool kBand>
 __device__ __forceinline__ void tc2_item_at(const Tc2Params& p, int s, int t, int pair,
                                             Tc2Item& it) {
   const int len = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
@@ -542,7 +552,7 @@ __device__ __forceinline__ void tc2_item_at(const Tc2Params& p, int s, int t, in
   it.ctx = p.context_lens ? p.context_lens[s] : 0;
   it.kv_len = it.ctx + len;
   it.ok = it.kv_len <= p.max_blocks * p.block_size;
-  tc2_tiles(p, it);
+  tc2_tiles<kBand>(p, it);
   it.tok0 = p.cu_seqlens[s] + it.q0;
 }
 
@@ -572,7 +582,7 @@ __device__ __forceinline__ int tc2_tiles_of_weight(const Tc2Params& p, int s, in
   if (nq > 0 && tc2_weight(ctx, len, nq - 1) == n) t_out[cnt++] = nq - 1;
   return cnt;
 }
-template <int D>
+template <int D, bool kBand>
 __device__ int tc2_build_schedule(const Tc2Params& p, uint8_t* smem, int tid, int warp, int lane,
                                   int c, int G) {
   using L = Tc2Layout<D>;
@@ -584,7 +594,7 @@ __device__ int tc2_build_schedule(const Tc2Params& p, uint8_t* smem, int tid, in
   if (tid == 0) {
     misc[0] = 0;
     // The closed forms below assume causal weights; a band walks unsorted.
-    misc[1] = pairs > 255 || p.window > 0 ? 1 : 0;
+    misc[1] = pairs > 255 || kBand ? 1 : 0;
   }
   __syncthreads();
   for (int s = tid; s < p.num_seqs; s += kThreads) {
@@ -677,7 +687,7 @@ __device__ int tc2_build_schedule(const Tc2Params& p, uint8_t* smem, int tid, in
 // queries, K/V tiles and first S are loaded and computed while the softmax
 // warps finish the previous item's epilogue.  An item whose sequence does not
 // fit the block table is skipped (KVC_FLAG_LEN_RANGE, nothing written).
-template <typename T, int D, bool kBf16>
+template <typename T, int D, bool kBf16, bool kBand>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -707,17 +717,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const int nsched = tc2_build_schedule<D>(p, smem, tid, warp, lane, c, G);
+  const int nsched = tc2_build_schedule<D, kBand>(p, smem, tid, warp, lane, c, G);
   const int2* list = reinterpret_cast<const int2*>(smem + L::kList);
   // The k-th item of this CTA: from the sorted schedule, or items c + k*G.
   auto next_item = [&](int k, Tc2Item& it) -> bool {
     if (nsched >= 0) {
       if (k >= nsched) return false;
       const int2 e = list[k];
-      tc2_item_at(p, e.x, e.y >> 8, e.y & 255, it);
+      tc2_item_at<kBand>(p, e.x, e.y >> 8, e.y & 255, it);
       return true;
     }
-    return tc2_item(p, c + k * G, lane, it);
+    return tc2_item<kBand>(p, c + k * G, lane, it);
   };
 
   int gj0 = 0, ni = 0;
@@ -727,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Tc2Item it;
       if (!next_item(k, it)) break;
       if (!it.ok) continue;
-      tc2_softmax<T, D>(p, smem, bars, abort_flag, tmem, x, tid % kHeadThreads, it.j0,
+      tc2_softmax<T, D, kBand>(p, smem, bars, abort_flag, tmem, x, tid % kHeadThreads, it.j0,
                         it.n_tiles, it.q0, it.ctx, it.kv_len, it.q_rows, it.tok0, it.h0 + x,
                         gj0, ni);
       gj0 += it.n_tiles;
@@ -749,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc2_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, it.s, it.h0,
                       it.h0 / p.group, it.tok0, it.kv_len, it.j0, it.n_tiles,
-                      band_start(it.ctx + it.q0, p.window), gj0, ni, lane);
+                      band_start(it.ctx + it.q0, window_of<kBand>(p)), gj0, ni, lane);
       gj0 += it.n_tiles;
       ++ni;
       if (*abort_flag) break;
@@ -784,11 +794,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int D, bool kBf16>
+template <typename T, int D, bool kBf16, bool kBand>
 kvc_status run_prefill_tc2(const PrefillArgs& a) {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(prefill_tc2_kernel<T, D, kBf16>,
+    cudaFuncSetAttribute(prefill_tc2_kernel<T, D, kBf16, kBand>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Layout<D>::kTotal);
   });
   CUtensorMap tq, tk, tv;
@@ -834,22 +844,26 @@ kvc_status run_prefill_tc2(const PrefillArgs& a) {
   if (sms <= 0) return KVC_ERR_CUDA;
   const long long grid = items < sms ? items : sms;
   if (grid <= 0) return KVC_OK;
-  prefill_tc2_kernel<T, D, kBf16><<<static_cast<unsigned>(grid), kThreads, Tc2Layout<D>::kTotal,
-                                    a.stream>>>(tq, tk, tv, p);
+  prefill_tc2_kernel<T, D, kBf16, kBand><<<static_cast<unsigned>(grid), kThreads,
+                                           Tc2Layout<D>::kTotal, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
+// Two heads per CTA; the caller checks that the GQA group size is even.
+template <bool kBand>
+kvc_status launch_tc2(const PrefillArgs& a) {
+  if (a.head_dim == 64)
+    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 64, true, kBand>(a)
+                               : run_prefill_tc2<__half, 64, false, kBand>(a);
+  if (a.head_dim == 128)
+    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 128, true, kBand>(a)
+                               : run_prefill_tc2<__half, 128, false, kBand>(a);
+  return KVC_ERR_UNSUPPORTED;
+}
 }  // namespace
 
-// Two heads per CTA; the caller checks that the GQA group size is even.
 kvc_status launch_prefill_attention_tc2(const PrefillArgs& a) {
-  if (a.head_dim == 64)
-    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 64, true>(a)
-                               : run_prefill_tc2<__half, 64, false>(a);
-  if (a.head_dim == 128)
-    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 128, true>(a)
-                               : run_prefill_tc2<__half, 128, false>(a);
-  return KVC_ERR_UNSUPPORTED;
+  return a.window > 0 ? launch_tc2<true>(a) : launch_tc2<false>(a);
 }
 
 }  // namespace kvc
