@@ -633,6 +633,38 @@ def measure_serving_loop(kvc, dev, rank, steps):
     return res
 
 
+def measure_fused_write(kvc, dev, rank, steps, warmup):
+    """The MLA decode step's fused latent write: 64 rows [compressed kv 512 | key rope 64],
+    RMSNorm of the first part into cache_nope and RoPE (at seq_lens - 1) of the second into
+    cache_rope, on the MLA workload's caches."""
+    c = make_config("mla_decode", seed=rank, value_device=str(dev))
+    B, bs = c.q_nope.shape[0], c.block_size
+    g = torch.Generator(device=dev).manual_seed(rank + 7)
+    kv = torch.randn(B, 1, 576, generator=g, device=dev).to(c.q_nope.dtype)
+    gamma = torch.ones(512, dtype=c.q_nope.dtype, device=dev)
+    table = kvc.rope_cos_sin_table(8192, 64, 10000.0, device=dev)
+    slots = kvc.build_slot_mapping(c.block_table.to(dev), bs, c.write_pos.to(dev),
+                                   c.cache_nope.shape[0])
+    pos = c.write_pos.to(dev)
+
+    def write():
+        kvc.rmsnorm_rope_cache(kv, gamma, 1e-6, table, pos, slots, c.cache_nope, c.cache_rope)
+
+    for _ in range(warmup):
+        write()
+    torch.cuda.synchronize()
+    graphs = [("write", capture(write))]
+    with ClockSampler(dev.index or 0) as clk:
+        _, per = time_graphs(graphs, steps)
+    by = B * 576 * 2 * 2 + B * 64 * 4 + 2 * B * 4 + 512 * 2
+    hp, hkind = peaks()
+    fig = _roofline("rmsnorm_rope_cache_kernel (kvc_rmsnorm_rope_cache, 64 latent rows)",
+                    per["write"], by, "GB/s", hp, hkind, clk.summary(), bound="launch",
+                    rows=B)
+    del c, kv, table, graphs
+    return fig
+
+
 def run_mixed(args, kvc, dev, rank):
     pf, dc, ms = measure_mixed(kvc, dev, rank, max(3, args.steps // 4), args.warmup)
     print(json.dumps({"workload": CONFIGS["mixed_packed"]["about"], "ms_per_step": ms,
@@ -652,6 +684,7 @@ MEASURES = {
     "gqa8b_decode_int8": measure_int8,
     "serving_loop": lambda kvc, dev, rank, steps, warmup: measure_serving_loop(kvc, dev, rank,
                                                                                steps),
+    "mla_fused_write": measure_fused_write,
 }
 
 
@@ -668,6 +701,8 @@ def secondary(kvc, dev, rank, steps, warmup):
     out["gqa8b_decode_int8"] = measure_int8(kvc, dev, rank, steps, warmup)
     torch.cuda.empty_cache()
     out["serving_loop"] = measure_serving_loop(kvc, dev, rank, steps)
+    torch.cuda.empty_cache()
+    out["mla_fused_write"] = measure_fused_write(kvc, dev, rank, steps, warmup)
     torch.cuda.empty_cache()
     return out
 
