@@ -479,22 +479,17 @@ def measure_mla(kvc, dev, rank, steps, warmup):
     slots = torch.empty(B, dtype=torch.int32, device=dev)
     out = torch.empty_like(d["q_nope"])
     ws = torch.zeros(max(kvc.mla_workspace_size(), 16), dtype=torch.uint8, device=dev)
-    nb = d["cache_nope"].shape[0]
 
-    def write():
-        kvc.build_slot_mapping(d["block_table"], c.block_size, d["write_pos"], nb, out=slots)
-        kvc.reshape_and_cache(d["new_nope"], d["new_rope"], d["cache_nope"], d["cache_rope"],
-                              slots)
-
-    def decode():
-        kvc.mla_paged_decode(d["q_nope"], d["q_rope"], d["cache_nope"], d["cache_rope"],
-                             d["block_table"], d["seq_lens"], c.scale, out=out, workspace=ws)
+    def step():  # latent write of the new token and MLA decode, one call
+        kvc.mla_paged_decode_append(d["q_nope"], d["q_rope"], d["new_nope"], d["new_rope"],
+                                    d["cache_nope"], d["cache_rope"], d["block_table"],
+                                    d["seq_lens"], c.scale, out=out, slot_mapping=slots,
+                                    workspace=ws)
 
     for _ in range(warmup):
-        write()
-        decode()
+        step()
     torch.cuda.synchronize()
-    graphs = [("write", capture(write)), ("decode", capture(decode))]
+    graphs = [("decode", capture(step))]
     for _ in range(warmup):
         for _, g in graphs:
             g.replay()
@@ -507,12 +502,13 @@ def measure_mla(kvc, dev, rank, steps, warmup):
     flops = toks * 128 * (2 * 576 + 2 * 512)
     hp, hkind = peaks()
     tp, tkind = tensor_peak()
-    fig = _roofline("mla_decode_kernel + mla_merge_kernel (kvc_mla_paged_decode)", per["decode"],
+    by += B * 576 * 2 * 2 + 4 * B          # the new latent rows read and written, slots
+    fig = _roofline("mla_decode_kernel + mla_merge_kernel (kvc_mla_paged_decode_append: latent "
+                    "write of the new token and MLA decode in one call)", per["decode"],
                     by, "GB/s", hp, hkind, clk.summary(), bound="hbm",
                     tflops=flops / (per["decode"] * 1e-3) / 1e12, tensor_peak=tp,
                     tensor_frac=flops / (per["decode"] * 1e-3) / 1e12 / tp,
-                    write_ms=per["write"], ms_per_step=total_ms / steps,
-                    tokens_per_s=B / (total_ms / steps * 1e-3))
+                    ms_per_step=total_ms / steps, tokens_per_s=B / (total_ms / steps * 1e-3))
     del d, out, ws, c, graphs
     return fig
 

@@ -463,6 +463,39 @@ kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const vo
                                 kvc_stream_t stream);
 
 /*
+ * kvc_mla_paged_decode_append -- one MLA decode step in one call: the latent
+ * row of each sequence's new token is written into the cache, then attended.
+ * Identical in effect to kvc_build_slot_mapping (start_pos = seq_lens - 1) +
+ * kvc_reshape_and_cache (cache_nope as key, cache_rope as value) +
+ * kvc_mla_paged_decode for every sequence with seq_lens[b] >= 1: [SKILL] 3.6
+ * and [ATB] 4.2 put the cache write before the attention that reads it;
+ * Mode 3 stores the latent as cache_nope + cache_rope.
+ *
+ *   p = seq_lens[b] - 1;  slot = block_table[b][p / block_size] * block_size
+ *                                + p % block_size;
+ *   cache_nope row `slot` <- new_nope[b];  cache_rope row `slot` <- new_rope[b];
+ *   slot_mapping[b] = slot (or -1 when seq_lens[b] == 0: nothing is written);
+ *   out = kvc_mla_paged_decode over the updated caches.
+ *
+ * new_nope: [batch, 512], new_rope: [batch, 64] (device, 16-byte aligned);
+ * slot_mapping: int32 [batch] output, may be NULL; every other argument, the
+ * workspace and the errors are those of kvc_mla_paged_decode.  Each CTA
+ * writes the columns of the new row that it then reads, before it reads
+ * them, so no other ordering is needed.  A block_table entry outside
+ * [0, num_blocks) sets KVC_FLAG_BLOCK_ID_RANGE and that row is not written.
+ */
+kvc_status kvc_mla_paged_decode_append(const void* q_nope, const void* q_rope,
+                                       const void* new_nope, const void* new_rope,
+                                       void* cache_nope, void* cache_rope,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       int32_t* slot_mapping, void* out, int batch,
+                                       int num_heads, int d_nope, int d_rope, int block_size,
+                                       int max_blocks_per_seq, int num_blocks, float scale,
+                                       kvc_dtype dtype, int num_ctas, void* workspace,
+                                       size_t workspace_bytes, uint32_t* err_flag,
+                                       kvc_stream_t stream);
+
+/*
  * kvc_paged_decode_no_alloc -- kvc_paged_decode for callers that cannot
  * allocate device memory.  The source pages have no counterpart to this entry
  * point; it exists for callers such as a host application that gives this

@@ -43,6 +43,8 @@ _SIGS = {
     "kvc_mla_paged_decode_workspace_size": (_S, [_I, _I, _I, _I]),
     "kvc_mla_paged_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                   _I, _P, _S, _P, _P]),
+    "kvc_mla_paged_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                         _I, _I, _I, _F, _I, _I, _P, _S, _P, _P]),
     "kvc_varlen_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _I, _I, _F, _I, _P, _P]),
     "kvc_varlen_prefill_paged_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
@@ -495,6 +497,47 @@ def mla_paged_decode(q_nope: torch.Tensor, q_rope: torch.Tensor, cache_nope: tor
         bs, block_table.shape[1], NB, float(scale), _DT[q_nope.dtype], num_ctas,
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _flag(err_flag),
         _stream()))
+    return out
+
+
+def mla_paged_decode_append(q_nope: torch.Tensor, q_rope: torch.Tensor, new_nope: torch.Tensor,
+                            new_rope: torch.Tensor, cache_nope: torch.Tensor,
+                            cache_rope: torch.Tensor, block_table: torch.Tensor,
+                            seq_lens: torch.Tensor, scale: float,
+                            out: Optional[torch.Tensor] = None,
+                            slot_mapping: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                            workspace: Optional[torch.Tensor] = None,
+                            err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One MLA decode step in one call: write new_nope [B, 512] / new_rope [B, 64] (or
+    [B, 1, width]) at position seq_lens[b] - 1 of each sequence (slot into slot_mapping, -1
+    for an empty sequence), then decode as mla_paged_decode over seq_lens."""
+    _cuda("q_nope", q_nope)
+    _cuda("q_rope", q_rope, q_nope.dtype)
+    _cuda("new_nope", new_nope, q_nope.dtype)
+    _cuda("new_rope", new_rope, q_nope.dtype)
+    _cuda("cache_nope", cache_nope, q_nope.dtype)
+    _cuda("cache_rope", cache_rope, q_nope.dtype)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("seq_lens", seq_lens, torch.int32)
+    B, H, dn = q_nope.shape
+    if new_nope.numel() != B * dn or new_rope.numel() != B * q_rope.shape[-1]:
+        raise ValueError("new_nope / new_rope must hold one latent row per sequence")
+    NB, bs = cache_nope.shape[0], cache_nope.shape[1]
+    if out is None:
+        out = torch.empty_like(q_nope)
+    _cuda("out", out, q_nope.dtype)
+    if slot_mapping is not None:
+        _cuda("slot_mapping", slot_mapping, torch.int32)
+    if workspace is None:
+        workspace = torch.empty(max(mla_workspace_size(num_ctas), 16), dtype=torch.uint8,
+                                device=q_nope.device)
+    _cuda("workspace", workspace)
+    _check("kvc_mla_paged_decode_append", lib().kvc_mla_paged_decode_append(
+        q_nope.data_ptr(), q_rope.data_ptr(), new_nope.data_ptr(), new_rope.data_ptr(),
+        cache_nope.data_ptr(), cache_rope.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+        _ptr(slot_mapping), out.data_ptr(), B, H, dn, q_rope.shape[-1], bs, block_table.shape[1],
+        NB, float(scale), _DT[q_nope.dtype], num_ctas, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _flag(err_flag), _stream()))
     return out
 
 

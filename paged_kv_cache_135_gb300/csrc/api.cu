@@ -461,13 +461,14 @@ size_t kvc_mla_paged_decode_workspace_size(int num_heads, int d_nope, int d_rope
   return ctas >= 2 ? kvc::mla_decode_workspace_bytes(ctas) : 0;
 }
 
-kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
-                                const void* cache_rope, const int32_t* block_table,
-                                const int32_t* seq_lens, void* out, int batch, int num_heads,
-                                int d_nope, int d_rope, int block_size, int max_blocks_per_seq,
-                                int num_blocks, float scale, kvc_dtype dtype, int num_ctas,
-                                void* workspace, size_t workspace_bytes, uint32_t* err_flag,
-                                kvc_stream_t stream) {
+namespace {
+kvc_status mla_decode(const void* q_nope, const void* q_rope, const void* new_nope,
+                      const void* new_rope, const void* cache_nope, const void* cache_rope,
+                      const int32_t* block_table, const int32_t* seq_lens, int32_t* slot_mapping,
+                      void* out, int batch, int num_heads, int d_nope, int d_rope,
+                      int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                      kvc_dtype dtype, int num_ctas, void* workspace, size_t workspace_bytes,
+                      uint32_t* err_flag, kvc_stream_t stream) {
   if (dtype != KVC_F16 && dtype != KVC_BF16) return KVC_ERR_INVALID_ARG;
   if (batch < 0 || num_heads <= 0 || d_nope <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
       num_blocks <= 0 || num_ctas < 0 || num_ctas == 1)
@@ -479,13 +480,16 @@ kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const vo
   if (num_heads != 128 || d_nope != 512) return KVC_ERR_UNSUPPORTED;
   if (!is_pow2(block_size) || block_size < 8) return KVC_ERR_UNSUPPORTED;
   if (batch > 1024) return KVC_ERR_UNSUPPORTED;
-  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL ||
+      static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL)
     return KVC_ERR_UNSUPPORTED;
   if (batch == 0) return KVC_OK;
   if (!q_nope || !cache_nope || !block_table || !seq_lens || !out) return KVC_ERR_INVALID_ARG;
   if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(cache_nope) ||
       !aligned16(cache_rope) || !aligned16(out) || !aligned16(workspace))
     return KVC_ERR_INVALID_ARG;
+  if ((new_nope == nullptr) != (new_rope == nullptr)) return KVC_ERR_INVALID_ARG;
+  if (new_nope && (!aligned16(new_nope) || !aligned16(new_rope))) return KVC_ERR_INVALID_ARG;
   kvc::MlaArgs a;
   a.q_nope = q_nope;
   a.q_rope = q_rope;
@@ -505,7 +509,41 @@ kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const vo
   a.workspace_bytes = workspace_bytes;
   a.err_flag = err_flag;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.new_nope = new_nope;
+  a.new_rope = new_rope;
+  a.slot_out = slot_mapping;
   return kvc::launch_mla_decode(a);
+}
+}  // namespace
+
+kvc_status kvc_mla_paged_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
+                                const void* cache_rope, const int32_t* block_table,
+                                const int32_t* seq_lens, void* out, int batch, int num_heads,
+                                int d_nope, int d_rope, int block_size, int max_blocks_per_seq,
+                                int num_blocks, float scale, kvc_dtype dtype, int num_ctas,
+                                void* workspace, size_t workspace_bytes, uint32_t* err_flag,
+                                kvc_stream_t stream) {
+  return mla_decode(q_nope, q_rope, nullptr, nullptr, cache_nope, cache_rope, block_table,
+                    seq_lens, nullptr, out, batch, num_heads, d_nope, d_rope, block_size,
+                    max_blocks_per_seq, num_blocks, scale, dtype, num_ctas, workspace,
+                    workspace_bytes, err_flag, stream);
+}
+
+kvc_status kvc_mla_paged_decode_append(const void* q_nope, const void* q_rope,
+                                       const void* new_nope, const void* new_rope,
+                                       void* cache_nope, void* cache_rope,
+                                       const int32_t* block_table, const int32_t* seq_lens,
+                                       int32_t* slot_mapping, void* out, int batch,
+                                       int num_heads, int d_nope, int d_rope, int block_size,
+                                       int max_blocks_per_seq, int num_blocks, float scale,
+                                       kvc_dtype dtype, int num_ctas, void* workspace,
+                                       size_t workspace_bytes, uint32_t* err_flag,
+                                       kvc_stream_t stream) {
+  if (batch > 0 && (!new_nope || !new_rope)) return KVC_ERR_INVALID_ARG;
+  return mla_decode(q_nope, q_rope, new_nope, new_rope, cache_nope, cache_rope, block_table,
+                    seq_lens, slot_mapping, out, batch, num_heads, d_nope, d_rope, block_size,
+                    max_blocks_per_seq, num_blocks, scale, dtype, num_ctas, workspace,
+                    workspace_bytes, err_flag, stream);
 }
 
 }  // extern "C"

@@ -155,6 +155,10 @@ struct MlaArgs {
   size_t workspace_bytes;
   uint32_t* err_flag;
   cudaStream_t stream;
+  // Appending decode (all null for plain decode): see kvc_mla_paged_decode_append.
+  const void* new_nope = nullptr;
+  const void* new_rope = nullptr;
+  int32_t* slot_out = nullptr;
 };
 
 // CTAs (an even number: pairs) the MLA kernel runs with (num_ctas <= 0: auto).

@@ -86,6 +86,16 @@ struct MlaParams {
   float* ws_o;    // [clusters][2][2][128][256]
   float* ws_ml;   // [clusters][2][2][128][2]
   uint32_t* err_flag;
+  // Appending decode (all null for plain decode): the latent row of each
+  // sequence's new token, new_nope [B, 512] and new_rope [B, 64], is written
+  // at position seq_lens[b] - 1 into cache_nope / cache_rope by the CTAs that
+  // then read that position, each rank the columns it loads; slot_out[b]
+  // (nullable) gets its slot.
+  const void* new_nope;
+  const void* new_rope;
+  void* cache_nope;
+  void* cache_rope;
+  int32_t* slot_out;
   int batch, block_size, log2_bs, max_blocks, num_blocks, box_tokens;
   float scale_log2;
 };
@@ -203,6 +213,33 @@ __device__ __forceinline__ void mla_producer(const MlaParams& p, const CUtensorM
     const int stage = it % kStages;
     const uint32_t phase = static_cast<uint32_t>(it / kStages) & 1u;
     const int tok = cur.j * kTok + lane * p.box_tokens;
+    if (p.new_nope != nullptr && cur.last()) {
+      // The sequence's last tile holds its new token: write the columns this
+      // rank loads (rank 0: nope 0..255; rank 1: nope 256..511 and rope), 16
+      // bytes per lane, make them visible to the TMA unit, then load the tile
+      // as usual.  No other CTA reads them.
+      const int pos = cur.len - 1;
+      const int pbn = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks +
+                                           (pos >> p.log2_bs)]);
+      if (pbn >= 0 && pbn < p.num_blocks) {
+        const long long row = static_cast<long long>(pbn) * p.block_size + (pos & (p.block_size - 1));
+        const uint4* src = reinterpret_cast<const uint4*>(p.new_nope) +
+                           static_cast<long long>(cur.b) * (kNope / 8) + rank * (kOutCols / 8);
+        uint4* dst = reinterpret_cast<uint4*>(p.cache_nope) + row * (kNope / 8) + rank * (kOutCols / 8);
+        dst[lane] = __ldg(src + lane);  // 32 lanes x 8 elements = the rank's 256 columns
+        if (rank == 1 && lane < kRope / 8)
+          reinterpret_cast<uint4*>(p.cache_rope)[row * (kRope / 8) + lane] =
+              __ldg(reinterpret_cast<const uint4*>(p.new_rope) +
+                    static_cast<long long>(cur.b) * (kRope / 8) + lane);
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        if (rank == 0 && lane == 0 && p.slot_out) p.slot_out[cur.b] = static_cast<int32_t>(row);
+      } else if (lane == 0) {
+        set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
+        if (rank == 0 && p.slot_out) p.slot_out[cur.b] = -1;
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     int pb = -1;
     if (lane < nsub && tok < cur.len)
       pb = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks + (tok >> p.log2_bs)]);
@@ -704,12 +741,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const long long N = cum[B];
   const long long tb = sched::share_begin(cl, N, P), te = sched::share_begin(cl + 1, N, P);
   {  // sequences with no cached token: rows of zeros (this rank's columns)
+     // and, when appending, no slot (-1): there is no new token to write
     T* out = static_cast<T*>(p.out);
     for (int b = cl; b < B; b += P)
-      if (lens[b] == 0)
+      if (lens[b] == 0) {
         for (int e = tid; e < kH * kOutCols; e += kThreads)
           out[(static_cast<long long>(b) * kH + e / kOutCols) * kNope + rank * kOutCols +
               e % kOutCols] = Pack<T>::cvt(0.f);
+        if (tid == 0 && rank == 0 && p.slot_out) p.slot_out[b] = -1;
+      }
   }
   MlaCursor cur;
   if (tb < te) cur.locate(tb, cum, lens, B);
@@ -940,6 +980,11 @@ kvc_status run_mla(const MlaArgs& a, int clusters) {
   p.num_blocks = a.num_blocks;
   p.box_tokens = box_tokens;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.new_nope = a.new_nope;
+  p.new_rope = a.new_rope;
+  p.cache_nope = const_cast<void*>(a.cache_nope);
+  p.cache_rope = const_cast<void*>(a.cache_rope);
+  p.slot_out = a.slot_out;
   mla_decode_kernel<T, kBf16><<<2 * clusters, kThreads, MlaLayout::kBytes, a.stream>>>(qr, cn, cr,
                                                                                        p);
   if (cudaGetLastError() != cudaSuccess) return KVC_ERR_CUDA;

@@ -162,3 +162,70 @@ def test_full_size_mla_step_sampled(kvc_lib):
                                  c.scale)[0]
         worst = max(worst, excess(out[b], ref, "bf16"))
     assert worst <= 0, worst
+
+
+@pytest.mark.parametrize("bs,num_ctas", [(16, 0), (128, 6), (8, 2)])
+def test_mla_append_equals_the_three_call_step(kvc_lib, bs, num_ctas):
+    """kvc_mla_paged_decode_append = slot mapping + latent write + MLA decode, bit for bit;
+    an empty sequence gets slot -1 and no write."""
+    lens = [300, 0, 129, 64, 1, 700]
+    c = mla_case(44, len(lens), lens, block_size=bs, dtype="bf16")
+    d = {k: to_cuda(getattr(c, k)) for k in ("q_nope", "q_rope", "block_table", "seq_lens",
+                                             "write_pos", "new_nope", "new_rope")}
+    cn1, cr1 = to_cuda(c.cache_nope), to_cuda(c.cache_rope)
+    cn2, cr2 = cn1.clone(), cr1.clone()
+    nb = c.cache_nope.shape[0]
+    wp = d["write_pos"].clone()
+    slots = kvc_lib.build_slot_mapping(d["block_table"], bs, wp, nb)
+    live = d["seq_lens"] > 0
+    slots = torch.where(live, slots, torch.full_like(slots, -1))
+    kvc_lib.reshape_and_cache(d["new_nope"], d["new_rope"], cn1, cr1, slots)
+    ref = kvc_lib.mla_paged_decode(d["q_nope"], d["q_rope"], cn1, cr1, d["block_table"],
+                                   d["seq_lens"], c.scale, num_ctas=num_ctas)
+    slot_out = torch.full((len(lens),), -7, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kvc_lib.mla_paged_decode_append(d["q_nope"], d["q_rope"], d["new_nope"], d["new_rope"],
+                                          cn2, cr2, d["block_table"], d["seq_lens"], c.scale,
+                                          slot_mapping=slot_out, num_ctas=num_ctas, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert slot_out.cpu().tolist() == slots.cpu().tolist()
+    sm = O.slot_mapping(c.block_table.numpy(), bs, c.write_pos.numpy())
+    assert [s if L > 0 else -1 for s, L in zip(sm.tolist(), lens)] == slot_out.cpu().tolist()
+    assert torch.equal(cn1.view(torch.int16), cn2.view(torch.int16))
+    assert torch.equal(cr1.view(torch.int16), cr2.view(torch.int16))
+    assert torch.equal(ref.view(torch.int16), out.view(torch.int16))
+
+
+def test_full_size_mla_append_step_sampled(kvc_lib):
+    """The MLA workload's step as the benchmark times it (one append call): slots, the
+    written rows and 11 of the 64 sequences against the oracle."""
+    c = make_config("mla_decode", seed=0, value_device="cuda")
+    cn0, cr0 = c.cache_nope.clone(), c.cache_rope.clone()
+    slot_out = torch.empty(c.q_nope.shape[0], dtype=torch.int32, device="cuda")
+    out = kvc_lib.mla_paged_decode_append(c.q_nope, c.q_rope, c.new_nope, c.new_rope,
+                                          c.cache_nope, c.cache_rope, c.block_table.cuda(),
+                                          c.seq_lens.cuda(), c.scale, slot_mapping=slot_out)
+    torch.cuda.synchronize()
+    ref_slots = O.slot_mapping(c.block_table.numpy(), c.block_size, c.write_pos.numpy())
+    assert slot_out.cpu().numpy().tolist() == ref_slots.tolist()
+    bs = c.block_size
+    idx_b, idx_o = ref_slots // bs, ref_slots % bs
+    got_n = c.cache_nope[torch.from_numpy(idx_b).cuda(), torch.from_numpy(idx_o).cuda()]
+    assert np.array_equal(bits(got_n), bits(c.new_nope))
+    worst = -1.0
+    for b in range(0, 64, 6):
+        L = int(c.seq_lens[b])
+        nblk = -(-L // bs)
+        ids = c.block_table[b, :nblk].long().cuda()
+        cn = cn0[ids].double().cpu().numpy()
+        cr = cr0[ids].double().cpu().numpy()
+        table = np.arange(nblk)[None]
+        sm = O.slot_mapping(table, bs, [L - 1])
+        cn, cr = O.reshape_and_cache(c.new_nope[b:b + 1].double().cpu().numpy(),
+                                     c.new_rope[b:b + 1].double().cpu().numpy(), cn, cr, sm)
+        ref = O.mla_paged_decode(c.q_nope[b:b + 1].double().cpu().numpy(),
+                                 c.q_rope[b:b + 1].double().cpu().numpy(), cn, cr, table, [L],
+                                 c.scale)[0]
+        worst = max(worst, excess(out[b], ref, "bf16"))
+    assert worst <= 0, worst
