@@ -70,11 +70,23 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType type, int rank, const voi
     e[i] = 1;
     if (i + 1 < rank) s[i] = strides_bytes[i];
   }
+  // L2 promotion no wider than the contiguous bytes a box covers: one row of
+  // dimension 0, or box[1] such rows when they are adjacent and the box spans
+  // the whole row.  A wider promotion fetches the neighbouring row (another
+  // head's 128-byte code row of an INT8 cache, say), which the box does not use.
+  const uint64_t elt = type == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1
+                       : type == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
+  uint64_t span = dims[0] * elt;
+  if (rank > 1 && box[0] == dims[0] && strides_bytes[0] == span) span *= box[1];
+  const CUtensorMapL2promotion promo = span >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                       : span >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                       : span >= 64 ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                                                    : CU_TENSOR_MAP_L2_PROMOTION_NONE;
   const CUresult r = fn(map, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s,
                         b, e,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

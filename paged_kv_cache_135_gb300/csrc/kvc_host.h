@@ -28,7 +28,8 @@ int device_sm_count();
 bool encode_tmap_16bit(CUtensorMap* map, kvc_dtype dtype, int rank, const void* base,
                        const uint64_t* dims, const uint64_t* strides_bytes,
                        const uint32_t* box, bool swizzle128);
-// The same for any element type.
+// The same for any element type.  The L2 promotion is the widest of 64 / 128 /
+// 256 bytes that the box's contiguous bytes fill (none below 64).
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base,
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                  bool swizzle128);
