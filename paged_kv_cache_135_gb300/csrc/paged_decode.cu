@@ -50,10 +50,16 @@ namespace {
 constexpr int kTile = 64;            // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;    // 16 tokens each
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-// Pipeline depth: 3 stages of ~33 KB (16-bit cache) or 4 of ~17 KB (INT8,
-// whose stages also hold scales; 4 keeps two CTAs per SM).
+// Pipeline depth: 3 stages, of ~33 KB over a 16-bit cache (two CTAs per SM)
+// or ~20 KB over an INT8 cache (codes, scales and query rows; three CTAs per
+// SM, which measured faster than two with 4 stages).
 template <bool kI8>
-constexpr int stages_of() { return kI8 ? 4 : 3; }
+constexpr int stages_of() { return 3; }
+// Resident CTAs per SM the kernel is compiled for (register budget): three
+// for an INT8 cache with one 8-row query tile, else two (the two-tile INT8
+// kernel would spill under three's 128 registers a thread).
+template <int kQ>
+constexpr int min_ctas_of() { return kQ == 1 ? 3 : 2; }
 constexpr int kMaxBatch = 1024;
 constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a K or V tile
 constexpr int kMaxPieces = 62;           // split shares merged from a shared-memory list
@@ -91,9 +97,8 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 // V tile and the query rows of the tile's (b, g) (all 128-byte swizzled, each
 // 1024-byte aligned as the TMA swizzle requires); every other region starts
 // on a 16-byte boundary.  Over an INT8 cache (kI8) the K and V tiles hold the
-// int8 codes (one 128-byte row per token), the stage also holds the tile's
-// per-token K and V scales, and each consumer warp owns a staging tile for
-// its 16 value rows converted to 16 bits.
+// int8 codes (one 128-byte row per token) and the stage also holds the tile's
+// per-token K and V scales.
 template <int D, bool kI8>
 struct Layout {
   static constexpr int kHalves = D / 64;  // 64-element halves of a 16-bit row
@@ -101,8 +106,6 @@ struct Layout {
   int q_half;   // bytes of one 64-wide half of the G query rows (1024-aligned)
   int scales;   // INT8: K scales then V scales of the stage, kTile floats each
   int qoff;     // query rows of the stage (1024-aligned)
-  int vstg;     // INT8: per consumer warp, its 16 value rows as 16-bit values
-  int qfrag;    // INT8: the segment's fp16 query fragments, [D/16][32 lanes][4 words]
   int stage;    // K tile, V tile, (scales), query rows
   static constexpr int kStages = stages_of<kI8>();
   int bar;      // full[kStages], empty[kStages]
@@ -123,10 +126,7 @@ struct Layout {
     lens = align_up(pieces + kMaxPieces * 4, 16);
     cum = align_up(lens + batch * 4, 16);
     cmb = align_up(cum + (batch + 1) * 4, 16);
-    vstg = align_up(cmb + kConsumerWarps * group * (D + 2) * 4, 1024);
-    qfrag = vstg + kConsumerWarps * 16 * D * 2;
-    total = 1024 + (kI8 ? qfrag + (D / 16) * 32 * 16
-                        : cmb + kConsumerWarps * group * (D + 2) * 4);
+    total = 1024 + cmb + kConsumerWarps * group * (D + 2) * 4;
   }
 };
 
@@ -291,22 +291,14 @@ __device__ __forceinline__ void attend_16(uint32_t kbase, uint32_t vbase, int wa
 
 // ---- INT8 cache: codes to 16-bit values, scales, and one warp's 16 tokens.
 
-__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
-}
-__device__ __forceinline__ void sts_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
-                                       uint32_t w) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z),
-               "r"(w)
-               : "memory");
-}
 __device__ __forceinline__ float lds_f32(uint32_t a) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 
@@ -324,6 +316,28 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
   lo = *reinterpret_cast<const uint32_t*>(&ra);
   hi = *reinterpret_cast<const uint32_t*>(&rb);
 }
+
+// The codes of two tokens at the same four elements (wa, wb: byte k =
+// element k) as four fp16 pairs {token a, token b}, one per element,
+// exactly as i8x4_to_f16: the bytes are first interleaved a0 b0 a1 b1 /
+// a2 b2 a3 b3, then each pair is widened.
+__device__ __forceinline__ void i8x4x2_to_f16_pairs(uint32_t wa, uint32_t wb,
+                                                    uint32_t (&r)[4]) {
+  const uint32_t xa = wa ^ 0x80808080u, xb = wb ^ 0x80808080u;
+  const uint32_t lo = __byte_perm(xa, xb, 0x5140u);
+  const uint32_t hi = __byte_perm(xa, xb, 0x7362u);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const uint32_t t[4] = {__byte_perm(lo, 0x64646464u, 0x4140u),
+                         __byte_perm(lo, 0x64646464u, 0x4342u),
+                         __byte_perm(hi, 0x64646464u, 0x4140u),
+                         __byte_perm(hi, 0x64646464u, 0x4342u)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t[i]), bias);
+    r[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
 
 // A pair of 16-bit query values as an fp16 pair: unchanged for fp16; for bf16
 // exact whenever the values lie in fp16's normal range (|q| in [2^-14, 65504]),
@@ -344,177 +358,171 @@ __device__ __forceinline__ uint32_t scale_addr(uint32_t base, int t, int log2_bo
   return base + ((t >> log2_box) << 7) + ((t & ((1 << log2_box) - 1)) << 2);
 }
 
-// The query fragments of S = Q K^T over an INT8 cache, in fp16 and with the
-// 16 dims of every k-step permuted: lane (g = lane/4, c = lane%4) holds dims
-// 16kk + 4c .. 4c+3 of query rows g and g + 8, so that its key operand is the
-// 4 contiguous codes at the same dims (one 32-bit load).  The dot product does
-// not depend on the order of its terms.  Rows >= G are padding and read row
-// 0.  They are the same for every consumer warp and every tile of a (b, g)
-// segment: at the segment's first tile each warp builds two k-steps of them
-// (from the stage's query rows) into shared memory, [kk][lane] as 16 bytes.
-template <typename T, int D>
-__device__ __forceinline__ void build_q_i8(uint32_t qbase, int q_half, int group, int warp,
-                                           int lane, uint32_t qfrag) {
+// Over an INT8 cache the products run transposed, S^T = K Q^T and
+// O^T = V^T P^T (mma m16n8k16, fp16 operands, fp32 accumulation): the warp's
+// 16 tokens are the M side of the score product and the K side of the value
+// product, and the query group is the N side, NT tiles of 8 query rows (rows
+// >= G are zero queries whose results are dropped).  For G <= 8 this is half
+// the tensor ops and half the accumulator registers of padding the group to
+// 16 rows.
+//
+// Score product, k-step kk (dims 16kk .. 16kk+15, permuted): lane (g =
+// lane/4, c = lane%4) holds dims 16kk + 4c .. 4c+3 of tokens g and g+8 (one
+// 32-bit load of codes each) and of query row g of each tile, in the slots
+// of k = 2c, 2c+1, 2c+8, 2c+9; a dot product does not depend on the order of
+// its terms.  Value product, dims 32blk .. 32blk+31: lane (g, c) loads the
+// codes of tokens 2c, 2c+1, 2c+8, 2c+9 at dims 32blk + 4g .. 4g+3, and the
+// output rows of m-tiles 2blk and 2blk+1 are permuted to match: row g / g+8
+// of m-tile 2blk+h is dim 32blk + 4g + 2h / 32blk + 4g + 2h + 1.
+
+// The segment's query fragments (B of the score product) from the stage's
+// query rows, as fp16: qb[kk][nt] = dims 16kk + 4c .. 4c+3 of row 8nt + g.
+template <typename T, int D, int NT>
+__device__ __forceinline__ void load_q_i8(uint32_t qbase, int q_half, int group, int lane,
+                                          uint32_t (&qb)[D / 16][NT][2]) {
   const int g = lane >> 2, c = lane & 3;
-  const int r0 = g < group ? g : 0, r1 = g + 8 < group ? g + 8 : 0;
 #pragma unroll
-  for (int i = 0; i < D / 16 / kConsumerWarps; ++i) {
-    const int kk = warp * (D / 16 / kConsumerWarps) + i;
-    const uint32_t off = (kk >> 2) * q_half;
-    const int chunk = (kk & 3) * 2 + (c >> 1), byte = (c & 1) * 8;
-    uint32_t w0, w1, w2, w3;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                 : "=r"(w0), "=r"(w1) : "r"(qbase + off + swz128(r0, chunk) + byte));
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                 : "=r"(w2), "=r"(w3) : "r"(qbase + off + swz128(r1, chunk) + byte));
-    // a0: row g dims 4c, 4c+1; a1: row g+8 same; a2: row g dims 4c+2, 4c+3; a3: row g+8 same
-    sts_v4(qfrag + (kk * 32 + lane) * 16, q_pair_f16<T>(w0), q_pair_f16<T>(w2), q_pair_f16<T>(w1),
-           q_pair_f16<T>(w3));
-  }
+  for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r = nt * 8 + g;
+      uint32_t w0 = 0, w1 = 0;
+      if (r < group)
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                     : "=r"(w0), "=r"(w1)
+                     : "r"(qbase + (kk >> 2) * q_half + swz128(r, (kk & 3) * 2 + (c >> 1)) +
+                           (c & 1) * 8));
+      qb[kk][nt][0] = q_pair_f16<T>(w0);
+      qb[kk][nt][1] = q_pair_f16<T>(w1);
+    }
 }
 
 // One warp's 16 tokens of a stage over an INT8 cache.  A cached row is
 // code * scale, so q . k = scale_k * (q . codes_k) and sum_j p_j v_j =
-// sum_j (p_j * scale_v_j) codes_v_j.  Both products run on the tensor cores
-// in fp16 with fp32 accumulation: the codes are exact in fp16, the queries
-// are (qa, see load_q_i8), and the weights p * scale_v keep 11 bits (l sums
-// the plain p, so the weights are not renormalised after rounding).  Each
-// score column is multiplied by its key scale.  The warp's 16 value rows are
-// first converted into `vst`, in the layout of a 16-bit tile, so P V reads
-// them with ldmatrix.trans as the 16-bit path does.
-template <int D>
+// sum_j (p_j * scale_v_j) codes_v_j.  The codes are exact in fp16, the
+// queries are (load_q_i8), and the weights p * scale_v keep 11 bits (l sums
+// the plain p, so the weights are not renormalised after rounding).  State
+// per lane: m, l and O for query rows 8nt + 2c and 8nt + 2c + 1; l is this
+// lane's share (tokens g and g+8), summed over the 8 lanes of a query at the
+// end of the segment.
+template <int D, int NT>
 __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
                                              uint32_t vscale, int log2_box, int warp, int lane,
                                              int vlo, int valid, float scale_log2,
-                                             uint32_t qfrag, uint32_t vst,
-                                             float (&o)[D / 8][4], float (&m)[2],
-                                             float (&l)[2]) {
+                                             const uint32_t (&qb)[D / 16][NT][2],
+                                             float (&o)[NT][D / 16][4], float (&m)[NT][2],
+                                             float (&l)[NT][2]) {
   static_assert(D == 128, "one 128-byte code row per token");
-  const int mi = lane >> 3, rr = lane & 7;
-  const int c0 = 2 * (lane & 3);
-  // Shared-memory loads are issued in groups ahead of their use (the asm
-  // statements keep program order), so their latencies overlap.
-  float ksr[2][2], vsr[2][2];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int t = warp * 16 + nt * 8 + c0 + e;
-      ksr[nt][e] = lds_f32(scale_addr(kscale, t, log2_box));
-      vsr[nt][e] = lds_f32(scale_addr(vscale, t, log2_box));
-    }
-  {  // value codes -> fp16: lane converts 64 codes of row lane / 2
-    const int row = lane >> 1, tok = warp * 16 + row;
-    uint4 u[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) u[i] = lds_v4(vbase + swz128(tok, (lane & 1) * 4 + i));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = (lane & 1) * 4 + i;  // 16 dims
-      uint32_t w[8];
-      i8x4_to_f16(u[i].x, w[0], w[1]);
-      i8x4_to_f16(u[i].y, w[2], w[3]);
-      i8x4_to_f16(u[i].z, w[4], w[5]);
-      i8x4_to_f16(u[i].w, w[6], w[7]);
-      const uint32_t half = vst + (c >> 2) * (16 * 128);
-      sts_v4(half + swz128(row, (c & 3) * 2), w[0], w[1], w[2], w[3]);
-      sts_v4(half + swz128(row, (c & 3) * 2 + 1), w[4], w[5], w[6], w[7]);
-    }
-    __syncwarp();
-  }
-  // Key operands: token lane/4 of each octet, codes at dims 16kk + 4c .. 4c+3.
+  const int g = lane >> 2, c = lane & 3;
+  const int t0 = warp * 16 + g, tv = warp * 16 + 2 * c;
+  // All shared-memory loads first (the asm statements keep program order),
+  // so their latencies overlap.
+  const float ks0 = lds_f32(scale_addr(kscale, t0, log2_box));
+  const float ks1 = lds_f32(scale_addr(kscale, t0 + 8, log2_box));
+  const float vs0 = lds_f32(scale_addr(vscale, t0, log2_box));
+  const float vs1 = lds_f32(scale_addr(vscale, t0 + 8, log2_box));
   uint32_t kw[D / 16][2];
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
+  for (int kk = 0; kk < D / 16; ++kk) {
+    kw[kk][0] = lds_u32(kbase + swz128(t0, kk) + 4 * c);
+    kw[kk][1] = lds_u32(kbase + swz128(t0 + 8, kk) + 4 * c);
+  }
+  uint32_t vw[D / 32][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int tk = warp * 16 + nt * 8 + (lane >> 2);
-      asm volatile("ld.shared.u32 %0, [%1];"
-                   : "=r"(kw[kk][nt])
-                   : "r"(kbase + swz128(tk, kk) + 4 * (lane & 3)));
-    }
-  float s[2][4];
+  for (int blk = 0; blk < D / 32; ++blk) {
+    const int ch = 2 * blk + (g >> 2), off = 4 * (g & 3);
+    vw[blk][0] = lds_u32(vbase + swz128(tv, ch) + off);
+    vw[blk][1] = lds_u32(vbase + swz128(tv + 1, ch) + off);
+    vw[blk][2] = lds_u32(vbase + swz128(tv + 8, ch) + off);
+    vw[blk][3] = lds_u32(vbase + swz128(tv + 9, ch) + off);
+  }
+  float s[NT][4];
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[i][e] = 0.f;
-  uint4 qn = lds_v4(qfrag + lane * 16);
+    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t qa[4] = {qn.x, qn.y, qn.z, qn.w};
-    if (kk + 1 < D / 16) qn = lds_v4(qfrag + ((kk + 1) * 32 + lane) * 16);
+    uint32_t a[4];
+    i8x4_to_f16(kw[kk][0], a[0], a[2]);
+    i8x4_to_f16(kw[kk][1], a[1], a[3]);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      uint32_t b0, b1;
-      i8x4_to_f16(kw[kk][nt], b0, b1);
-      MmaOp<__half>::run(s[nt], qa, b0, b1);
-    }
+    for (int nt = 0; nt < NT; ++nt) MmaOp<__half>::run(s[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
   }
-  float vsc[2][2];
+  // s[nt][0, 1]: token g, queries 2c, 2c+1; s[nt][2, 3]: token g+8.  Stale
+  // stage contents outside [vlo, valid) never enter arithmetic.
+  const bool in0 = g >= vlo && g < valid, in1 = g + 8 >= vlo && g + 8 < valid;
+  const float f0 = in0 ? scale_log2 * ks0 : 0.f, f1 = in1 ? scale_log2 * ks1 : 0.f;
+  const float w0 = in0 ? vs0 : 0.f, w1 = in1 ? vs1 : 0.f;
+  bool grew = false;
+  float corr[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int nt = 0; nt < NT; ++nt) {
+    s[nt][0] = in0 ? s[nt][0] * f0 : -INFINITY;
+    s[nt][1] = in0 ? s[nt][1] * f0 : -INFINITY;
+    s[nt][2] = in1 ? s[nt][2] * f1 : -INFINITY;
+    s[nt][3] = in1 ? s[nt][3] * f1 : -INFINITY;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int k = nt * 8 + c0 + e;
-      const bool in = k >= vlo && k < valid;
-      // Stale stage contents outside [vlo, valid) never enter arithmetic.
-      const float ks = in ? ksr[nt][e] : 0.f;
-      vsc[nt][e] = in ? vsr[nt][e] : 0.f;
-      s[nt][e] = in ? s[nt][e] * (scale_log2 * ks) : -INFINITY;
-      s[nt][e + 2] = in ? s[nt][e + 2] * (scale_log2 * ks) : -INFINITY;
+      float mx = fmaxf(s[nt][e], s[nt][e + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mn = fmaxf(m[nt][e], mx);
+      grew |= mn != m[nt][e];
+      corr[nt][e] = fast_exp2(m[nt][e] - mn);
+      m[nt][e] = mn;
     }
-  float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-  float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-  const bool grew = mn0 != m[0] || mn1 != m[1];
-  const float corr0 = fast_exp2(m[0] - mn0), corr1 = fast_exp2(m[1] - mn1);
-  m[0] = mn0;
-  m[1] = mn1;
-  float p[2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    p[nt][0] = fast_exp2(s[nt][0] - mn0);
-    p[nt][1] = fast_exp2(s[nt][1] - mn0);
-    p[nt][2] = fast_exp2(s[nt][2] - mn1);
-    p[nt][3] = fast_exp2(s[nt][3] - mn1);
   }
-  l[0] = l[0] * corr0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-  l[1] = l[1] * corr1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-  uint32_t pa[4];
-  float ra, rb;
-  pa[0] = Pack<__half>::run(p[0][0] * vsc[0][0], p[0][1] * vsc[0][1], ra, rb);
-  pa[1] = Pack<__half>::run(p[0][2] * vsc[0][0], p[0][3] * vsc[0][1], ra, rb);
-  pa[2] = Pack<__half>::run(p[1][0] * vsc[1][0], p[1][1] * vsc[1][1], ra, rb);
-  pa[3] = Pack<__half>::run(p[1][2] * vsc[1][0], p[1][3] * vsc[1][1], ra, rb);
+  // The B fragments of P^T: lane (g, c) needs the weights of query row 8nt+g
+  // at tokens 2c, 2c+1 (lanes 8c + g/2 and 8c + 4 + g/2 hold them, as the
+  // low or high half of their packed pair) and at tokens 2c+8, 2c+9 (the same
+  // lanes' second pair).
+  const int src_a = 8 * c + (g >> 1), src_b = src_a + 4;
+  const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+  uint32_t pb[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float p0 = fast_exp2(s[nt][0] - m[nt][0]), p1 = fast_exp2(s[nt][1] - m[nt][1]);
+    const float p2 = fast_exp2(s[nt][2] - m[nt][0]), p3 = fast_exp2(s[nt][3] - m[nt][1]);
+    l[nt][0] = l[nt][0] * corr[nt][0] + (p0 + p2);
+    l[nt][1] = l[nt][1] * corr[nt][1] + (p1 + p3);
+    float ra, rb;
+    const uint32_t x = Pack<__half>::run(p0 * w0, p1 * w0, ra, rb);
+    const uint32_t y = Pack<__half>::run(p2 * w1, p3 * w1, ra, rb);
+    const uint32_t xa = __shfl_sync(0xffffffffu, x, src_a);
+    const uint32_t xb = __shfl_sync(0xffffffffu, x, src_b);
+    const uint32_t ya = __shfl_sync(0xffffffffu, y, src_a);
+    const uint32_t yb = __shfl_sync(0xffffffffu, y, src_b);
+    pb[nt][0] = __byte_perm(xa, xb, sel);
+    pb[nt][1] = __byte_perm(ya, yb, sel);
+  }
   if (__any_sync(0xffffffffu, grew)) {  // O keeps its scale while no row max grows
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= corr0;
-      o[n][1] *= corr0;
-      o[n][2] *= corr1;
-      o[n][3] *= corr1;
-    }
-  }
-  const int tok = (mi & 1) * 8 + rr;  // row of the warp's staging tile
-  uint32_t vb[D / 16][4];
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-  for (int dp = 0; dp < D / 16; ++dp) {
-    const int dcol = dp * 16 + (mi >> 1) * 8;
-    ldsm_x4_t(vst + (dcol >> 6) * (16 * 128) + swz128(tok, (dcol & 63) >> 3), vb[dp][0],
-              vb[dp][1], vb[dp][2], vb[dp][3]);
+      for (int dm = 0; dm < D / 16; ++dm) {
+        o[nt][dm][0] *= corr[nt][0];
+        o[nt][dm][1] *= corr[nt][1];
+        o[nt][dm][2] *= corr[nt][0];
+        o[nt][dm][3] *= corr[nt][1];
+      }
   }
   // Codes are finite, and the weights outside [vlo, valid) are exact zeros,
   // so no value row needs masking here.
 #pragma unroll
-  for (int dp = 0; dp < D / 16; ++dp) {
-    MmaOp<__half>::run(o[2 * dp], pa, vb[dp][0], vb[dp][1]);
-    MmaOp<__half>::run(o[2 * dp + 1], pa, vb[dp][2], vb[dp][3]);
+  for (int blk = 0; blk < D / 32; ++blk) {
+    uint32_t r01[4], r89[4];
+    i8x4x2_to_f16_pairs(vw[blk][0], vw[blk][1], r01);
+    i8x4x2_to_f16_pairs(vw[blk][2], vw[blk][3], r89);
+    const uint32_t a0[4] = {r01[0], r01[1], r89[0], r89[1]};
+    const uint32_t a1[4] = {r01[2], r01[3], r89[2], r89[3]};
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      MmaOp<__half>::run(o[nt][2 * blk], a0, pb[nt][0], pb[nt][1]);
+      MmaOp<__half>::run(o[nt][2 * blk + 1], a1, pb[nt][0], pb[nt][1]);
+    }
   }
-  __syncwarp();  // the staging tile is rewritten by the warp's next tile
 }
 
 // The end of one segment share (cold path, kept out of line to spare the
@@ -631,14 +639,17 @@ __device__ __noinline__ void finish_share(const DecodeParams& p, const float* cm
 }
 
 // tm_ks / tm_vs: the INT8 cache's K and V scales (unused for a 16-bit cache).
-template <typename T, int D, bool kI8>
-__global__ void __launch_bounds__(kThreads, 2)
+// kQ = 0: 16-bit cache; kQ = 1, 2: INT8 cache, query group of at most 8 kQ rows.
+template <typename T, int D, int kQ>
+__global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_ks,
                         const __grid_constant__ CUtensorMap tm_vs,
                         const __grid_constant__ DecodeParams p) {
+  constexpr bool kI8 = kQ > 0;
+  constexpr int kNT = kI8 ? kQ : 1;
   constexpr int kHalves = Layout<D, kI8>::kHalves;
   constexpr int kKBytes = Layout<D, kI8>::kKBytes;
   constexpr int kStages = Layout<D, kI8>::kStages;
@@ -827,17 +838,33 @@ __global__ void __launch_bounds__(kThreads, 2)
   Cursor cur;
   cur.locate(t_begin, cum, B, hkv);
   const int ctid = warp * 32 + lane;
-  float o[D / 8][4], m[2], l[2];
+  // 16-bit cache: o, m, l of query rows g, g+8 (mma M side).  INT8 cache:
+  // o8, m8, l8 of query rows 8nt + 2c, 2c+1 (N side), qb the query fragments.
+  float o[kI8 ? 1 : D / 8][4], m[2], l[2];
+  float o8[kNT][kI8 ? D / 16 : 1][4], m8[kNT][2], l8[kNT][2];
+  uint32_t qb[kI8 ? D / 16 : 1][kNT][2];
   auto reset = [&]() {
+    if constexpr (kI8) {
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n)
+      for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
-    m[0] = m[1] = -INFINITY;
-    l[0] = l[1] = 0.f;
+        for (int n = 0; n < D / 16; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o8[nt][n][e] = 0.f;
+        m8[nt][0] = m8[nt][1] = -INFINITY;
+        l8[nt][0] = l8[nt][1] = 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
+      m[0] = m[1] = -INFINITY;
+      l[0] = l[1] = 0.f;
+    }
   };
   reset();
-  bool need_q = true;  // INT8: the segment's query fragments are still to be built
+  bool need_q = true;  // INT8: the segment's query fragments are still to be loaded
   int seg_first_j = cur.j;
   int slot = 0;  // 0 for the first segment this CTA touches, 1 afterwards
   const uint32_t sbase = smem_u32(smem);
@@ -848,14 +875,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = !*abort_flag && mbar_wait_bounded(&full[stage], phase, p.err_flag);
     if (!ok) *abort_flag = 1;
     if constexpr (kI8) {
-      // Every consumer warp reaches this point at the same tile (need_q is
-      // set at the same segment boundaries for all of them), whether or not
-      // its tokens are attended, so the barrier always completes; after a
-      // failed wait the stage's query rows are stale but still in bounds.
+      // The first tile of a segment share: its query rows into registers
+      // (after a failed wait they are stale but still in bounds).
       if (need_q) {
-        build_q_i8<T, D>(sbase + stage * L.stage + L.qoff, L.q_half, G, warp, lane,
-                         sbase + L.qfrag);
-        named_bar_sync(2, kConsumerWarps * 32);
+        load_q_i8<T, D, kNT>(sbase + stage * L.stage + L.qoff, L.q_half, G, lane, qb);
         need_q = false;
       }
     }
@@ -866,9 +889,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (ok && valid > vlo) {
       const uint32_t kb = sbase + stage * L.stage;
       if constexpr (kI8)
-        attend_16_i8<D>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
-                        p.log2_box, warp, lane, vlo, valid, p.scale_log2, sbase + L.qfrag,
-                        sbase + L.vstg + warp * 16 * D * 2, o, m, l);
+        attend_16_i8<D, kNT>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
+                             p.log2_box, warp, lane, vlo, valid, p.scale_log2, qb, o8, m8, l8);
       else
         attend_16<T, D>(kb, kb + kKBytes, warp, lane, vlo, valid, p.scale_log2, kb + L.qoff,
                         L.q_half, G, o, m, l);
@@ -880,24 +902,51 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (last_of_seg || t == t_end - 1) {
       // ---- finalize this segment's share: merge the 4 warps' states.
       const bool complete = seg_first_j == 0 && last_of_seg;
-      float l0 = l[0], l1 = l[1];
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      const int r0 = lane >> 2, r1 = r0 + 8, c0 = 2 * (lane & 3);
-      if ((lane & 3) == 0) {
-        if (r0 < G) { cmb_m[warp * G + r0] = m[0]; cmb_l[warp * G + r0] = l0; }
-        if (r1 < G) { cmb_m[warp * G + r1] = m[1]; cmb_l[warp * G + r1] = l1; }
-      }
+      if constexpr (kI8) {
+        // l: sum the 8 lanes (g) of each query; m is already the same there.
+        // Lane (g, c) holds dims 32blk + 4g .. 4g+3 of query rows 8nt + 2c + e.
+        const int g8 = lane >> 2, c8 = lane & 3;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        if (r0 < G)
-          *reinterpret_cast<float2*>(&cmb_o[(warp * G + r0) * D + n * 8 + c0]) =
-              make_float2(o[n][0], o[n][1]);
-        if (r1 < G)
-          *reinterpret_cast<float2*>(&cmb_o[(warp * G + r1) * D + n * 8 + c0]) =
-              make_float2(o[n][2], o[n][3]);
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x = l8[nt][e];
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            x += __shfl_xor_sync(0xffffffffu, x, 8);
+            x += __shfl_xor_sync(0xffffffffu, x, 16);
+            const int r = nt * 8 + 2 * c8 + e;
+            if (r < G) {
+              if (g8 == 0) {
+                cmb_m[warp * G + r] = m8[nt][e];
+                cmb_l[warp * G + r] = x;
+              }
+#pragma unroll
+              for (int blk = 0; blk < D / 32; ++blk)
+                *reinterpret_cast<float4*>(&cmb_o[(warp * G + r) * D + 32 * blk + 4 * g8]) =
+                    make_float4(o8[nt][2 * blk][e], o8[nt][2 * blk][e + 2],
+                                o8[nt][2 * blk + 1][e], o8[nt][2 * blk + 1][e + 2]);
+            }
+          }
+      } else {
+        float l0 = l[0], l1 = l[1];
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        const int r0 = lane >> 2, r1 = r0 + 8, c0 = 2 * (lane & 3);
+        if ((lane & 3) == 0) {
+          if (r0 < G) { cmb_m[warp * G + r0] = m[0]; cmb_l[warp * G + r0] = l0; }
+          if (r1 < G) { cmb_m[warp * G + r1] = m[1]; cmb_l[warp * G + r1] = l1; }
+        }
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          if (r0 < G)
+            *reinterpret_cast<float2*>(&cmb_o[(warp * G + r0) * D + n * 8 + c0]) =
+                make_float2(o[n][0], o[n][1]);
+          if (r1 < G)
+            *reinterpret_cast<float2*>(&cmb_o[(warp * G + r1) * D + n * 8 + c0]) =
+                make_float2(o[n][2], o[n][3]);
+        }
       }
       named_bar_sync(1, kConsumerWarps * 32);
       finish_share<T, D>(p, cmb_m, cmb_l, cmb_o, last_flag, abort_flag + 2,
@@ -918,7 +967,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <typename T, int D, bool kI8>
+template <typename T, int D, int kQ>
 struct DecodeKernel {
   // Resident CTAs per SM for a launch with `smem` bytes of dynamic shared
   // memory (cached per device and size; also sets the kernel's smem limit).
@@ -930,11 +979,11 @@ struct DecodeKernel {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find({dev, smem});
     if (it != cache.end()) return it->second;
-    cudaFuncSetAttribute(paged_decode_kernel<T, D, kI8>,
+    cudaFuncSetAttribute(paged_decode_kernel<T, D, kQ>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Layout<D, kI8>(kMaxBatch, 16).total);
+                         Layout<D, (kQ > 0)>(kMaxBatch, 16).total);
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<T, D, kI8>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<T, D, kQ>,
                                                       kThreads, smem) != cudaSuccess ||
         occ < 1)
       occ = 1;
@@ -943,11 +992,12 @@ struct DecodeKernel {
   }
 };
 
-template <typename T, int D, bool kI8>
+template <typename T, int D, int kQ>
 kvc_status run_decode(const DecodeArgs& a) {
+  constexpr bool kI8 = kQ > 0;
   const int G = a.num_q_heads / a.num_kv_heads;
   const size_t smem = Layout<D, kI8>(a.batch, G).total;
-  const int occ = DecodeKernel<T, D, kI8>::occupancy(smem);  // also sets the smem limit
+  const int occ = DecodeKernel<T, D, kQ>::occupancy(smem);  // also sets the smem limit
   const int P = a.num_ctas > 0 ? a.num_ctas : device_sm_count() * occ;
   if (a.workspace_bytes < paged_decode_workspace_bytes(G, D, P) || a.workspace == nullptr)
     return KVC_ERR_WORKSPACE;
@@ -1027,24 +1077,25 @@ kvc_status run_decode(const DecodeArgs& a) {
   p.window = a.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
 
-  paged_decode_kernel<T, D, kI8><<<P, kThreads, smem, a.stream>>>(tk, tv, tq, tks, tvs, p);
+  paged_decode_kernel<T, D, kQ><<<P, kThreads, smem, a.stream>>>(tk, tv, tq, tks, tvs, p);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
-template <bool kI8>
+template <int kQ>
 int num_ctas_for(int group, int head_dim, kvc_dtype dtype) {
+  constexpr bool kI8 = kQ > 0;
   const int sms = device_sm_count();
   if (sms <= 0) return 0;
   // The smallest batch needs the least shared memory, hence the most CTAs.
   if (head_dim == 64 && !kI8) {
     const size_t smem = Layout<64, false>(1, group).total;
-    return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 64, false>::occupancy(smem)
-                                    : DecodeKernel<__half, 64, false>::occupancy(smem));
+    return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 64, 0>::occupancy(smem)
+                                    : DecodeKernel<__half, 64, 0>::occupancy(smem));
   }
   if (head_dim == 128) {
     const size_t smem = Layout<128, kI8>(1, group).total;
-    return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 128, kI8>::occupancy(smem)
-                                    : DecodeKernel<__half, 128, kI8>::occupancy(smem));
+    return sms * (dtype == KVC_BF16 ? DecodeKernel<__nv_bfloat16, 128, kQ>::occupancy(smem)
+                                    : DecodeKernel<__half, 128, kQ>::occupancy(smem));
   }
   return 0;
 }
@@ -1057,22 +1108,25 @@ size_t paged_decode_workspace_bytes(int group, int head_dim, int ctas) {
 
 int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas, bool int8) {
   if (num_ctas > 0) return num_ctas;
-  return int8 ? num_ctas_for<true>(group, head_dim, dtype)
-              : num_ctas_for<false>(group, head_dim, dtype);
+  if (!int8) return num_ctas_for<0>(group, head_dim, dtype);
+  return group <= 8 ? num_ctas_for<1>(group, head_dim, dtype)
+                    : num_ctas_for<2>(group, head_dim, dtype);
 }
 
 kvc_status launch_paged_decode(const DecodeArgs& a) {
   if (a.key_scales != nullptr) {  // INT8 cache (head_dim 128, plain decode)
     if (a.head_dim != 128 || a.new_key != nullptr) return KVC_ERR_UNSUPPORTED;
-    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 128, true>(a)
-                               : run_decode<__half, 128, true>(a);
+    const bool wide = a.num_q_heads / a.num_kv_heads > 8;  // two 8-row query tiles
+    if (a.dtype == KVC_BF16)
+      return wide ? run_decode<__nv_bfloat16, 128, 2>(a) : run_decode<__nv_bfloat16, 128, 1>(a);
+    return wide ? run_decode<__half, 128, 2>(a) : run_decode<__half, 128, 1>(a);
   }
   if (a.head_dim == 64)
-    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 64, false>(a)
-                               : run_decode<__half, 64, false>(a);
+    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 64, 0>(a)
+                               : run_decode<__half, 64, 0>(a);
   if (a.head_dim == 128)
-    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 128, false>(a)
-                               : run_decode<__half, 128, false>(a);
+    return a.dtype == KVC_BF16 ? run_decode<__nv_bfloat16, 128, 0>(a)
+                               : run_decode<__half, 128, 0>(a);
   return KVC_ERR_UNSUPPORTED;
 }
 

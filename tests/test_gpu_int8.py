@@ -74,6 +74,9 @@ SHAPES = [
     ([40, 513, 77], 4, 4, 8, "f16"),
     ([1000, 64, 3], 16, 1, 64, "bf16"),
     ([90, 91, 92], 12, 4, 32, "f16"),
+    ([300, 17, 4096], 16, 2, 16, "f16"),      # G = 8: one full 8-row query tile
+    ([77, 200], 9, 1, 64, "bf16"),             # G = 9: two query tiles, 7 padding rows
+    ([500, 1], 2, 1, 128, "f16"),              # G = 2
 ]
 
 
@@ -140,3 +143,23 @@ def test_int8_rejects_other_head_dims(kvc_lib):
     args = [P, P, P, P, P, P, P, P, 2, 8, 2, 64, 16, 4, 8, 0.1, kvc_lib.KVC_BF16, 0, P, 1 << 30,
             None, None]
     assert f(*args) == kvc_lib.KVC_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_int8_long_sequences_wide_values(kvc_lib, dtype):
+    """8192-token sequences whose values are N(0, 10^2), so the output (a weighted mean near
+    0) is small against the value scales: the accumulation over 128 tiles of one share
+    must keep its error relative to the output, not to the codes' magnitude."""
+    case = decode_case(74, 3, [8192, 8000, 6000], 16, 2, 128, 64, dtype=dtype)
+    case.value_cache = (case.value_cache.float() * 10.0).to(case.value_cache.dtype)
+    kq, vq, ks, vs = _quantised_pool(case)
+    for num_ctas in (0, 1):
+        out = kvc_lib.paged_decode_int8(to_cuda(case.q), to_cuda(torch.from_numpy(kq)),
+                                        to_cuda(torch.from_numpy(vq)),
+                                        to_cuda(torch.from_numpy(ks)),
+                                        to_cuda(torch.from_numpy(vs)), to_cuda(case.block_table),
+                                        to_cuda(case.seq_lens), case.scale, num_ctas=num_ctas)
+        torch.cuda.synchronize()
+        ref = O.paged_decode_int8(case.q.double().numpy(), kq, vq, ks, vs,
+                                  case.block_table.numpy(), case.seq_lens.numpy(), case.scale)
+        assert excess(out, ref, dtype) <= 0, num_ctas
