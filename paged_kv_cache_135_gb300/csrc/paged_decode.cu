@@ -352,12 +352,6 @@ __device__ __forceinline__ uint32_t q_pair_f16<__nv_bfloat16>(uint32_t w) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Address of token t's scale in a stage's scale region (one 128-byte slot per
-// TMA box of 2^log2_box tokens).
-__device__ __forceinline__ uint32_t scale_addr(uint32_t base, int t, int log2_box) {
-  return base + ((t >> log2_box) << 7) + ((t & ((1 << log2_box) - 1)) << 2);
-}
-
 // Over an INT8 cache the products run transposed, S^T = K Q^T and
 // O^T = V^T P^T (mma m16n8k16, fp16 operands, fp32 accumulation): the warp's
 // 16 tokens are the M side of the score product and the K side of the value
@@ -397,6 +391,31 @@ __device__ __forceinline__ void load_q_i8(uint32_t qbase, int q_half, int group,
     }
 }
 
+// Per-lane shared-memory offsets of the INT8 consumer, the same for every
+// tile (relative to a stage's K or V tile and scale region).  With the
+// 128-byte swizzle a row r's chunk x sits at r * 128 + ((x ^ (r % 8)) << 4);
+// the warp's rows start at a multiple of 8, so rows g and g+8 share one XOR
+// pattern (g), and so do rows 2c, 2c+8 (2c) and 2c+1, 2c+9 (2c+1).
+struct I8Lane {
+  uint32_t k_row;    // row g, byte 4c
+  uint32_t k_xor;    // g << 4
+  uint32_t v_row;    // row 2c, byte 4 (g % 4)
+  uint32_t v_xor;    // (2c << 4) ^ ((g / 4) << 4), the chunk bits of row 2c for blk = 0
+  uint32_t ks0, ks1;  // scales of tokens g and g+8 (one 128-byte slot per TMA box
+                      // of 2^log2_box tokens)
+  __device__ __forceinline__ I8Lane(int warp, int lane, int log2_box) {
+    const int g = lane >> 2, c = lane & 3;
+    const int t0 = warp * 16 + g;
+    k_row = static_cast<uint32_t>(t0 * 128 + 4 * c);
+    k_xor = static_cast<uint32_t>(g << 4);
+    v_row = static_cast<uint32_t>((warp * 16 + 2 * c) * 128 + 4 * (g & 3));
+    v_xor = static_cast<uint32_t>(((2 * c) ^ (g >> 2)) << 4);
+    const int box = 1 << log2_box;
+    ks0 = static_cast<uint32_t>(((t0 >> log2_box) << 7) + ((t0 & (box - 1)) << 2));
+    ks1 = static_cast<uint32_t>((((t0 + 8) >> log2_box) << 7) + (((t0 + 8) & (box - 1)) << 2));
+  }
+};
+
 // One warp's 16 tokens of a stage over an INT8 cache.  A cached row is
 // code * scale, so q . k = scale_k * (q . codes_k) and sum_j p_j v_j =
 // sum_j (p_j * scale_v_j) codes_v_j.  The codes are exact in fp16, the
@@ -407,34 +426,36 @@ __device__ __forceinline__ void load_q_i8(uint32_t qbase, int q_half, int group,
 // end of the segment.
 template <int D, int NT>
 __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
-                                             uint32_t vscale, int log2_box, int warp, int lane,
+                                             uint32_t vscale, const I8Lane& ofs, int lane,
                                              int vlo, int valid, float scale_log2,
                                              const uint32_t (&qb)[D / 16][NT][2],
                                              float (&o)[NT][D / 16][4], float (&m)[NT][2],
                                              float (&l)[NT][2]) {
   static_assert(D == 128, "one 128-byte code row per token");
   const int g = lane >> 2, c = lane & 3;
-  const int t0 = warp * 16 + g, tv = warp * 16 + 2 * c;
   // All shared-memory loads first (the asm statements keep program order),
-  // so their latencies overlap.
-  const float ks0 = lds_f32(scale_addr(kscale, t0, log2_box));
-  const float ks1 = lds_f32(scale_addr(kscale, t0 + 8, log2_box));
-  const float vs0 = lds_f32(scale_addr(vscale, t0, log2_box));
-  const float vs1 = lds_f32(scale_addr(vscale, t0 + 8, log2_box));
+  // so their latencies overlap.  Rows +8 are +1024 bytes with the same
+  // swizzle; row 2c+1 is row 2c + 128 bytes with chunk bit 0 flipped.
+  const float ks0 = lds_f32(kscale + ofs.ks0), ks1 = lds_f32(kscale + ofs.ks1);
+  const float vs0 = lds_f32(vscale + ofs.ks0), vs1 = lds_f32(vscale + ofs.ks1);
   uint32_t kw[D / 16][2];
+  const uint32_t kr = kbase + ofs.k_row;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    kw[kk][0] = lds_u32(kbase + swz128(t0, kk) + 4 * c);
-    kw[kk][1] = lds_u32(kbase + swz128(t0 + 8, kk) + 4 * c);
+    const uint32_t a = kr + ((kk << 4) ^ ofs.k_xor);
+    kw[kk][0] = lds_u32(a);
+    kw[kk][1] = lds_u32(a + 1024);
   }
   uint32_t vw[D / 32][4];
+  const uint32_t vr = vbase + ofs.v_row;
 #pragma unroll
   for (int blk = 0; blk < D / 32; ++blk) {
-    const int ch = 2 * blk + (g >> 2), off = 4 * (g & 3);
-    vw[blk][0] = lds_u32(vbase + swz128(tv, ch) + off);
-    vw[blk][1] = lds_u32(vbase + swz128(tv + 1, ch) + off);
-    vw[blk][2] = lds_u32(vbase + swz128(tv + 8, ch) + off);
-    vw[blk][3] = lds_u32(vbase + swz128(tv + 9, ch) + off);
+    const uint32_t x = (blk << 5) ^ ofs.v_xor;  // row 2c: chunk 2 blk + g/4, swizzled
+    const uint32_t a0 = vr + x, a1 = vr + 128 + (x ^ 16);
+    vw[blk][0] = lds_u32(a0);
+    vw[blk][1] = lds_u32(a1);
+    vw[blk][2] = lds_u32(a0 + 1024);
+    vw[blk][3] = lds_u32(a1 + 1024);
   }
   float s[NT][4];
 #pragma unroll
@@ -865,6 +886,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
   };
   reset();
   bool need_q = true;  // INT8: the segment's query fragments are still to be loaded
+  const I8Lane i8ofs(warp, lane, p.log2_box);
   int seg_first_j = cur.j;
   int slot = 0;  // 0 for the first segment this CTA touches, 1 afterwards
   const uint32_t sbase = smem_u32(smem);
@@ -890,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
       const uint32_t kb = sbase + stage * L.stage;
       if constexpr (kI8)
         attend_16_i8<D, kNT>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
-                             p.log2_box, warp, lane, vlo, valid, p.scale_log2, qb, o8, m8, l8);
+                             i8ofs, lane, vlo, valid, p.scale_log2, qb, o8, m8, l8);
       else
         attend_16<T, D>(kb, kb + kKBytes, warp, lane, vlo, valid, p.scale_log2, kb + L.qoff,
                         L.q_half, G, o, m, l);
