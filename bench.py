@@ -545,8 +545,16 @@ def int8_decode_bytes(seq_lens, Hq, Hkv, D, bs):
     return toks * Hkv * (D + 4) * 2 + 2 * B * Hq * D * 2 + 4 * blocks + 4 * B
 
 
+def int8_write_bytes(B, Hkv, D):
+    """The INT8 step's write: new 16-bit K/V rows read, their codes and fp32 scales written,
+    slot ints written."""
+    return 2 * B * Hkv * D * 2 + 2 * B * Hkv * (D + 4) + 4 * B
+
+
 def measure_int8(kvc, dev, rank, steps, warmup):
-    """The GQA 8B-shape decode over an INT8 cache (codes + one fp32 scale per row)."""
+    """The GQA 8B-shape decode step over an INT8 cache (codes + one fp32 scale per row): the
+    new token's rows quantised into the cache and the decode, one kvc_paged_decode_int8_append
+    launch."""
     case = make_config(WORKLOAD, seed=rank, value_device=str(dev))
     m = case.meta
     Hq, Hkv, D, bs = m["num_q_heads"], m["num_kv_heads"], m["head_dim"], case.block_size
@@ -560,13 +568,15 @@ def measure_int8(kvc, dev, rank, steps, warmup):
                                scales[0], scales[1], allslots)
     del case.key_cache, case.value_cache
     q, bt, sl = case.q.to(dev), case.block_table.to(dev), case.seq_lens.to(dev)
+    nk, nv = case.new_key.to(dev), case.new_value.to(dev)
     out = torch.empty_like(q)
+    slots = torch.empty(q.shape[0], dtype=torch.int32, device=dev)
     ws = torch.zeros(max(kvc.decode_workspace_size(Hq, Hkv, D), 16), dtype=torch.uint8,
                      device=dev)
 
     def decode():
-        kvc.paged_decode_int8(q, codes[0], codes[1], scales[0], scales[1], bt, sl, case.scale,
-                              out=out, workspace=ws)
+        kvc.paged_decode_int8_append(q, nk, nv, codes[0], codes[1], scales[0], scales[1], bt, sl,
+                                     case.scale, out=out, slot_mapping=slots, workspace=ws)
 
     for _ in range(warmup):
         decode()
@@ -577,12 +587,15 @@ def measure_int8(kvc, dev, rank, steps, warmup):
     with ClockSampler(dev.index or 0) as clk:
         _, per = time_graphs(graphs, steps)
     lens = case.seq_lens.tolist()
-    by = int8_decode_bytes(lens, Hq, Hkv, D, bs)
+    B = len(lens)
+    by = int8_decode_bytes(lens, Hq, Hkv, D, bs) + int8_write_bytes(B, Hkv, D)
     hp, hkind = peaks()
-    fig = _roofline("paged_decode_kernel, INT8 cache (kvc_paged_decode_int8)", per["decode"], by,
-                    "GB/s", hp, hkind, clk.summary(), bound="hbm",
-                    bytes_vs_16bit=by / decode_bytes(lens, Hq, Hkv, D, bs))
-    del codes, scales, q, bt, sl, out, ws, graphs
+    fig = _roofline("paged_decode_kernel, INT8 cache (kvc_paged_decode_int8_append: quantising "
+                    "write of the new token, decode and split-KV merge in one launch)",
+                    per["decode"], by, "GB/s", hp, hkind, clk.summary(), bound="hbm",
+                    bytes_vs_16bit=by / (decode_bytes(lens, Hq, Hkv, D, bs) +
+                                         write_bytes(B, Hkv, D)))
+    del codes, scales, q, bt, sl, nk, nv, out, slots, ws, graphs
     return fig
 
 

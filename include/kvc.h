@@ -332,6 +332,40 @@ kvc_status kvc_paged_decode_int8(const void* q, const int8_t* key_codes,
                                  kvc_stream_t stream);
 
 /*
+ * kvc_paged_decode_int8_append -- one decode step over an INT8 cache in one
+ * launch: identical in effect to kvc_build_slot_mapping (start_pos =
+ * seq_lens - 1) + kvc_reshape_and_cache_int8 + kvc_paged_decode_int8 for every
+ * sequence with seq_lens[b] >= 1.  [SKILL] 3.6 (the cache write before the
+ * attention that reads it) and Mode 2 / 4 with the quantized cache of
+ * Appendix A; not a separate operation on the pages: it exists so an INT8
+ * decode step costs one launch.
+ *
+ *   p = seq_lens[b] - 1; slot = block_table[b][p / block_size] * block_size
+ *   + p % block_size; the rows new_key[b][g] / new_value[b][g] are quantised
+ *   exactly as kvc_reshape_and_cache_int8 does (codes into key_codes /
+ *   value_codes at `slot`, scales into key_scales / value_scales);
+ *   slot_mapping[b] = slot (or -1 when seq_lens[b] == 0: nothing is written);
+ *   out = kvc_paged_decode_int8 over the updated cache.
+ *
+ * new_key, new_value: [batch, num_kv_heads, 128] in `dtype` (device, 16-byte
+ * aligned); slot_mapping: int32 [batch] output, may be NULL; every other
+ * argument, the workspace rules and the errors are those of
+ * kvc_paged_decode_int8.  Each new row is written by the CTA that then reads
+ * it, before it reads it.  A block_table entry outside [0, num_blocks) sets
+ * KVC_FLAG_BLOCK_ID_RANGE and that row is not written.
+ */
+kvc_status kvc_paged_decode_int8_append(const void* q, const void* new_key,
+                                        const void* new_value, int8_t* key_codes,
+                                        int8_t* value_codes, float* key_scales,
+                                        float* value_scales, const int32_t* block_table,
+                                        const int32_t* seq_lens, int32_t* slot_mapping,
+                                        void* out, int batch, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_blocks_per_seq,
+                                        int num_blocks, float scale, kvc_dtype dtype,
+                                        int num_ctas, void* workspace, size_t workspace_bytes,
+                                        uint32_t* err_flag, kvc_stream_t stream);
+
+/*
  * kvc_paged_decode_append -- one decode step in one launch: the slot mapping,
  * the cache write of the new token and the paged decode with split-KV,
  * fused.  Identical in effect to kvc_build_slot_mapping (start_pos =

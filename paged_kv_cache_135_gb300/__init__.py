@@ -59,6 +59,8 @@ _SIGS = {
                                         _P]),
     "kvc_paged_decode_int8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                    _F, _I, _I, _P, _S, _P, _P]),
+    "kvc_paged_decode_int8_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I,
+                                          _I, _I, _I, _I, _F, _I, _I, _P, _S, _P, _P]),
     "kvc_bm_create": (_I, [_I, _I, _I, _P]),
     "kvc_bm_destroy": (None, [_P]),
     "kvc_bm_num_free": (_I, [_P]),
@@ -349,6 +351,47 @@ def paged_decode_int8(q: torch.Tensor, key_codes: torch.Tensor, value_codes: tor
         q.data_ptr(), key_codes.data_ptr(), value_codes.data_ptr(), key_scales.data_ptr(),
         value_scales.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(), B,
         Hq, Hkv, D, bs, block_table.shape[1], NB, float(scale), _DT[q.dtype], num_ctas,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _flag(err_flag),
+        _stream()))
+    return out
+
+
+def paged_decode_int8_append(q: torch.Tensor, new_key: torch.Tensor, new_value: torch.Tensor,
+                             key_codes: torch.Tensor, value_codes: torch.Tensor,
+                             key_scales: torch.Tensor, value_scales: torch.Tensor,
+                             block_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                             out: Optional[torch.Tensor] = None,
+                             slot_mapping: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                             workspace: Optional[torch.Tensor] = None,
+                             err_flag: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step over an INT8 cache in one launch: quantise new_key / new_value
+    [B, Hkv, 128] into the cache at position seq_lens[b] - 1 (slot into slot_mapping, -1 for
+    an empty sequence), then decode as paged_decode_int8 over seq_lens."""
+    _cuda("q", q)
+    _cuda("new_key", new_key, q.dtype)
+    _cuda("new_value", new_value, q.dtype)
+    _cuda("key_codes", key_codes, torch.int8)
+    _cuda("value_codes", value_codes, torch.int8)
+    _cuda("key_scales", key_scales, torch.float32)
+    _cuda("value_scales", value_scales, torch.float32)
+    _cuda("block_table", block_table, torch.int32)
+    _cuda("seq_lens", seq_lens, torch.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = key_codes.shape
+    if tuple(new_key.shape) != (B, Hkv, D) or tuple(new_value.shape) != (B, Hkv, D):
+        raise ValueError("new_key / new_value must be [batch, num_kv_heads, head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda("out", out, q.dtype)
+    if slot_mapping is not None:
+        _cuda("slot_mapping", slot_mapping, torch.int32)
+    workspace = _decode_ws(workspace, Hq, Hkv, D, num_ctas, q.device)
+    _check("kvc_paged_decode_int8_append", lib().kvc_paged_decode_int8_append(
+        q.data_ptr(), new_key.data_ptr(), new_value.data_ptr(), key_codes.data_ptr(),
+        value_codes.data_ptr(), key_scales.data_ptr(), value_scales.data_ptr(),
+        block_table.data_ptr(), seq_lens.data_ptr(),
+        slot_mapping.data_ptr() if slot_mapping is not None else None, out.data_ptr(),
+        B, Hq, Hkv, D, bs, block_table.shape[1], NB, float(scale), _DT[q.dtype], num_ctas,
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _flag(err_flag),
         _stream()))
     return out

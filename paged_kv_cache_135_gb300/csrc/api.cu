@@ -382,6 +382,36 @@ kvc_status kvc_paged_decode_int8(const void* q, const int8_t* key_codes,
   return kvc::launch_paged_decode(a);
 }
 
+kvc_status kvc_paged_decode_int8_append(const void* q, const void* new_key,
+                                        const void* new_value, int8_t* key_codes,
+                                        int8_t* value_codes, float* key_scales,
+                                        float* value_scales, const int32_t* block_table,
+                                        const int32_t* seq_lens, int32_t* slot_mapping,
+                                        void* out, int batch, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_blocks_per_seq,
+                                        int num_blocks, float scale, kvc_dtype dtype,
+                                        int num_ctas, void* workspace, size_t workspace_bytes,
+                                        uint32_t* err_flag, kvc_stream_t stream) {
+  if (batch > 0 && (!new_key || !new_value || !aligned16(new_key) || !aligned16(new_value)))
+    return KVC_ERR_INVALID_ARG;
+  kvc::DecodeArgs a = kvc::make_decode_args(
+      q, key_codes, value_codes, block_table, seq_lens, out, batch, num_q_heads, num_kv_heads,
+      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, num_ctas, workspace,
+      workspace_bytes, err_flag, stream);
+  bool empty = false;
+  const kvc_status st = kvc::check_decode_args(a, &empty);
+  if (st != KVC_OK || empty) return st;
+  if (head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (!key_scales || !value_scales || !aligned16(key_scales) || !aligned16(value_scales))
+    return KVC_ERR_INVALID_ARG;
+  a.key_scales = key_scales;
+  a.value_scales = value_scales;
+  a.new_key = new_key;
+  a.new_value = new_value;
+  a.slot_out = slot_mapping;
+  return kvc::launch_paged_decode(a);
+}
+
 namespace {
 kvc_status varlen_prefill(const void* q, const void* key, const void* value,
                           const int32_t* cu_seqlens, const int32_t* context_lens,

@@ -172,26 +172,14 @@ __global__ void reshape_and_cache_int8_kernel(const T* __restrict__ key,
 #pragma unroll
       for (int e = 0; e < 2; ++e) x[e] = to_f32(pv[e]);
     }
-    float amax = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
-    const float scale = __fdiv_rn(amax, 127.f);
-    uint32_t packed = 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      int c = __float2int_rn(__fmul_rn(x[e], inv));
-      c = c > 127 ? 127 : (c < -127 ? -127 : c);
-      packed |= (static_cast<uint32_t>(c) & 0xffu) << (8 * e);
-    }
+    uint32_t packed[1];
+    float scale;
+    quantize_row_int8<E, 32>(x, packed, scale);
     const int64_t blk = slot / block_size, in_blk = slot - blk * block_size;
     int8_t* dst = (is_v ? value_codes : key_codes) +
                   (static_cast<int64_t>(slot) * num_kv_heads + h) * D + lane * E;
-    if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = packed;
-    else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+    if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed[0]);
     if (lane == 0)
       (is_v ? value_scales : key_scales)[(blk * num_kv_heads + h) * block_size + in_blk] = scale;
   }

@@ -222,6 +222,36 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Symmetric INT8 codes of one row spread over kLanes consecutive lanes of a
+// warp (32 or 16; an aligned group), E consecutive elements per lane (lane l
+// of the group holds elements l*E .. l*E+E-1): amax over the row by
+// shuffles, scale = amax / 127, code = rint(x * (127 / amax)) with ties to
+// even, clamped to [-127, 127]; the divisions and the product are correctly
+// rounded fp32, so the codes do not depend on how the row is spread.
+// packed[i]: codes 4i .. 4i+3 of the lane, byte e = element 4i + e.  An
+// all-zero row gets scale 0 and codes 0.  Every lane of the warp must call it.
+template <int E, int kLanes>
+__device__ __forceinline__ void quantize_row_int8(const float (&x)[E],
+                                                  uint32_t (&packed)[(E + 3) / 4],
+                                                  float& scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
+  scale = __fdiv_rn(amax, 127.f);
+#pragma unroll
+  for (int i = 0; i < (E + 3) / 4; ++i) packed[i] = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    int c = __float2int_rn(__fmul_rn(x[e], inv));
+    c = c > 127 ? 127 : (c < -127 ? -127 : c);
+    packed[e / 4] |= (static_cast<uint32_t>(c) & 0xffu) << (8 * (e % 4));
+  }
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a tile of
 // 128-byte rows written by TMA with CU_TENSOR_MAP_SWIZZLE_128B (the tile base
 // is 1024-byte aligned): the chunk index is XORed with row % 8.

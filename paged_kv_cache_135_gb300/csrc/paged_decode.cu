@@ -80,10 +80,15 @@ struct DecodeParams {
   // at position seq_lens[b] - 1; its K/V rows come from new_k / new_v
   // [B, Hkv, D] and are written into k_cache / v_cache by the CTA that loads
   // that position, before it loads it; slot_out[b] (nullable) gets its slot.
+  // Over an INT8 cache the new rows are quantised (quantize_row_int8) into
+  // the code arrays k_cache / v_cache and their scales into k_scales /
+  // v_scales [num_blocks, Hkv, block_size].
   const void* new_k;
   const void* new_v;
   void* k_cache;
   void* v_cache;
+  float* k_scales;
+  float* v_scales;
   int32_t* slot_out;
   int batch, num_q_heads, num_kv_heads, group, head_dim;
   int block_size, log2_bs, max_blocks, num_blocks, box_tokens, log2_box;
@@ -756,6 +761,22 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
     // box_tokens whole 128-byte code rows.
     const uint32_t box_bytes = static_cast<uint32_t>(p.box_tokens) * 128u;
     const uint32_t q_bytes = static_cast<uint32_t>(G) * 128u * kHalves;
+    // Appending: the lane's 16-byte piece of the new K row (lanes < kChunks)
+    // or V row (lanes kChunks .. 2 kChunks - 1) of segment (b, g), loaded one
+    // tile before the segment's last tile so its latency is off the path.
+    constexpr int kChunks = D * 2 / 16;
+    const bool new_is_v = lane >= kChunks;
+    const int new_q16 = lane - (new_is_v ? kChunks : 0);
+    uint4 new_piece = make_uint4(0u, 0u, 0u, 0u);
+    bool new_ready = false;
+    auto load_new_piece = [&](const Cursor& at) {
+      if (lane < 2 * kChunks)
+        new_piece = __ldg(reinterpret_cast<const uint4*>(
+                              static_cast<const T*>(new_is_v ? p.new_v : p.new_k) +
+                              (static_cast<long long>(at.b) * p.num_kv_heads + at.g) * D) +
+                          new_q16);
+      new_ready = true;
+    };
     int it = 0;
     for (long long t = t_begin; t < t_end; ++t, ++it) {
       const int stage = it % kStages;
@@ -770,31 +791,48 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
       if (wanted)
         pb = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks +
                                   (tok >> p.log2_bs)]);
-      if (!kI8 && p.new_k != nullptr && cur.j == cur.n - 1) {
+      if (p.new_k != nullptr && cur.j + 2 == cur.n) load_new_piece(cur);
+      if (p.new_k != nullptr && cur.j == cur.n - 1) {
         // The last tile of segment (b, g) holds the new token: write its K/V
-        // rows for head g (16 bytes per lane), make the writes visible to the
-        // TMA unit, then load the tile as usual.  No other CTA reads them.
+        // rows for head g, make the writes visible to the TMA unit, then load
+        // the tile as usual.  No other CTA reads them.
+        if (!new_ready) load_new_piece(cur);
+        new_ready = false;
         const int pos = Lb - 1;
         const int pbn = __ldg(&p.block_table[static_cast<long long>(cur.b) * p.max_blocks +
                                              (pos >> p.log2_bs)]);
-        constexpr int kChunks = D * 2 / 16;  // 16-byte pieces of one row
         if (pbn >= 0 && pbn < p.num_blocks) {
-          if (lane < 2 * kChunks) {
-            const bool is_v = lane >= kChunks;
-            const int q16 = lane - (is_v ? kChunks : 0);
-            const long long src_row = static_cast<long long>(cur.b) * p.num_kv_heads + cur.g;
-            const long long dst_row =
-                (static_cast<long long>(pbn) * p.block_size + (pos & (p.block_size - 1))) *
-                    p.num_kv_heads + cur.g;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                                      static_cast<const T*>(is_v ? p.new_v : p.new_k) + src_row * D) +
-                                  q16);
-            *(reinterpret_cast<uint4*>(static_cast<T*>(is_v ? p.v_cache : p.k_cache) + dst_row * D) +
-              q16) = v;
+          const int in_blk = pos & (p.block_size - 1);
+          const long long dst_row =
+              (static_cast<long long>(pbn) * p.block_size + in_blk) * p.num_kv_heads + cur.g;
+          if constexpr (kI8) {
+            // Lanes 0-15 quantise the K row, lanes 16-31 the V row, 8
+            // elements each (the arithmetic of kvc_reshape_and_cache_int8).
+            static_assert(D == 128, "8 elements per lane, 16 lanes per row");
+            const bool is_v = new_is_v;
+            const int l16 = new_q16;
+            const T* pv = reinterpret_cast<const T*>(&new_piece);
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = static_cast<float>(pv[e]);
+            uint32_t packed[2];
+            float sc;
+            quantize_row_int8<8, 16>(x, packed, sc);
+            reinterpret_cast<uint2*>(static_cast<int8_t*>(is_v ? p.v_cache : p.k_cache) +
+                                     dst_row * D)[l16] = make_uint2(packed[0], packed[1]);
+            if (l16 == 0)
+              (is_v ? p.v_scales : p.k_scales)[(static_cast<long long>(pbn) * p.num_kv_heads +
+                                                cur.g) * p.block_size + in_blk] = sc;
             asm volatile("fence.proxy.async.global;" ::: "memory");
+          } else {
+            if (lane < 2 * kChunks) {
+              *(reinterpret_cast<uint4*>(static_cast<T*>(new_is_v ? p.v_cache : p.k_cache) +
+                                         dst_row * D) + new_q16) = new_piece;
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
           }
           if (lane == 0 && cur.g == 0 && p.slot_out)
-            p.slot_out[cur.b] = pbn * p.block_size + (pos & (p.block_size - 1));
+            p.slot_out[cur.b] = pbn * p.block_size + in_blk;
         } else if (lane == 0) {
           set_flag(p.err_flag, KVC_FLAG_BLOCK_ID_RANGE);
           if (cur.g == 0 && p.slot_out) p.slot_out[cur.b] = -1;
@@ -1084,6 +1122,8 @@ kvc_status run_decode(const DecodeArgs& a) {
   p.new_v = a.new_value;
   p.k_cache = const_cast<void*>(a.key_cache);
   p.v_cache = const_cast<void*>(a.value_cache);
+  p.k_scales = const_cast<float*>(a.key_scales);
+  p.v_scales = const_cast<float*>(a.value_scales);
   p.slot_out = a.slot_out;
   p.batch = a.batch;
   p.num_q_heads = a.num_q_heads;
@@ -1136,8 +1176,8 @@ int paged_decode_num_ctas(int group, int head_dim, kvc_dtype dtype, int num_ctas
 }
 
 kvc_status launch_paged_decode(const DecodeArgs& a) {
-  if (a.key_scales != nullptr) {  // INT8 cache (head_dim 128, plain decode)
-    if (a.head_dim != 128 || a.new_key != nullptr) return KVC_ERR_UNSUPPORTED;
+  if (a.key_scales != nullptr) {  // INT8 cache (head_dim 128)
+    if (a.head_dim != 128) return KVC_ERR_UNSUPPORTED;
     const bool wide = a.num_q_heads / a.num_kv_heads > 8;  // two 8-row query tiles
     if (a.dtype == KVC_BF16)
       return wide ? run_decode<__nv_bfloat16, 128, 2>(a) : run_decode<__nv_bfloat16, 128, 1>(a);

@@ -72,3 +72,10 @@ def test_int8_decode_bytes_counts_codes_scales_and_rows():
     want = sum(L * Hkv * (D + 4) * 2 for L in lens) + 3 * 2 * Hq * D * 2 + \
         4 * sum(math.ceil(L / bs) for L in lens) + 4 * 3
     assert bench.int8_decode_bytes(lens, Hq, Hkv, D, bs) == want
+
+
+def test_int8_write_bytes_counts_rows_codes_scales_slots():
+    B, Hkv, D = 3, 2, 128
+    # 16-bit rows read (K and V), int8 codes + one fp32 scale per row written, slots written
+    want = 2 * B * Hkv * D * 2 + 2 * B * Hkv * D + 2 * B * Hkv * 4 + 4 * B
+    assert bench.int8_write_bytes(B, Hkv, D) == want

@@ -163,3 +163,85 @@ def test_int8_long_sequences_wide_values(kvc_lib, dtype):
         ref = O.paged_decode_int8(case.q.double().numpy(), kq, vq, ks, vs,
                                   case.block_table.numpy(), case.seq_lens.numpy(), case.scale)
         assert excess(out, ref, dtype) <= 0, num_ctas
+
+
+def _int8_pool_on_gpu(case):
+    kq, vq, ks, vs = _quantised_pool(case)
+    return (kq, vq, ks, vs), {n: to_cuda(torch.from_numpy(a)) for n, a in
+                              (("kq", kq), ("vq", vq), ("ks", ks), ("vs", vs))}
+
+
+@pytest.mark.parametrize("num_ctas", [0, 7])
+@pytest.mark.parametrize("dtype,Hq,Hkv,bs", [("bf16", 8, 2, 16), ("f16", 32, 8, 128),
+                                             ("bf16", 18, 2, 64)])
+def test_int8_append_step_matches_oracle(kvc_lib, num_ctas, dtype, Hq, Hkv, bs):
+    """kvc_paged_decode_int8_append: the new rows' codes and scales are bit-exact with the
+    oracle's quantising write at the oracle's slots, the output is within tolerance of the
+    oracle's INT8 decode of the updated cache, and a sequence of length 0 writes nothing
+    and reports slot -1."""
+    lens = [300, 17, 0, 1024, 5, 129]
+    case = decode_case(75, len(lens), lens, Hq, Hkv, 128, bs, dtype=dtype)
+    (kq, vq, ks, vs), d = _int8_pool_on_gpu(case)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.full((len(lens),), -7, dtype=torch.int32, device="cuda")
+    out = kvc_lib.paged_decode_int8_append(
+        to_cuda(case.q), to_cuda(case.new_key), to_cuda(case.new_value), d["kq"], d["vq"],
+        d["ks"], d["vs"], to_cuda(case.block_table), to_cuda(case.seq_lens), case.scale,
+        slot_mapping=slots, num_ctas=num_ctas, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    wp = case.write_pos.numpy()
+    live = np.array(lens) > 0
+    sm = O.slot_mapping(case.block_table.numpy()[live], case.block_size, wp[live])
+    exp_slots = np.full(len(lens), -1)
+    exp_slots[live] = sm
+    assert slots.cpu().numpy().tolist() == exp_slots.tolist()
+    rk, rv, rks, rvs = O.reshape_and_cache_int8(case.new_key.float().numpy()[live],
+                                                case.new_value.float().numpy()[live],
+                                                kq, vq, ks, vs, sm)
+    assert np.array_equal(d["kq"].cpu().numpy(), rk) and np.array_equal(d["vq"].cpu().numpy(), rv)
+    assert np.array_equal(d["ks"].cpu().numpy().view(np.uint32), rks.view(np.uint32))
+    assert np.array_equal(d["vs"].cpu().numpy().view(np.uint32), rvs.view(np.uint32))
+    ref = O.paged_decode_int8(case.q.double().numpy(), rk, rv, rks, rvs, case.block_table.numpy(),
+                              case.seq_lens.numpy(), case.scale)
+    assert excess(out, ref, dtype) <= 0
+
+
+def test_int8_append_equals_write_then_decode(kvc_lib):
+    """The fused step is bitwise the two-call path (quantising write, then INT8 decode) at
+    the same CTA count, and a block-table entry outside the pool is flagged, not written."""
+    lens = [300, 17, 1024, 5, 640, 129]
+    case = decode_case(76, len(lens), lens, 8, 2, 128, 16, dtype="bf16")
+    _, d1 = _int8_pool_on_gpu(case)
+    _, d2 = _int8_pool_on_gpu(case)
+    bt, sl = to_cuda(case.block_table), to_cuda(case.seq_lens)
+    q, nk, nv = to_cuda(case.q), to_cuda(case.new_key), to_cuda(case.new_value)
+    fused = kvc_lib.paged_decode_int8_append(q, nk, nv, d1["kq"], d1["vq"], d1["ks"], d1["vs"],
+                                             bt, sl, case.scale, num_ctas=37)
+    slots = kvc_lib.build_slot_mapping(bt, case.block_size, to_cuda(case.write_pos),
+                                       d2["kq"].shape[0])
+    kvc_lib.reshape_and_cache_int8(nk, nv, d2["kq"], d2["vq"], d2["ks"], d2["vs"], slots)
+    two = kvc_lib.paged_decode_int8(q, d2["kq"], d2["vq"], d2["ks"], d2["vs"], bt, sl,
+                                    case.scale, num_ctas=37)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
+    for n in ("kq", "vq", "ks", "vs"):
+        assert torch.equal(d1[n], d2[n]), n
+    # a bogus table entry at the new token's block: flagged, slot -1, nothing written there
+    bad = case.block_table.clone()
+    b = 1
+    bad[b, (lens[b] - 1) // case.block_size] = 10_000
+    _, d3 = _int8_pool_on_gpu(case)
+    before = d3["kq"].clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots3 = torch.zeros(len(lens), dtype=torch.int32, device="cuda")
+    kvc_lib.paged_decode_int8_append(q, nk, nv, d3["kq"], d3["vq"], d3["ks"], d3["vs"],
+                                     to_cuda(bad), sl, case.scale, slot_mapping=slots3,
+                                     err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & kvc_lib.FLAG_BLOCK_ID_RANGE
+    assert int(slots3[b].item()) == -1
+    changed = (d3["kq"] != before).any(dim=(1, 2, 3)).cpu().numpy()
+    good_blocks = {int(case.block_table[i, (L - 1) // case.block_size]) for i, L in
+                   enumerate(lens) if i != b}
+    assert set(np.nonzero(changed)[0].tolist()) <= good_blocks
