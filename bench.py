@@ -833,7 +833,11 @@ def main():
 
     # End to end through the public API: per step, the step's inputs (staged
     # in one pinned host buffer, as a serving loop would) -> device in one
-    # copy, the step, device -> pinned host output, synchronised.
+    # copy, the step, device -> pinned host output, and the host waits for
+    # that output.  Serial: each step synchronised before the next.
+    # Pipelined: two buffer sets; step i+1's inputs copy (copy stream) while
+    # step i runs (compute stream) and step i-1's output copies back (a third
+    # stream); the host waits for step i's output before it stages step i+2.
     names = ("q", "new_key", "new_value", "block_table", "seq_lens")
     src = {k: getattr(case, k).cpu().contiguous() for k in names}
     offs, total = {}, 0
@@ -841,28 +845,65 @@ def main():
         offs[k] = total
         total += (src[k].numel() * src[k].element_size() + 255) // 256 * 256
     h_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
-    d_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+    d_packs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    outs = [step.out, torch.empty_like(step.out)]
 
     def view(buf, k):
         n = src[k].numel() * src[k].element_size()
         return buf[offs[k]:offs[k] + n].view(src[k].dtype).view(src[k].shape)
 
+    sets = [tuple(view(d_packs[j], k) for k in names) for j in range(2)]
+
+    def use(i):  # point the step at buffer set i % 2
+        step.q, step.nk, step.nv, step.bt, step.sl = sets[i % 2]
+        step.out = outs[i % 2]
+
     for k in names:
         view(h_pack, k).copy_(src[k])
-    step.q, step.nk, step.nv, step.bt, step.sl = (view(d_pack, k) for k in names)
-    h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h_outs = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
     h2d = total
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
     for i in range(3 + args.e2e_steps):
         if i == 3:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        d_pack.copy_(h_pack, non_blocking=True)
+        use(0)
+        d_packs[0].copy_(h_pack, non_blocking=True)
         step.step()
-        h_out.copy_(step.out, non_blocking=True)
+        h_outs[0].copy_(step.out, non_blocking=True)
         torch.cuda.synchronize()
+    e2e_serial_s = (time.perf_counter() - t0) / max(1, args.e2e_steps)
+
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    n_pipe = 3 + args.e2e_steps
+    ev_in = [torch.cuda.Event() for _ in range(n_pipe)]
+    ev_done = [torch.cuda.Event() for _ in range(n_pipe)]
+    ev_out = [torch.cuda.Event() for _ in range(n_pipe)]
+    torch.cuda.synchronize()
+    for i in range(n_pipe):
+        if i == 3:
+            ev_out[2].synchronize()
+            t0 = time.perf_counter()
+        if i >= 2:
+            ev_out[i - 2].synchronize()    # step i-2's result is on the host
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_done[i - 2])  # its input buffer is free again
+            d_packs[i % 2].copy_(h_pack, non_blocking=True)
+            ev_in[i].record(s_in)
+        stream.wait_event(ev_in[i])
+        use(i)
+        step.step()
+        ev_done[i].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[i])
+            h_outs[i % 2].copy_(outs[i % 2], non_blocking=True)
+            ev_out[i].record(s_out)
+    ev_out[n_pipe - 1].synchronize()
     e2e_s = (time.perf_counter() - t0) / max(1, args.e2e_steps)
+    torch.cuda.synchronize()
     e2e_s = max_over_ranks(e2e_s, dev)
+    e2e_serial_s = max_over_ranks(e2e_serial_s, dev)
 
     peak, peak_kind = peaks()
     dec_avg_ms = statistics.mean(dec_ms)
@@ -900,12 +941,16 @@ def main():
             },
             "e2e": {"value": ws * step_bytes / e2e_s / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_s * 1e3, "tokens_per_s": ws * B / e2e_s},
+                    "ms_per_step": e2e_s * 1e3, "tokens_per_s": ws * B / e2e_s,
+                    "pipelined": "2 buffer sets: step i+1's H2D and step i-1's D2H overlap "
+                                 "step i; the host waits for each step's output",
+                    "serial": {"value": ws * step_bytes / e2e_serial_s / 1e9,
+                               "ms_per_step": e2e_serial_s * 1e3}},
             "gpu_launches": DecodeStep.LAUNCHES * args.steps,
             "clocks": clk.summary(),
         }
         if not args.no_secondary:
-            del step, g_dec, d_pack, h_pack, h_out
+            del step, g_dec, d_packs, outs, h_pack, h_outs
             torch.cuda.empty_cache()
             res["secondary"] = secondary(kvc, dev, rank, min(args.steps, 100), args.warmup)
         if not args.no_cpu_baseline:

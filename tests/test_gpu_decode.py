@@ -242,16 +242,23 @@ def test_full_size_config_step(kvc_lib, name):
     bt = case.block_table.numpy()
     ref_slots = O.slot_mapping(bt, case.block_size, case.write_pos.numpy())
     assert slots.cpu().numpy().tolist() == ref_slots.tolist()
-    # the write changed exactly the rows at those slots, to the new rows, bit for bit
-    exp_k, exp_v = kc0.clone(), vc0.clone()
+    # the touched blocks equal the oracle's write into them, bit for bit (the blocks are
+    # gathered into a compact pool and the oracle's slots renumbered), and every other
+    # block is unchanged
     bs = case.block_size
-    idx_b = torch.from_numpy(ref_slots // bs).cuda()
-    idx_o = torch.from_numpy(ref_slots % bs).cuda()
-    exp_k[idx_b, idx_o] = case.new_key
-    exp_v[idx_b, idx_o] = case.new_value
-    assert torch.equal(exp_k.view(torch.int16), d["key_cache"].view(torch.int16))
-    assert torch.equal(exp_v.view(torch.int16), d["value_cache"].view(torch.int16))
-    del exp_k, exp_v
+    touched = np.unique(ref_slots // bs)
+    where = {int(b): i for i, b in enumerate(touched)}
+    small = np.array([where[int(s) // bs] * bs + int(s) % bs for s in ref_slots])
+    tb = torch.from_numpy(touched).cuda()
+    rk, rv = O.reshape_and_cache(bits(case.new_key), bits(case.new_value), bits(kc0[tb]),
+                                 bits(vc0[tb]), small)
+    assert np.array_equal(bits(d["key_cache"][tb]), rk)
+    assert np.array_equal(bits(d["value_cache"][tb]), rv)
+    rest = torch.ones(kc0.shape[0], dtype=torch.bool, device="cuda")
+    rest[tb] = False
+    assert torch.equal(d["key_cache"][rest].view(torch.int16), kc0[rest].view(torch.int16))
+    assert torch.equal(d["value_cache"][rest].view(torch.int16), vc0[rest].view(torch.int16))
+    del rest
     worst = -1.0
     for b in range(case.q.shape[0]):
         ref = oracle_step_seq(case, b, kc0, vc0)
