@@ -108,7 +108,7 @@ def decode_workload(name, case, ws):
 
 def kernel_source_digest():
     h = hashlib.sha256()
-    for name in ("paged_decode.cu", "kvc_device.cuh"):
+    for name in ("paged_decode.cu", "kvc_device.cuh", "api.cu"):  # api.cu: tensor-map encoding
         with open(os.path.join(ROOT, "paged_kv_cache_135_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -594,7 +594,9 @@ def measure_int8(kvc, dev, rank, steps, warmup):
                     "write of the new token, decode and split-KV merge in one launch)",
                     per["decode"], by, "GB/s", hp, hkind, clk.summary(), bound="hbm",
                     bytes_vs_16bit=by / (decode_bytes(lens, Hq, Hkv, D, bs) +
-                                         write_bytes(B, Hkv, D)))
+                                         write_bytes(B, Hkv, D)),
+                    traffic=recorded_traffic("paged_decode_kernel_int8/" + WORKLOAD,
+                                             kernel_source_digest()))
     del codes, scales, q, bt, sl, nk, nv, out, slots, ws, graphs
     return fig
 
