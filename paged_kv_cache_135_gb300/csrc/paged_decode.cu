@@ -47,25 +47,28 @@ namespace kvc {
 
 namespace {
 
-constexpr int kTile = 64;            // tokens per pipeline stage
+constexpr int kTile = 64;            // tokens per pipeline stage over a 16-bit cache
 constexpr int kConsumerWarps = 4;    // 16 tokens each
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-// Pipeline depth: 3 stages, of ~33 KB over a 16-bit cache (two CTAs per SM)
-// or ~20 KB over an INT8 cache (codes, scales and query rows; three CTAs per
-// SM, which measured faster than two with 4 stages).
+// Over an INT8 cache a stage holds 128 tokens (the bytes of a 64-token
+// stage of a 16-bit cache), so the per-tile work of a consumer warp (waits,
+// cursor, masks, one online-softmax update) is paid per 32 tokens, not 16.
 template <bool kI8>
-constexpr int stages_of() { return 3; }
-// Resident CTAs per SM the kernel is compiled for (register budget): three
-// for an INT8 cache with one 8-row query tile, else two (the two-tile INT8
-// kernel would spill under three's 128 registers a thread).
+constexpr int tile_of() { return kI8 ? 128 : kTile; }
+// Pipeline depth: 3 stages of ~33 KB over a 16-bit cache, 2 of ~38 KB over
+// an INT8 cache (codes, scales and query rows); two CTAs per SM either way.
+template <bool kI8>
+constexpr int stages_of() { return kI8 ? 2 : 3; }
+// Resident CTAs per SM the kernel is compiled for (register budget).
 template <int kQ>
-constexpr int min_ctas_of() { return kQ == 1 ? 3 : 2; }
+constexpr int min_ctas_of() { return 2; }
 constexpr int kMaxBatch = 1024;
 constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a K or V tile
 constexpr int kMaxPieces = 62;           // split shares merged from a shared-memory list
 // INT8 cache: a tile's per-token scales arrive as one TMA box per physical
-// block (min(block_size, 64) floats); each box gets its own 128-byte slot.
-constexpr int kScaleBytes = (kTile / 8) * 128;
+// block (min(block_size, 128) floats); each box gets its own slot of
+// max(128, 4 * box) bytes, so every TMA destination is 128-byte aligned.
+constexpr int kScaleBytes = (tile_of<true>() / 8) * 128;
 
 struct DecodeParams {
   const void* q;
@@ -92,6 +95,7 @@ struct DecodeParams {
   int32_t* slot_out;
   int batch, num_q_heads, num_kv_heads, group, head_dim;
   int block_size, log2_bs, max_blocks, num_blocks, box_tokens, log2_box;
+  int log2_sslot;  // INT8: log2 of a scale box's slot in the stage (>= 7)
   int window;  // band of the last `window` cached tokens (0: the whole sequence)
   float scale_log2;
 };
@@ -107,9 +111,9 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 template <int D, bool kI8>
 struct Layout {
   static constexpr int kHalves = D / 64;  // 64-element halves of a 16-bit row
-  static constexpr int kKBytes = kI8 ? kTile * D : kHalves * kHalfBytes;  // one K or V tile
+  static constexpr int kKBytes = kI8 ? tile_of<true>() * D : kHalves * kHalfBytes;  // K or V tile
   int q_half;   // bytes of one 64-wide half of the G query rows (1024-aligned)
-  int scales;   // INT8: K scales then V scales of the stage, kTile floats each
+  int scales;   // INT8: K scales then V scales of the stage, kScaleBytes each
   int qoff;     // query rows of the stage (1024-aligned)
   int stage;    // K tile, V tile, (scales), query rows
   static constexpr int kStages = stages_of<kI8>();
@@ -194,11 +198,12 @@ __device__ __forceinline__ uint32_t keep_rows(uint32_t x, int k, int vlo, int va
 
 // Band attention (sliding window): a sequence of L cached tokens attends to
 // positions band_lo .. L-1 only, the last `window` of them (0: all).  Its
-// tiles start at the 64-token tile holding band_lo.
+// tiles start at the kT-token tile holding band_lo.
 __device__ __forceinline__ int band_lo(int L, int window) {
   return window > 0 && L > window ? L - window : 0;
 }
-__device__ __forceinline__ int first_tile(int L, int window) { return band_lo(L, window) / kTile; }
+template <int kT>
+__device__ __forceinline__ int first_tile(int L, int window) { return band_lo(L, window) / kT; }
 
 // out[0..3] = v * inv, rounded to T (one 8-byte store).
 template <typename T>
@@ -301,11 +306,6 @@ __device__ __forceinline__ float lds_f32(uint32_t a) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
 
 // Four int8 codes (one 32-bit word, byte k = element k) as two fp16 pairs,
 // exactly: each code c (|c| <= 127) is biased to the byte c + 128, placed as
@@ -321,28 +321,6 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
   lo = *reinterpret_cast<const uint32_t*>(&ra);
   hi = *reinterpret_cast<const uint32_t*>(&rb);
 }
-
-// The codes of two tokens at the same four elements (wa, wb: byte k =
-// element k) as four fp16 pairs {token a, token b}, one per element,
-// exactly as i8x4_to_f16: the bytes are first interleaved a0 b0 a1 b1 /
-// a2 b2 a3 b3, then each pair is widened.
-__device__ __forceinline__ void i8x4x2_to_f16_pairs(uint32_t wa, uint32_t wb,
-                                                    uint32_t (&r)[4]) {
-  const uint32_t xa = wa ^ 0x80808080u, xb = wb ^ 0x80808080u;
-  const uint32_t lo = __byte_perm(xa, xb, 0x5140u);
-  const uint32_t hi = __byte_perm(xa, xb, 0x7362u);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-  const uint32_t t[4] = {__byte_perm(lo, 0x64646464u, 0x4140u),
-                         __byte_perm(lo, 0x64646464u, 0x4342u),
-                         __byte_perm(hi, 0x64646464u, 0x4140u),
-                         __byte_perm(hi, 0x64646464u, 0x4342u)};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t[i]), bias);
-    r[i] = *reinterpret_cast<const uint32_t*>(&v);
-  }
-}
-
 
 // A pair of 16-bit query values as an fp16 pair: unchanged for fp16; for bf16
 // exact whenever the values lie in fp16's normal range (|q| in [2^-14, 65504]),
@@ -367,12 +345,12 @@ __device__ __forceinline__ uint32_t q_pair_f16<__nv_bfloat16>(uint32_t w) {
 //
 // Score product, k-step kk (dims 16kk .. 16kk+15, permuted): lane (g =
 // lane/4, c = lane%4) holds dims 16kk + 4c .. 4c+3 of tokens g and g+8 (one
-// 32-bit load of codes each) and of query row g of each tile, in the slots
+// 32-bit word of codes each) and of query row g of each tile, in the slots
 // of k = 2c, 2c+1, 2c+8, 2c+9; a dot product does not depend on the order of
-// its terms.  Value product, dims 32blk .. 32blk+31: lane (g, c) loads the
-// codes of tokens 2c, 2c+1, 2c+8, 2c+9 at dims 32blk + 4g .. 4g+3, and the
-// output rows of m-tiles 2blk and 2blk+1 are permuted to match: row g / g+8
-// of m-tile 2blk+h is dim 32blk + 4g + 2h / 32blk + 4g + 2h + 1.
+// its terms.  Value product, dims 16ch .. 16ch+15 (m-tile ch of O^T): lane
+// (g, c) holds the codes of tokens 2c, 2c+1 (and 2c+8, 2c+9) at dims
+// 16ch + 2g and 2g+1, and the m-tile's output rows are permuted to match:
+// row g is dim 16ch + 2g, row g+8 dim 16ch + 2g + 1.
 
 // The segment's query fragments (B of the score product) from the stage's
 // query rows, as fp16: qb[kk][nt] = dims 16kk + 4c .. 4c+3 of row 8nt + g.
@@ -397,40 +375,47 @@ __device__ __forceinline__ void load_q_i8(uint32_t qbase, int q_half, int group,
 }
 
 // Per-lane shared-memory offsets of the INT8 consumer, the same for every
-// tile (relative to a stage's K or V tile and scale region).  With the
-// 128-byte swizzle a row r's chunk x sits at r * 128 + ((x ^ (r % 8)) << 4);
-// the warp's rows start at a multiple of 8, so rows g and g+8 share one XOR
-// pattern (g), and so do rows 2c, 2c+8 (2c) and 2c+1, 2c+9 (2c+1).
+// tile (relative to a stage's K or V tile and scale region).  A consumer
+// warp takes 32 tokens of a 128-token stage, as two 16-token sub-tiles
+// (+2048 bytes).  With the 128-byte swizzle a row r's chunk x sits at
+// r * 128 + ((x ^ (r % 8)) << 4), and the sub-tiles start at multiples of 8
+// rows.  Codes are read with ldmatrix (8 rows of 16 bytes per matrix):
+// without .trans lane (g, c) receives bytes 4c .. 4c+3 of row g, with .trans
+// (16-bit elements) bytes 2g, 2g+1 of rows 2c and 2c+1.
 struct I8Lane {
-  uint32_t k_row;    // row g, byte 4c
-  uint32_t k_xor;    // g << 4
-  uint32_t v_row;    // row 2c, byte 4 (g % 4)
-  uint32_t v_xor;    // (2c << 4) ^ ((g / 4) << 4), the chunk bits of row 2c for blk = 0
-  uint32_t ks0, ks1;  // scales of tokens g and g+8 (one 128-byte slot per TMA box
-                      // of 2^log2_box tokens)
-  __device__ __forceinline__ I8Lane(int warp, int lane, int log2_box) {
-    const int g = lane >> 2, c = lane & 3;
-    const int t0 = warp * 16 + g;
-    k_row = static_cast<uint32_t>(t0 * 128 + 4 * c);
-    k_xor = static_cast<uint32_t>(g << 4);
-    v_row = static_cast<uint32_t>((warp * 16 + 2 * c) * 128 + 4 * (g & 3));
-    v_xor = static_cast<uint32_t>(((2 * c) ^ (g >> 2)) << 4);
+  // ldmatrix.x4 row addresses: lane L gives row (L / 8 % 2) * 8 + L % 8 of
+  // a 16-token sub-tile in chunk x + L / 16, at row_ofs + ((x << 4) ^ xr) for
+  // an even chunk x.
+  uint32_t row_ofs;
+  uint32_t xr;
+  uint32_t sc[4];    // scales of the warp's tokens g, g+8, g+16, g+24 (one slot of
+                     // 2^log2_slot bytes per TMA box of 2^log2_box tokens)
+  __device__ __forceinline__ I8Lane(int warp, int lane, int log2_box, int log2_slot) {
+    const int g = lane >> 2;
+    const int t0 = warp * 32 + g;
+    const int r = lane & 7;
+    row_ofs = static_cast<uint32_t>((warp * 32 + ((lane >> 3) & 1) * 8 + r) * 128);
+    xr = static_cast<uint32_t>(((lane >> 4) ^ r) << 4);
     const int box = 1 << log2_box;
-    ks0 = static_cast<uint32_t>(((t0 >> log2_box) << 7) + ((t0 & (box - 1)) << 2));
-    ks1 = static_cast<uint32_t>((((t0 + 8) >> log2_box) << 7) + (((t0 + 8) & (box - 1)) << 2));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + 8 * i;
+      sc[i] = static_cast<uint32_t>(((t >> log2_box) << log2_slot) + ((t & (box - 1)) << 2));
+    }
   }
 };
 
-// One warp's 16 tokens of a stage over an INT8 cache.  A cached row is
-// code * scale, so q . k = scale_k * (q . codes_k) and sum_j p_j v_j =
-// sum_j (p_j * scale_v_j) codes_v_j.  The codes are exact in fp16, the
-// queries are (load_q_i8), and the weights p * scale_v keep 11 bits (l sums
-// the plain p, so the weights are not renormalised after rounding).  State
-// per lane: m, l and O for query rows 8nt + 2c and 8nt + 2c + 1; l is this
-// lane's share (tokens g and g+8), summed over the 8 lanes of a query at the
-// end of the segment.
+// One warp's 32 tokens of a stage over an INT8 cache, two sub-tiles of 16
+// sharing one online-softmax update.  A cached row is code * scale, so
+// q . k = scale_k * (q . codes_k) and sum_j p_j v_j = sum_j (p_j * scale_v_j)
+// codes_v_j.  The codes are exact in fp16, the queries are (load_q_i8), and
+// the weights p * scale_v keep 11 bits (l sums the plain p, so the weights
+// are not renormalised after rounding).  State per lane: m, l and O for
+// query rows 8nt + 2c and 8nt + 2c + 1; l is this lane's share (tokens g and
+// g+8 of each sub-tile), summed over the 8 lanes of a query at the end of
+// the segment.  Rows [vlo, valid) of the warp's 32 are attended.
 template <int D, int NT>
-__device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
+__device__ __forceinline__ void attend_32_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
                                              uint32_t vscale, const I8Lane& ofs, int lane,
                                              int vlo, int valid, float scale_log2,
                                              const uint32_t (&qb)[D / 16][NT][2],
@@ -439,58 +424,79 @@ __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uin
   static_assert(D == 128, "one 128-byte code row per token");
   const int g = lane >> 2, c = lane & 3;
   // All shared-memory loads first (the asm statements keep program order),
-  // so their latencies overlap.  Rows +8 are +1024 bytes with the same
+  // so their latencies overlap.  Row +8 is +1024 bytes with the same
   // swizzle; row 2c+1 is row 2c + 128 bytes with chunk bit 0 flipped.
-  const float ks0 = lds_f32(kscale + ofs.ks0), ks1 = lds_f32(kscale + ofs.ks1);
-  const float vs0 = lds_f32(vscale + ofs.ks0), vs1 = lds_f32(vscale + ofs.ks1);
-  uint32_t kw[D / 16][2];
-  const uint32_t kr = kbase + ofs.k_row;
+  float ks[4], vs[4];
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t a = kr + ((kk << 4) ^ ofs.k_xor);
-    kw[kk][0] = lds_u32(a);
-    kw[kk][1] = lds_u32(a + 1024);
+  for (int i = 0; i < 4; ++i) ks[i] = lds_f32(kscale + ofs.sc[i]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) vs[i] = lds_f32(vscale + ofs.sc[i]);
+  // K: one ldmatrix.x4 per two k-steps gives a lane its codes at dims
+  // 16kk + 4c .. 4c+3 of tokens g and g+8 for kk and kk+1.  V: one
+  // ldmatrix.x4.trans per two 16-dim chunks gives a lane, per chunk, the codes
+  // of tokens 2c, 2c+1 (and 2c+8, 2c+9) at dims 16 ch + 2g, 2g+1.
+  // With two query tiles (NT = 2) the V loads wait until the scores are done,
+  // to keep the live registers within the two-CTAs-per-SM budget.
+  uint32_t kw[2][D / 16][2], vw[2][D / 16][2];
+  auto load_v = [&]() {
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+      for (int ch = 0; ch < D / 16; ch += 2)
+        ldsm_x4_t(vbase + ofs.row_ofs + sub * 2048 + ((ch << 4) ^ ofs.xr), vw[sub][ch][0],
+                  vw[sub][ch][1], vw[sub][ch + 1][0], vw[sub][ch + 1][1]);
+  };
+#pragma unroll
+  for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+    for (int kk = 0; kk < D / 16; kk += 2)
+      ldsm_x4(kbase + ofs.row_ofs + sub * 2048 + ((kk << 4) ^ ofs.xr), kw[sub][kk][0],
+              kw[sub][kk][1], kw[sub][kk + 1][0], kw[sub][kk + 1][1]);
+  if constexpr (NT == 1) load_v();
+  float s[2][NT][4];
+#pragma unroll
+  for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[sub][nt][e] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+      uint32_t a[4];
+      i8x4_to_f16(kw[sub][kk][0], a[0], a[2]);
+      i8x4_to_f16(kw[sub][kk][1], a[1], a[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        MmaOp<__half>::run(s[sub][nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+    }
+  if constexpr (NT != 1) load_v();
+  // s[sub][nt][0, 1]: token 16 sub + g, queries 2c, 2c+1; [2, 3]: token 16 sub
+  // + g + 8.  Stale stage contents outside [vlo, valid) never enter arithmetic.
+  bool in[4];
+  float f[4], w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // token 8 i + g of the warp's 32
+    in[i] = 8 * i + g >= vlo && 8 * i + g < valid;
+    f[i] = in[i] ? scale_log2 * ks[i] : 0.f;
+    w[i] = in[i] ? vs[i] : 0.f;
   }
-  uint32_t vw[D / 32][4];
-  const uint32_t vr = vbase + ofs.v_row;
-#pragma unroll
-  for (int blk = 0; blk < D / 32; ++blk) {
-    const uint32_t x = (blk << 5) ^ ofs.v_xor;  // row 2c: chunk 2 blk + g/4, swizzled
-    const uint32_t a0 = vr + x, a1 = vr + 128 + (x ^ 16);
-    vw[blk][0] = lds_u32(a0);
-    vw[blk][1] = lds_u32(a1);
-    vw[blk][2] = lds_u32(a0 + 1024);
-    vw[blk][3] = lds_u32(a1 + 1024);
-  }
-  float s[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    uint32_t a[4];
-    i8x4_to_f16(kw[kk][0], a[0], a[2]);
-    i8x4_to_f16(kw[kk][1], a[1], a[3]);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) MmaOp<__half>::run(s[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
-  }
-  // s[nt][0, 1]: token g, queries 2c, 2c+1; s[nt][2, 3]: token g+8.  Stale
-  // stage contents outside [vlo, valid) never enter arithmetic.
-  const bool in0 = g >= vlo && g < valid, in1 = g + 8 >= vlo && g + 8 < valid;
-  const float f0 = in0 ? scale_log2 * ks0 : 0.f, f1 = in1 ? scale_log2 * ks1 : 0.f;
-  const float w0 = in0 ? vs0 : 0.f, w1 = in1 ? vs1 : 0.f;
   bool grew = false;
   float corr[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    s[nt][0] = in0 ? s[nt][0] * f0 : -INFINITY;
-    s[nt][1] = in0 ? s[nt][1] * f0 : -INFINITY;
-    s[nt][2] = in1 ? s[nt][2] * f1 : -INFINITY;
-    s[nt][3] = in1 ? s[nt][3] * f1 : -INFINITY;
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+      const int i0 = 2 * sub, i1 = 2 * sub + 1;
+      s[sub][nt][0] = in[i0] ? s[sub][nt][0] * f[i0] : -INFINITY;
+      s[sub][nt][1] = in[i0] ? s[sub][nt][1] * f[i0] : -INFINITY;
+      s[sub][nt][2] = in[i1] ? s[sub][nt][2] * f[i1] : -INFINITY;
+      s[sub][nt][3] = in[i1] ? s[sub][nt][3] * f[i1] : -INFINITY;
+    }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float mx = fmaxf(s[nt][e], s[nt][e + 2]);
+      float mx = fmaxf(fmaxf(s[0][nt][e], s[0][nt][e + 2]), fmaxf(s[1][nt][e], s[1][nt][e + 2]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -501,27 +507,35 @@ __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uin
     }
   }
   // The B fragments of P^T: lane (g, c) needs the weights of query row 8nt+g
-  // at tokens 2c, 2c+1 (lanes 8c + g/2 and 8c + 4 + g/2 hold them, as the
-  // low or high half of their packed pair) and at tokens 2c+8, 2c+9 (the same
-  // lanes' second pair).
+  // at tokens 2c, 2c+1 of a sub-tile (lanes 8c + g/2 and 8c + 4 + g/2 hold
+  // them, as the low or high half of their packed pair) and at tokens 2c+8,
+  // 2c+9 (the same lanes' second pair).
   const int src_a = 8 * c + (g >> 1), src_b = src_a + 4;
   const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
-  uint32_t pb[NT][2];
+  uint32_t pb[2][NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const float p0 = fast_exp2(s[nt][0] - m[nt][0]), p1 = fast_exp2(s[nt][1] - m[nt][1]);
-    const float p2 = fast_exp2(s[nt][2] - m[nt][0]), p3 = fast_exp2(s[nt][3] - m[nt][1]);
-    l[nt][0] = l[nt][0] * corr[nt][0] + (p0 + p2);
-    l[nt][1] = l[nt][1] * corr[nt][1] + (p1 + p3);
-    float ra, rb;
-    const uint32_t x = Pack<__half>::run(p0 * w0, p1 * w0, ra, rb);
-    const uint32_t y = Pack<__half>::run(p2 * w1, p3 * w1, ra, rb);
-    const uint32_t xa = __shfl_sync(0xffffffffu, x, src_a);
-    const uint32_t xb = __shfl_sync(0xffffffffu, x, src_b);
-    const uint32_t ya = __shfl_sync(0xffffffffu, y, src_a);
-    const uint32_t yb = __shfl_sync(0xffffffffu, y, src_b);
-    pb[nt][0] = __byte_perm(xa, xb, sel);
-    pb[nt][1] = __byte_perm(ya, yb, sel);
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub) {
+      const float p0 = fast_exp2(s[sub][nt][0] - m[nt][0]);
+      const float p1 = fast_exp2(s[sub][nt][1] - m[nt][1]);
+      const float p2 = fast_exp2(s[sub][nt][2] - m[nt][0]);
+      const float p3 = fast_exp2(s[sub][nt][3] - m[nt][1]);
+      ls0 += p0 + p2;
+      ls1 += p1 + p3;
+      float ra, rb;
+      const uint32_t x = Pack<__half>::run(p0 * w[2 * sub], p1 * w[2 * sub], ra, rb);
+      const uint32_t y = Pack<__half>::run(p2 * w[2 * sub + 1], p3 * w[2 * sub + 1], ra, rb);
+      const uint32_t xa = __shfl_sync(0xffffffffu, x, src_a);
+      const uint32_t xb = __shfl_sync(0xffffffffu, x, src_b);
+      const uint32_t ya = __shfl_sync(0xffffffffu, y, src_a);
+      const uint32_t yb = __shfl_sync(0xffffffffu, y, src_b);
+      pb[sub][nt][0] = __byte_perm(xa, xb, sel);
+      pb[sub][nt][1] = __byte_perm(ya, yb, sel);
+    }
+    l[nt][0] = l[nt][0] * corr[nt][0] + ls0;
+    l[nt][1] = l[nt][1] * corr[nt][1] + ls1;
   }
   if (__any_sync(0xffffffffu, grew)) {  // O keeps its scale while no row max grows
 #pragma unroll
@@ -535,20 +549,28 @@ __device__ __forceinline__ void attend_16_i8(uint32_t kbase, uint32_t vbase, uin
       }
   }
   // Codes are finite, and the weights outside [vlo, valid) are exact zeros,
-  // so no value row needs masking here.
+  // so no value row needs masking here.  m-tile ch of O^T: row g is dim
+  // 16 ch + 2g, row g+8 dim 16 ch + 2g + 1.
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
 #pragma unroll
-  for (int blk = 0; blk < D / 32; ++blk) {
-    uint32_t r01[4], r89[4];
-    i8x4x2_to_f16_pairs(vw[blk][0], vw[blk][1], r01);
-    i8x4x2_to_f16_pairs(vw[blk][2], vw[blk][3], r89);
-    const uint32_t a0[4] = {r01[0], r01[1], r89[0], r89[1]};
-    const uint32_t a1[4] = {r01[2], r01[3], r89[2], r89[3]};
+  for (int sub = 0; sub < 2; ++sub)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      MmaOp<__half>::run(o[nt][2 * blk], a0, pb[nt][0], pb[nt][1]);
-      MmaOp<__half>::run(o[nt][2 * blk + 1], a1, pb[nt][0], pb[nt][1]);
+    for (int ch = 0; ch < D / 16; ++ch) {
+      const uint32_t x0 = vw[sub][ch][0] ^ 0x80808080u, x1 = vw[sub][ch][1] ^ 0x80808080u;
+      const uint32_t t[4] = {__byte_perm(x0, 0x64646464u, 0x4240u),
+                             __byte_perm(x0, 0x64646464u, 0x4341u),
+                             __byte_perm(x1, 0x64646464u, 0x4240u),
+                             __byte_perm(x1, 0x64646464u, 0x4341u)};
+      uint32_t a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t[i]), bias);
+        a[i] = *reinterpret_cast<const uint32_t*>(&v);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        MmaOp<__half>::run(o[nt][ch], a, pb[sub][nt][0], pb[sub][nt][1]);
     }
-  }
 }
 
 // The end of one segment share (cold path, kept out of line to spare the
@@ -676,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
                         const __grid_constant__ DecodeParams p) {
   constexpr bool kI8 = kQ > 0;
   constexpr int kNT = kI8 ? kQ : 1;
+  constexpr int kT = tile_of<kI8>();  // tokens per stage
   constexpr int kHalves = Layout<D, kI8>::kHalves;
   constexpr int kKBytes = Layout<D, kI8>::kKBytes;
   constexpr int kStages = Layout<D, kI8>::kStages;
@@ -721,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
     int carry = 0;
     for (int base = 0; base < B; base += 32) {
       const int i = base + lane;
-      const int n = i < B ? (lens[i] + kTile - 1) / kTile - first_tile(lens[i], p.window) : 0;
+      const int n = i < B ? (lens[i] + kT - 1) / kT - first_tile<kT>(lens[i], p.window) : 0;
       int x = n;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -756,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
     // ------------------------------------------------------------ producer
     Cursor cur;
     cur.locate(t_begin, cum, B, hkv);
-    const int nsub = kTile / p.box_tokens;
+    const int nsub = kT / p.box_tokens;
     // Bytes of one box: a 64-element half of box_tokens 16-bit rows, or
     // box_tokens whole 128-byte code rows.
     const uint32_t box_bytes = static_cast<uint32_t>(p.box_tokens) * 128u;
@@ -784,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
       // Look up this tile's physical blocks first: the table load's latency
       // overlaps the wait for a free stage.
       const int Lb = lens[cur.b];
-      const int tok = (first_tile(Lb, p.window) + cur.j) * kTile + lane * p.box_tokens;
+      const int tok = (first_tile<kT>(Lb, p.window) + cur.j) * kT + lane * p.box_tokens;
       // A box wholly below the band is not fetched (its rows are masked).
       const bool wanted = lane < nsub && tok < Lb && tok + p.box_tokens > band_lo(Lb, p.window);
       int pb = -1;
@@ -868,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
           if constexpr (kI8) {
             tma_load_4d(kdst, &tm_k, &full[stage], 0, cur.g, in_blk, pb);
             tma_load_4d(kdst + kKBytes, &tm_v, &full[stage], 0, cur.g, in_blk, pb);
-            uint8_t* sdst = st + L.scales + lane * 128;
+            uint8_t* sdst = st + L.scales + (lane << p.log2_sslot);
             tma_load_3d(sdst, &tm_ks, &full[stage], in_blk, cur.g, pb);
             tma_load_3d(sdst + kScaleBytes, &tm_vs, &full[stage], in_blk, cur.g, pb);
           } else {
@@ -924,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
   };
   reset();
   bool need_q = true;  // INT8: the segment's query fragments are still to be loaded
-  const I8Lane i8ofs(warp, lane, p.log2_box);
+  const I8Lane i8ofs(warp, lane, p.log2_box, p.log2_sslot);
   int seg_first_j = cur.j;
   int slot = 0;  // 0 for the first segment this CTA touches, 1 afterwards
   const uint32_t sbase = smem_u32(smem);
@@ -943,13 +966,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
       }
     }
     const int Lc = lens[cur.b];
-    const int row0 = (first_tile(Lc, p.window) + cur.j) * kTile + warp * 16;
-    const int valid = min(16, Lc - row0);                     // rows [vlo, valid) of the
-    const int vlo = max(0, band_lo(Lc, p.window) - row0);     // warp's 16 are attended
+    constexpr int kRows = kT / kConsumerWarps;                // the warp's rows: 16 or 32
+    const int row0 = (first_tile<kT>(Lc, p.window) + cur.j) * kT + warp * kRows;
+    const int valid = min(kRows, Lc - row0);                  // rows [vlo, valid) of the
+    const int vlo = max(0, band_lo(Lc, p.window) - row0);     // warp's are attended
     if (ok && valid > vlo) {
       const uint32_t kb = sbase + stage * L.stage;
       if constexpr (kI8)
-        attend_16_i8<D, kNT>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
+        attend_32_i8<D, kNT>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
                              i8ofs, lane, vlo, valid, p.scale_log2, qb, o8, m8, l8);
       else
         attend_16<T, D>(kb, kb + kKBytes, warp, lane, vlo, valid, p.scale_log2, kb + L.qoff,
@@ -964,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
       const bool complete = seg_first_j == 0 && last_of_seg;
       if constexpr (kI8) {
         // l: sum the 8 lanes (g) of each query; m is already the same there.
-        // Lane (g, c) holds dims 32blk + 4g .. 4g+3 of query rows 8nt + 2c + e.
+        // Lane (g, c) holds dims 16ch + 2g, 2g+1 of query rows 8nt + 2c + e.
         const int g8 = lane >> 2, c8 = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt)
@@ -981,10 +1005,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
                 cmb_l[warp * G + r] = x;
               }
 #pragma unroll
-              for (int blk = 0; blk < D / 32; ++blk)
-                *reinterpret_cast<float4*>(&cmb_o[(warp * G + r) * D + 32 * blk + 4 * g8]) =
-                    make_float4(o8[nt][2 * blk][e], o8[nt][2 * blk][e + 2],
-                                o8[nt][2 * blk + 1][e], o8[nt][2 * blk + 1][e + 2]);
+              for (int ch = 0; ch < D / 16; ++ch)
+                *reinterpret_cast<float2*>(&cmb_o[(warp * G + r) * D + 16 * ch + 2 * g8]) =
+                    make_float2(o8[nt][ch][e], o8[nt][ch][e + 2]);
             }
           }
       } else {
@@ -1062,7 +1085,8 @@ kvc_status run_decode(const DecodeArgs& a) {
   if (a.workspace_bytes < paged_decode_workspace_bytes(G, D, P) || a.workspace == nullptr)
     return KVC_ERR_WORKSPACE;
 
-  const int box_tokens = a.block_size < kTile ? a.block_size : kTile;
+  constexpr int kT = tile_of<kI8>();
+  const int box_tokens = a.block_size < kT ? a.block_size : kT;
   const uint64_t elt = kI8 ? 1 : 2;
   const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_kv_heads),
                             static_cast<uint64_t>(a.block_size),
@@ -1136,6 +1160,7 @@ kvc_status run_decode(const DecodeArgs& a) {
   p.num_blocks = a.num_blocks;
   p.box_tokens = box_tokens;
   p.log2_box = ilog2(box_tokens);
+  p.log2_sslot = p.log2_box + 2 > 7 ? p.log2_box + 2 : 7;
   p.window = a.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
 
