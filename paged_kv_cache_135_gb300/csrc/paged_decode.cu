@@ -50,18 +50,21 @@ namespace {
 constexpr int kTile = 64;            // tokens per pipeline stage over a 16-bit cache
 constexpr int kConsumerWarps = 4;    // 16 tokens each
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-// Over an INT8 cache a stage holds 128 tokens (the bytes of a 64-token
-// stage of a 16-bit cache), so the per-tile work of a consumer warp (waits,
-// cursor, masks, one online-softmax update) is paid per 32 tokens, not 16.
+// Over an INT8 cache each consumer warp takes kI8Sub 16-token sub-tiles of a
+// stage under one online-softmax update: with 2, a stage holds 128 tokens
+// (the bytes of a 64-token stage of a 16-bit cache) and the per-tile work of
+// a warp (waits, cursor, masks, the softmax update) is paid per 32 tokens.
+constexpr int kI8Sub = 2;
 template <bool kI8>
-constexpr int tile_of() { return kI8 ? 128 : kTile; }
-// Pipeline depth: 3 stages of ~33 KB over a 16-bit cache, 2 of ~38 KB over
-// an INT8 cache (codes, scales and query rows); two CTAs per SM either way.
+constexpr int tile_of() { return kI8 ? 64 * kI8Sub : kTile; }
+// Pipeline depth: 3 stages of ~33 KB over a 16-bit cache; over an INT8 cache
+// 2 stages of ~38 KB (128-token tiles, two CTAs per SM) or 3 of ~20 KB
+// (64-token tiles, three CTAs per SM).
 template <bool kI8>
-constexpr int stages_of() { return kI8 ? 2 : 3; }
+constexpr int stages_of() { return kI8 && kI8Sub == 2 ? 2 : 3; }
 // Resident CTAs per SM the kernel is compiled for (register budget).
 template <int kQ>
-constexpr int min_ctas_of() { return 2; }
+constexpr int min_ctas_of() { return kQ == 1 && kI8Sub == 1 ? 3 : 2; }
 constexpr int kMaxBatch = 1024;
 constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a K or V tile
 constexpr int kMaxPieces = 62;           // split shares merged from a shared-memory list
@@ -376,8 +379,7 @@ __device__ __forceinline__ void load_q_i8(uint32_t qbase, int q_half, int group,
 
 // Per-lane shared-memory offsets of the INT8 consumer, the same for every
 // tile (relative to a stage's K or V tile and scale region).  A consumer
-// warp takes 32 tokens of a 128-token stage, as two 16-token sub-tiles
-// (+2048 bytes).  With the 128-byte swizzle a row r's chunk x sits at
+// warp takes kI8Sub 16-token sub-tiles of a stage (2048 bytes apart).  With the 128-byte swizzle a row r's chunk x sits at
 // r * 128 + ((x ^ (r % 8)) << 4), and the sub-tiles start at multiples of 8
 // rows.  Codes are read with ldmatrix (8 rows of 16 bytes per matrix):
 // without .trans lane (g, c) receives bytes 4c .. 4c+3 of row g, with .trans
@@ -388,74 +390,74 @@ struct I8Lane {
   // an even chunk x.
   uint32_t row_ofs;
   uint32_t xr;
-  uint32_t sc[4];    // scales of the warp's tokens g, g+8, g+16, g+24 (one slot of
+  uint32_t sc[2 * kI8Sub];  // scales of the warp's tokens g, g+8, (g+16, g+24) (one slot of
                      // 2^log2_slot bytes per TMA box of 2^log2_box tokens)
   __device__ __forceinline__ I8Lane(int warp, int lane, int log2_box, int log2_slot) {
     const int g = lane >> 2;
-    const int t0 = warp * 32 + g;
+    const int t0 = warp * 16 * kI8Sub + g;
     const int r = lane & 7;
-    row_ofs = static_cast<uint32_t>((warp * 32 + ((lane >> 3) & 1) * 8 + r) * 128);
+    row_ofs = static_cast<uint32_t>((warp * 16 * kI8Sub + ((lane >> 3) & 1) * 8 + r) * 128);
     xr = static_cast<uint32_t>(((lane >> 4) ^ r) << 4);
     const int box = 1 << log2_box;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2 * kI8Sub; ++i) {
       const int t = t0 + 8 * i;
       sc[i] = static_cast<uint32_t>(((t >> log2_box) << log2_slot) + ((t & (box - 1)) << 2));
     }
   }
 };
 
-// One warp's 32 tokens of a stage over an INT8 cache, two sub-tiles of 16
-// sharing one online-softmax update.  A cached row is code * scale, so
+// One warp's 16 kI8Sub tokens of a stage over an INT8 cache: kI8Sub
+// sub-tiles of 16 sharing one online-softmax update.  A cached row is code * scale, so
 // q . k = scale_k * (q . codes_k) and sum_j p_j v_j = sum_j (p_j * scale_v_j)
 // codes_v_j.  The codes are exact in fp16, the queries are (load_q_i8), and
 // the weights p * scale_v keep 11 bits (l sums the plain p, so the weights
 // are not renormalised after rounding).  State per lane: m, l and O for
 // query rows 8nt + 2c and 8nt + 2c + 1; l is this lane's share (tokens g and
 // g+8 of each sub-tile), summed over the 8 lanes of a query at the end of
-// the segment.  Rows [vlo, valid) of the warp's 32 are attended.
+// the segment.  Rows [vlo, valid) of the warp's 16 kI8Sub are attended.
 template <int D, int NT>
-__device__ __forceinline__ void attend_32_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
-                                             uint32_t vscale, const I8Lane& ofs, int lane,
-                                             int vlo, int valid, float scale_log2,
-                                             const uint32_t (&qb)[D / 16][NT][2],
-                                             float (&o)[NT][D / 16][4], float (&m)[NT][2],
-                                             float (&l)[NT][2]) {
+__device__ __forceinline__ void attend_i8(uint32_t kbase, uint32_t vbase, uint32_t kscale,
+                                          uint32_t vscale, const I8Lane& ofs, int lane, int vlo,
+                                          int valid, float scale_log2,
+                                          const uint32_t (&qb)[D / 16][NT][2],
+                                          float (&o)[NT][D / 16][4], float (&m)[NT][2],
+                                          float (&l)[NT][2]) {
   static_assert(D == 128, "one 128-byte code row per token");
   const int g = lane >> 2, c = lane & 3;
   // All shared-memory loads first (the asm statements keep program order),
   // so their latencies overlap.  Row +8 is +1024 bytes with the same
   // swizzle; row 2c+1 is row 2c + 128 bytes with chunk bit 0 flipped.
-  float ks[4], vs[4];
+  float ks[2 * kI8Sub], vs[2 * kI8Sub];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) ks[i] = lds_f32(kscale + ofs.sc[i]);
+  for (int i = 0; i < 2 * kI8Sub; ++i) ks[i] = lds_f32(kscale + ofs.sc[i]);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) vs[i] = lds_f32(vscale + ofs.sc[i]);
+  for (int i = 0; i < 2 * kI8Sub; ++i) vs[i] = lds_f32(vscale + ofs.sc[i]);
   // K: one ldmatrix.x4 per two k-steps gives a lane its codes at dims
   // 16kk + 4c .. 4c+3 of tokens g and g+8 for kk and kk+1.  V: one
   // ldmatrix.x4.trans per two 16-dim chunks gives a lane, per chunk, the codes
   // of tokens 2c, 2c+1 (and 2c+8, 2c+9) at dims 16 ch + 2g, 2g+1.
   // With two query tiles (NT = 2) the V loads wait until the scores are done,
   // to keep the live registers within the two-CTAs-per-SM budget.
-  uint32_t kw[2][D / 16][2], vw[2][D / 16][2];
+  uint32_t kw[kI8Sub][D / 16][2], vw[kI8Sub][D / 16][2];
   auto load_v = [&]() {
 #pragma unroll
-    for (int sub = 0; sub < 2; ++sub)
+    for (int sub = 0; sub < kI8Sub; ++sub)
 #pragma unroll
       for (int ch = 0; ch < D / 16; ch += 2)
         ldsm_x4_t(vbase + ofs.row_ofs + sub * 2048 + ((ch << 4) ^ ofs.xr), vw[sub][ch][0],
                   vw[sub][ch][1], vw[sub][ch + 1][0], vw[sub][ch + 1][1]);
   };
 #pragma unroll
-  for (int sub = 0; sub < 2; ++sub)
+  for (int sub = 0; sub < kI8Sub; ++sub)
 #pragma unroll
     for (int kk = 0; kk < D / 16; kk += 2)
       ldsm_x4(kbase + ofs.row_ofs + sub * 2048 + ((kk << 4) ^ ofs.xr), kw[sub][kk][0],
               kw[sub][kk][1], kw[sub][kk + 1][0], kw[sub][kk + 1][1]);
   if constexpr (NT == 1) load_v();
-  float s[2][NT][4];
+  float s[kI8Sub][NT][4];
 #pragma unroll
-  for (int sub = 0; sub < 2; ++sub)
+  for (int sub = 0; sub < kI8Sub; ++sub)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -463,7 +465,7 @@ __device__ __forceinline__ void attend_32_i8(uint32_t kbase, uint32_t vbase, uin
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk)
 #pragma unroll
-    for (int sub = 0; sub < 2; ++sub) {
+    for (int sub = 0; sub < kI8Sub; ++sub) {
       uint32_t a[4];
       i8x4_to_f16(kw[sub][kk][0], a[0], a[2]);
       i8x4_to_f16(kw[sub][kk][1], a[1], a[3]);
@@ -474,10 +476,10 @@ __device__ __forceinline__ void attend_32_i8(uint32_t kbase, uint32_t vbase, uin
   if constexpr (NT != 1) load_v();
   // s[sub][nt][0, 1]: token 16 sub + g, queries 2c, 2c+1; [2, 3]: token 16 sub
   // + g + 8.  Stale stage contents outside [vlo, valid) never enter arithmetic.
-  bool in[4];
-  float f[4], w[4];
+  bool in[2 * kI8Sub];
+  float f[2 * kI8Sub], w[2 * kI8Sub];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // token 8 i + g of the warp's 32
+  for (int i = 0; i < 2 * kI8Sub; ++i) {  // token 8 i + g of the warp's
     in[i] = 8 * i + g >= vlo && 8 * i + g < valid;
     f[i] = in[i] ? scale_log2 * ks[i] : 0.f;
     w[i] = in[i] ? vs[i] : 0.f;
@@ -487,7 +489,7 @@ __device__ __forceinline__ void attend_32_i8(uint32_t kbase, uint32_t vbase, uin
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-    for (int sub = 0; sub < 2; ++sub) {
+    for (int sub = 0; sub < kI8Sub; ++sub) {
       const int i0 = 2 * sub, i1 = 2 * sub + 1;
       s[sub][nt][0] = in[i0] ? s[sub][nt][0] * f[i0] : -INFINITY;
       s[sub][nt][1] = in[i0] ? s[sub][nt][1] * f[i0] : -INFINITY;
@@ -496,7 +498,10 @@ __device__ __forceinline__ void attend_32_i8(uint32_t kbase, uint32_t vbase, uin
     }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float mx = fmaxf(fmaxf(s[0][nt][e], s[0][nt][e + 2]), fmaxf(s[1][nt][e], s[1][nt][e + 2]));
+      float mx = fmaxf(s[0][nt][e], s[0][nt][e + 2]);
+#pragma unroll
+      for (int sub = 1; sub < kI8Sub; ++sub)
+        mx = fmaxf(mx, fmaxf(s[sub][nt][e], s[sub][nt][e + 2]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -512,12 +517,12 @@ __device__ __forceinline__ void attend_32_i8(uint32_t kbase, uint32_t vbase, uin
   // 2c+9 (the same lanes' second pair).
   const int src_a = 8 * c + (g >> 1), src_b = src_a + 4;
   const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
-  uint32_t pb[2][NT][2];
+  uint32_t pb[kI8Sub][NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-    for (int sub = 0; sub < 2; ++sub) {
+    for (int sub = 0; sub < kI8Sub; ++sub) {
       const float p0 = fast_exp2(s[sub][nt][0] - m[nt][0]);
       const float p1 = fast_exp2(s[sub][nt][1] - m[nt][1]);
       const float p2 = fast_exp2(s[sub][nt][2] - m[nt][0]);
@@ -553,7 +558,7 @@ __device__ __forceinline__ void attend_32_i8(uint32_t kbase, uint32_t vbase, uin
   // 16 ch + 2g, row g+8 dim 16 ch + 2g + 1.
   const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
 #pragma unroll
-  for (int sub = 0; sub < 2; ++sub)
+  for (int sub = 0; sub < kI8Sub; ++sub)
 #pragma unroll
     for (int ch = 0; ch < D / 16; ++ch) {
       const uint32_t x0 = vw[sub][ch][0] ^ 0x80808080u, x1 = vw[sub][ch][1] ^ 0x80808080u;
@@ -973,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
     if (ok && valid > vlo) {
       const uint32_t kb = sbase + stage * L.stage;
       if constexpr (kI8)
-        attend_32_i8<D, kNT>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
+        attend_i8<D, kNT>(kb, kb + kKBytes, kb + L.scales, kb + L.scales + kScaleBytes,
                              i8ofs, lane, vlo, valid, p.scale_log2, qb, o8, m8, l8);
       else
         attend_16<T, D>(kb, kb + kKBytes, warp, lane, vlo, valid, p.scale_log2, kb + L.qoff,
