@@ -68,8 +68,8 @@ constexpr int min_ctas_of() { return kQ == 1 && kI8Sub == 1 ? 3 : 2; }
 constexpr int kMaxBatch = 1024;
 constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a K or V tile
 constexpr int kMaxPieces = 62;           // split shares merged from a shared-memory list
-// INT8 cache: a tile's per-token scales arrive as one TMA box per physical
-// block (min(block_size, 128) floats); each box gets its own slot of
+// INT8 cache: a tile's per-token scales arrive as one TMA box per box of
+// codes (min(block_size, 64) floats); each box gets its own slot of
 // max(128, 4 * box) bytes, so every TMA destination is 128-byte aligned.
 constexpr int kScaleBytes = (tile_of<true>() / 8) * 128;
 
@@ -1090,8 +1090,9 @@ kvc_status run_decode(const DecodeArgs& a) {
   if (a.workspace_bytes < paged_decode_workspace_bytes(G, D, P) || a.workspace == nullptr)
     return KVC_ERR_WORKSPACE;
 
-  constexpr int kT = tile_of<kI8>();
-  const int box_tokens = a.block_size < kT ? a.block_size : kT;
+  // Boxes of at most 64 tokens: a box wholly past a sequence's end is not
+  // fetched, so the tail of its last tile costs less than 64 rows.
+  const int box_tokens = a.block_size < kTile ? a.block_size : kTile;
   const uint64_t elt = kI8 ? 1 : 2;
   const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_kv_heads),
                             static_cast<uint64_t>(a.block_size),
