@@ -316,8 +316,12 @@ kvc_status kvc_reshape_and_cache_int8(const void* key, const void* value, int8_t
  *   (blk = block_table[b][j / block_size], off = j % block_size; V alike)
  *
  * q, out: fp16/bf16 [batch, num_q_heads, 128] (`dtype`); the kernel reads the
- * codes and scales (about half the bytes of a 16-bit cache) and computes in
- * fp32 as kvc_paged_decode does.  head_dim 128 only (KVC_ERR_UNSUPPORTED
+ * codes and scales (about half the bytes of a 16-bit cache).  Its products
+ * run on fp16 tensor-core operands with fp32 accumulation: the codes are
+ * exact in fp16, bf16 queries are converted to fp16 (exact within fp16's
+ * normal range), the scores are scaled in fp32, and the softmax weights
+ * times the value scales are rounded to fp16 for the value product (the row
+ * sums use the unrounded weights).  head_dim 128 only (KVC_ERR_UNSUPPORTED
  * otherwise); every other argument, the workspace (same size query) and the
  * errors are those of kvc_paged_decode.
  */

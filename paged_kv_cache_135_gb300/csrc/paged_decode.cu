@@ -9,7 +9,7 @@
 // describe for paged attention kernels.
 //
 // GB300 design (not on the pages):
-//  * Work unit = a 64-token tile of one (sequence b, kv head g) segment.
+//  * Work unit = a 64-token tile (INT8: 128) of one (sequence b, kv head g) segment.
 //    All tiles of all segments form one linear list ordered (b, g, tile);
 //    each of the P persistent CTAs takes one contiguous 1/P share of it
 //    ("stream-K" split-KV), so every SM streams the same number of bytes
@@ -32,6 +32,11 @@
 //    rounded P so that normalisation matches the weights actually applied.
 //  * Rows of a partial tile past the sequence length are masked in S (-inf)
 //    and zeroed in V, so stale or non-finite cache contents cannot leak.
+//  * Over an INT8 cache (codes + one fp32 scale per row) the same kernel
+//    runs with 128-token tiles of codes and scales, each consumer warp taking
+//    two 16-token sub-tiles under one softmax update, and the products
+//    transposed (S^T = K Q^T, O^T = V^T P^T: the tokens are the M side, the
+//    query group the N side), the codes widened to fp16 exactly in registers.
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -742,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
       prefetch_tmap(&tm_vs);
     }
   }
-  // Plan: clamped lengths and the prefix sum of 64-token tiles per sequence.
+  // Plan: clamped lengths and the prefix sum of kT-token tiles per sequence.
   for (int i = tid; i < B; i += kThreads) lens[i] = clamp_len(p.seq_lens[i], cap, p.err_flag);
   __syncthreads();
   if (warp == 0) {
