@@ -245,3 +245,23 @@ def test_int8_append_equals_write_then_decode(kvc_lib):
     good_blocks = {int(case.block_table[i, (L - 1) // case.block_size]) for i, L in
                    enumerate(lens) if i != b}
     assert set(np.nonzero(changed)[0].tolist()) <= good_blocks
+
+
+@pytest.mark.parametrize("num_ctas", [1, 2, 600])
+def test_int8_tile_edges_and_many_ctas(kvc_lib, num_ctas):
+    """Lengths around the INT8 kernel's 128-token tiles (and its 64-token boxes), with one
+    CTA, two, and more CTAs than tiles (empty shares, every segment split)."""
+    lens = [127, 128, 129, 255, 256, 257, 63, 64, 65, 1]
+    case = decode_case(77, len(lens), lens, 8, 2, 128, 64, dtype="bf16")
+    kq, vq, ks, vs = _quantised_pool(case)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kvc_lib.paged_decode_int8(to_cuda(case.q), to_cuda(torch.from_numpy(kq)),
+                                    to_cuda(torch.from_numpy(vq)), to_cuda(torch.from_numpy(ks)),
+                                    to_cuda(torch.from_numpy(vs)), to_cuda(case.block_table),
+                                    to_cuda(case.seq_lens), case.scale, num_ctas=num_ctas,
+                                    err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = O.paged_decode_int8(case.q.double().numpy(), kq, vq, ks, vs, case.block_table.numpy(),
+                              case.seq_lens.numpy(), case.scale)
+    assert excess(out, ref, "bf16") <= 0
