@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from synth import CONFIGS, make_config  # noqa: E402
+from synth import CONFIGS, decode_case, make_config  # noqa: E402
 
 WORKLOAD = "gqa8b_decode"
 NOMINAL_HBM_GBS = 8000.0
@@ -536,6 +536,44 @@ def measure_decode(kvc, dev, rank, name, steps, warmup):
     return fig
 
 
+def launch_percentiles(ms):
+    """p10, median and p90 of per-launch times (each replay's mean over its launches)."""
+    q = np.percentile(np.asarray(ms, dtype=np.float64), [10, 50, 90])
+    return [float(x) for x in q]
+
+
+def measure_block_sizes(kvc, dev, rank, steps, warmup, sizes=(16, 64, 128)):
+    """The GQA 8B-shape decode step at block sizes 16, 64 and 128: the same lengths (drawn
+    first from the same seed), the same pool of 524,288 token slots, a block table per size."""
+    c = CONFIGS[WORKLOAD]
+    slots = c["num_blocks"] * c["block_size"]
+    max_tokens = c["max_blocks_per_seq"] * c["block_size"]
+    out = {}
+    for bs in sizes:
+        case = decode_case(rank, c["batch"], c["lens"], c["num_q_heads"], c["num_kv_heads"],
+                           c["head_dim"], bs, slots // bs, max_tokens // bs, c["dtype"],
+                           c["scale"], value_device=str(dev))
+        step = DecodeStep(kvc, case, dev)
+        for _ in range(warmup):
+            step.step()
+        torch.cuda.synchronize()
+        graphs = [("step", capture(step.step))]
+        for _ in range(warmup):
+            graphs[0][1].replay()
+        with ClockSampler(dev.index or 0) as clk:
+            _, per = time_graphs(graphs, steps)
+        lens = case.seq_lens.tolist()
+        by = decode_bytes(lens, c["num_q_heads"], c["num_kv_heads"], c["head_dim"], bs) + \
+            write_bytes(len(lens), c["num_kv_heads"], c["head_dim"])
+        hp, hkind = peaks()
+        out[f"block_size_{bs}"] = _roofline("paged_decode_kernel (kvc_paged_decode_append)",
+                                            per["step"], by, "GB/s", hp, hkind, clk.summary(),
+                                            bound="hbm")
+        del step, case, graphs
+        torch.cuda.empty_cache()
+    return out
+
+
 def int8_decode_bytes(seq_lens, Hq, Hkv, D, bs):
     """Algorithmic bytes of one INT8-cache decode: codes and fp32 scales of the K/V rows
     attended, Q and O (16-bit), table entries, lengths."""
@@ -696,6 +734,7 @@ MEASURES = {
     "serving_loop": lambda kvc, dev, rank, steps, warmup: measure_serving_loop(kvc, dev, rank,
                                                                                steps),
     "mla_fused_write": measure_fused_write,
+    "gqa8b_block_size_sweep": measure_block_sizes,
 }
 
 
@@ -715,6 +754,7 @@ def secondary(kvc, dev, rank, steps, warmup):
     torch.cuda.empty_cache()
     out["mla_fused_write"] = measure_fused_write(kvc, dev, rank, steps, warmup)
     torch.cuda.empty_cache()
+    out["gqa8b_block_size_sweep"] = measure_block_sizes(kvc, dev, rank, min(steps, 50), warmup)
     return out
 
 
@@ -938,6 +978,7 @@ def main():
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
                 "algorithmic_bytes_per_launch": step_bytes, "avg_launch_ms": dec_avg_ms,
+                "launch_ms_p10_p50_p90": launch_percentiles(dec_ms),
                 "eager_launch_ms": eager_ms,
                 "frac_of_nominal_8tbps": achieved / NOMINAL_HBM_GBS,
             },

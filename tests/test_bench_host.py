@@ -79,3 +79,8 @@ def test_int8_write_bytes_counts_rows_codes_scales_slots():
     # 16-bit rows read (K and V), int8 codes + one fp32 scale per row written, slots written
     want = 2 * B * Hkv * D * 2 + 2 * B * Hkv * D + 2 * B * Hkv * 4 + 4 * B
     assert bench.int8_write_bytes(B, Hkv, D) == want
+
+
+def test_launch_percentiles_order_and_values():
+    p10, p50, p90 = bench.launch_percentiles([0.1, 0.2, 0.3, 0.4, 0.5])
+    assert p10 <= p50 <= p90 and abs(p50 - 0.3) < 1e-12
