@@ -322,15 +322,22 @@ def cpu_oracle_rate_all_cores(case, budget_s=10.0):
 
 
 def cpu_baseline(case):
-    """The oracle timed on this host: all cores (the reported value) and one core."""
+    """The oracle timed on this host: all cores (the reported value) and one core, plus one
+    core on the tiny and Llama-7B-shape decode workloads (a bounded sample of each)."""
     gbs1, n1, B, t1 = cpu_oracle_rate(case)
     gbs, n, workers, t = cpu_oracle_rate_all_cores(case)
+    others = {}
+    for name, budget in (("tiny_decode", 1.0), ("llama7b_mha_decode", 4.0)):
+        g, k, _, tt = cpu_oracle_rate(make_config(name, seed=0), budget_s=budget)
+        others[name] = {"value": g, "unit": "GB/s", "cores": 1,
+                        "sample": f"{k} sequence evaluations, {tt:.1f} s"}
     return {"value": gbs, "unit": "GB/s", "cores": workers, "kind": "oracle",
             "sample": f"{n} sequence evaluations ({n // B} passes over the {B} sequences) "
                       f"spread over {workers} spawned single-threaded worker processes, fp64 "
                       f"NumPy oracle, {t:.1f} s wall",
             "single_core": {"value": gbs1, "unit": "GB/s", "cores": 1,
                             "sample": f"{n1} sequence evaluations, {t1:.1f} s"},
+            "single_core_other_workloads": others,
             "cpu_count": os.cpu_count(), "cpu_model": cpu_model(), "blas_threads_per_worker": 1}
 
 
