@@ -263,7 +263,6 @@ size_t kvc_paged_decode_workspace_size(int num_q_heads, int num_kv_heads, int he
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
   const int group = num_q_heads / num_kv_heads;
   if (group > 16 || (head_dim != 64 && head_dim != 128)) return 0;
-  // Enough for either dtype: the automatic CTA count may differ between them.
   // Enough for every variant (dtype, 16-bit or INT8 cache): the automatic
   // CTA count may differ between them.
   int ctas = 0;
