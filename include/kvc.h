@@ -209,9 +209,9 @@ kvc_status kvc_rmsnorm_rope_cache(const void* kv, const void* gamma, float eps,
  * Bytes of workspace kvc_paged_decode needs for this head shape when it runs
  * with `num_ctas` persistent CTAs (0 = the automatic choice for the current
  * device: SM count x resident CTAs per SM).  Independent of batch and lengths.
- * The same size serves every decode entry point of this shape (the band,
- * appending, INT8 and no-alloc calls): with num_ctas 0 it is the largest of
- * their automatic choices.
+ * The same size serves the band, appending and INT8 decode calls of this
+ * shape (with num_ctas 0 it covers the largest of their automatic choices);
+ * kvc_paged_decode_no_alloc checks its own scratch against it.
  */
 size_t kvc_paged_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
                                        int num_ctas);
