@@ -58,12 +58,15 @@ struct Cursor {
 
 // Clamped lengths and the exclusive prefix sum of ceil(len / tile) for B
 // sequences, computed by the calling warp into shared memory (cum[B] = total).
+// With extra > 0 every sequence with at least one tile counts extra more
+// units (work-split weights that stand for a sequence's fixed costs).
 __device__ __forceinline__ void plan_tiles(const int* lens, int* cum, int B, int tile,
-                                           int lane) {
+                                           int lane, int extra = 0) {
   int carry = 0;
   for (int base = 0; base < B; base += 32) {
     const int i = base + lane;
-    const int n = i < B ? (lens[i] + tile - 1) / tile : 0;
+    const int t = i < B ? (lens[i] + tile - 1) / tile : 0;
+    const int n = t > 0 ? t + extra : 0;
     int x = n;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
