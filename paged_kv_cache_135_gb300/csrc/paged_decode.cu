@@ -71,6 +71,18 @@ constexpr int stages_of() { return kI8 && kI8Sub == 2 ? 2 : 3; }
 template <int kQ>
 constexpr int min_ctas_of() { return kQ == 1 && kI8Sub == 1 ? 3 : 2; }
 constexpr int kMaxBatch = 1024;
+// Work split: each (sequence, kv head) segment counts seg_units_of<kI8>()
+// units of work beyond its tiles, for its end-of-segment finish (combine,
+// partial state, arrival, merge), so that CTAs whose shares end more
+// segments get fewer tiles.  The units are virtual: no role visits them.
+// Measured: over an INT8 cache, whose 128-token tiles carry the same finish
+// cost per segment as 64-token 16-bit ones, 1 unit is 5 % faster than none
+// (2 is between); over a 16-bit cache 3 units gained 0.2-0.5 % on the GQA
+// 8B shape but cost 2.5 % on the MHA shape's many short segments, so none.
+constexpr int kSegUnits16 = 0;  // 16-bit cache
+constexpr int kSegUnitsI8 = 1;  // INT8 cache
+template <bool kI8>
+constexpr int seg_units_of() { return kI8 ? kSegUnitsI8 : kSegUnits16; }
 constexpr int kHalfBytes = kTile * 128;  // one 64-element half of a K or V tile
 constexpr int kMaxPieces = 62;           // split shares merged from a shared-memory list
 // INT8 cache: a tile's per-token scales arrive as one TMA box per box of
@@ -129,7 +141,8 @@ struct Layout {
   int flags;    // abort, last, npieces
   int pieces;   // int[kMaxPieces]
   int lens;     // int[batch]
-  int cum;      // int[batch + 1]
+  int cum;      // int[batch + 1]: tiles per kv head before each sequence
+  int ucum;     // int[batch + 1]: work units (tiles + seg_units_of) per kv head before it
   int cmb;      // cross-warp combine: m[4G], l[4G], o[4G][D]
   int total;    // bytes to request (with 1024 bytes of alignment slack)
   __host__ __device__ Layout(int batch, int group) {
@@ -142,7 +155,8 @@ struct Layout {
     pieces = align_up(flags + 12, 16);
     lens = align_up(pieces + kMaxPieces * 4, 16);
     cum = align_up(lens + batch * 4, 16);
-    cmb = align_up(cum + (batch + 1) * 4, 16);
+    ucum = align_up(cum + (batch + 1) * 4, 16);
+    cmb = align_up(ucum + (batch + 1) * 4, 16);
     total = 1024 + cmb + kConsumerWarps * group * (D + 2) * 4;
   }
 };
@@ -172,17 +186,21 @@ __device__ __forceinline__ long long tile_begin(int c, long long N, int P) {
 // Walks the linear tile list (b, g, j) in order.
 struct Cursor {
   int b, g, j, n;
-  __device__ __forceinline__ void locate(long long t, const int* cum, int batch, int hkv) {
-    int lo = 0, hi = batch - 1;  // largest b with hkv*cum[b] <= t
+  // The first tile at or after work unit t (units: ucum, seg_units virtual
+  // units before each segment's tiles; tiles: cum).
+  __device__ __forceinline__ void locate(long long t, const int* cum, const int* ucum, int batch,
+                                         int hkv, int seg_units) {
+    int lo = 0, hi = batch - 1;  // largest b with hkv*ucum[b] <= t
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (static_cast<long long>(hkv) * cum[mid] <= t) lo = mid; else hi = mid - 1;
+      if (static_cast<long long>(hkv) * ucum[mid] <= t) lo = mid; else hi = mid - 1;
     }
     b = lo;
     n = cum[b + 1] - cum[b];
-    const long long r = t - static_cast<long long>(hkv) * cum[b];
-    g = static_cast<int>(r / n);
-    j = static_cast<int>(r - static_cast<long long>(g) * n);
+    const long long r = t - static_cast<long long>(hkv) * ucum[b];
+    g = static_cast<int>(r / (n + seg_units));
+    const int jj = static_cast<int>(r - static_cast<long long>(g) * (n + seg_units)) - seg_units;
+    j = jj > 0 ? jj : 0;
   }
   __device__ __forceinline__ void advance(const int* cum, int batch, int hkv) {
     if (++j < n) return;
@@ -594,7 +612,7 @@ __device__ __noinline__ void finish_share(const DecodeParams& p, const float* cm
                                           volatile int* last_flag, volatile int* npieces,
                                           int* pieces, int ctid, int b, int g,
                                           bool complete, int c, int slot, long long seg0,
-                                          int seg_tiles, long long N, int P) {
+                                          int seg_tiles, int seg_units, long long N, int P) {
   constexpr int kQuads = D / 4;
   const int G = p.group;
   T* out = static_cast<T*>(p.out);
@@ -629,8 +647,11 @@ __device__ __noinline__ void finish_share(const DecodeParams& p, const float* cm
   // arrives last merges all shares in ascending CTA order and resets the
   // counter -- no second kernel and no waiting.
   named_bar_sync(1, kConsumerWarps * 32);
+  // seg0: the work unit of the segment's first tile (seg_units virtual units
+  // precede it).  The segment is the first one of CTA cfirst's share iff that
+  // share starts within the segment's units.
   const int cfirst = cta_of(seg0, N, P), clast = cta_of(seg0 + seg_tiles - 1, N, P);
-  const int slot0 = tile_begin(cfirst, N, P) == seg0 ? 0 : 1;
+  const int slot0 = tile_begin(cfirst, N, P) >= seg0 - seg_units ? 0 : 1;
   if (ctid == 0) {
     // Workspace rows (cta * 2 + slot) of every non-empty share, in CTA order.
     int n = 0;
@@ -709,6 +730,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
   constexpr bool kI8 = kQ > 0;
   constexpr int kNT = kI8 ? kQ : 1;
   constexpr int kT = tile_of<kI8>();  // tokens per stage
+  constexpr int kSegUnits = seg_units_of<kI8>();
   constexpr int kHalves = Layout<D, kI8>::kHalves;
   constexpr int kKBytes = Layout<D, kI8>::kKBytes;
   constexpr int kStages = Layout<D, kI8>::kStages;
@@ -722,6 +744,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
   volatile int* last_flag = abort_flag + 1;
   int* lens = reinterpret_cast<int*>(smem + L.lens);
   int* cum = reinterpret_cast<int*>(smem + L.cum);
+  int* ucum = reinterpret_cast<int*>(smem + L.ucum);
   float* cmb_m = reinterpret_cast<float*>(smem + L.cmb);
   float* cmb_l = cmb_m + kConsumerWarps * p.group;
   float* cmb_o = cmb_l + kConsumerWarps * p.group;
@@ -751,24 +774,27 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
   for (int i = tid; i < B; i += kThreads) lens[i] = clamp_len(p.seq_lens[i], cap, p.err_flag);
   __syncthreads();
   if (warp == 0) {
-    int carry = 0;
+    int carry = 0, ucarry = 0;
     for (int base = 0; base < B; base += 32) {
       const int i = base + lane;
       const int n = i < B ? (lens[i] + kT - 1) / kT - first_tile<kT>(lens[i], p.window) : 0;
-      int x = n;
+      const int u = n > 0 ? n + kSegUnits : 0;
+      int x = n, y = u;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off) x += y;
+        const int xs = __shfl_up_sync(0xffffffffu, x, off);
+        const int ys = __shfl_up_sync(0xffffffffu, y, off);
+        if (lane >= off) { x += xs; y += ys; }
       }
-      if (i < B) cum[i] = carry + x - n;
+      if (i < B) { cum[i] = carry + x - n; ucum[i] = ucarry + y - u; }
       carry += __shfl_sync(0xffffffffu, x, 31);
+      ucarry += __shfl_sync(0xffffffffu, y, 31);
     }
-    if (lane == 0) cum[B] = carry;
+    if (lane == 0) { cum[B] = carry; ucum[B] = ucarry; }
   }
   __syncthreads();
 
-  const long long N = static_cast<long long>(hkv) * cum[B];
+  const long long N = static_cast<long long>(hkv) * ucum[B];  // work units
   const int P = gridDim.x, c = blockIdx.x;
   // Sequences with no cached token get a row of zeros (CTA b % P writes them)
   // and, when appending, no slot (-1): there is no new token to write.
@@ -782,13 +808,29 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
         if (tid == 0 && p.slot_out) p.slot_out[b] = -1;
       }
   }
+  // This CTA's share: units [t_begin, t_end), n_real tiles of them.
   const long long t_begin = tile_begin(c, N, P), t_end = tile_begin(c + 1, N, P);
-  if (t_begin >= t_end) return;
+  auto tiles_before = [&](long long x) -> long long {
+    if (x >= N) return static_cast<long long>(hkv) * cum[B];
+    int lo = 0, hi = B - 1;  // largest b with hkv*ucum[b] <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<long long>(hkv) * ucum[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int nb = cum[lo + 1] - cum[lo];
+    const long long r = x - static_cast<long long>(hkv) * ucum[lo];
+    const long long g = r / (nb + kSegUnits);
+    const long long jj = r - g * (nb + kSegUnits) - kSegUnits;
+    return static_cast<long long>(hkv) * cum[lo] + g * nb + (jj < 0 ? 0 : (jj > nb ? nb : jj));
+  };
+  const int n_real = t_begin < t_end ? static_cast<int>(tiles_before(t_end) - tiles_before(t_begin))
+                                     : 0;
+  if (n_real <= 0) return;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     Cursor cur;
-    cur.locate(t_begin, cum, B, hkv);
+    cur.locate(t_begin, cum, ucum, B, hkv, kSegUnits);
     const int nsub = kT / p.box_tokens;
     // Bytes of one box: a 64-element half of box_tokens 16-bit rows, or
     // box_tokens whole 128-byte code rows.
@@ -811,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
       new_ready = true;
     };
     int it = 0;
-    for (long long t = t_begin; t < t_end; ++t, ++it) {
+    for (; it < n_real; ++it) {
       const int stage = it % kStages;
       const uint32_t phase = (it / kStages) & 1;
       // Look up this tile's physical blocks first: the table load's latency
@@ -928,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
 
   // -------------------------------------------------------------- consumers
   Cursor cur;
-  cur.locate(t_begin, cum, B, hkv);
+  cur.locate(t_begin, cum, ucum, B, hkv, kSegUnits);
   const int ctid = warp * 32 + lane;
   // 16-bit cache: o, m, l of query rows g, g+8 (mma M side).  INT8 cache:
   // o8, m8, l8 of query rows 8nt + 2c, 2c+1 (N side), qb the query fragments.
@@ -962,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
   int slot = 0;  // 0 for the first segment this CTA touches, 1 afterwards
   const uint32_t sbase = smem_u32(smem);
   int it = 0;
-  for (long long t = t_begin; t < t_end; ++t, ++it) {
+  for (; it < n_real; ++it) {
     const int stage = it % kStages;
     const uint32_t phase = (it / kStages) & 1;
     bool ok = !*abort_flag && mbar_wait_bounded(&full[stage], phase, p.err_flag);
@@ -993,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
     if (lane == 0) mbar_arrive(&empty[stage]);
 
     const bool last_of_seg = cur.j == cur.n - 1;
-    if (last_of_seg || t == t_end - 1) {
+    if (last_of_seg || it == n_real - 1) {
       // ---- finalize this segment's share: merge the 4 warps' states.
       const bool complete = seg_first_j == 0 && last_of_seg;
       if constexpr (kI8) {
@@ -1045,9 +1087,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_of<kQ>())
       finish_share<T, D>(p, cmb_m, cmb_l, cmb_o, last_flag, abort_flag + 2,
                          reinterpret_cast<int*>(smem + L.pieces), ctid, cur.b, cur.g,
                          complete, c, slot,
-                         static_cast<long long>(hkv) * cum[cur.b] +
-                             static_cast<long long>(cur.g) * cur.n,
-                         cur.n, N, P);
+                         static_cast<long long>(hkv) * ucum[cur.b] +
+                             static_cast<long long>(cur.g) * (cur.n + kSegUnits) + kSegUnits,
+                         cur.n, kSegUnits, N, P);
       named_bar_sync(1, kConsumerWarps * 32);
       slot = 1;
       cur.advance(cum, B, hkv);
