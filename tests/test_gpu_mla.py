@@ -67,6 +67,24 @@ def test_mla_many_splits(kvc_lib):
         assert e <= 0, (ctas, e)
 
 
+def test_mla_many_short_sequences_and_shares_without_tiles(kvc_lib):
+    """Forty short sequences (0 to 150 tokens) over up to 300 CTA pairs: the work split
+    counts a few virtual units per sequence, so some shares hold no tile at all and many
+    sequences are split into one-tile pieces."""
+    g = torch.Generator().manual_seed(5)
+    lens = torch.randint(0, 151, (40,), generator=g).tolist()
+    lens[3] = 0
+    lens[4] = 1
+    c = mla_case(47, len(lens), lens, block_size=16, dtype="bf16")
+    ref = oracle_mla(c)
+    for ctas in (2, 20, 152, 600):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        _, out = gpu_mla(kvc_lib, c, ctas, err)
+        assert int(err.item()) == 0, ctas
+        e = excess(out, ref, "bf16")
+        assert e <= 0, (ctas, e)
+
+
 def test_mla_workspace_needs_no_zeroing(kvc_lib):
     """A workspace full of NaN bit patterns gives the same output as the oracle, twice in a row."""
     c = mla_case(43, 4, [900, 33, 2048, 5], block_size=32, dtype="bf16")
