@@ -430,6 +430,11 @@ kvc_status kvc_paged_decode_append(const void* q, const void* new_key, const voi
  * Supported: head_dim 64 or 128; block_size a power of two >= 8.  A sequence
  * whose context_lens + length exceeds max_blocks_per_seq * block_size gets
  * no output and sets KVC_FLAG_LEN_RANGE.
+ * With context_lens NULL and an even group size the two steps run in one
+ * launch: the attention takes K_s/V_s straight from key/value (the rows step 1
+ * copies into the cache, since slot_mapping is the packed form over
+ * block_table) while the same kernel writes them at slot_mapping; the cache
+ * and the output are those of the two steps in sequence.
  */
 kvc_status kvc_varlen_prefill_paged(const void* q, const void* key, const void* value,
                                     const int32_t* cu_seqlens, const int32_t* context_lens,

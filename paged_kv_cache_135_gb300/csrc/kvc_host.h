@@ -139,6 +139,10 @@ kvc_status launch_varlen_prefill(const PrefillArgs& a);
 kvc_status launch_prefill_attention_tc(const PrefillArgs& a);
 // Two query heads per CTA; requires an even GQA group size.
 kvc_status launch_prefill_attention_tc2(const PrefillArgs& a);
+// The cache write and the attention in one launch, for chunks without cached
+// context (context_lens null): K/V tiles come from the packed input and a
+// writer warp stores the chunk's rows at slot_mapping; even GQA group size.
+kvc_status launch_prefill_fused_tc2(const PrefillArgs& a);
 
 struct MlaArgs {
   const void* q_nope;

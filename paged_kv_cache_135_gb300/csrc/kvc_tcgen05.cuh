@@ -235,6 +235,25 @@ __device__ __forceinline__ uint32_t pack_pair<__half>(float a, float b) {
   __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// acc += the two values of a pair packed by pack_pair (low half into acc.x),
+// each widened exactly and added in fp32 with round-to-nearest (the
+// mixed-precision add of sm_100 and later, one instruction per value).
+template <typename T>
+__device__ __forceinline__ void acc_pair(float2& acc, uint32_t w);
+template <>
+__device__ __forceinline__ void acc_pair<__nv_bfloat16>(float2& acc, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w));
+}
+template <>
+__device__ __forceinline__ void acc_pair<__half>(float2& acc, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w));
+}
 
 // --------------------------------------------------------------- cluster
 

@@ -31,6 +31,14 @@
 // log2 domain; O is rescaled only when a row's max grows by more than 2^8.
 // The epilogue passes each warp's output rows through shared memory so that
 // every store instruction writes whole 64-byte row segments.
+//
+// Fused write (chunks without cached context): the K/V tiles are read from
+// the packed key/value input itself -- the write copies those rows unchanged
+// into the cache, so they are the rows the cache would hold -- and an extra
+// writer warp in every CTA copies its share of the chunk's rows to the cache
+// at slot_mapping, beside the attention and independent of it.  The write
+// then runs under the compute-bound attention instead of as a launch before
+// it.
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -49,8 +57,11 @@ constexpr int kBM = 128;                    // query rows per head = MMA M
 constexpr int kBN = 128;                    // kv tokens per tile
 constexpr int kHeadThreads = 128;           // softmax threads per head
 constexpr int kSmxThreads = 2 * kHeadThreads;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kWriterWarp = 10;
 constexpr int kThreads = kSmxThreads + 64;
+// Threads of a kernel instance: the fused-write instance adds the writer warp.
+template <bool kFused>
+constexpr int threads_of() { return kFused ? kThreads + 32 : kThreads; }
 constexpr int kStages = 2;
 constexpr int kChunk = 128 * 128;           // one [128 rows][64 elements] swizzled region
 constexpr float kRescaleThreshold = 8.0f;
@@ -76,6 +87,14 @@ struct Tc2Params {
   int block_size, log2_bs, max_blocks, num_blocks, box_tokens;
   int window;  // band: a query at position p sees p - window + 1 .. p (0: all of 0 .. p)
   float scale_log2;
+  // Fused write only: the rows to store and where.
+  const uint8_t* key;
+  const uint8_t* value;
+  uint8_t* key_cache;
+  uint8_t* value_cache;
+  const int32_t* slot_mapping;
+  int num_tokens, num_kv_heads;
+  long long num_slots;
 };
 
 // First key position of the band of a query at position `pos` (0 without a band).
@@ -99,7 +118,7 @@ struct Tc2Layout {
   static constexpr int kV = kK + kStages * kStageBytes;
   static constexpr int kBar = kV + kStages * kStageBytes;
   static constexpr int kNumBars = 19;
-  static constexpr int kMisc = kBar + kNumBars * 8;            // tmem slot, abort, schedule ints
+  static constexpr int kMisc = kBar + kNumBars * 8;  // tmem slot, abort, schedule ints, progress
   static constexpr int kHist = kMisc + 64;                     // int[kMaxN]
   static constexpr int kList = kHist + kMaxN * 4;              // int2[kMaxSched]
   static constexpr int kStg = (kList + kMaxSched * 8 + 15) & ~15;  // epilogue staging, per warp
@@ -158,14 +177,16 @@ __device__ __forceinline__ bool tc2_locate(const Tc2Params& p, int item, int lan
 }
 
 // TMA producer (one warp): both heads' query tiles once, then each 128-token
-// K and V tile, one box per physical block per 64-wide chunk.
-template <int D>
+// K and V tile, one box per physical block per 64-wide chunk (fused write:
+// one box of the packed input per 64-wide chunk; tokens past the sequence
+// are masked, and zeroed in V, like cache rows past it).
+template <int D, bool kFused>
 __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint8_t* smem, uint64_t* bars,
                                              volatile int* abort_flag, int s, int h0, int g,
-                                             int tok0, int kv_len, int j0, int n_tiles,
-                                             int band0, int gj0, int kit, int lane) {
+                                             int tok0, int seq_tok0, int kv_len, int j0,
+                                             int n_tiles, int band0, int gj0, int kit, int lane) {
   using L = Tc2Layout<D>;
   // This item's query tiles replace the previous item's once its last S is
   // done (q_empty).
@@ -198,20 +219,37 @@ __device__ __forceinline__ void tc2_producer(const Tc2Params& p, const CUtensorM
     }
     const int in_blk = tok & (p.block_size - 1);
     // K(j) once both heads' S(j-2) have consumed its stage, V(j) once both
-    // heads' P V(j-2) have.
-    for (int part = 0; part < 2; ++part) {
-      const int empty = part ? kVEmpty0 : kKEmpty0, full = part ? kVFull0 : kKFull0;
-      const bool ok = wait_t2(&bars[empty + stage], ((gj >> 1) & 1) ^ 1, abort_flag, p.err_flag);
-      const bool go = valid && ok;
-      const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, go));
-      if (lane == 0) mbar_arrive_expect_tx(&bars[full + stage], nvalid * box_bytes * L::kHalves);
-      __syncwarp();
-      if (go) {
-        uint8_t* dst = smem + (part ? L::kV : L::kK) + stage * L::kStageBytes + lane * box_bytes;
+    // heads' P V(j-2) have (fused write: and the writer is done with it).
+    if constexpr (kFused) {
+      for (int part = 0; part < 2; ++part) {
+        const int empty = part ? kVEmpty0 : kKEmpty0, full = part ? kVFull0 : kKFull0;
+        const bool ok = wait_t2(&bars[empty + stage], ((gj >> 1) & 1) ^ 1, abort_flag, p.err_flag);
+        if (__any_sync(0xffffffffu, !ok)) return;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[full + stage], L::kStageBytes);
+          uint8_t* dst = smem + (part ? L::kV : L::kK) + stage * L::kStageBytes;
 #pragma unroll
-        for (int c = 0; c < L::kHalves; ++c)
-          tma_load_4d(dst + c * kChunk, part ? tm_v : tm_k, &bars[full + stage], c * 64, g, in_blk,
-                      pb);
+          for (int c = 0; c < L::kHalves; ++c)
+            tma_load_3d(dst + c * kChunk, part ? tm_v : tm_k, &bars[full + stage], c * 64, g,
+                        seq_tok0 + (j0 + j) * kBN);
+        }
+        __syncwarp();
+      }
+    } else {
+      for (int part = 0; part < 2; ++part) {
+        const int empty = part ? kVEmpty0 : kKEmpty0, full = part ? kVFull0 : kKFull0;
+        const bool ok = wait_t2(&bars[empty + stage], ((gj >> 1) & 1) ^ 1, abort_flag, p.err_flag);
+        const bool go = valid && ok;
+        const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, go));
+        if (lane == 0) mbar_arrive_expect_tx(&bars[full + stage], nvalid * box_bytes * L::kHalves);
+        __syncwarp();
+        if (go) {
+          uint8_t* dst = smem + (part ? L::kV : L::kK) + stage * L::kStageBytes + lane * box_bytes;
+#pragma unroll
+          for (int c = 0; c < L::kHalves; ++c)
+            tma_load_4d(dst + c * kChunk, part ? tm_v : tm_k, &bars[full + stage], c * 64, g,
+                        in_blk, pb);
+        }
       }
     }
   }
@@ -423,9 +461,11 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
       fence_proxy_async_smem();
     }
     // p = 2^(s * scale_log2 - m_used); a row with nothing visible yet keeps
-    // m_used = -inf and all its scores at -inf, so its p are 0.  The row sum
-    // l adds the exponentials before rounding (P itself is rounded to T for
-    // the tensor core).  P goes to the first 64 columns of the head's S (two
+    // m_used = -inf and all its scores at -inf, so its p are 0.  P is rounded
+    // to T for the tensor core, and the row sum l adds the rounded values, so
+    // the output is a convex combination of V rows with exactly the weights
+    // P V used (a peaked row then keeps its dominant row almost exactly,
+    // whatever that row's magnitude).  P goes to the first 64 columns of the head's S (two
     // 16-bit tokens per column, token 2c in the low half of column c) in two
     // halves: tokens 0-63 (already in registers) are released (p_half) before
     // tokens 64-127 are read again and computed, so the first half of P V
@@ -455,7 +495,7 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
         const float2 y = fma2(make_float2(s[2 * k], s[2 * k + 1]), sc2, nm2);
         const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
         pk[k] = pack_pair<T>(e.x, e.y);
-        ps2[k & 1] = add2(ps2[k & 1], e);
+        acc_pair<T>(ps2[k & 1], pk[k]);
       }
 #pragma unroll
       for (int c = 0; c < kBN / 64; ++c)
@@ -507,6 +547,73 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
     __syncwarp();
   }
   tc_fence_before();
+}
+
+// Fused write.  The writer warp of each CTA walks the CTA's own items and,
+// for each item of the first head pair of a KV head g, copies the item's
+// query-tile rows -- packed tokens tok .. tok + rows - 1, head g, the rows of
+// its diagonal K/V tile -- from key/value to the cache row of slot
+// slot_mapping[t]: a negative slot is skipped, one outside the pool is
+// skipped and flagged, as in kvc_reshape_and_cache.  Every packed token of a
+// sequence lies in exactly one query tile, so each (token, head) row is
+// copied once.  The copies run beside the attention, which reads the same
+// rows from the input at about the same time (they meet in L2), and touch no
+// ring stage or barrier: a writer that held a stage until it had read the
+// rows out of shared memory stalled the K/V ring.  One warp is
+// latency-bound, so each lane keeps kBatch K and V loads in flight; the
+// item's slots are staged in shared memory (the schedule histogram's space,
+// unused after the prologue).
+// The writer paces itself by the producer's progress: kWriteBatch loads in
+// flight while it is less than two items ahead of the producer, kWriteBatchAhead
+// once it is further ahead -- fewer loads in flight take less from the
+// attention (measured: 2 in flight 406 us, 8 in flight 418 us on 16 prompts
+// of 50-3000 tokens, whose long items leave the writer ahead), while short
+// items need the higher rate to keep up (96 prompts of 64-512 tokens: 2 in
+// flight 312 us, 8 in flight 194 us).
+constexpr int kWriteBatch = 8, kWriteBatchAhead = 2;
+template <int D, int kBatch>
+__device__ __forceinline__ void tc2_write_rows(const Tc2Params& p, int* slots, int tok, int rows,
+                                               int g, int lane) {
+  rows = min(rows, p.num_tokens - tok);
+#pragma unroll
+  for (int i = 0; i < kBM / 32; ++i) {
+    const int r = lane + 32 * i;
+    slots[r] = r < rows ? __ldg(&p.slot_mapping[tok + r]) : -1;
+  }
+  __syncwarp();
+  constexpr int kCR = D / 8, kRPI = 32 / kCR;  // lanes per row, rows per warp access
+  const int k = lane % kCR, rsub = lane / kCR;
+  const long long rb = static_cast<long long>(p.num_kv_heads) * D * 2;
+  const long long off = static_cast<long long>(g) * D * 2 + k * 16;
+  bool outside = false;  // a slot outside the pool (flagged once, after the loop)
+#pragma unroll 1
+  for (int r0 = 0; r0 < rows; r0 += kBatch * kRPI) {
+    uint4 kv[kBatch], vv[kBatch];
+    int sl[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int r = r0 + u * kRPI + rsub;
+      sl[u] = r < rows ? slots[r] : -1;
+      if (r < rows) {
+        kv[u] = __ldg(reinterpret_cast<const uint4*>(p.key + (tok + r) * rb + off));
+        vv[u] = __ldg(reinterpret_cast<const uint4*>(p.value + (tok + r) * rb + off));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (sl[u] < 0) continue;
+      if (sl[u] >= p.num_slots) {
+        outside = true;
+        continue;
+      }
+      __stcs(reinterpret_cast<uint4*>(p.key_cache + sl[u] * rb + off), kv[u]);
+      __stcs(reinterpret_cast<uint4*>(p.value_cache + sl[u] * rb + off), vv[u]);
+    }
+  }
+  // The flag is set outside the copy loop: an atomic in the loop measured
+  // 5 % slower for the whole kernel.
+  if (outside) set_flag(p.err_flag, KVC_FLAG_SLOT_RANGE);
+  __syncwarp();
 }
 
 // One work item: (sequence, 128-query tile, pair of query heads); every
@@ -590,14 +697,15 @@ __device__ int tc2_build_schedule(const Tc2Params& p, uint8_t* smem, int tid, in
   int2* list = reinterpret_cast<int2*>(smem + L::kList);
   volatile int* misc = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);  // qtot, bad, nsched
   const int pairs = p.num_q_heads / 2;
-  for (int i = tid; i < kMaxN; i += kThreads) hist[i] = 0;
+  const int nthr = blockDim.x;
+  for (int i = tid; i < kMaxN; i += nthr) hist[i] = 0;
   if (tid == 0) {
     misc[0] = 0;
     // The closed forms below assume causal weights; a band walks unsorted.
     misc[1] = pairs > 255 || kBand ? 1 : 0;
   }
   __syncthreads();
-  for (int s = tid; s < p.num_seqs; s += kThreads) {
+  for (int s = tid; s < p.num_seqs; s += nthr) {
     const int len = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
     const int ctx = p.context_lens ? p.context_lens[s] : 0;
     const int nq = len > 0 ? (len + kBM - 1) / kBM : 0;
@@ -686,9 +794,10 @@ __device__ int tc2_build_schedule(const Tc2Params& p, uint8_t* smem, int tid, in
 // the CTA's running tile count (gj0) and item count (ni), so the next item's
 // queries, K/V tiles and first S are loaded and computed while the softmax
 // warps finish the previous item's epilogue.  An item whose sequence does not
-// fit the block table is skipped (KVC_FLAG_LEN_RANGE, nothing written).
-template <typename T, int D, bool kBf16, bool kBand>
-__global__ void __launch_bounds__(kThreads, 1)
+// fit the block table is skipped (KVC_FLAG_LEN_RANGE, no output; the fused
+// write still copies its rows, as the separate write does).
+template <typename T, int D, bool kBf16, bool kBand, bool kFused>
+__global__ void __launch_bounds__(threads_of<kFused>(), 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -700,6 +809,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  // The item the producer works on (fused write: paces the writer).
+  volatile int* progress = reinterpret_cast<volatile int*>(smem + L::kMisc + 32);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
 
@@ -710,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[i], cnt);
     }
     *abort_flag = 0;
+    *progress = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(tslot, kTmemCols);
@@ -753,13 +865,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0;; ++k) {
       Tc2Item it;
       if (!next_item(k, it)) break;
+      if (kFused && lane == 0) *progress = k;
       if (!it.ok) {
         if (lane == 0) set_flag(p.err_flag, KVC_FLAG_LEN_RANGE);
         continue;
       }
-      tc2_producer<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, it.s, it.h0,
-                      it.h0 / p.group, it.tok0, it.kv_len, it.j0, it.n_tiles,
-                      band_start(it.ctx + it.q0, window_of<kBand>(p)), gj0, ni, lane);
+      tc2_producer<D, kFused>(p, &tm_q, &tm_k, &tm_v, smem, bars, abort_flag, it.s, it.h0,
+                              it.h0 / p.group, it.tok0, it.tok0 - it.q0, it.kv_len, it.j0,
+                              it.n_tiles, band_start(it.ctx + it.q0, window_of<kBand>(p)), gj0,
+                              ni, lane);
       gj0 += it.n_tiles;
       ++ni;
       if (*abort_flag) break;
@@ -769,7 +883,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(&bars[kKFull0 + (gj & 1)], (gj >> 1) & 1, p.err_flag);
       mbar_wait_bounded(&bars[kVFull0 + (gj & 1)], (gj >> 1) & 1, p.err_flag);
     }
-  } else {
+  } else if (kFused && warp == kWriterWarp) {
+    int* slots = reinterpret_cast<int*>(smem + L::kHist);
+    for (int k = 0;; ++k) {
+      Tc2Item it;
+      if (!next_item(k, it)) break;
+      if (it.h0 % p.group != 0) continue;
+      if (k > *progress + 1)
+        tc2_write_rows<D, kWriteBatchAhead>(p, slots, it.tok0, it.q_rows, it.h0 / p.group, lane);
+      else
+        tc2_write_rows<D, kWriteBatch>(p, slots, it.tok0, it.q_rows, it.h0 / p.group, lane);
+    }
+    // Tokens after the last sequence belong to no item: every head of them,
+    // 128 tokens per CTA in turn.
+    for (int t = p.cu_seqlens[p.num_seqs] + c * kBM; t < p.num_tokens; t += G * kBM)
+      for (int g = 0; g < p.num_kv_heads; ++g)
+        tc2_write_rows<D, kWriteBatch>(p, slots, t, kBM, g, lane);
+  } else if (warp == kMmaWarp) {
     const uint32_t leader = elect_one_sync();
     for (int k = 0;; ++k) {
       Tc2Item it;
@@ -794,11 +924,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int D, bool kBf16, bool kBand>
+template <typename T, int D, bool kBf16, bool kBand, bool kFused>
 kvc_status run_prefill_tc2(const PrefillArgs& a) {
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(prefill_tc2_kernel<T, D, kBf16, kBand>,
+    cudaFuncSetAttribute(prefill_tc2_kernel<T, D, kBf16, kBand, kFused>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Layout<D>::kTotal);
   });
   CUtensorMap tq, tk, tv;
@@ -815,9 +945,18 @@ kvc_status run_prefill_tc2(const PrefillArgs& a) {
                                static_cast<uint64_t>(a.num_kv_heads) * D * 2,
                                static_cast<uint64_t>(a.block_size) * a.num_kv_heads * D * 2};
   const uint32_t box[4] = {64, 1, static_cast<uint32_t>(box_tokens), 1};
-  if (!encode_tmap_16bit(&tq, a.dtype, 3, a.q, qdims, qstrides, qbox, true) ||
-      !encode_tmap_16bit(&tk, a.dtype, 4, a.key_cache, dims, strides, box, true) ||
-      !encode_tmap_16bit(&tv, a.dtype, 4, a.value_cache, dims, strides, box, true))
+  // Fused write: K/V tiles of 128 packed tokens straight from the input.
+  const uint64_t kvdims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_kv_heads),
+                              static_cast<uint64_t>(a.num_tokens)};
+  const uint64_t kvstrides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(a.num_kv_heads) * D * 2};
+  const uint32_t kvbox[3] = {64, 1, kBN};
+  if (!encode_tmap_16bit(&tq, a.dtype, 3, a.q, qdims, qstrides, qbox, true))
+    return KVC_ERR_CUDA;
+  if (kFused ? !encode_tmap_16bit(&tk, a.dtype, 3, a.key, kvdims, kvstrides, kvbox, true) ||
+                   !encode_tmap_16bit(&tv, a.dtype, 3, a.value, kvdims, kvstrides, kvbox, true)
+             : !encode_tmap_16bit(&tk, a.dtype, 4, a.key_cache, dims, strides, box, true) ||
+                   !encode_tmap_16bit(&tv, a.dtype, 4, a.value_cache, dims, strides, box, true))
     return KVC_ERR_CUDA;
   Tc2Params p;
   p.out = a.out;
@@ -835,6 +974,14 @@ kvc_status run_prefill_tc2(const PrefillArgs& a) {
   p.box_tokens = box_tokens;
   p.window = a.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.key = static_cast<const uint8_t*>(a.key);
+  p.value = static_cast<const uint8_t*>(a.value);
+  p.key_cache = static_cast<uint8_t*>(a.key_cache);
+  p.value_cache = static_cast<uint8_t*>(a.value_cache);
+  p.slot_mapping = a.slot_mapping;
+  p.num_tokens = a.num_tokens;
+  p.num_kv_heads = a.num_kv_heads;
+  p.num_slots = static_cast<long long>(a.num_blocks) * a.block_size;
   // Work items: (query tile, head pair); query tiles <= T / BM + S.  One
   // persistent CTA per SM, or fewer when there are fewer items.
   const long long items =
@@ -844,26 +991,31 @@ kvc_status run_prefill_tc2(const PrefillArgs& a) {
   if (sms <= 0) return KVC_ERR_CUDA;
   const long long grid = items < sms ? items : sms;
   if (grid <= 0) return KVC_OK;
-  prefill_tc2_kernel<T, D, kBf16, kBand><<<static_cast<unsigned>(grid), kThreads,
-                                           Tc2Layout<D>::kTotal, a.stream>>>(tq, tk, tv, p);
+  prefill_tc2_kernel<T, D, kBf16, kBand, kFused>
+      <<<static_cast<unsigned>(grid), threads_of<kFused>(), Tc2Layout<D>::kTotal, a.stream>>>(
+          tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
 
 // Two heads per CTA; the caller checks that the GQA group size is even.
-template <bool kBand>
+template <bool kBand, bool kFused>
 kvc_status launch_tc2(const PrefillArgs& a) {
   if (a.head_dim == 64)
-    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 64, true, kBand>(a)
-                               : run_prefill_tc2<__half, 64, false, kBand>(a);
+    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 64, true, kBand, kFused>(a)
+                               : run_prefill_tc2<__half, 64, false, kBand, kFused>(a);
   if (a.head_dim == 128)
-    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 128, true, kBand>(a)
-                               : run_prefill_tc2<__half, 128, false, kBand>(a);
+    return a.dtype == KVC_BF16 ? run_prefill_tc2<__nv_bfloat16, 128, true, kBand, kFused>(a)
+                               : run_prefill_tc2<__half, 128, false, kBand, kFused>(a);
   return KVC_ERR_UNSUPPORTED;
 }
 }  // namespace
 
 kvc_status launch_prefill_attention_tc2(const PrefillArgs& a) {
-  return a.window > 0 ? launch_tc2<true>(a) : launch_tc2<false>(a);
+  return a.window > 0 ? launch_tc2<true, false>(a) : launch_tc2<false, false>(a);
+}
+
+kvc_status launch_prefill_fused_tc2(const PrefillArgs& a) {
+  return a.window > 0 ? launch_tc2<true, true>(a) : launch_tc2<false, true>(a);
 }
 
 }  // namespace kvc

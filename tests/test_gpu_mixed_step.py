@@ -33,8 +33,10 @@ def test_full_size_mixed_step(kvc_lib):
     dt, dl = dec.block_table.cuda(), dec.seq_lens.cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     slots_p = kvc.build_slot_mapping(pt, bs, ctx, NB, cu_seqlens=cu, num_tokens=T, err_flag=err)
+    # the prompts have no cached context: context_lens None, as the benchmark times the step
+    # (the cache write then rides in the attention kernel)
     out_p = kvc.varlen_prefill_paged(pre.q, pre.key, pre.value, cu, slots_p, pt, kc, vc,
-                                     pre.scale, pre.max_seqlen_q, context_lens=ctx, err_flag=err)
+                                     pre.scale, pre.max_seqlen_q, context_lens=None, err_flag=err)
     slots_d = torch.full((dec.q.shape[0],), -7, dtype=torch.int32, device="cuda")
     out_d = kvc.paged_decode_append(dec.q, dec.new_key, dec.new_value, kc, vc, dt, dl, dec.scale,
                                     slot_mapping=slots_d, err_flag=err)

@@ -1,7 +1,10 @@
 """GPU parity of the packed-varlen paged prefill against the oracle.
 
 The chunk's cache write must match bit for bit; attention outputs must be
-within max-abs 2e-3 (fp16) / 1e-2 (bf16) of the fp64 oracle.
+within max-abs 2e-3 (fp16) / 1e-2 (bf16) of the fp64 oracle.  Chunks without
+cached context are run both ways: with context_lens all zero (write, then
+attention through the cache) and with context_lens None (the write fused into
+the attention kernel for an even GQA group).
 """
 
 import numpy as np
@@ -15,16 +18,21 @@ from synth import make_config, prefill_case
 pytestmark = pytest.mark.gpu
 
 
-def gpu_prefill(kvc, c, err=None):
+def gpu_prefill(kvc, c, err=None, no_context=False):
+    """no_context: pass context_lens=None (every context length must be 0)."""
     d = {k: to_cuda(getattr(c, k)) for k in ("q", "key", "value", "cu_seqlens", "context_lens",
                                              "block_table", "key_cache", "value_cache")}
+    if no_context:
+        assert int(c.context_lens.abs().sum()) == 0
     T = c.q.shape[0]
     slots = kvc.build_slot_mapping(d["block_table"], c.block_size, d["context_lens"],
                                    c.key_cache.shape[0], cu_seqlens=d["cu_seqlens"], num_tokens=T,
                                    err_flag=err)
     out = kvc.varlen_prefill_paged(d["q"], d["key"], d["value"], d["cu_seqlens"], slots,
                                    d["block_table"], d["key_cache"], d["value_cache"], c.scale,
-                                   c.max_seqlen_q, context_lens=d["context_lens"], err_flag=err)
+                                   c.max_seqlen_q,
+                                   context_lens=None if no_context else d["context_lens"],
+                                   err_flag=err)
     torch.cuda.synchronize()
     return slots, d, out
 
@@ -51,6 +59,18 @@ CASES = [
 ]
 
 
+NO_CONTEXT_CASES = [
+    # (lens, Hq, Hkv, D, bs, dtype): chunks without cached context, context_lens None
+    ([5, 3], 4, 2, 64, 8, "f16"),
+    ([1, 127, 128, 129], 8, 2, 128, 16, "bf16"),
+    ([257], 2, 2, 64, 128, "f16"),
+    ([500, 77, 250], 32, 8, 128, 64, "bf16"),
+    ([300, 0, 45, 256, 1], 16, 4, 128, 32, "f16"),
+    ([640, 129], 4, 1, 128, 128, "bf16"),     # group 4, one KV head
+    ([200, 13, 385], 12, 4, 64, 8, "bf16"),   # odd group: the write then the one-head kernel
+]
+
+
 @pytest.mark.parametrize("lens,ctx,Hq,Hkv,D,bs,dtype", CASES)
 def test_prefill_matches_oracle(kvc_lib, lens, ctx, Hq, Hkv, D, bs, dtype):
     c = prefill_case(31, lens, Hq, Hkv, D, bs, context=ctx, dtype=dtype)
@@ -64,6 +84,66 @@ def test_prefill_matches_oracle(kvc_lib, lens, ctx, Hq, Hkv, D, bs, dtype):
     assert np.array_equal(bits(d["key_cache"]), kc) and np.array_equal(bits(d["value_cache"]), vc)
     e = excess(out, ref, dtype)
     assert e <= 0, e
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,D,bs,dtype", NO_CONTEXT_CASES)
+def test_prefill_without_context_matches_oracle(kvc_lib, lens, Hq, Hkv, D, bs, dtype):
+    """context_lens None: the cache bits and outputs of the fused write + attention."""
+    c = prefill_case(37, lens, Hq, Hkv, D, bs, dtype=dtype)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots, d, out = gpu_prefill(kvc_lib, c, err, no_context=True)
+    assert int(err.item()) == 0
+    sm, ref = oracle_prefill(c)
+    assert slots.cpu().numpy().tolist() == sm.tolist()
+    kc, vc = O.reshape_and_cache(bits(c.key), bits(c.value), bits(c.key_cache),
+                                 bits(c.value_cache), sm)
+    assert np.array_equal(bits(d["key_cache"]), kc) and np.array_equal(bits(d["value_cache"]), vc)
+    e = excess(out, ref, dtype)
+    assert e <= 0, e
+    # the same outputs, bit for bit, as the write followed by attention through the cache
+    _, _, through_cache = gpu_prefill(kvc_lib, c)
+    assert torch.equal(out.view(torch.int16), through_cache.view(torch.int16))
+
+
+def test_prefill_without_context_write_edges(kvc_lib):
+    """Fused write: skipped (-1) and out-of-pool slots, tokens after the last sequence, and a
+    sequence longer than its table row are written exactly as kvc_reshape_and_cache writes them."""
+    lens = [40, 150, 0, 30]
+    c = prefill_case(38, lens, 8, 2, 128, 8, dtype="bf16", num_blocks=64)
+    c.block_table = c.block_table[:, :5].contiguous()   # sequence 1 (150 > 40 slots) overflows
+    T0 = sum(lens)
+    extra = 20                                        # tokens after cu_seqlens[-1]
+    g = torch.Generator().manual_seed(9)
+    for name in ("q", "key", "value"):
+        t = getattr(c, name)
+        setattr(c, name, torch.cat([t, torch.randn((extra,) + tuple(t.shape[1:]), generator=g)
+                                    .to(t.dtype)]))
+    d = {k: to_cuda(getattr(c, k)) for k in ("q", "key", "value", "cu_seqlens", "block_table",
+                                             "key_cache", "value_cache")}
+    nslots = 64 * 8
+    bt = c.block_table.numpy()
+    sm, cu = [], c.cu_seqlens.tolist()
+    for s_ in range(len(lens)):
+        for p in range(lens[s_]):
+            sm.append(int(bt[s_, p // 8]) * 8 + p % 8 if p // 8 < 5 else -1)
+    used = {int(bt[s_, j]) for s_ in range(len(lens)) for j in range(min(5, -(-lens[s_] // 8)))}
+    free = [b for b in range(64) if b not in used]
+    tail = [free[i // 8] * 8 + i % 8 for i in range(extra)]
+    sm = np.asarray(sm + tail, dtype=np.int64)
+    sm[3] = -1                                          # skipped
+    sm[7] = nslots + 5                                  # outside the pool: skipped, flagged
+    slots = torch.from_numpy(sm.astype(np.int32)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvc_lib.varlen_prefill_paged(d["q"], d["key"], d["value"], d["cu_seqlens"], slots,
+                                 d["block_table"], d["key_cache"], d["value_cache"], c.scale,
+                                 max(lens), context_lens=None, err_flag=err)
+    torch.cuda.synchronize()
+    flags = int(err.item())
+    assert flags & kvc_lib.FLAG_SLOT_RANGE and flags & kvc_lib.FLAG_LEN_RANGE
+    kc, vc = O.reshape_and_cache(bits(c.key), bits(c.value), bits(c.key_cache),
+                                 bits(c.value_cache), np.where(sm >= nslots, -1, sm))
+    assert np.array_equal(bits(d["key_cache"]), kc) and np.array_equal(bits(d["value_cache"]), vc)
+    assert T0 + extra == c.q.shape[0] and cu[-1] == T0
 
 
 def test_prefill_packed_equals_independent_and_is_bitwise_stable(kvc_lib):
@@ -143,11 +223,13 @@ def test_prefill_length_beyond_table_is_flagged(kvc_lib):
     assert int(err.item()) & kvc_lib.FLAG_LEN_RANGE
 
 
-def test_full_size_mixed_prefill_sampled(kvc_lib):
-    """The mixed workload's 16 packed prefills, sampled rows checked against the oracle."""
+@pytest.mark.parametrize("no_context", [False, True])
+def test_full_size_mixed_prefill_sampled(kvc_lib, no_context):
+    """The mixed workload's 16 packed prefills, sampled rows checked against the oracle
+    (context_lens None: the fused write, as the benchmark calls it)."""
     pre, _ = make_config("mixed_packed", seed=0, value_device="cuda")
     kc0, vc0 = pre.key_cache.clone(), pre.value_cache.clone()
-    slots, d, out = gpu_prefill(kvc_lib, pre)
+    slots, d, out = gpu_prefill(kvc_lib, pre, no_context=no_context)
     bt = pre.block_table.numpy()
     sm = O.slot_mapping(bt, pre.block_size, pre.context_lens.numpy(), pre.cu_seqlens.numpy())
     assert slots.cpu().numpy().tolist() == sm.tolist()
@@ -155,6 +237,7 @@ def test_full_size_mixed_prefill_sampled(kvc_lib):
     bs = pre.block_size
     g = torch.Generator().manual_seed(1)
     worst = -1.0
+    touched = torch.zeros(kc0.shape[0], dtype=torch.bool, device=kc0.device)
     for s in range(len(cu) - 1):
         n = cu[s + 1] - cu[s]
         nblk = -(-n // bs)
@@ -165,6 +248,11 @@ def test_full_size_mixed_prefill_sampled(kvc_lib):
         ssm = O.slot_mapping(table, bs, [0], [0, n])
         kc, vc = O.reshape_and_cache(pre.key[cu[s]:cu[s + 1]].double().cpu().numpy(),
                                      pre.value[cu[s]:cu[s + 1]].double().cpu().numpy(), kc, vc, ssm)
+        # every written row (and the rest of the sequence's blocks) bit for bit
+        dt = d["key_cache"].dtype
+        assert np.array_equal(bits(d["key_cache"][ids]), bits(torch.from_numpy(kc).to(dt)))
+        assert np.array_equal(bits(d["value_cache"][ids]), bits(torch.from_numpy(vc).to(dt)))
+        touched[ids] = True
         K = O.gather_sequence(kc, table[0], n)
         V = O.gather_sequence(vc, table[0], n)
         rows = sorted(set([0, n - 1] + torch.randint(0, n, (6,), generator=g).tolist()))
@@ -176,9 +264,13 @@ def test_full_size_mixed_prefill_sampled(kvc_lib):
                 ref = O.softmax_attention(qrow[h], K[:i + 1, gg], V[:i + 1, gg], pre.scale)
                 worst = max(worst, excess(out[t, h], ref, "bf16"))
     assert worst <= 0, worst
+    # blocks of no sequence are untouched
+    assert torch.equal(d["key_cache"][~touched], kc0[~touched])
+    assert torch.equal(d["value_cache"][~touched], vc0[~touched])
 
 
-def test_prefill_head_pairs_repeatable_at_tile_boundaries(kvc_lib):
+@pytest.mark.parametrize("no_context", [False, True])
+def test_prefill_head_pairs_repeatable_at_tile_boundaries(kvc_lib, no_context):
     """Two heads per CTA share one P buffer: lengths that end one row into a new tile, repeated.
 
     Repeats must match the oracle and each other bit for bit (a premature reuse of
@@ -191,7 +283,7 @@ def test_prefill_head_pairs_repeatable_at_tile_boundaries(kvc_lib):
         first = None
         for _ in range(4):
             err = torch.zeros(1, dtype=torch.int32, device="cuda")
-            _, _, out = gpu_prefill(kvc_lib, c, err)
+            _, _, out = gpu_prefill(kvc_lib, c, err, no_context=no_context)
             assert int(err.item()) == 0
             e = excess(out, ref, "bf16")
             assert e <= 0, (Hq, Hkv, e)

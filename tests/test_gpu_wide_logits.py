@@ -48,8 +48,10 @@ def test_decode_wide_logits(kvc_lib, dtype, num_ctas):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_prefill_wide_logits(kvc_lib, dtype):
-    lens, ctx = [300, 45, 129], [17, 200, 0]
+@pytest.mark.parametrize("no_context", [False, True])
+def test_prefill_wide_logits(kvc_lib, dtype, no_context):
+    """no_context: prompts without cached context, context_lens None (fused cache write)."""
+    lens, ctx = [300, 45, 129], ([0, 0, 0] if no_context else [17, 200, 0])
     for Hq, Hkv in ((8, 2), (3, 1)):            # even group (two heads per CTA) and odd
         c = prefill_case(52, lens, Hq, Hkv, 128, 64, context=ctx, dtype=dtype)
         c.q = (c.q.float() * WIDE).to(c.q.dtype)
@@ -62,7 +64,8 @@ def test_prefill_wide_logits(kvc_lib, dtype):
                                            num_tokens=T)
         out = kvc_lib.varlen_prefill_paged(d["q"], d["key"], d["value"], d["cu_seqlens"], slots,
                                            d["block_table"], d["key_cache"], d["value_cache"],
-                                           c.scale, c.max_seqlen_q, context_lens=d["context_lens"])
+                                           c.scale, c.max_seqlen_q,
+                                           context_lens=None if no_context else d["context_lens"])
         torch.cuda.synchronize()
         bt = c.block_table.numpy()
         sm = O.slot_mapping(bt, c.block_size, c.context_lens.numpy(), c.cu_seqlens.numpy())

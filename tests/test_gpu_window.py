@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import excess, to_cuda
+from gpu_util import bits, excess, to_cuda
 from oracle import kvc_oracle as O
 from synth import decode_case
 
@@ -157,6 +157,35 @@ def test_prefill_window_matches_oracle(kvc_lib, lens, ctx, Hq, Hkv, D, bs, dtype
         c.cu_seqlens.numpy(), c.context_lens.numpy(), sm, bt, c.key_cache.double().numpy(),
         c.value_cache.double().numpy(), c.scale, window)
     assert excess(out, ref, dtype) <= 0
+
+
+@pytest.mark.parametrize("window", [1, 37, 128, 129, 300])
+def test_prefill_window_without_context_matches_oracle(kvc_lib, window):
+    """context_lens None with an even group: the band kernel with the fused cache write."""
+    lens = [300, 45, 129, 1, 256]
+    c = prefill_case(67, lens, 8, 2, 128, 64, dtype="bf16")
+    d = {k: to_cuda(getattr(c, k)) for k in ("q", "key", "value", "cu_seqlens", "context_lens",
+                                             "block_table", "key_cache", "value_cache")}
+    slots = kvc_lib.build_slot_mapping(d["block_table"], c.block_size, d["context_lens"],
+                                       c.key_cache.shape[0], cu_seqlens=d["cu_seqlens"],
+                                       num_tokens=c.q.shape[0])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kvc_lib.varlen_prefill_paged_window(d["q"], d["key"], d["value"], d["cu_seqlens"], slots,
+                                              d["block_table"], d["key_cache"], d["value_cache"],
+                                              c.scale, c.max_seqlen_q, window, context_lens=None,
+                                              err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bt = c.block_table.numpy()
+    sm = O.slot_mapping(bt, c.block_size, c.context_lens.numpy(), c.cu_seqlens.numpy())
+    ref, kc, vc = O.windowed_varlen_prefill_paged(
+        c.q.double().numpy(), c.key.double().numpy(), c.value.double().numpy(),
+        c.cu_seqlens.numpy(), c.context_lens.numpy(), sm, bt, c.key_cache.double().numpy(),
+        c.value_cache.double().numpy(), c.scale, window)
+    assert excess(out, ref, "bf16") <= 0
+    ek, ev = O.reshape_and_cache(bits(c.key), bits(c.value), bits(c.key_cache),
+                                 bits(c.value_cache), sm)
+    assert np.array_equal(bits(d["key_cache"]), ek) and np.array_equal(bits(d["value_cache"]), ev)
 
 
 @pytest.mark.parametrize("case", PREFILL_CASES[:3])
