@@ -67,6 +67,7 @@ NO_CONTEXT_CASES = [
     ([500, 77, 250], 32, 8, 128, 64, "bf16"),
     ([300, 0, 45, 256, 1], 16, 4, 128, 32, "f16"),
     ([640, 129], 4, 1, 128, 128, "bf16"),     # group 4, one KV head
+    ([130, 7, 300], 8, 4, 64, 16, "bf16"),    # D 64, bf16
     ([200, 13, 385], 12, 4, 64, 8, "bf16"),   # odd group: the write then the one-head kernel
 ]
 

@@ -160,10 +160,11 @@ def test_prefill_window_matches_oracle(kvc_lib, lens, ctx, Hq, Hkv, D, bs, dtype
 
 
 @pytest.mark.parametrize("window", [1, 37, 128, 129, 300])
-def test_prefill_window_without_context_matches_oracle(kvc_lib, window):
+@pytest.mark.parametrize("D,bs,dtype", [(128, 64, "bf16"), (64, 16, "f16")])
+def test_prefill_window_without_context_matches_oracle(kvc_lib, window, D, bs, dtype):
     """context_lens None with an even group: the band kernel with the fused cache write."""
     lens = [300, 45, 129, 1, 256]
-    c = prefill_case(67, lens, 8, 2, 128, 64, dtype="bf16")
+    c = prefill_case(67, lens, 8, 2, D, bs, dtype=dtype)
     d = {k: to_cuda(getattr(c, k)) for k in ("q", "key", "value", "cu_seqlens", "context_lens",
                                              "block_table", "key_cache", "value_cache")}
     slots = kvc_lib.build_slot_mapping(d["block_table"], c.block_size, d["context_lens"],
@@ -182,7 +183,7 @@ def test_prefill_window_without_context_matches_oracle(kvc_lib, window):
         c.q.double().numpy(), c.key.double().numpy(), c.value.double().numpy(),
         c.cu_seqlens.numpy(), c.context_lens.numpy(), sm, bt, c.key_cache.double().numpy(),
         c.value_cache.double().numpy(), c.scale, window)
-    assert excess(out, ref, "bf16") <= 0
+    assert excess(out, ref, dtype) <= 0
     ek, ev = O.reshape_and_cache(bits(c.key), bits(c.value), bits(c.key_cache),
                                  bits(c.value_cache), sm)
     assert np.array_equal(bits(d["key_cache"]), ek) and np.array_equal(bits(d["value_cache"]), ev)
