@@ -563,13 +563,13 @@ __device__ __forceinline__ void tc2_softmax(const Tc2Params& p, uint8_t* smem, u
 // latency-bound, so each lane keeps kBatch K and V loads in flight; the
 // item's slots are staged in shared memory (the schedule histogram's space,
 // unused after the prologue).
-// The writer paces itself by the producer's progress: kWriteBatch loads in
-// flight while it is less than two items ahead of the producer, kWriteBatchAhead
-// once it is further ahead -- fewer loads in flight take less from the
-// attention (measured: 2 in flight 406 us, 8 in flight 418 us on 16 prompts
-// of 50-3000 tokens, whose long items leave the writer ahead), while short
-// items need the higher rate to keep up (96 prompts of 64-512 tokens: 2 in
-// flight 312 us, 8 in flight 194 us).
+// The writer paces itself by the producer's progress: kWriteBatchAhead loads
+// in flight while it is two or more items ahead of the producer on an item of
+// at least 4 key tiles, kWriteBatch otherwise -- fewer loads in flight take
+// less from the attention (measured: 2 in flight 406 us, 8 in flight 418 us
+// on 16 prompts of 50-3000 tokens, whose long items leave the writer ahead),
+// while short items need the higher rate to keep up (96 prompts of 64-512
+// tokens: 2 in flight 312 us, 8 in flight 194 us, paced 197 us).
 constexpr int kWriteBatch = 8, kWriteBatchAhead = 2;
 template <int D, int kBatch>
 __device__ __forceinline__ void tc2_write_rows(const Tc2Params& p, int* slots, int tok, int rows,
@@ -889,7 +889,7 @@ __global__ void __launch_bounds__(threads_of<kFused>(), 1)
       Tc2Item it;
       if (!next_item(k, it)) break;
       if (it.h0 % p.group != 0) continue;
-      if (k > *progress + 1)
+      if (k > *progress + 1 && it.n_tiles >= 4)
         tc2_write_rows<D, kWriteBatchAhead>(p, slots, it.tok0, it.q_rows, it.h0 / p.group, lane);
       else
         tc2_write_rows<D, kWriteBatch>(p, slots, it.tok0, it.q_rows, it.h0 / p.group, lane);
